@@ -1,0 +1,155 @@
+"""CPU oracle for MoE expert-parallel Dispatch / Combine (test infrastructure only).
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg may import
+this package.  The product path (the CUDA library and its Python binding) never does.
+
+The arithmetic lives in plain C (``ep_oracle.c``, single-threaded, ``-O2 -ffp-contract=off``);
+this module builds it with gcc on first use and marshals numpy arrays through ctypes.
+Every function restates the definitions of the MORI-EP pages (gfx1201 PR, "How the gfx1201
+kernels work"; MORI-EP guide, "Operator API"), see the C file's header for the readings.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ep_oracle.c")
+_LIB = os.path.join(_HERE, "libep_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+ERR_ARG = -1
+ERR_INDEX = -6
+
+_p = ctypes.c_void_p
+
+
+def build(force: bool = False) -> str:
+    """Compile ep_oracle.c into libep_oracle.so next to it (gcc, no CUDA)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+                               "-fPIC", "-shared", "-o", tmp, _SRC])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            lib.ep_oracle_dispatch.restype = ctypes.c_int
+            lib.ep_oracle_dispatch.argtypes = [ctypes.c_int] * 7 + [_p] * 12
+            lib.ep_oracle_combine.restype = ctypes.c_int
+            lib.ep_oracle_combine.argtypes = [ctypes.c_int] * 5 + [_p] * 6
+            for name in ("ep_oracle_bf16_from_f32_array", "ep_oracle_f16_from_f32_array",
+                         "ep_oracle_f32_from_f16_array"):
+                fn = getattr(lib, name)
+                fn.restype = None
+                fn.argtypes = [_p, _p, ctypes.c_int64]
+            _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"], "oracle arrays must be C-contiguous"
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def dispatch(W, E, k, H, elem_bytes, sd, M, x, weights, scales, indices, n_tok):
+    """Dispatch every source token to one receive row per distinct destination rank.
+
+    Returns a dict with ``recv_x [W][W*M][H]`` (raw bits), ``recv_idx``, ``recv_w`` (or None),
+    ``recv_scales`` (or None), ``src_pos [W][W*M]``, ``slot_of [W][M][W]`` (row of token (s,t)
+    on rank r, -1 if not sent there), ``recv_count [W]`` and ``status`` (0, or -6 when an expert
+    id was out of range).  Receive rows at or past ``recv_count[r]`` are zero.
+    """
+    lib = _load()
+    rows = W * M
+    x = np.ascontiguousarray(x)
+    indices = np.ascontiguousarray(indices, dtype=np.int32)
+    n_tok = np.ascontiguousarray(n_tok, dtype=np.int32)
+    dt = np.uint8 if elem_bytes == 1 else np.uint16
+    out = {
+        "recv_x": np.zeros((W, rows, H), dtype=dt),
+        "recv_idx": np.zeros((W, rows, k), dtype=np.int32),
+        "recv_w": np.zeros((W, rows, k), dtype=np.float32) if weights is not None else None,
+        "recv_scales": np.zeros((W, rows, sd), dtype=np.float32) if sd else None,
+        "src_pos": np.full((W, rows), -1, dtype=np.int32),
+        "slot_of": np.full((W, M, W), -1, dtype=np.int32),
+        "recv_count": np.zeros(W, dtype=np.int32),
+    }
+    w = None if weights is None else np.ascontiguousarray(weights, dtype=np.float32)
+    sc = None if not sd else np.ascontiguousarray(scales, dtype=np.float32)
+    st = lib.ep_oracle_dispatch(W, E, k, H, elem_bytes, sd, M, _ptr(x), _ptr(w), _ptr(sc),
+                                _ptr(indices), _ptr(n_tok), _ptr(out["recv_x"]),
+                                _ptr(out["recv_idx"]), _ptr(out["recv_w"]),
+                                _ptr(out["recv_scales"]), _ptr(out["src_pos"]),
+                                _ptr(out["slot_of"]), _ptr(out["recv_count"]))
+    if st == ERR_ARG:
+        raise ValueError("ep_oracle_dispatch: invalid arguments")
+    out["status"] = st
+    return out
+
+
+def combine(W, k, H, out_fp16, M, n_tok, slot_of, expert_out, w_in=None, out=None):
+    """Gather each source token's rows back, sum in FP32 in ascending rank order, round to
+    nearest even into BF16 (``out_fp16=False``) or FP16.  Returns ``(out [W][M][H] uint16,
+    out_w [W][M][k] float32 or None)``; rows past ``n_tok[s]`` are zero (or ``out``'s content)."""
+    lib = _load()
+    n_tok = np.ascontiguousarray(n_tok, dtype=np.int32)
+    slot_of = np.ascontiguousarray(slot_of, dtype=np.int32)
+    expert_out = np.ascontiguousarray(expert_out).view(np.uint16)
+    if out is None:
+        out = np.zeros((W, M, H), dtype=np.uint16)
+    out_w = np.zeros((W, M, k), dtype=np.float32) if w_in is not None else None
+    w_in = None if w_in is None else np.ascontiguousarray(w_in, dtype=np.float32)
+    st = lib.ep_oracle_combine(W, k, H, 1 if out_fp16 else 0, M, _ptr(n_tok), _ptr(slot_of),
+                               _ptr(expert_out), _ptr(w_in), _ptr(out), _ptr(out_w))
+    if st != 0:
+        raise ValueError("ep_oracle_combine: invalid arguments")
+    return out, out_w
+
+
+def bf16_from_f32(a):
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    o = np.empty(a.shape, dtype=np.uint16)
+    _load().ep_oracle_bf16_from_f32_array(_ptr(a), _ptr(o), a.size)
+    return o
+
+
+def f16_from_f32(a):
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    o = np.empty(a.shape, dtype=np.uint16)
+    _load().ep_oracle_f16_from_f32_array(_ptr(a), _ptr(o), a.size)
+    return o
+
+
+def f32_from_f16(a):
+    a = np.ascontiguousarray(a, dtype=np.uint16)
+    o = np.empty(a.shape, dtype=np.float32)
+    _load().ep_oracle_f32_from_f16_array(_ptr(a), _ptr(o), a.size)
+    return o
+
+
+def run_workload(wl, expert_out_fn=None):
+    """Oracle dispatch -> harness expert -> oracle combine for one workload.
+
+    ``expert_out_fn(wl, disp)`` returns the expert output rows ``[W][W*M][H]`` (16-bit bits);
+    None means the identity expert on a 16-bit payload (expert output = receive rows).
+    """
+    disp = dispatch(wl.W, wl.E, wl.k, wl.H, wl.elem_bytes, wl.sd, wl.M, wl.x, wl.weights,
+                    wl.scales, wl.indices, wl.n_tok)
+    eo = disp["recv_x"] if expert_out_fn is None else expert_out_fn(wl, disp)
+    out, out_w = combine(wl.W, wl.k, wl.H, wl.combine_dtype == "fp16", wl.M, wl.n_tok,
+                         disp["slot_of"], eo, disp["recv_w"])
+    return disp, eo, out, out_w

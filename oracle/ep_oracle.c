@@ -1,0 +1,235 @@
+/*
+ * ep_oracle.c -- plain, slow, single-threaded CPU oracle for MoE expert-parallel
+ * Dispatch and Combine.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or call this
+ * file; only the tests, the smoke check and the benchmark's CPU-baseline leg do.  It shares
+ * no code, header, table or helper with the CUDA implementation.
+ *
+ * What it computes (MORI-EP gfx1201 PR "feat(ep): add opt-in gfx1201 EP2/EP4 support",
+ * section "How the gfx1201 kernels work", Dispatch and Combine bullets; MORI-EP guide,
+ * section 3 "Operator API", dispatch(), combine(), get_dispatch_src_token_pos()):
+ *
+ *   Dispatch.  Every token t < n_tok[s] of source rank s names k experts idx[s][t][0..k).
+ *   Expert e lives on rank floor(e / E) (contiguous blocks of E experts per rank; the pages
+ *   only say "num_experts_per_rank").  The token gets ONE receive row on each DISTINCT
+ *   destination rank (experts on the same rank share one hidden payload).  The row holds
+ *   the token's whole hidden vector, its whole top-k index row, its FP32 weight row (if
+ *   given) and its FP32 scale row (if scale_dim > 0).  Rows are handed out per destination
+ *   rank in (source rank ascending, token ascending) order.  The reverse map entry of the
+ *   row is src_rank * (W * M) + src_token (guide, get_dispatch_src_token_pos()).  Receive
+ *   capacity per rank is W * M rows (each source sends at most one row per token).
+ *
+ *   Combine.  For each source token the rows it was sent to are read back, in ascending
+ *   destination-rank order, converted to FP32, summed starting from +0.0f with plain float
+ *   additions (no fused multiply-add; compiled with -ffp-contract=off), and the sum is
+ *   rounded to nearest even into BF16 or FP16 ("The source sums its local and received
+ *   contributions in FP32, then converts the output to BF16/FP16").  Optional FP32 weight
+ *   rows are summed the same way, separately; routing weights are never applied to the
+ *   payload ("applying routing weights to expert outputs remain the caller's
+ *   responsibility").
+ *
+ *   Expert ids outside [0, W*E) route nowhere and make dispatch return EP_ORACLE_ERR_INDEX.
+ *
+ * Conversions are written from the IEEE 754 binary16 / bfloat16 definitions
+ * (round to nearest, ties to even; overflow to infinity; NaN stays NaN).
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define EP_ORACLE_OK 0
+#define EP_ORACLE_ERR_ARG (-1)
+#define EP_ORACLE_ERR_INDEX (-6)
+
+/* ---- IEEE conversions ------------------------------------------------------------- */
+
+static uint32_t f32_bits(float f) { uint32_t b; memcpy(&b, &f, 4); return b; }
+static float bits_f32(uint32_t b) { float f; memcpy(&f, &b, 4); return f; }
+
+/* float -> bfloat16, round to nearest even.  bfloat16 is the top half of a binary32, so
+ * rounding drops the low 16 bits: add half of the dropped range, plus one more when the
+ * kept part is odd (ties go to the even neighbour), then truncate.  A carry out of the
+ * mantissa correctly bumps the exponent; past the largest finite value it lands on Inf. */
+uint16_t ep_oracle_bf16_from_f32(float f)
+{
+    uint32_t b = f32_bits(f);
+    if ((b & 0x7FFFFFFFu) > 0x7F800000u)        /* NaN: keep sign, force a quiet NaN */
+        return (uint16_t)(((b >> 16) & 0x8000u) | 0x7FC0u);
+    uint32_t kept_lsb = (b >> 16) & 1u;
+    b += 0x7FFFu + kept_lsb;
+    return (uint16_t)(b >> 16);
+}
+
+float ep_oracle_f32_from_bf16(uint16_t h) { return bits_f32((uint32_t)h << 16); }
+
+/* float -> binary16 (1 sign, 5 exponent bits with bias 15, 10 fraction bits), RNE. */
+uint16_t ep_oracle_f16_from_f32(float f)
+{
+    uint32_t b = f32_bits(f);
+    uint16_t sign = (uint16_t)((b >> 16) & 0x8000u);
+    uint32_t a = b & 0x7FFFFFFFu;
+    if (a > 0x7F800000u) return (uint16_t)(sign | 0x7E00u);     /* NaN */
+    if (a >= 0x477FF000u) return (uint16_t)(sign | 0x7C00u);    /* >= 65520: rounds to Inf */
+    if (a >= 0x38800000u) {                                     /* >= 2^-14: normal half */
+        uint32_t exp = (a >> 23) - 127u + 15u;
+        uint32_t h = (exp << 10) | ((a & 0x7FFFFFu) >> 13);
+        uint32_t rem = a & 0x1FFFu;                             /* 13 dropped bits */
+        if (rem > 0x1000u || (rem == 0x1000u && (h & 1u))) h += 1u;
+        return (uint16_t)(sign | h);
+    }
+    /* subnormal half: value / 2^-24 rounded to an integer.  With the binary32 significand
+     * m (implicit bit included) and biased exponent E, value = m * 2^(E - 150), so the
+     * integer is m * 2^(E - 126), i.e. m shifted right by 126 - E. */
+    uint32_t E = a >> 23;
+    if (E < 102u) return sign;                                  /* below 2^-25: rounds to 0 */
+    uint32_t m = (a & 0x7FFFFFu) | 0x800000u;
+    uint32_t shift = 126u - E;                                  /* 14 .. 24 */
+    uint32_t h = m >> shift;
+    uint32_t rem = m & ((1u << shift) - 1u);
+    uint32_t half = 1u << (shift - 1u);
+    if (rem > half || (rem == half && (h & 1u))) h += 1u;       /* may carry into 0x400 */
+    return (uint16_t)(sign | h);
+}
+
+/* binary16 -> float, exact. */
+float ep_oracle_f32_from_f16(uint16_t h)
+{
+    uint32_t sign = ((uint32_t)h & 0x8000u) << 16;
+    uint32_t exp = ((uint32_t)h >> 10) & 0x1Fu;
+    uint32_t frac = (uint32_t)h & 0x3FFu;
+    if (exp == 0x1Fu) return bits_f32(sign | 0x7F800000u | (frac << 13));
+    if (exp == 0) {
+        /* subnormal: frac * 2^-24, exact in binary32 */
+        float v = (float)frac * bits_f32(0x33800000u);          /* 2^-24 */
+        return sign ? -v : v;
+    }
+    return bits_f32(sign | ((exp - 15u + 127u) << 23) | (frac << 13));
+}
+
+void ep_oracle_bf16_from_f32_array(const float* in, uint16_t* out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = ep_oracle_bf16_from_f32(in[i]);
+}
+
+void ep_oracle_f16_from_f32_array(const float* in, uint16_t* out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = ep_oracle_f16_from_f32(in[i]);
+}
+
+void ep_oracle_f32_from_f16_array(const uint16_t* in, float* out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = ep_oracle_f32_from_f16(in[i]);
+}
+
+/* ---- Dispatch ---------------------------------------------------------------------- */
+
+/*
+ * Arguments (all host pointers, row-major):
+ *   x        [W][M][H] elements of elem_bytes bytes (raw bits)
+ *   w        [W][M][k] float or NULL
+ *   scales   [W][M][sd] float, NULL iff sd == 0
+ *   idx      [W][M][k] int32
+ *   n_tok    [W] tokens per source rank, each in 0..M
+ * Outputs (caller-allocated):
+ *   recv_x      [W][W*M][H]      recv_idx [W][W*M][k]      recv_w [W][W*M][k] (if w)
+ *   recv_scales [W][W*M][sd] (if sd)
+ *   src_pos     [W][W*M]         reverse map, src_rank * (W*M) + src_token
+ *   slot_of     [W][M][W]        slot_of[s][t][r] = row of (s,t) on rank r, or -1
+ *   recv_count  [W]
+ */
+int ep_oracle_dispatch(int W, int E, int k, int H, int elem_bytes, int sd, int M,
+                       const void* x, const float* w, const float* scales, const int32_t* idx,
+                       const int32_t* n_tok,
+                       void* recv_x, int32_t* recv_idx, float* recv_w, float* recv_scales,
+                       int32_t* src_pos, int32_t* slot_of, int32_t* recv_count)
+{
+    if (W < 1 || E < 1 || k < 1 || H < 1 || M < 1 || sd < 0) return EP_ORACLE_ERR_ARG;
+    if (elem_bytes != 1 && elem_bytes != 2) return EP_ORACLE_ERR_ARG;
+    const int64_t rows = (int64_t)W * M;                 /* receive rows per rank */
+    const int64_t n_experts = (int64_t)W * E;
+    const size_t row_bytes = (size_t)H * (size_t)elem_bytes;
+    int64_t* cnt = (int64_t*)calloc((size_t)W, sizeof(int64_t));
+    unsigned char* in_D = (unsigned char*)malloc((size_t)W);
+    if (!cnt || !in_D) { free(cnt); free(in_D); return EP_ORACLE_ERR_ARG; }
+    int status = EP_ORACLE_OK;
+
+    for (int s = 0; s < W; ++s) {
+        if (n_tok[s] < 0 || n_tok[s] > M) { status = EP_ORACLE_ERR_ARG; break; }
+        for (int t = 0; t < n_tok[s]; ++t) {
+            const int64_t tok = (int64_t)s * M + t;
+            const int32_t* ids = idx + tok * k;
+            /* D(s,t): the distinct destination ranks of the token's experts */
+            memset(in_D, 0, (size_t)W);
+            for (int j = 0; j < k; ++j) {
+                int64_t e = ids[j];
+                if (e < 0 || e >= n_experts) { status = EP_ORACLE_ERR_INDEX; continue; }
+                in_D[e / E] = 1;
+            }
+            for (int r = 0; r < W; ++r) {
+                slot_of[tok * W + r] = -1;
+                if (!in_D[r]) continue;
+                const int64_t slot = cnt[r]++;
+                const int64_t row = (int64_t)r * rows + slot;
+                memcpy((char*)recv_x + (size_t)row * row_bytes,
+                       (const char*)x + (size_t)tok * row_bytes, row_bytes);
+                memcpy(recv_idx + row * k, ids, (size_t)k * sizeof(int32_t));
+                if (w) memcpy(recv_w + row * k, w + tok * k, (size_t)k * sizeof(float));
+                if (sd > 0) memcpy(recv_scales + row * sd, scales + tok * sd, (size_t)sd * sizeof(float));
+                src_pos[(int64_t)r * rows + slot] = (int32_t)((int64_t)s * rows + t);
+                slot_of[tok * W + r] = (int32_t)slot;
+            }
+        }
+    }
+    for (int r = 0; r < W; ++r) recv_count[r] = (int32_t)cnt[r];
+    free(cnt);
+    free(in_D);
+    return status;
+}
+
+/* ---- Combine ----------------------------------------------------------------------- */
+
+/*
+ *   expert_out [W][W*M][H] 16-bit elements (BF16 if out_fp16 == 0, FP16 otherwise)
+ *   w_in       [W][W*M][k] float or NULL
+ *   slot_of    [W][M][W] as written by ep_oracle_dispatch
+ *   out        [W][M][H] 16-bit elements; rows t >= n_tok[s] are left untouched
+ *   out_w      [W][M][k] float or NULL (written iff w_in and out_w are both given)
+ */
+int ep_oracle_combine(int W, int k, int H, int out_fp16, int M, const int32_t* n_tok,
+                      const int32_t* slot_of, const uint16_t* expert_out, const float* w_in,
+                      uint16_t* out, float* out_w)
+{
+    if (W < 1 || k < 1 || H < 1 || M < 1) return EP_ORACLE_ERR_ARG;
+    const int64_t rows = (int64_t)W * M;
+    float* acc = (float*)malloc((size_t)H * sizeof(float));
+    float* accw = (float*)malloc((size_t)k * sizeof(float));
+    if (!acc || !accw) { free(acc); free(accw); return EP_ORACLE_ERR_ARG; }
+    for (int s = 0; s < W; ++s) {
+        for (int t = 0; t < n_tok[s]; ++t) {
+            const int64_t tok = (int64_t)s * M + t;
+            for (int h = 0; h < H; ++h) acc[h] = 0.0f;
+            for (int j = 0; j < k; ++j) accw[j] = 0.0f;
+            for (int r = 0; r < W; ++r) {                 /* ascending destination rank */
+                const int32_t slot = slot_of[tok * W + r];
+                if (slot < 0) continue;
+                const int64_t row = (int64_t)r * rows + slot;
+                const uint16_t* src = expert_out + row * H;
+                for (int h = 0; h < H; ++h) {
+                    float v = out_fp16 ? ep_oracle_f32_from_f16(src[h]) : ep_oracle_f32_from_bf16(src[h]);
+                    acc[h] = acc[h] + v;
+                }
+                if (w_in)
+                    for (int j = 0; j < k; ++j) accw[j] = accw[j] + w_in[row * k + j];
+            }
+            uint16_t* dst = out + tok * H;
+            for (int h = 0; h < H; ++h)
+                dst[h] = out_fp16 ? ep_oracle_f16_from_f32(acc[h]) : ep_oracle_bf16_from_f32(acc[h]);
+            if (w_in && out_w)
+                for (int j = 0; j < k; ++j) out_w[tok * k + j] = accw[j];
+        }
+    }
+    free(acc);
+    free(accw);
+    return EP_ORACLE_OK;
+}

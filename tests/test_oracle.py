@@ -1,0 +1,321 @@
+"""Pins for the CPU oracle (no GPU).
+
+Each test checks the oracle against something other than itself: IEEE conversions of numpy and
+torch, brute-force enumeration on tiny inputs written directly in Python, closed forms that
+follow from the pages' definitions, and hand-worked values (tests/golden).  Passages pinned:
+MORI-EP gfx1201 PR, "How the gfx1201 kernels work" (Dispatch: one receive row per token per
+destination rank, shared hidden payload, reverse mapping; Combine: FP32 sum, BF16/FP16
+conversion, weights summed separately, routing weights not applied) and the MORI-EP guide,
+"Operator API" (output shapes, src_token_pos encoding).
+"""
+import itertools
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from combine_ep_dispatch_02_gb300 import workloads as wlmod
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------- conversions
+
+def _edge_f32():
+    v = [0.0, -0.0, 1.0, -1.0, 65504.0, 65519.99, 65520.0, 65536.0, 1e30, -1e30, 3.3895314e38,
+         3.4028235e38, np.inf, -np.inf, 2.0 ** -14, 2.0 ** -15, 2.0 ** -24, 2.0 ** -25,
+         1.5 * 2.0 ** -25, 2.0 ** -26, 2.0 ** -126, 2.0 ** -149, 1.0 + 2.0 ** -8,
+         1.0 + 3 * 2.0 ** -8, 1.0 + 2.0 ** -11, 1.0 + 3 * 2.0 ** -11, 1.0 + 2.0 ** -8 + 2.0 ** -23]
+    return np.array(v + [-a for a in v], dtype=np.float32)
+
+
+def _random_f32(n, seed):
+    rng = np.random.default_rng(seed)
+    bits = rng.integers(0, 2 ** 32, size=n, dtype=np.uint64).astype(np.uint32)
+    return bits.view(np.float32)
+
+
+def test_bf16_rne_matches_torch_cast():
+    a = np.concatenate([_edge_f32(), _random_f32(200000, 1),
+                        np.random.default_rng(2).standard_normal(100000).astype(np.float32)])
+    mine = oracle.bf16_from_f32(a)
+    ref = torch.from_numpy(a).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    nan = np.isnan(a)
+    assert np.array_equal(mine[~nan], ref[~nan])
+    assert np.all((mine[nan] & 0x7F80) == 0x7F80) and np.all((mine[nan] & 0x7F) != 0)
+
+
+def test_f16_rne_matches_numpy_cast():
+    # numpy's float32 -> float16 cast is IEEE round-to-nearest-even, subnormals included
+    a = np.concatenate([_edge_f32(), _random_f32(200000, 3),
+                        (np.random.default_rng(4).standard_normal(100000) * 1e-5).astype(np.float32),
+                        (np.random.default_rng(5).standard_normal(100000) * 3e4).astype(np.float32)])
+    mine = oracle.f16_from_f32(a)
+    with np.errstate(over="ignore"):
+        ref = a.astype(np.float16).view(np.uint16)
+    nan = np.isnan(a)
+    assert np.array_equal(mine[~nan], ref[~nan])
+    assert np.all((mine[nan] & 0x7C00) == 0x7C00) and np.all((mine[nan] & 0x3FF) != 0)
+
+
+def test_f32_from_f16_exact_all_codes():
+    h = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    mine = oracle.f32_from_f16(h)
+    ref = h.view(np.float16).astype(np.float32)
+    nan = np.isnan(ref)
+    assert np.array_equal(mine[~nan].view(np.uint32), ref[~nan].view(np.uint32))
+    assert np.all(np.isnan(mine[nan]))
+
+
+# ---------------------------------------------------------------- dispatch invariants
+
+def _brute_pairs(wl):
+    """(s, t, r) for every token and every DISTINCT valid destination rank, by enumeration."""
+    pairs = []
+    for s in range(wl.W):
+        for t in range(int(wl.n_tok[s])):
+            ranks = set()
+            for e in wl.indices[s, t]:
+                if 0 <= int(e) < wl.W * wl.E:
+                    ranks.add(int(e) // wl.E)
+            pairs += [(s, t, r) for r in sorted(ranks)]
+    return pairs
+
+
+def _check_dispatch(wl, disp):
+    W, M = wl.W, wl.M
+    rows = W * M
+    pairs = _brute_pairs(wl)
+    # counts: brute-force tally of tokens per destination rank
+    tally = np.zeros(W, dtype=np.int64)
+    for (_, _, r) in pairs:
+        tally[r] += 1
+    assert np.array_equal(disp["recv_count"], tally)
+    # every (token, destination) pair appears exactly once, found by inverting src_pos
+    got = []
+    for r in range(W):
+        for i in range(int(disp["recv_count"][r])):
+            s, t = divmod(int(disp["src_pos"][r, i]), rows)
+            got.append((s, t, r))
+            # round trip: every byte of the row is the named source token's
+            assert np.array_equal(disp["recv_x"][r, i], wl.x[s, t])
+            assert np.array_equal(disp["recv_idx"][r, i], wl.indices[s, t])
+            if wl.weights is not None:
+                assert np.array_equal(disp["recv_w"][r, i].view(np.uint32), wl.weights[s, t].view(np.uint32))
+            if wl.sd:
+                assert np.array_equal(disp["recv_scales"][r, i].view(np.uint32), wl.scales[s, t].view(np.uint32))
+            # the forward map points back at this row
+            assert disp["slot_of"][s, t, r] == i
+    assert sorted(got) == sorted(pairs)
+    assert len(set(got)) == len(got)
+    # rows are handed out in (source rank, token) order on each destination rank
+    for r in range(W):
+        n = int(disp["recv_count"][r])
+        assert np.all(np.diff(disp["src_pos"][r, :n].astype(np.int64)) > 0)
+    # slot_of is -1 exactly where the token was not sent
+    sent = {(s, t, r) for (s, t, r) in pairs}
+    for s in range(W):
+        for t in range(int(wl.n_tok[s])):
+            for r in range(W):
+                assert (disp["slot_of"][s, t, r] >= 0) == ((s, t, r) in sent)
+
+
+def _run(wl):
+    return oracle.dispatch(wl.W, wl.E, wl.k, wl.H, wl.elem_bytes, wl.sd, wl.M, wl.x, wl.weights,
+                           wl.scales, wl.indices, wl.n_tok)
+
+
+CASES = [
+    dict(W=2, E=4, k=2, H=64, M=16, n_tok=[16, 9]),
+    dict(W=3, E=2, k=4, H=32, M=8, n_tok=[0, 8, 5]),
+    dict(W=5, E=3, k=7, H=16, M=12, n_tok=[12, 1, 0, 7, 11]),
+    dict(W=1, E=6, k=3, H=40, M=10, n_tok=[10]),
+    dict(W=4, E=8, k=1, H=24, M=9, n_tok=[9, 9, 2, 4]),
+    dict(W=4, E=16, k=33, H=8, M=6, n_tok=[6, 3, 6, 1]),
+    dict(W=8, E=2, k=6, H=16, M=5, n_tok=[5, 0, 4, 5, 1, 2, 3, 5], sd=3),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"W{c['W']}E{c['E']}k{c['k']}")
+def test_dispatch_invariants(case):
+    wl = wlmod.custom_workload(dtype="bf16", seed=7, **case)
+    disp = _run(wl)
+    assert disp["status"] == 0
+    _check_dispatch(wl, disp)
+
+
+def test_dispatch_fp8_payload_and_scales():
+    wl = wlmod.make_workload("fp8", max_tok=24)
+    disp = _run(wl)
+    _check_dispatch(wl, disp)
+
+
+def test_brute_force_every_subset():
+    """W in {1,2,3}, E in {1,2}, every k-subset of the W*E experts as one token."""
+    for W in (1, 2, 3):
+        for E in (1, 2):
+            n_exp = W * E
+            for k in range(1, n_exp + 1):
+                subsets = list(itertools.combinations(range(n_exp), k))
+                M = -(-len(subsets) // W)
+                n_tok = np.zeros(W, dtype=np.int32)
+                idx = np.full((W, M, k), -1, dtype=np.int32)
+                for i, sub in enumerate(subsets):
+                    s, t = i % W, i // W
+                    idx[s, t] = sub[::-1] if i % 2 else sub
+                    n_tok[s] = max(n_tok[s], t + 1)
+                rng = np.random.default_rng(W * 100 + E * 10 + k)
+                x = torch.from_numpy(rng.standard_normal((W, M, 8)).astype(np.float32)) \
+                    .to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+                wl = wlmod.Workload("brute", W, E, k, 8, "bf16", 0, M, n_tok, x, idx, None, None,
+                                    "identity")
+                disp = _run(wl)
+                _check_dispatch(wl, disp)
+                # combine with the identity expert: |D| * x, exactly representable before rounding
+                out, _ = oracle.combine(W, k, 8, False, M, n_tok, disp["slot_of"], disp["recv_x"])
+                for i, sub in enumerate(subsets):
+                    s, t = i % W, i // W
+                    nd = len({e // E for e in sub})
+                    xf = (x[s, t].astype(np.uint32) << 16).view(np.float32)
+                    exp = torch.from_numpy(xf * np.float32(nd)).to(torch.bfloat16).view(torch.int16) \
+                        .numpy().view(np.uint16)
+                    assert np.array_equal(out[s, t], exp), (W, E, k, sub)
+
+
+def test_invalid_expert_ids_route_nowhere():
+    wl = wlmod.custom_workload(W=3, E=2, k=3, H=16, M=4, n_tok=[4, 4, 4], seed=3)
+    wl.indices[0, 1, 0] = -5
+    wl.indices[2, 3, 2] = 6          # == W*E: out of range
+    disp = _run(wl)
+    assert disp["status"] == oracle.ERR_INDEX
+    _check_dispatch(wl, disp)        # brute force skips the same ids
+
+
+def test_capacity_rejected():
+    wl = wlmod.custom_workload(W=2, E=2, k=2, H=8, M=4, n_tok=[4, 4], seed=1)
+    with pytest.raises(ValueError):
+        oracle.dispatch(2, 2, 2, 8, 2, 0, 4, wl.x, wl.weights, None, wl.indices,
+                        np.array([5, 0], dtype=np.int32))
+
+
+# ---------------------------------------------------------------- combine
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_identity_combine_closed_form(dtype):
+    """Identity expert: out = RNE(|D(s,t)| * x).  x has 8 (BF16) or 11 (FP16) significant bits,
+    so every partial sum j*x is exact in FP32 and the FP32 sum equals |D| * x before rounding."""
+    wl = wlmod.custom_workload(W=8, E=4, k=8, H=96, M=40, n_tok=[40, 17, 0, 40, 3, 40, 25, 1],
+                               dtype=dtype, seed=11)
+    disp = _run(wl)
+    out, out_w = oracle.combine(wl.W, wl.k, wl.H, dtype == "fp16", wl.M, wl.n_tok, disp["slot_of"],
+                                disp["recv_x"], disp["recv_w"])
+    for s in range(wl.W):
+        for t in range(int(wl.n_tok[s])):
+            nd = len({int(e) // wl.E for e in wl.indices[s, t]})
+            if dtype == "bf16":
+                xf = (wl.x[s, t].astype(np.uint32) << 16).view(np.float32)
+                exp = torch.from_numpy(xf * np.float32(nd)).to(torch.bfloat16).view(torch.int16).numpy()
+            else:
+                xf = wl.x[s, t].view(np.float16).astype(np.float32)
+                exp = (xf * np.float32(nd)).astype(np.float16).view(np.int16)
+            assert np.array_equal(out[s, t].view(np.int16), exp)
+    # rows past n_tok stay untouched (zero)
+    assert not out[2].any() and not out[7, 1:].any()
+
+
+def test_combine_order_golden():
+    rows = []
+    for line in open(os.path.join(GOLDEN, "combine_order.txt")):
+        if line.strip() and not line.startswith("#"):
+            rows.append([int(v, 16) for v in line.split()])
+    W, H, M = 4, 24, 1
+    for vals in rows:
+        slot_of = np.zeros((W, M, W), dtype=np.int32)       # the token's row is slot 0 on every rank
+        eo = np.zeros((W, W * M, H), dtype=np.uint16)
+        for r in range(W):
+            eo[r, 0, :] = vals[r]
+        out, _ = oracle.combine(W, 4, H, False, M, np.array([1, 0, 0, 0], np.int32), slot_of, eo)
+        assert np.all(out[0, 0] == vals[4]), [hex(v) for v in vals]
+
+
+def test_combine_weights_dyadic_closed_form():
+    """Weights with few significant bits add exactly: out_w[s,t,j] = |D| * w[s,t,j]."""
+    wl = wlmod.custom_workload(W=4, E=8, k=6, H=16, M=20, n_tok=[20, 20, 7, 13], seed=5)
+    rng = np.random.default_rng(9)
+    wl.weights[:] = rng.integers(-64, 64, size=wl.weights.shape).astype(np.float32) / np.float32(256)
+    disp = _run(wl)
+    _, out_w = oracle.combine(wl.W, wl.k, wl.H, False, wl.M, wl.n_tok, disp["slot_of"],
+                              disp["recv_x"], disp["recv_w"])
+    for s in range(wl.W):
+        for t in range(int(wl.n_tok[s])):
+            nd = len({int(e) // wl.E for e in wl.indices[s, t]})
+            assert np.array_equal(out_w[s, t], wl.weights[s, t] * np.float32(nd))
+
+
+def test_single_destination_returns_expert_row():
+    """k = 1, or all of a token's experts on one rank: |D| = 1, so combine returns the expert
+    row unchanged (0.0f + v is exact, except that -0 becomes +0)."""
+    for k, E in ((1, 8), (4, 16)):
+        W, M, H = 4, 16, 40
+        wl = wlmod.custom_workload(W=W, E=E, k=k, H=H, M=M, n_tok=[16, 5, 16, 9], seed=k)
+        if k > 1:    # force every token's experts into one rank
+            for s in range(W):
+                for t in range(int(wl.n_tok[s])):
+                    r = (s + t) % W
+                    wl.indices[s, t] = r * E + np.arange(k)
+        disp = _run(wl)
+        rng = np.random.default_rng(1)
+        eo = torch.from_numpy(rng.standard_normal((W, W * M, H)).astype(np.float32)) \
+            .to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        out, _ = oracle.combine(W, k, H, False, M, wl.n_tok, disp["slot_of"], eo)
+        for s in range(W):
+            for t in range(int(wl.n_tok[s])):
+                r = int(wl.indices[s, t, 0]) // E
+                exp = eo[r, disp["slot_of"][s, t, r]].copy()
+                exp[exp == 0x8000] = 0
+                assert np.array_equal(out[s, t], exp)
+
+
+def test_single_rank_is_a_permuted_copy():
+    """W = 1: every token has exactly one row, in order; identity combine returns x."""
+    wl = wlmod.custom_workload(W=1, E=8, k=3, H=64, M=50, n_tok=[37], seed=2)
+    disp = _run(wl)
+    assert disp["recv_count"][0] == 37
+    assert np.array_equal(disp["recv_x"][0, :37], wl.x[0, :37])
+    assert np.array_equal(disp["src_pos"][0, :37], np.arange(37))
+    out, _ = oracle.combine(1, 3, 64, False, 50, wl.n_tok, disp["slot_of"], disp["recv_x"])
+    assert np.array_equal(out[0, :37], wl.x[0, :37])
+
+
+def test_scalar_expert_pipeline_close_to_dense_formula():
+    """Sanity (not a parity criterion): with the per-expert scalar expert, the combined output is
+    sum_j w_j c_j x within a few BF16 ulps."""
+    import harness
+    wl = wlmod.make_workload("small", max_tok=12)
+    disp, eo, out, _ = oracle.run_workload(wl, harness.expert_np)
+    c = wl.expert_scale
+    for s in range(wl.W):
+        for t in range(int(wl.n_tok[s])):
+            xf = (wl.x[s, t].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+            coef = sum(float(wl.weights[s, t, j]) * float(c[wl.indices[s, t, j]]) for j in range(wl.k))
+            got = (out[s, t].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+            err = np.abs(got - coef * xf)
+            assert np.all(err <= 2.0 ** -6 * np.abs(coef * xf) + 1e-30)
+
+
+def test_workload_generator_is_seeded():
+    a = wlmod.make_workload("tiny")
+    b = wlmod.make_workload("tiny")
+    assert np.array_equal(a.x, b.x) and np.array_equal(a.indices, b.indices)
+    assert np.array_equal(a.weights.view(np.uint32), b.weights.view(np.uint32))
+    c = wlmod.make_workload("tiny", seed=1)
+    assert not np.array_equal(a.x, c.x)
+    # routing draws k distinct experts per token
+    for name, kk in (("tiny", None), ("topk", 33), ("fp8", None)):
+        wl = wlmod.make_workload(name, k=kk, max_tok=32)
+        for s in range(wl.W):
+            for t in range(int(wl.n_tok[s])):
+                row = wl.indices[s, t]
+                assert len(set(row.tolist())) == wl.k and row.min() >= 0 and row.max() < wl.W * wl.E
