@@ -1,0 +1,415 @@
+#!/usr/bin/env python3
+"""Benchmark: MoE expert-parallel Dispatch + Combine on one GB300 (W logical ranks in HBM).
+
+Workload (DeepSeek-V3 shape): W=8 logical ranks, 32 experts per rank (256), top-8, hidden 7168
+BF16, 4096 tokens per rank, Zipf(1.2) expert popularity, FP32 softmax weights, identity expert
+(combine reads the dispatch's receive rows in place).  A step = one dispatch (routing kernel +
+payload scatter kernel) and one combine over the whole batch, inputs resident in HBM.
+
+Prints one JSON line.  ``value`` is the effective HBM bandwidth of the dispatch+combine pair:
+minimal (algorithmic) bytes of both phases / measured time per step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU (the path does not
+shard across GPUs); timing is the max over ranks.  ``--impl reference`` times the CPU oracle on
+the host cores instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from combine_ep_dispatch_02_gb300 import workloads as wlmod  # noqa: E402
+
+METRIC = "dispatch+combine µs/call & effective HBM GB/s (% of GB300 peak), 1 GPU"
+WORKLOAD = "dsv3"
+WORKLOAD_DESC = ("W=8 logical EP ranks, 32 experts/rank (256), top-8, hidden 7168 BF16, "
+                 "4096 tokens/rank, Zipf(s=1.2) routing, FP32 softmax weights, identity expert")
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 2 ** 20
+CLOCK_QUERY = ("index,timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+# ----------------------------------------------------------------------------- bytes model
+
+def phase_bytes(wl, P: int) -> dict:
+    """Minimal bytes each phase must move (the method's algorithmic traffic).
+
+    dispatch = N*(H*b + 8k + 4sd)   read x, index, weight and scale rows once
+             + P*(H*b + 8k + 4sd + 4) write every (token, destination) row and its reverse-map entry
+    combine  = P*(2H + 4k)           read every expert-output row and weight row
+             + N*(2H + 4k)           write the combined row and weights
+             + N*4*min(W,k)          read the forward map
+    Per kernel: route = N*4k + P*4; scatter = N*(H*b + 8k + 4sd) + P*(H*b + 8k + 4sd).
+    """
+    N, H, b, k, sd, F = wl.N, wl.H, wl.elem_bytes, wl.k, wl.sd, min(wl.W, wl.k)
+    wk = 8 * k if wl.weights is not None else 4 * k
+    d = N * (H * b + wk + 4 * sd) + P * (H * b + wk + 4 * sd + 4)
+    cw = 4 * k if wl.weights is not None else 0
+    c = P * (2 * H + cw) + N * (2 * H + cw) + N * 4 * F
+    return {"dispatch": d, "combine": c, "pair": d + c,
+            "route": N * 4 * k + P * 4,
+            "scatter": N * (H * b + wk + 4 * sd) + P * (H * b + wk + 4 * sd)}
+
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current
+    source of the kernel's file (a sha256 recorded beside the figure)."""
+    src = {"scatter": "ep_scatter.cu", "combine": "ep_combine.cu", "route": "ep_route.cu"}[kernel]
+    path = os.path.join(ROOT, "profiles", f"ncu_{kernel}_dsv3.md")
+    try:
+        text = open(path).read()
+        cur = hashlib.sha256(open(os.path.join(ROOT, "combine_ep_dispatch_02_gb300", "csrc", src),
+                                  "rb").read()).hexdigest()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*(\d+)\s+source_sha256:\s*([0-9a-f]{64})", text)
+    if not m or m.group(2) != cur:
+        return None
+    return int(m.group(1))
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={CLOCK_QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.5)
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self, t0: float, t1: float):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, mx, reasons, n = [], None, set(), 0
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(f[1].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+            except ValueError:
+                continue
+            if ts < int(t0) or ts > t1 + 1:
+                continue
+            n += 1
+            try:
+                sm.append(float(f[2]))
+                mx = float(f[3])
+            except ValueError:
+                pass
+            for name, v in zip(names, f[6:10]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": n}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_ours(args, rank, world, dist):
+    import combine_ep_dispatch_02_gb300 as ep
+    from combine_ep_dispatch_02_gb300 import build
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    build.build()
+    wl = wlmod.make_workload(WORKLOAD)
+    plan = ep.Plan(wl.W, wl.E, wl.k, wl.H, wl.dtype, wl.sd, wl.M, device=dev)
+    x = torch.from_numpy(wl.x.view(np.int16)).to(dev)
+    idx = torch.from_numpy(wl.indices).to(dev)
+    w = torch.from_numpy(wl.weights).to(dev)
+    out = torch.empty((wl.W, wl.M, wl.H), dtype=torch.bfloat16, device=dev)
+    out_w = torch.empty((wl.W, wl.M, wl.k), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        d = plan.dispatch_route(idx, wl.n_tok, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        plan.dispatch_scatter(x, w, None, idx, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+        plan.combine(d.recv_x, d.recv_w, d.epoch, out=out, out_w=out_w, stream=stream)
+        if ev is not None:
+            ev[3].record(stream)
+        return d
+
+    for _ in range(max(3, args.warmup)):
+        d = step()
+    torch.cuda.synchronize(dev)
+    if plan.status() != 0:
+        raise RuntimeError("device status after warm-up: %d" % plan.status())
+    P = int(d.recv_count.sum().item())
+    nbytes = phase_bytes(wl, P)
+
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    for i in range(args.steps):
+        step(evs[i])
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    if dist is not None:
+        dist.barrier()
+    # keep the GPU busy with the same steps for a second if the timed region was too short to
+    # sample clocks during it
+    t_extra = t1
+    while t_extra - t0 < 1.2:
+        for _ in range(20):
+            step()
+        torch.cuda.synchronize(dev)
+        t_extra = time.time()
+    sampler.stop()
+
+    route = [e[0].elapsed_time(e[1]) for e in evs]
+    scat = [e[1].elapsed_time(e[2]) for e in evs]
+    comb = [e[2].elapsed_time(e[3]) for e in evs]
+    total_ms = evs[0][0].elapsed_time(evs[-1][3])
+    if dist is not None:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / args.steps
+    avg = lambda v: sum(v) / len(v)  # noqa: E731
+    k_ms = {"route": avg(route), "scatter": avg(scat), "combine": avg(comb)}
+    disp_ms = k_ms["route"] + k_ms["scatter"]
+    peak, peak_src = hbm_peak()
+    gbs = lambda b, ms: b / (ms * 1e-3) / 1e9  # noqa: E731
+    dom = "scatter" if k_ms["scatter"] >= k_ms["combine"] else "combine"
+    achieved = gbs(nbytes[dom], k_ms[dom])
+
+    # end to end through the public API: pinned host inputs in, results back to pinned host
+    e2e = measure_e2e(plan, wl, dev, stream, nbytes["pair"], steps=max(3, min(args.steps, 20)))
+    if plan.status() != 0:
+        raise RuntimeError("device status after timing: %d" % plan.status())
+
+    result = None
+    if rank == 0:
+        cpu = cpu_baseline(wl, out) if world == 1 else None
+        result = {
+            "metric": METRIC,
+            "value": round(world * gbs(nbytes["pair"], ms_step), 2),
+            "unit": "GB/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": max(3, args.warmup),
+            "ms_per_step": round(ms_step, 5),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD_DESC, "tokens": wl.N, "token_dest_pairs": P,
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": "inputs larger than L2 (x 470 MB read, 2.5 GB of receive rows "
+                             "written then read per step vs 129 MB L2); no flush",
+                       "variant": "auto"},
+            "pair_us": round(ms_step * 1e3, 2),
+            "dispatch_us": round(disp_ms * 1e3, 2),
+            "combine_us": round(k_ms["combine"] * 1e3, 2),
+            "kernel_us": {k: round(v * 1e3, 2) for k, v in k_ms.items()},
+            "dispatch_gbs": round(gbs(nbytes["dispatch"], disp_ms), 1),
+            "combine_gbs": round(gbs(nbytes["combine"], k_ms["combine"]), 1),
+            "dispatch_frac": round(gbs(nbytes["dispatch"], disp_ms) / peak, 4),
+            "combine_frac": round(gbs(nbytes["combine"], k_ms["combine"]) / peak, 4),
+            "algorithmic_bytes": nbytes,
+            "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
+                         "peak": peak, "peak_source": f"hbm_gbs of {peak_src}", "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": recorded_traffic(dom)},
+            "clocks": sampler.summary(t0, t_extra),
+            "e2e": e2e,
+            "gpu_launches": 3 * args.steps,
+            "cpu_baseline": cpu,
+        }
+    plan.close()
+    return result
+
+
+def measure_e2e(plan, wl, dev, stream, pair_bytes, steps):
+    """Same metric through the public API with host buffers: every step copies the inputs from
+    pinned host memory, dispatches, combines and copies the outputs back to pinned host memory."""
+    hx = torch.from_numpy(wl.x.view(np.int16)).pin_memory()
+    hidx = torch.from_numpy(wl.indices).pin_memory()
+    hw = torch.from_numpy(wl.weights).pin_memory()
+    dx = torch.empty_like(hx, device=dev)
+    didx = torch.empty_like(hidx, device=dev)
+    dw = torch.empty_like(hw, device=dev)
+    out = torch.empty((wl.W, wl.M, wl.H), dtype=torch.bfloat16, device=dev)
+    out_w = torch.empty((wl.W, wl.M, wl.k), dtype=torch.float32, device=dev)
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    hout_w = torch.empty(out_w.shape, dtype=out_w.dtype).pin_memory()
+
+    def one():
+        dx.copy_(hx, non_blocking=True)
+        didx.copy_(hidx, non_blocking=True)
+        dw.copy_(hw, non_blocking=True)
+        d = plan.dispatch(dx, dw, None, didx, wl.n_tok, stream=stream)
+        plan.combine(d.recv_x, d.recv_w, d.epoch, out=out, out_w=out_w, stream=stream)
+        hout.copy_(out, non_blocking=True)
+        hout_w.copy_(out_w, non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        one()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b) / steps
+    return {"value": round(pair_bytes / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": hx.nbytes + hidx.nbytes + hw.nbytes,
+            "d2h_bytes_per_step": hout.nbytes + hout_w.nbytes}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+SAMPLE_TOKENS = 1024  # tokens per rank of the CPU sample (same routing, first tokens of each rank)
+
+
+def _sample(wl, tokens):
+    n_tok = np.minimum(wl.n_tok, tokens).astype(np.int32)
+    return wlmod.Workload(**{**wl.__dict__, "n_tok": n_tok})
+
+
+def _time_oracle(sub, repeats=1):
+    import oracle
+    oracle.build()
+    best = None
+    res = None
+    for _ in range(repeats):
+        t = time.perf_counter()
+        res = oracle.run_workload(sub)
+        dt = time.perf_counter() - t
+        best = dt if best is None else min(best, dt)
+    disp = res[0]
+    return best, int(disp["recv_count"].sum()), res
+
+
+def cpu_baseline(wl, gpu_out=None):
+    sub = _sample(wl, SAMPLE_TOKENS)
+    dt, P, res = _time_oracle(sub, repeats=3)
+    nb = phase_bytes(sub, P)
+    info = {"value": round(nb["pair"] / dt / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {SAMPLE_TOKENS} tokens of each of the 8 ranks ({sub.N} tokens, "
+                      f"{P} token-destination pairs), dispatch+combine, best of 3, single-threaded C",
+            "seconds": round(dt, 3), "host_cores": os.cpu_count()}
+    if gpu_out is not None:
+        # the oracle's combined rows of the sampled tokens must equal the GPU's bit for bit
+        o_out = res[2]
+        g = gpu_out.view(torch.int16).cpu().numpy().view(np.uint16)
+        ok = all(np.array_equal(g[s, :n], o_out[s, :n]) for s, n in enumerate(sub.n_tok))
+        info["parity_sampled_tokens"] = "bit-exact" if ok else "MISMATCH"
+    return info
+
+
+def run_reference(args):
+    wl = wlmod.make_workload(WORKLOAD)
+    sub = _sample(wl, SAMPLE_TOKENS)
+    for _ in range(max(3, args.warmup)):
+        _time_oracle(sub)
+    times, P = [], 0
+    for _ in range(args.steps):
+        dt, P, _ = _time_oracle(sub)
+        times.append(dt)
+    nb = phase_bytes(sub, P)
+    ms = 1e3 * sum(times) / len(times)
+    v = round(nb["pair"] / (ms * 1e-3) / 1e9, 3)
+    sample = (f"first {SAMPLE_TOKENS} tokens of each of the 8 ranks ({sub.N} tokens, {P} pairs) "
+              "per step, single-threaded C oracle")
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": round(ms, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD_DESC, "tokens": sub.N, "token_dest_pairs": P,
+                       "parallelism": "host cores, 1 thread"},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+# ----------------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    dist = None
+    if world > 1:
+        import torch.distributed as dist  # noqa: F811
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group("nccl")
+    res = run_ours(args, rank, world, dist)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

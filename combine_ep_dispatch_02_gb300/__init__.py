@@ -1,0 +1,236 @@
+"""GB300-native MoE expert-parallel Dispatch / Combine.
+
+A thin Python binding over ``libep.so`` (C ABI in ``include/ep.h``).  Every step of dispatch and
+combine runs in the library's CUDA kernels; this module only marshals arguments.  PyTorch
+supplies device memory, the current stream and zero-copy tensor views of the plan's buffers.
+If ``libep.so`` is missing the binding raises; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libep.so")
+
+EP_BF16, EP_FP16, EP_FP8_E4M3 = 0, 1, 2
+DTYPE_CODES = {"bf16": EP_BF16, "fp16": EP_FP16, "fp8": EP_FP8_E4M3}
+EP_OK, EP_ERR_ARG, EP_ERR_ALLOC, EP_ERR_CUDA, EP_ERR_STATE = 0, -1, -2, -3, -4
+EP_ERR_CAPACITY, EP_ERR_INDEX, EP_ERR_DEVICE_TIMEOUT = -5, -6, -7
+VARIANTS = {"auto": 0, "whole_row": 1, "tiled_512": 2, "tiled_1024": 3}
+
+# every entry point include/ep.h declares
+EXPORTS = ("ep_plan_create", "ep_plan_destroy", "ep_plan_set_variant", "ep_plan_device_bytes",
+           "ep_dispatch", "ep_dispatch_route", "ep_dispatch_scatter", "ep_combine", "ep_reset",
+           "ep_status", "ep_strerror", "ep_last_error")
+
+
+class EpError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"[{code}] {msg}")
+        self.code = code
+
+
+class DispatchOut(ctypes.Structure):
+    _fields_ = [("recv_x", ctypes.c_void_p), ("recv_idx", ctypes.c_void_p),
+                ("recv_w", ctypes.c_void_p), ("recv_scales", ctypes.c_void_p),
+                ("recv_count", ctypes.c_void_p), ("src_token_pos", ctypes.c_void_p),
+                ("rows_per_rank", ctypes.c_int64), ("epoch", ctypes.c_uint64)]
+
+
+_lib = None
+
+
+def load_library(path: Optional[str] = None):
+    """Load libep.so (built by ``build.build()``); raises if it is absent."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"libep.so not found at {p}: build it with "
+                           "combine_ep_dispatch_02_gb300.build.build()")
+    lib = ctypes.CDLL(p)
+    V, I, U64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64, ctypes.c_size_t
+    sig = {
+        "ep_plan_create": (I, [ctypes.POINTER(V), I, I, I, I, I, I, I]),
+        "ep_plan_destroy": (I, [V]),
+        "ep_plan_set_variant": (I, [V, I]),
+        "ep_plan_device_bytes": (SZ, [I, I, I, I, I, I, I]),
+        "ep_dispatch": (I, [V, V, V, V, V, V, V, ctypes.POINTER(DispatchOut)]),
+        "ep_dispatch_route": (I, [V, V, V, V, ctypes.POINTER(DispatchOut)]),
+        "ep_dispatch_scatter": (I, [V, V, V, V, V, V]),
+        "ep_combine": (I, [V, V, V, V, V, U64, V]),
+        "ep_reset": (I, [V, V]),
+        "ep_status": (I, [V, ctypes.POINTER(I)]),
+        "ep_strerror": (ctypes.c_char_p, [I]),
+        "ep_last_error": (ctypes.c_char_p, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype, fn.argtypes = res, args
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _check(rc: int):
+    if rc != EP_OK:
+        lib = load_library()
+        raise EpError(rc, f"{lib.ep_strerror(rc).decode()}: {lib.ep_last_error().decode()}")
+
+
+def plan_device_bytes(W, experts_per_rank, topk, hidden, dtype, scale_dim, max_tok_per_rank) -> int:
+    code = DTYPE_CODES[dtype] if isinstance(dtype, str) else dtype
+    return load_library().ep_plan_device_bytes(W, experts_per_rank, topk, hidden, code, scale_dim,
+                                               max_tok_per_rank)
+
+
+class _DevPtr:
+    """Zero-copy __cuda_array_interface__ view of plan-owned device memory."""
+
+    def __init__(self, ptr: int, shape, typestr: str):
+        self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": typestr,
+                                         "data": (ptr, False), "version": 2, "strides": None}
+
+
+def _view(ptr, shape, typestr, device):
+    if not ptr:
+        return None
+    return torch.as_tensor(_DevPtr(ptr, shape, typestr), device=device)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError("arguments must be contiguous CUDA tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+@dataclasses.dataclass
+class Dispatched:
+    """Views of the plan's receive buffers after one dispatch (valid until the next dispatch or
+    reset of the plan; the plan must outlive them)."""
+    recv_x: torch.Tensor          # [W][W*M][H] payload dtype
+    recv_idx: torch.Tensor        # [W][W*M][k] int32
+    recv_w: Optional[torch.Tensor]       # [W][W*M][k] float32
+    recv_scales: Optional[torch.Tensor]  # [W][W*M][sd] float32
+    recv_count: torch.Tensor      # [W] int32
+    src_token_pos: torch.Tensor   # [W][W*M] int32
+    epoch: int
+
+
+class Plan:
+    """One expert-parallel Dispatch/Combine problem shape; owns the receive buffers.
+
+    ``Plan(W, experts_per_rank, topk, hidden, dtype, scale_dim, max_tok_per_rank)`` maps to
+    ``ep_plan_create``; dtype is "bf16", "fp16" or "fp8" (e4m3)."""
+
+    def __init__(self, W: int, experts_per_rank: int, topk: int, hidden: int, dtype: str = "bf16",
+                 scale_dim: int = 0, max_tok_per_rank: int = 1, device=None):
+        self._lib = load_library()
+        self.W, self.E, self.k, self.H = W, experts_per_rank, topk, hidden
+        self.dtype, self.sd, self.M = dtype, scale_dim, max_tok_per_rank
+        self.device = torch.device("cuda", torch.cuda.current_device() if device is None
+                                   else torch.device(device).index or 0)
+        self._h = ctypes.c_void_p()
+        with torch.cuda.device(self.device):
+            _check(self._lib.ep_plan_create(ctypes.byref(self._h), W, experts_per_rank, topk, hidden,
+                                            DTYPE_CODES[dtype], scale_dim, max_tok_per_rank))
+        self.rows = W * max_tok_per_rank
+        self.payload_torch_dtype = {"bf16": torch.bfloat16, "fp16": torch.float16,
+                                    "fp8": torch.float8_e4m3fn}[dtype]
+        self.combine_torch_dtype = torch.float16 if dtype == "fp16" else torch.bfloat16
+
+    # -- lifetime
+    def close(self):
+        if getattr(self, "_h", None) and self._h.value:
+            _check(self._lib.ep_plan_destroy(self._h))
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def set_variant(self, variant: str):
+        _check(self._lib.ep_plan_set_variant(self._h, VARIANTS[variant]))
+
+    # -- calls
+    def _n_tok(self, n_tok: Sequence[int]):
+        arr = np.ascontiguousarray(np.asarray(n_tok, dtype=np.int32).reshape(self.W))
+        return arr, arr.ctypes.data_as(ctypes.c_void_p)
+
+    def _wrap(self, o: DispatchOut) -> Dispatched:
+        W, R, k, H, sd, dev = self.W, self.rows, self.k, self.H, self.sd, self.device
+        if self.dtype == "fp8":
+            rx = _view(o.recv_x, (W, R, H), "|u1", dev).view(torch.float8_e4m3fn)
+        else:
+            rx = _view(o.recv_x, (W, R, H), "<i2", dev).view(self.payload_torch_dtype)
+        return Dispatched(recv_x=rx, recv_idx=_view(o.recv_idx, (W, R, k), "<i4", dev),
+                          recv_w=_view(o.recv_w, (W, R, k), "<f4", dev),
+                          recv_scales=_view(o.recv_scales, (W, R, sd), "<f4", dev) if sd else None,
+                          recv_count=_view(o.recv_count, (W,), "<i4", dev),
+                          src_token_pos=_view(o.src_token_pos, (W, R), "<i4", dev),
+                          epoch=int(o.epoch))
+
+    def dispatch(self, x: torch.Tensor, weights: Optional[torch.Tensor], scales: Optional[torch.Tensor],
+                 indices: torch.Tensor, n_tok: Sequence[int], stream=None) -> Dispatched:
+        """x [W][M][H], weights [W][M][k] fp32 or None, scales [W][M][sd] fp32 or None,
+        indices [W][M][k] int32, n_tok: W host ints."""
+        arr, nt = self._n_tok(n_tok)
+        o = DispatchOut()
+        _check(self._lib.ep_dispatch(self._h, _ptr(x), _ptr(weights), _ptr(scales), _ptr(indices),
+                                     nt, _stream(stream), ctypes.byref(o)))
+        return self._wrap(o)
+
+    def dispatch_route(self, indices: torch.Tensor, n_tok: Sequence[int], stream=None) -> Dispatched:
+        arr, nt = self._n_tok(n_tok)
+        o = DispatchOut()
+        _check(self._lib.ep_dispatch_route(self._h, _ptr(indices), nt, _stream(stream), ctypes.byref(o)))
+        return self._wrap(o)
+
+    def dispatch_scatter(self, x, weights, scales, indices, stream=None):
+        _check(self._lib.ep_dispatch_scatter(self._h, _ptr(x), _ptr(weights), _ptr(scales),
+                                             _ptr(indices), _stream(stream)))
+
+    def combine(self, expert_out: torch.Tensor, weights: Optional[torch.Tensor], epoch: int,
+                out: Optional[torch.Tensor] = None, out_w: Optional[torch.Tensor] = None,
+                want_weights: bool = True, stream=None):
+        """expert_out [W][W*M][H] (BF16, or FP16 for FP16 plans); returns (out [W][M][H],
+        out_w [W][M][k] or None)."""
+        if out is None:
+            out = torch.zeros((self.W, self.M, self.H), dtype=self.combine_torch_dtype,
+                              device=self.device)
+        if out_w is None and weights is not None and want_weights:
+            out_w = torch.zeros((self.W, self.M, self.k), dtype=torch.float32, device=self.device)
+        _check(self._lib.ep_combine(self._h, _ptr(expert_out), _ptr(weights), _ptr(out), _ptr(out_w),
+                                    ctypes.c_uint64(epoch), _stream(stream)))
+        return out, out_w
+
+    def reset(self, stream=None):
+        _check(self._lib.ep_reset(self._h, _stream(stream)))
+
+    def status(self) -> int:
+        v = ctypes.c_int(0)
+        _check(self._lib.ep_status(self._h, ctypes.byref(v)))
+        return v.value

@@ -1,0 +1,418 @@
+// ep_api.cu -- the C ABI declared in include/ep.h: plan lifetime, host-side validation, kernel
+// launches.  Every condition the host can check fails here with a code and a message, before
+// any launch (the pages' staging refactor likewise validates on the host and reports a
+// RuntimeError naming the argument rather than risking a device fault).
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+#include "ep_common.cuh"
+
+using namespace ep;
+
+struct ep_plan {
+    int W, E, k, H, dtype, sd, M, F, elem_bytes, tiles;
+    int64_t rows;        // W*M receive rows per rank
+    int64_t row_bytes;   // H * element size
+    int device, num_sms, variant;
+
+    void* base;
+    size_t bytes;
+    uint8_t* recv_x;
+    int32_t* recv_idx;
+    float* recv_w;
+    float* recv_scales;
+    int32_t* src_pos;
+    int32_t* fwd;
+    int32_t* recv_count;
+    unsigned long long* flags;
+    unsigned long long* ticket;
+    int* status;
+
+    // host state of the live dispatch
+    uint64_t epoch;
+    bool routed, live, has_w;
+    const int32_t* routed_idx;
+    int N;
+    int tok_off[kMaxRanks + 1];
+};
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what)
+{
+    return fail(EP_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+struct Layout {
+    size_t recv_x, recv_idx, recv_w, recv_scales, src_pos, fwd, recv_count, flags, ticket, status,
+        total;
+};
+
+int elem_bytes_of(int dtype)
+{
+    switch (dtype) {
+    case EP_BF16:
+    case EP_FP16: return 2;
+    case EP_FP8_E4M3: return 1;
+    default: return 0;
+    }
+}
+
+int check_shape(int W, int E, int k, int H, int dtype, int sd, int M)
+{
+    if (W < 1 || W > kMaxRanks) return fail(EP_ERR_ARG, "W=%d outside 1..%d", W, kMaxRanks);
+    if (E < 1) return fail(EP_ERR_ARG, "experts_per_rank=%d < 1", E);
+    if ((int64_t)W * E >= (int64_t)1 << 31) return fail(EP_ERR_ARG, "W*experts_per_rank >= 2^31");
+    if (k < 1 || k > kMaxTopk) return fail(EP_ERR_ARG, "topk=%d outside 1..%d", k, kMaxTopk);
+    const int eb = elem_bytes_of(dtype);
+    if (eb == 0) return fail(EP_ERR_ARG, "dtype=%d is not an ep_dtype", dtype);
+    if (H < 1 || ((int64_t)H * eb) % 16 != 0)
+        return fail(EP_ERR_ARG, "hidden=%d: hidden * %d bytes must be a positive multiple of 16", H, eb);
+    if ((int64_t)H * eb >= (int64_t)1 << 31) return fail(EP_ERR_ARG, "hidden=%d too large", H);
+    if (sd < 0 || sd > 65536) return fail(EP_ERR_ARG, "scale_dim=%d outside 0..65536", sd);
+    if (M < 1) return fail(EP_ERR_ARG, "max_tok_per_rank=%d < 1", M);
+    if ((int64_t)W * W * M >= (int64_t)1 << 31)
+        return fail(EP_ERR_ARG, "W*W*max_tok_per_rank >= 2^31 overflows the int32 src_token_pos");
+    return EP_OK;
+}
+
+Layout layout_of(int W, int k, int H, int dtype, int sd, int M)
+{
+    Layout L{};
+    const size_t rows = (size_t)W * M;
+    const int F = W < k ? W : k;
+    const int tiles = (int)((rows + kRouteTile - 1) / kRouteTile);
+    size_t o = 0;
+    auto put = [&](size_t& field, size_t bytes) {
+        field = o;
+        o += align256(bytes);
+    };
+    put(L.recv_x, (size_t)W * rows * H * elem_bytes_of(dtype));
+    put(L.recv_idx, (size_t)W * rows * k * 4);
+    put(L.recv_w, (size_t)W * rows * k * 4);
+    put(L.recv_scales, (size_t)W * rows * sd * 4);
+    put(L.src_pos, (size_t)W * rows * 4);
+    put(L.fwd, rows * F * 4);
+    put(L.recv_count, (size_t)W * 4);
+    put(L.flags, (size_t)tiles * W * 8);
+    put(L.ticket, 8);
+    put(L.status, 4);
+    L.total = o;
+    return L;
+}
+
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = true;
+    explicit DeviceGuard(int dev)
+    {
+        if (cudaGetDevice(&prev) != cudaSuccess) { ok = false; return; }
+        if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
+    }
+    ~DeviceGuard()
+    {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+int pick_chunk_elems(const ep_plan* p, int N)
+{
+    switch (p->variant) {
+    case EP_VARIANT_WHOLE_ROW: return p->H;
+    case EP_VARIANT_TILED_512: return p->H < 512 ? p->H : 512;
+    case EP_VARIANT_TILED_1024: return p->H < 1024 ? p->H : 1024;
+    default: break;
+    }
+    // Whole rows once there are enough tokens to give every resident warp a few rows;
+    // otherwise split rows so small calls still spread over all SMs (the pages use 512- or
+    // 1024-element tiles up to 256 tokens per source rank).
+    const int64_t warps = (int64_t)p->num_sms * 32;
+    if (N >= warps || p->H <= 1024) return p->H;
+    if ((int64_t)N * ((p->H + 1023) / 1024) >= warps) return 1024;
+    return 512;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ep_last_error(void) { return g_err; }
+
+const char* ep_strerror(int code)
+{
+    switch (code) {
+    case EP_OK: return "ok";
+    case EP_ERR_ARG: return "invalid argument";
+    case EP_ERR_ALLOC: return "device allocation failed";
+    case EP_ERR_CUDA: return "CUDA error";
+    case EP_ERR_STATE: return "no live dispatch for this epoch";
+    case EP_ERR_CAPACITY: return "token count exceeds max_tok_per_rank";
+    case EP_ERR_INDEX: return "expert id out of range (skipped on the device)";
+    case EP_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+    }
+}
+
+size_t ep_plan_device_bytes(int W, int E, int k, int H, int dtype, int sd, int M)
+{
+    char saved[sizeof g_err];
+    memcpy(saved, g_err, sizeof g_err);
+    const int rc = check_shape(W, E, k, H, dtype, sd, M);
+    memcpy(g_err, saved, sizeof g_err);
+    if (rc != EP_OK) return 0;
+    return layout_of(W, k, H, dtype, sd, M).total;
+}
+
+int ep_plan_create(ep_plan** out, int W, int E, int k, int H, int dtype, int sd, int M)
+{
+    if (!out) return fail(EP_ERR_ARG, "out is NULL");
+    *out = nullptr;
+    int rc = check_shape(W, E, k, H, dtype, sd, M);
+    if (rc != EP_OK) return rc;
+
+    ep_plan* p = new (std::nothrow) ep_plan();
+    if (!p) return fail(EP_ERR_ALLOC, "host allocation of the plan failed");
+    p->W = W; p->E = E; p->k = k; p->H = H; p->dtype = dtype; p->sd = sd; p->M = M;
+    p->F = W < k ? W : k;
+    p->elem_bytes = elem_bytes_of(dtype);
+    p->rows = (int64_t)W * M;
+    p->row_bytes = (int64_t)H * p->elem_bytes;
+    p->tiles = (int)((p->rows + kRouteTile - 1) / kRouteTile);
+    p->variant = EP_VARIANT_AUTO;
+
+    cudaError_t e = cudaGetDevice(&p->device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
+    if (e != cudaSuccess) { delete p; return cuda_fail(e, "ep_plan_create: device query"); }
+
+    const Layout L = layout_of(W, k, H, dtype, sd, M);
+    p->bytes = L.total;
+    e = cudaMalloc(&p->base, L.total);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        delete p;
+        return fail(EP_ERR_ALLOC, "cudaMalloc of %zu bytes failed: %s", L.total, cudaGetErrorString(e));
+    }
+    char* b = (char*)p->base;
+    p->recv_x = (uint8_t*)(b + L.recv_x);
+    p->recv_idx = (int32_t*)(b + L.recv_idx);
+    p->recv_w = (float*)(b + L.recv_w);
+    p->recv_scales = sd ? (float*)(b + L.recv_scales) : nullptr;
+    p->src_pos = (int32_t*)(b + L.src_pos);
+    p->fwd = (int32_t*)(b + L.fwd);
+    p->recv_count = (int32_t*)(b + L.recv_count);
+    p->flags = (unsigned long long*)(b + L.flags);
+    p->ticket = (unsigned long long*)(b + L.ticket);
+    p->status = (int*)(b + L.status);
+    // the control words start at zero once; scan flags are stamped per call after that
+    e = cudaMemset(b + L.recv_count, 0, L.total - L.recv_count);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        cudaFree(p->base);
+        delete p;
+        return cuda_fail(e, "ep_plan_create: clearing control words");
+    }
+    *out = p;
+    return EP_OK;
+}
+
+int ep_plan_destroy(ep_plan* p)
+{
+    if (!p) return EP_OK;
+    DeviceGuard g(p->device);
+    cudaError_t e = cudaDeviceSynchronize();
+    cudaError_t e2 = cudaFree(p->base);
+    delete p;
+    if (e != cudaSuccess) return cuda_fail(e, "ep_plan_destroy: synchronize");
+    if (e2 != cudaSuccess) return cuda_fail(e2, "ep_plan_destroy: cudaFree");
+    return EP_OK;
+}
+
+int ep_plan_set_variant(ep_plan* p, int variant)
+{
+    if (!p) return fail(EP_ERR_ARG, "plan is NULL");
+    if (variant < EP_VARIANT_AUTO || variant > EP_VARIANT_TILED_1024)
+        return fail(EP_ERR_ARG, "variant=%d is not an ep_variant", variant);
+    p->variant = variant;
+    return EP_OK;
+}
+
+static void fill_out(const ep_plan* p, ep_dispatch_out* out)
+{
+    out->recv_x = p->recv_x;
+    out->recv_idx = p->recv_idx;
+    out->recv_w = p->has_w ? p->recv_w : nullptr;
+    out->recv_scales = p->recv_scales;
+    out->recv_count = p->recv_count;
+    out->src_token_pos = p->src_pos;
+    out->rows_per_rank = p->rows;
+    out->epoch = p->epoch;
+}
+
+int ep_dispatch_route(ep_plan* p, const int32_t* indices, const int32_t* n_tok_host, void* stream,
+                      ep_dispatch_out* out)
+{
+    if (!p) return fail(EP_ERR_ARG, "plan is NULL");
+    if (!indices || !aligned(indices, 4)) return fail(EP_ERR_ARG, "indices is NULL or not 4-byte aligned");
+    if (!n_tok_host) return fail(EP_ERR_ARG, "n_tok_host is NULL");
+    int off[kMaxRanks + 1];
+    off[0] = 0;
+    for (int s = 0; s < p->W; ++s) {
+        if (n_tok_host[s] < 0) return fail(EP_ERR_ARG, "n_tok[%d]=%d < 0", s, n_tok_host[s]);
+        if (n_tok_host[s] > p->M)
+            return fail(EP_ERR_CAPACITY, "n_tok[%d]=%d exceeds max_tok_per_rank=%d", s, n_tok_host[s], p->M);
+        off[s + 1] = off[s] + n_tok_host[s];
+    }
+    DeviceGuard g(p->device);
+    if (!g.ok) return fail(EP_ERR_CUDA, "cannot select the plan's device %d", p->device);
+
+    RouteArgs a{};
+    a.idx = indices; a.fwd = p->fwd; a.src_pos = p->src_pos; a.recv_count = p->recv_count;
+    a.flags = p->flags; a.ticket = p->ticket; a.status = p->status;
+    a.rows = p->rows; a.W = p->W; a.E = p->E; a.k = p->k; a.F = p->F; a.M = p->M;
+    a.N = off[p->W]; a.tiles = p->tiles;
+    for (int s = 0; s <= p->W; ++s) a.tok_off[s] = off[s];
+    // the routing kernel always runs all `tiles` CTAs: the ticket arithmetic relies on it
+    cudaError_t e = launch_route(a, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "ep_dispatch_route: launch");
+
+    p->epoch += 1;
+    p->routed = true;
+    p->live = false;
+    p->has_w = false;
+    p->routed_idx = indices;
+    p->N = a.N;
+    memcpy(p->tok_off, off, sizeof off);
+    if (out) {
+        fill_out(p, out);
+        out->recv_w = p->recv_w;   // filled by the scatter when it is given weights
+    }
+    return EP_OK;
+}
+
+int ep_dispatch_scatter(ep_plan* p, const void* x, const float* weights, const float* scales,
+                        const int32_t* indices, void* stream)
+{
+    if (!p) return fail(EP_ERR_ARG, "plan is NULL");
+    if (!p->routed) return fail(EP_ERR_STATE, "ep_dispatch_scatter without a preceding ep_dispatch_route");
+    if (!x || !aligned(x, 16)) return fail(EP_ERR_ARG, "x is NULL or not 16-byte aligned");
+    if (weights && !aligned(weights, 4)) return fail(EP_ERR_ARG, "weights not 4-byte aligned");
+    if (p->sd > 0 && (!scales || !aligned(scales, 4)))
+        return fail(EP_ERR_ARG, "scale_dim=%d needs a 4-byte aligned scales array", p->sd);
+    if (p->sd == 0 && scales) return fail(EP_ERR_ARG, "scales given but the plan has scale_dim 0");
+    if (indices != p->routed_idx) return fail(EP_ERR_ARG, "indices differ from the routed ones");
+    DeviceGuard g(p->device);
+    if (!g.ok) return fail(EP_ERR_CUDA, "cannot select the plan's device %d", p->device);
+
+    ScatterArgs a{};
+    a.x = (const uint8_t*)x; a.w = weights; a.scales = scales; a.idx = indices; a.fwd = p->fwd;
+    a.recv_x = p->recv_x; a.recv_idx = p->recv_idx; a.recv_w = p->recv_w; a.recv_scales = p->recv_scales;
+    a.row_bytes = p->row_bytes;
+    a.W = p->W; a.k = p->k; a.F = p->F; a.M = p->M; a.sd = p->sd; a.N = p->N;
+    const int ce = pick_chunk_elems(p, p->N);
+    a.chunk_bytes = ce * p->elem_bytes;
+    a.chunks = (int)((p->row_bytes + a.chunk_bytes - 1) / a.chunk_bytes);
+    for (int s = 0; s <= p->W; ++s) a.tok_off[s] = p->tok_off[s];
+    cudaError_t e = launch_scatter(a, p->num_sms, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "ep_dispatch_scatter: launch");
+    p->routed = false;
+    p->live = true;
+    p->has_w = weights != nullptr;
+    return EP_OK;
+}
+
+int ep_dispatch(ep_plan* p, const void* x, const float* weights, const float* scales,
+                const int32_t* indices, const int32_t* n_tok_host, void* stream, ep_dispatch_out* out)
+{
+    if (!p) return fail(EP_ERR_ARG, "plan is NULL");
+    // check the payload arguments before the routing kernel starts a new epoch
+    if (!x || !aligned(x, 16)) return fail(EP_ERR_ARG, "x is NULL or not 16-byte aligned");
+    if (weights && !aligned(weights, 4)) return fail(EP_ERR_ARG, "weights not 4-byte aligned");
+    if (p->sd > 0 && (!scales || !aligned(scales, 4)))
+        return fail(EP_ERR_ARG, "scale_dim=%d needs a 4-byte aligned scales array", p->sd);
+    if (p->sd == 0 && scales) return fail(EP_ERR_ARG, "scales given but the plan has scale_dim 0");
+    if (!out) return fail(EP_ERR_ARG, "out is NULL");
+    int rc = ep_dispatch_route(p, indices, n_tok_host, stream, nullptr);
+    if (rc != EP_OK) return rc;
+    rc = ep_dispatch_scatter(p, x, weights, scales, indices, stream);
+    if (rc != EP_OK) return rc;
+    fill_out(p, out);
+    return EP_OK;
+}
+
+int ep_combine(ep_plan* p, const void* expert_out, const float* weights, void* out, float* out_w,
+               uint64_t epoch, void* stream)
+{
+    if (!p) return fail(EP_ERR_ARG, "plan is NULL");
+    if (!p->live || epoch != p->epoch)
+        return fail(EP_ERR_STATE, "epoch %llu is not the plan's live dispatch (live=%d, epoch %llu)",
+                    (unsigned long long)epoch, (int)p->live, (unsigned long long)p->epoch);
+    if (!expert_out || !aligned(expert_out, 16)) return fail(EP_ERR_ARG, "expert_out is NULL or not 16-byte aligned");
+    if (!out || !aligned(out, 16)) return fail(EP_ERR_ARG, "out is NULL or not 16-byte aligned");
+    if (out_w && !weights) return fail(EP_ERR_ARG, "out_w given without weights");
+    if (weights && !aligned(weights, 4)) return fail(EP_ERR_ARG, "weights not 4-byte aligned");
+    if (out_w && !aligned(out_w, 4)) return fail(EP_ERR_ARG, "out_w not 4-byte aligned");
+    {
+        const char* eo0 = (const char*)expert_out;
+        const char* eo1 = eo0 + (size_t)p->W * p->rows * p->H * 2;
+        const char* o0 = (const char*)out;
+        const char* o1 = o0 + (size_t)p->W * p->M * p->H * 2;
+        if (eo0 < o1 && o0 < eo1) return fail(EP_ERR_ARG, "expert_out overlaps out");
+    }
+    DeviceGuard g(p->device);
+    if (!g.ok) return fail(EP_ERR_CUDA, "cannot select the plan's device %d", p->device);
+
+    CombineArgs a{};
+    a.eo = (const uint16_t*)expert_out; a.w_in = weights; a.fwd = p->fwd;
+    a.out = (uint16_t*)out; a.out_w = out_w; a.H = p->H;
+    a.W = p->W; a.k = p->k; a.F = p->F; a.M = p->M; a.N = p->N;
+    a.chunk_elems = pick_chunk_elems(p, p->N);
+    a.chunks = (int)((p->H + a.chunk_elems - 1) / a.chunk_elems);
+    for (int s = 0; s <= p->W; ++s) a.tok_off[s] = p->tok_off[s];
+    cudaError_t e = launch_combine(a, p->dtype == EP_FP16, p->num_sms, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "ep_combine: launch");
+    return EP_OK;
+}
+
+int ep_reset(ep_plan* p, void* stream)
+{
+    (void)stream;
+    if (!p) return fail(EP_ERR_ARG, "plan is NULL");
+    p->epoch += 1;
+    p->routed = false;
+    p->live = false;
+    return EP_OK;
+}
+
+int ep_status(ep_plan* p, int* device_status)
+{
+    if (!p || !device_status) return fail(EP_ERR_ARG, "plan or device_status is NULL");
+    DeviceGuard g(p->device);
+    int v = 0;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpy(&v, p->status, sizeof v, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaMemset(p->status, 0, sizeof v);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "ep_status");
+    *device_status = v;
+    return EP_OK;
+}
+
+}  // extern "C"

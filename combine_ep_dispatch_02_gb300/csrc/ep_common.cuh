@@ -1,0 +1,136 @@
+// ep_common.cuh -- internal declarations shared by the dispatch / combine kernels and the C ABI.
+//
+// Layout in HBM (all row-major, one plan-owned allocation, sub-buffers 256-byte aligned):
+//   recv_x       [W][W*M][H]   payload rows received by each logical rank
+//   recv_idx     [W][W*M][k]   int32 top-k index rows
+//   recv_w       [W][W*M][k]   FP32 weight rows
+//   recv_scales  [W][W*M][sd]  FP32 scale rows
+//   src_pos      [W][W*M]      reverse map: src_rank * (W*M) + src_token
+//   fwd          [W][M][F]     forward map, F = min(W, k): the receive rows of token (s,t) as
+//                              r * (W*M) + slot, in ascending destination rank, -1 padded
+//   recv_count   [W]
+//   flags        [tiles][W]    decoupled-lookback scan words of the routing kernel
+//   ticket       u64           monotone tile ticket (never reset; also yields the call stamp)
+//   status       int32         first device-side error
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "ep.h"
+
+namespace ep {
+
+constexpr int kMaxRanks = 32;       // destination sets are uint32 bit masks
+constexpr int kMaxTopk = 64;        // two 32-slot batches
+constexpr int kRouteTile = 256;     // tokens per routing CTA, one per thread
+constexpr int kRouteThreads = 256;
+constexpr int kCopyThreads = 256;   // scatter / combine CTAs: 8 warps, one work unit per warp
+
+// Scan flag word: [63:34] call stamp (30 bits) | [33:32] status | [31:0] count.
+constexpr unsigned long long kFlagAggregate = 1ull;   // count = this tile's own total
+constexpr unsigned long long kFlagInclusive = 2ull;   // count = total of tiles 0..this one
+constexpr uint32_t kStampMask = 0x3FFFFFFFu;
+constexpr int kSpinLimit = 1 << 20; // polls before a wait gives up with EP_ERR_DEVICE_TIMEOUT
+
+struct RouteArgs {
+    const int32_t* idx;
+    int32_t* fwd;
+    int32_t* src_pos;
+    int32_t* recv_count;
+    unsigned long long* flags;
+    unsigned long long* ticket;
+    int* status;
+    int64_t rows;         // W*M
+    int W, E, k, F, M, N, tiles;
+    int tok_off[kMaxRanks + 1];   // exclusive prefix of per-rank token counts; tok_off[W] = N
+};
+
+struct ScatterArgs {
+    const uint8_t* x;
+    const float* w;
+    const float* scales;
+    const int32_t* idx;
+    const int32_t* fwd;
+    uint8_t* recv_x;
+    int32_t* recv_idx;
+    float* recv_w;
+    float* recv_scales;
+    int64_t row_bytes;    // H * element size, a multiple of 16
+    int W, k, F, M, sd, N;
+    int chunk_bytes;      // bytes of one work unit's slice of a row (multiple of 16)
+    int chunks;           // slices per row
+    int tok_off[kMaxRanks + 1];
+};
+
+struct CombineArgs {
+    const uint16_t* eo;
+    const float* w_in;
+    const int32_t* fwd;
+    uint16_t* out;
+    float* out_w;
+    int64_t H;
+    int W, k, F, M, N;
+    int chunk_elems;      // elements of one work unit's slice of a row (multiple of 8)
+    int chunks;
+    int tok_off[kMaxRanks + 1];
+};
+
+// Host-side launchers, one per kernel translation unit.
+cudaError_t launch_route(const RouteArgs& a, cudaStream_t stream);
+cudaError_t launch_scatter(const ScatterArgs& a, int num_sms, cudaStream_t stream);
+cudaError_t launch_combine(const CombineArgs& a, bool fp16, int num_sms, cudaStream_t stream);
+
+// ----------------------------------------------------------------------------- device helpers
+#ifdef __CUDACC__
+
+__device__ __forceinline__ void record_status(int* status, int code)
+{
+    if (*reinterpret_cast<volatile int*>(status) == 0) atomicCAS(status, 0, code);
+}
+
+// Source rank of flattened token g (tokens of rank 0 first, then rank 1, ...); off in shared.
+__device__ __forceinline__ int rank_of_token(const int* off, int W, int g)
+{
+    int s = 0;
+    while (s + 1 < W && off[s + 1] <= g) ++s;
+    return s;
+}
+
+// 16-byte streaming read of data nothing writes during the kernel: skip L1 allocation.
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p)
+{
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_v4(void* p, const uint4& v)
+{
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};"
+                 :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p)
+{
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v)
+{
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned lanemask_lt()
+{
+    unsigned m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+#endif  // __CUDACC__
+
+}  // namespace ep

@@ -1,0 +1,96 @@
+// ep_scatter.cu -- payload scatter of Dispatch.
+//
+// For every source token and every destination rank it was routed to, copy the token's hidden
+// row, its top-k index row, its FP32 weight row and its FP32 scale row into that rank's
+// receive row (MORI-EP gfx1201 PR, Dispatch bullet: "Multiple experts on the same rank share
+// one hidden payload"; guide, dispatch() outputs).  The receive rows come from the forward map
+// the routing kernel wrote.
+//
+// HBM-bound: each source row is READ ONCE into registers with 16-byte non-allocating loads and
+// WRITTEN once per destination with 16-byte stores, so the traffic is the minimum
+// N*row + P*row bytes (N tokens, P token-destination pairs).  Work units are (token, slice of
+// the row): whole rows for large token counts, 512- or 1024-element slices for small ones (the
+// pages' small-batch launch policy), one warp per unit, a persistent grid sized from the
+// occupancy of this kernel times the SM count.
+#include "ep_common.cuh"
+
+namespace ep {
+namespace {
+
+constexpr int kUnroll = 4;   // 16-byte vectors per lane in flight per step
+
+__global__ void __launch_bounds__(kCopyThreads) ep_scatter_kernel(const ScatterArgs a)
+{
+    __shared__ int s_off[kMaxRanks + 1];
+    if (threadIdx.x <= a.W) s_off[threadIdx.x] = a.tok_off[threadIdx.x];
+    __syncthreads();
+
+    const int lane = threadIdx.x & 31;
+    const int64_t warps_per_grid = (int64_t)gridDim.x * (kCopyThreads / 32);
+    const int64_t units = (int64_t)a.N * a.chunks;
+    for (int64_t u = (int64_t)blockIdx.x * (kCopyThreads / 32) + (threadIdx.x >> 5); u < units;
+         u += warps_per_grid) {
+        const int g = (int)(u / a.chunks);
+        const int c = (int)(u - (int64_t)g * a.chunks);
+        const int s = rank_of_token(s_off, a.W, g);
+        const int64_t tok = (int64_t)s * a.M + (g - s_off[s]);
+
+        // destination rows, compact and ascending in rank; lane d holds the d-th one
+        const int dest = lane < a.F ? __ldg(a.fwd + tok * a.F + lane) : -1;
+        const int nd = __popc(__ballot_sync(0xffffffffu, dest >= 0));
+
+        const int64_t off = (int64_t)c * a.chunk_bytes;
+        const int64_t rem = a.row_bytes - off;
+        const int nvec = (int)((rem < a.chunk_bytes ? rem : a.chunk_bytes) >> 4);
+        const uint8_t* src = a.x + tok * a.row_bytes + off;
+        for (int v0 = 0; v0 < nvec; v0 += 32 * kUnroll) {   // warp-uniform bounds
+            uint4 buf[kUnroll];
+#pragma unroll
+            for (int q = 0; q < kUnroll; ++q) {
+                const int v = v0 + q * 32 + lane;
+                if (v < nvec) buf[q] = ld_stream_v4(src + (int64_t)v * 16);
+            }
+            for (int d = 0; d < nd; ++d) {
+                const int row = __shfl_sync(0xffffffffu, dest, d);
+                uint8_t* dst = a.recv_x + (int64_t)row * a.row_bytes + off;
+#pragma unroll
+                for (int q = 0; q < kUnroll; ++q) {
+                    const int v = v0 + q * 32 + lane;
+                    if (v < nvec) st_v4(dst + (int64_t)v * 16, buf[q]);
+                }
+            }
+        }
+
+        if (c == 0) {   // the small per-token rows travel with the first slice
+            for (int d = 0; d < nd; ++d) {
+                const int64_t row = __shfl_sync(0xffffffffu, dest, d);
+                for (int e = lane; e < a.k; e += 32) {
+                    a.recv_idx[row * a.k + e] = __ldg(a.idx + tok * a.k + e);
+                    if (a.w) a.recv_w[row * a.k + e] = __ldg(a.w + tok * a.k + e);
+                }
+                for (int e = lane; e < a.sd; e += 32)
+                    a.recv_scales[row * a.sd + e] = __ldg(a.scales + tok * a.sd + e);
+            }
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_scatter(const ScatterArgs& a, int num_sms, cudaStream_t stream)
+{
+    const int64_t units = (int64_t)a.N * a.chunks;
+    if (units == 0) return cudaSuccess;
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ep_scatter_kernel,
+                                                                  kCopyThreads, 0);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    const int64_t need = (units + kCopyThreads / 32 - 1) / (kCopyThreads / 32);
+    const int64_t cap = (int64_t)per_sm * num_sms;
+    const int grid = (int)(need < cap ? need : cap);
+    ep_scatter_kernel<<<grid, kCopyThreads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace ep

@@ -1,0 +1,171 @@
+/*
+ * ep.h -- C ABI of libep.so: MoE expert-parallel token Dispatch and Combine on one GB300.
+ *
+ * The W expert-parallel ranks are logical partitions whose send and receive buffers all live
+ * in this GPU's HBM; every "transfer" is an HBM-to-HBM scatter or gather done by the library's
+ * own CUDA kernels (sm_103a).  No call here uses a second GPU, a collective or the CPU for any
+ * step of the computation.
+ *
+ * Semantics (MORI-EP gfx1201 PR "feat(ep): add opt-in gfx1201 EP2/EP4 support", section "How the
+ * gfx1201 kernels work"; MORI-EP guide, section 3 "Operator API"):
+ *   - Dispatch maps each token's top-k experts to destination ranks (expert e lives on rank
+ *     e / experts_per_rank) and reserves ONE receive row per (token, distinct destination rank):
+ *     experts on the same rank share one hidden payload.  The row carries the token's hidden
+ *     vector, its whole top-k index row, its FP32 weight row (if given) and its FP32 scale row
+ *     (if scale_dim > 0).  Rows are numbered per destination rank in (source rank, token)
+ *     order.  The reverse map src_token_pos[r][row] = src_rank * (W * M) + src_token (guide,
+ *     get_dispatch_src_token_pos()).
+ *   - Combine uses that map to gather, for every source token, the expert-output rows of the
+ *     ranks it was sent to, sums them in FP32 in ascending destination-rank order starting from
+ *     +0.0f, and rounds to nearest even into BF16 (BF16 and FP8 payloads) or FP16 (FP16
+ *     payload).  Optional FP32 weight rows are summed the same way into an FP32 output.  Routing
+ *     weights are never applied to the payload (the caller's responsibility, per the pages).
+ *
+ * Notation: W ranks, E experts per rank, k = top-k, H = hidden, M = max tokens per rank,
+ * sd = scale_dim, F = min(W, k).  All arrays are dense and row-major.  Pointers are DEVICE
+ * pointers unless marked "host".  A stream argument is a cudaStream_t passed as void*
+ * (NULL = the legacy default stream).  Every call on one plan must be ordered on one stream
+ * (or otherwise serialised): calls of one plan that overlap on the GPU race.
+ *
+ * Errors.  Every condition the host can check is reported before any launch, with a negative
+ * code and a message readable through ep_last_error().  Problems only the GPU can see (an
+ * expert id outside [0, W*E), a bounded spin that expired) never trap: the kernel records the
+ * first one in the plan's status word, skips the offending work and finishes; ep_status()
+ * reads and clears that word.
+ */
+#ifndef EP_H_
+#define EP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct ep_plan ep_plan; /* opaque; created and owned by the library */
+
+/* payload dtypes (the guide's data_type field) */
+enum ep_dtype { EP_BF16 = 0, EP_FP16 = 1, EP_FP8_E4M3 = 2 };
+
+enum ep_status_code {
+    EP_OK = 0,
+    EP_ERR_ARG = -1,            /* invalid argument (null, misaligned, out of range)        */
+    EP_ERR_ALLOC = -2,          /* device allocation failed                                 */
+    EP_ERR_CUDA = -3,           /* a CUDA runtime call or launch failed                     */
+    EP_ERR_STATE = -4,          /* combine without a live dispatch, or with a stale epoch   */
+    EP_ERR_CAPACITY = -5,       /* a rank's token count exceeds max_tok_per_rank            */
+    EP_ERR_INDEX = -6,          /* device: an expert id outside [0, W*E) was skipped        */
+    EP_ERR_DEVICE_TIMEOUT = -7  /* device: a bounded wait expired; outputs are not valid    */
+};
+
+/* Work split of the payload scatter and of combine (a performance choice; never changes
+ * results).  AUTO follows the gfx1201 launch policy of the pages: small token counts split the
+ * hidden dimension into 512- or 1024-element tiles, large ones move whole rows. */
+enum ep_variant { EP_VARIANT_AUTO = 0, EP_VARIANT_WHOLE_ROW = 1, EP_VARIANT_TILED_512 = 2,
+                  EP_VARIANT_TILED_1024 = 3 };
+
+/* Views of the plan's receive buffers after a dispatch (guide, dispatch() return values). */
+typedef struct {
+    void* recv_x;           /* [W][W*M][H] payload elements (BF16 / FP16 / FP8 bits)          */
+    int32_t* recv_idx;      /* [W][W*M][k] the token's whole top-k index row                 */
+    float* recv_w;          /* [W][W*M][k] FP32 weights, NULL if dispatch got none            */
+    float* recv_scales;     /* [W][W*M][sd] FP32 scales, NULL if sd == 0                      */
+    int32_t* recv_count;    /* [W] rows received by each rank (guide: recv_num_token)         */
+    int32_t* src_token_pos; /* [W][W*M] reverse map: src_rank * (W*M) + src_token             */
+    int64_t rows_per_rank;  /* W*M: stride, in rows, between ranks' receive regions           */
+    uint64_t epoch;         /* pass to ep_combine; identifies this dispatch                   */
+} ep_dispatch_out;
+
+/*
+ * Create a plan: validate the shape and allocate, once, every device buffer the calls use
+ * (receive rows, index/weight/scale rows, reverse and forward maps, scan flags, status word).
+ * Follows the guide's EpDispatchCombineConfig (section 2, "Configuration") with the receive
+ * capacity of W*M rows per rank.
+ *   W                 1..32 logical ranks
+ *   experts_per_rank  >= 1, W*experts_per_rank < 2^31
+ *   topk              1..64
+ *   hidden            >= 1, hidden * element size a multiple of 16 bytes
+ *   dtype             enum ep_dtype
+ *   scale_dim         0..65536 FP32 scales per token row
+ *   max_tok_per_rank  >= 1, W*W*max_tok_per_rank < 2^31 (int32 reverse map)
+ * The plan belongs to the CUDA device current at creation.  Returns EP_OK and *out, or an error
+ * with *out = NULL.
+ */
+int ep_plan_create(ep_plan** out, int W, int experts_per_rank, int topk, int hidden, int dtype,
+                   int scale_dim, int max_tok_per_rank);
+
+/* Wait for the device, then free the plan and its buffers.  NULL is a no-op. */
+int ep_plan_destroy(ep_plan* p);
+
+/* Select the work split (enum ep_variant) of later ep_dispatch / ep_combine calls. */
+int ep_plan_set_variant(ep_plan* p, int variant);
+
+/* Device bytes ep_plan_create allocates for this shape, 0 for an invalid shape. */
+size_t ep_plan_device_bytes(int W, int experts_per_rank, int topk, int hidden, int dtype,
+                            int scale_dim, int max_tok_per_rank);
+
+/*
+ * Dispatch (guide, dispatch(); gfx1201 PR, Dispatch bullet).
+ *   x           [W][M][H] payload elements, 16-byte aligned; rows t >= n_tok[s] are not read
+ *   weights     [W][M][k] FP32 or NULL
+ *   scales      [W][M][sd] FP32; must be NULL iff sd == 0
+ *   indices     [W][M][k] int32 expert ids
+ *   n_tok_host  host [W]: tokens on each source rank, each 0..M (EP_ERR_CAPACITY if above M)
+ *   out         host: receives views of the plan's buffers and the dispatch epoch
+ * Enqueues the routing kernel and the payload scatter kernel on `stream` and returns without
+ * waiting.  The views stay valid until the next ep_dispatch, ep_dispatch_route or ep_reset on
+ * the plan (guide: outputs must be consumed before the next dispatch overwrites them).  Receive
+ * rows at or past recv_count[r] hold unspecified data.
+ */
+int ep_dispatch(ep_plan* p, const void* x, const float* weights, const float* scales,
+                const int32_t* indices, const int32_t* n_tok_host, void* stream,
+                ep_dispatch_out* out);
+
+/*
+ * The two phases of ep_dispatch, exposed so a caller can time or overlap them separately.
+ * ep_dispatch_route runs the routing kernel alone (dedup of destination ranks, prefix scan of
+ * receive rows, reverse and forward maps, receive counts); it starts a new dispatch epoch and
+ * fills *out.  After ep_dispatch_route, out->recv_w is the weight buffer whether
+ * or not the scatter will be given weights.  ep_dispatch_scatter then copies payload, index, weight and scale rows to the
+ * rows routed by the preceding ep_dispatch_route (EP_ERR_STATE otherwise); `indices` must be
+ * the same array.  ep_dispatch(...) == ep_dispatch_route(...) + ep_dispatch_scatter(...).
+ */
+int ep_dispatch_route(ep_plan* p, const int32_t* indices, const int32_t* n_tok_host, void* stream,
+                      ep_dispatch_out* out);
+int ep_dispatch_scatter(ep_plan* p, const void* x, const float* weights, const float* scales,
+                        const int32_t* indices, void* stream);
+
+/*
+ * Combine (guide, combine(); gfx1201 PR, Combine bullet).
+ *   expert_out  [W][W*M][H] 16-bit expert outputs (BF16 for BF16/FP8 plans, FP16 for FP16),
+ *               16-byte aligned; may be the dispatch's recv_x (in-place expert)
+ *   weights     [W][W*M][k] FP32 rows to sum, or NULL
+ *   out         [W][M][H] 16-bit outputs, 16-byte aligned; rows t >= n_tok[s] are untouched
+ *   out_w       [W][M][k] FP32 summed weights; NULL to skip (must be NULL if weights is NULL)
+ *   epoch       the epoch of the dispatch whose rows are combined (EP_ERR_STATE if it is not
+ *               the plan's live dispatch)
+ * May be called more than once per dispatch.  expert_out must not overlap out.
+ */
+int ep_combine(ep_plan* p, const void* expert_out, const float* weights, void* out, float* out_w,
+               uint64_t epoch, void* stream);
+
+/* End the live dispatch (guide, reset()): its views become invalid and ep_combine on its epoch
+ * fails.  No device work is needed: the scan flags carry a per-call stamp. */
+int ep_reset(ep_plan* p, void* stream);
+
+/* Wait for the device, store the plan's device status word (EP_OK or the first EP_ERR_INDEX /
+ * EP_ERR_DEVICE_TIMEOUT recorded since the last call) in *device_status, and clear it. */
+int ep_status(ep_plan* p, int* device_status);
+
+/* Static description of a status code. */
+const char* ep_strerror(int code);
+
+/* Message of the last failed call on the calling host thread ("" if none). */
+const char* ep_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EP_H_ */

@@ -1,0 +1,94 @@
+"""C ABI checks that need no GPU: the library loads, exports every declared entry point, sizes
+its device buffers as documented, and rejects invalid shapes and calls on the host."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import combine_ep_dispatch_02_gb300 as ep
+from combine_ep_dispatch_02_gb300 import build as epbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    epbuild.build()
+    return ep.load_library()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "ep.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ep_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _declared_functions()
+    assert set(declared) == set(ep.EXPORTS), declared
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def _align(v):
+    return (v + 255) // 256 * 256
+
+
+def _layout_bytes(W, E, k, H, eb, sd, M):
+    rows = W * M
+    F = min(W, k)
+    tiles = -(-rows // 256)
+    parts = [W * rows * H * eb, W * rows * k * 4, W * rows * k * 4, W * rows * sd * 4, W * rows * 4,
+             rows * F * 4, W * 4, tiles * W * 8, 8, 4]
+    return sum(_align(p) for p in parts)
+
+
+def test_device_bytes_golden(lib):
+    # DeepSeek-V3 shape: recv rows 8 * 32768 * 14336 B, index / weight rows 8 MiB each,
+    # src_pos and forward map 1 MiB each, 128 tiles * 8 scan words, three control words
+    assert lib.ep_plan_device_bytes(8, 32, 8, 7168, ep.EP_BF16, 0, 4096) == 3776979712
+    # FP8 with 56 scales per row
+    assert lib.ep_plan_device_bytes(8, 96, 6, 7168, ep.EP_FP8_E4M3, 56, 4096) == \
+        _layout_bytes(8, 96, 6, 7168, 1, 56, 4096)
+    for shape in [(2, 4, 2, 256, 0, 0, 64), (4, 64, 64, 2048, 1, 0, 512), (1, 1, 1, 8, 0, 0, 1),
+                  (32, 8, 64, 16, 2, 3, 100)]:
+        W, E, k, H, dt, sd, M = shape
+        eb = 1 if dt == ep.EP_FP8_E4M3 else 2
+        assert lib.ep_plan_device_bytes(*shape) == _layout_bytes(W, E, k, H, eb, sd, M), shape
+
+
+@pytest.mark.parametrize("shape,why", [
+    ((0, 4, 2, 256, 0, 0, 64), "W"), ((33, 4, 2, 256, 0, 0, 64), "W"),
+    ((2, 0, 2, 256, 0, 0, 64), "experts_per_rank"), ((2, 4, 0, 256, 0, 0, 64), "topk"),
+    ((2, 4, 65, 256, 0, 0, 64), "topk"), ((2, 4, 2, 4, 0, 0, 64), "hidden"),
+    ((2, 4, 2, 8, 2, 0, 64), "hidden"), ((2, 4, 2, 256, 3, 0, 64), "dtype"),
+    ((2, 4, 2, 256, 0, -1, 64), "scale_dim"), ((2, 4, 2, 256, 0, 0, 0), "max_tok"),
+    ((32, 4, 2, 256, 0, 0, 1 << 21), "2^31"),
+])
+def test_invalid_shapes_rejected_on_host(lib, shape, why):
+    h = ctypes.c_void_p(123)
+    rc = lib.ep_plan_create(ctypes.byref(h), *shape)
+    assert rc == ep.EP_ERR_ARG
+    assert h.value is None
+    assert why in lib.ep_last_error().decode()
+    assert lib.ep_plan_device_bytes(*shape) == 0
+
+
+def test_null_plan_calls_fail_cleanly(lib):
+    o = ep.DispatchOut()
+    n = (ctypes.c_int32 * 2)(1, 1)
+    assert lib.ep_dispatch(None, None, None, None, None, n, None, ctypes.byref(o)) == ep.EP_ERR_ARG
+    assert lib.ep_combine(None, None, None, None, None, 0, None) == ep.EP_ERR_ARG
+    assert lib.ep_reset(None, None) == ep.EP_ERR_ARG
+    assert lib.ep_plan_set_variant(None, 0) == ep.EP_ERR_ARG
+    st = ctypes.c_int(0)
+    assert lib.ep_status(None, ctypes.byref(st)) == ep.EP_ERR_ARG
+    assert lib.ep_plan_destroy(None) == ep.EP_OK
+    for code in range(-7, 1):
+        assert lib.ep_strerror(code)
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    with pytest.raises(RuntimeError):
+        ep.load_library(str(tmp_path / "missing" / "libep.so"))

@@ -1,0 +1,295 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the same seeded inputs.
+
+Bar: dispatch counts, reverse map and every received row (payload, indices, weights, scales)
+bit-exact; combine outputs bit-exact under the fixed ascending-rank FP32 order (NaN compared as
+NaN); combined FP32 weights bit-exact.
+"""
+import numpy as np
+import pytest
+import torch
+
+import combine_ep_dispatch_02_gb300 as ep
+import gpu_path
+import harness
+import oracle
+from combine_ep_dispatch_02_gb300 import workloads as wlmod
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda", 0) if torch.cuda.is_available() else None
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA GPU")
+    from combine_ep_dispatch_02_gb300 import build
+    build.build()
+    oracle.build()
+
+
+def _oracle(wl):
+    return oracle.run_workload(wl, harness.expert_np)
+
+
+def _check(wl, variant="auto"):
+    disp, _, o_out, o_w = _oracle(wl)
+    gpu = gpu_path.run(wl, DEV, variant)
+    gpu_path.compare(wl, gpu, disp, o_out, o_w)
+    return gpu, disp
+
+
+# ---------------------------------------------------------------- the five workloads
+
+def test_tiny_full():
+    _check(wlmod.make_workload("tiny"))
+
+
+@pytest.mark.parametrize("variant", ["auto", "whole_row", "tiled_512", "tiled_1024"])
+def test_small_full_scalar_expert(variant):
+    _check(wlmod.make_workload("small"), variant)
+
+
+@pytest.mark.parametrize("k", wlmod.TOPK_SWEEP)
+def test_topk_sweep_fp16(k):
+    _check(wlmod.make_workload("topk", k=k))
+
+
+def test_dsv3_reduced_ragged_tiles():
+    # 300 tokens per rank: 2400 tokens = 9 full routing tiles of 256 and a ragged tail
+    _check(wlmod.make_workload("dsv3", max_tok=300))
+
+
+def test_fp8_reduced():
+    _check(wlmod.make_workload("fp8", max_tok=512))
+
+
+def test_fp8_full_ragged():
+    _check(wlmod.make_workload("fp8"))
+
+
+def test_dsv3_full():
+    """The DeepSeek-V3-shaped workload at full size, in the launch configuration the benchmark
+    times (AUTO variant), every row and every output compared."""
+    _check(wlmod.make_workload("dsv3"))
+
+
+# ---------------------------------------------------------------- edge cases
+
+@pytest.mark.parametrize("case", [
+    dict(W=1, E=8, k=3, H=64, M=40, n_tok=[37]),
+    dict(W=32, E=2, k=64, H=16, M=70, n_tok=list(range(0, 64, 2))),
+    dict(W=32, E=4, k=5, H=8, M=9, n_tok=[9] * 32),
+    dict(W=5, E=3, k=1, H=24, M=300, n_tok=[300, 0, 257, 1, 255]),
+    dict(W=3, E=5, k=9, H=520, M=600, n_tok=[600, 513, 0]),
+    dict(W=8, E=1, k=8, H=7168, M=64, n_tok=[64, 63, 1, 0, 2, 33, 64, 5]),
+    dict(W=4, E=64, k=33, H=2048, M=129, n_tok=[129, 128, 127, 1]),
+], ids=lambda c: f"W{c['W']}k{c['k']}H{c['H']}")
+def test_edge_shapes(case):
+    for dtype in ("bf16", "fp16"):
+        _check(wlmod.custom_workload(dtype=dtype, seed=3, **case))
+
+
+def test_fp8_with_odd_scale_dim():
+    _check(wlmod.custom_workload(W=4, E=4, k=4, H=256, dtype="fp8", sd=3, M=50, n_tok=[50, 7, 0, 31]))
+
+
+def test_empty_dispatch():
+    wl = wlmod.custom_workload(W=4, E=4, k=2, H=64, M=16, n_tok=[0, 0, 0, 0])
+    gpu = gpu_path.run(wl, DEV)
+    assert gpu["status"] == 0
+    assert not gpu["recv_count"].any()
+
+
+def test_zipf_hot_rank():
+    wl = wlmod.custom_workload(W=8, E=4, k=4, H=256, M=1000, n_tok=[1000] * 8, routing="zipf")
+    _check(wl)
+
+
+def test_invalid_ids_set_status_and_are_skipped():
+    wl = wlmod.custom_workload(W=3, E=2, k=3, H=64, M=300, n_tok=[300, 200, 100], seed=4)
+    wl.indices[0, 5, 1] = -1
+    wl.indices[1, 199, 0] = 6
+    disp, _, o_out, o_w = _oracle(wl)
+    assert disp["status"] == oracle.ERR_INDEX
+    gpu = gpu_path.run(wl, DEV)
+    assert gpu["status"] == ep.EP_ERR_INDEX
+    gpu["status"] = 0
+    gpu_path.compare(wl, gpu, disp, o_out, o_w)
+
+
+def test_no_weights():
+    wl = wlmod.custom_workload(W=4, E=8, k=4, H=128, M=100, n_tok=[100, 50, 3, 99],
+                               with_weights=False)
+    _check(wl)
+
+
+# ---------------------------------------------------------------- lifecycle
+
+def _setup(wl):
+    plan = gpu_path.make_plan(wl, DEV)
+    return plan, gpu_path.to_device(wl, DEV)
+
+
+def test_double_combine_is_bit_identical():
+    wl = wlmod.make_workload("small", max_tok=64)
+    plan, (x, w, sc, idx) = _setup(wl)
+    d = plan.dispatch(x, w, sc, idx, wl.n_tok)
+    eo = harness.expert_torch(wl, d.recv_x, d.recv_idx, d.recv_w, d.recv_scales, d.recv_count)
+    o1, w1 = plan.combine(eo, d.recv_w, d.epoch)
+    o2, w2 = plan.combine(eo, d.recv_w, d.epoch)
+    torch.cuda.synchronize()
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16)) and torch.equal(w1, w2)
+    plan.close()
+
+
+def test_handle_interleave_and_reset():
+    wl_a = wlmod.custom_workload(W=4, E=4, k=3, H=64, M=80, n_tok=[80, 10, 40, 79], seed=1)
+    wl_b = wlmod.custom_workload(W=4, E=4, k=3, H=64, M=80, n_tok=[5, 80, 0, 33], seed=2)
+    plan = gpu_path.make_plan(wl_a, DEV)
+    xa, wa, _, ia = gpu_path.to_device(wl_a, DEV)
+    xb, wb, _, ib = gpu_path.to_device(wl_b, DEV)
+    da = plan.dispatch(xa, wa, None, ia, wl_a.n_tok)
+    db = plan.dispatch(xb, wb, None, ib, wl_b.n_tok)
+    with pytest.raises(ep.EpError) as e:
+        plan.combine(da.recv_x, da.recv_w, da.epoch)
+    assert e.value.code == ep.EP_ERR_STATE
+    out_b, _ = plan.combine(db.recv_x, db.recv_w, db.epoch)
+    _, _, o_out_b, _ = oracle.run_workload(wl_b)
+    torch.cuda.synchronize()
+    assert np.array_equal(gpu_path.raw(out_b), o_out_b)
+    # re-dispatch A, combine A
+    da = plan.dispatch(xa, wa, None, ia, wl_a.n_tok)
+    out_a, _ = plan.combine(da.recv_x, da.recv_w, da.epoch)
+    _, _, o_out_a, _ = oracle.run_workload(wl_a)
+    torch.cuda.synchronize()
+    assert np.array_equal(gpu_path.raw(out_a), o_out_a)
+    plan.reset()
+    with pytest.raises(ep.EpError) as e:
+        plan.combine(da.recv_x, da.recv_w, da.epoch)
+    assert e.value.code == ep.EP_ERR_STATE
+    assert plan.status() == 0
+    plan.close()
+
+
+def test_host_errors_before_launch():
+    wl = wlmod.custom_workload(W=2, E=4, k=2, H=64, M=16, n_tok=[16, 16])
+    plan, (x, w, sc, idx) = _setup(wl)
+    with pytest.raises(ep.EpError) as e:
+        plan.dispatch(x, w, None, idx, [17, 0])
+    assert e.value.code == ep.EP_ERR_CAPACITY
+    with pytest.raises(ep.EpError) as e:
+        plan.dispatch(x, w, None, idx, [-1, 0])
+    assert e.value.code == ep.EP_ERR_ARG
+    with pytest.raises(ep.EpError) as e:   # scales on a plan without scale_dim
+        plan.dispatch(x, w, torch.zeros(4, device=DEV), idx, [1, 1])
+    assert e.value.code == ep.EP_ERR_ARG
+    with pytest.raises(ep.EpError) as e:   # misaligned x
+        plan.dispatch(x.view(-1)[1:], w, None, idx, [1, 1])
+    assert e.value.code == ep.EP_ERR_ARG
+    with pytest.raises(ep.EpError) as e:   # combine before any dispatch
+        plan.combine(x, None, 1)
+    assert e.value.code == ep.EP_ERR_STATE
+    d = plan.dispatch(x, w, None, idx, wl.n_tok)
+    with pytest.raises(ep.EpError) as e:   # out_w without weights
+        plan.combine(d.recv_x, None, d.epoch, out_w=torch.zeros((2, 16, 2), device=DEV))
+    assert e.value.code == ep.EP_ERR_ARG
+    with pytest.raises(ep.EpError) as e:   # scatter without route
+        plan.dispatch_scatter(x, w, None, idx)
+    assert e.value.code == ep.EP_ERR_STATE
+    assert plan.status() == 0
+    plan.close()
+
+
+def test_route_plus_scatter_equals_dispatch():
+    wl = wlmod.make_workload("dsv3", max_tok=200)
+    disp, _, o_out, o_w = _oracle(wl)
+    plan, (x, w, sc, idx) = _setup(wl)
+    gpu_path.poison(plan, DEV)
+    d = plan.dispatch_route(idx, wl.n_tok)
+    plan.dispatch_scatter(x, w, sc, idx)
+    out, out_w = plan.combine(d.recv_x, d.recv_w, d.epoch)
+    torch.cuda.synchronize()
+    res = {"recv_count": d.recv_count.cpu().numpy(), "recv_x": gpu_path.raw(d.recv_x),
+           "recv_idx": gpu_path.raw(d.recv_idx), "recv_w": gpu_path.raw(d.recv_w),
+           "recv_scales": None, "src_pos": gpu_path.raw(d.src_token_pos),
+           "out": gpu_path.raw(out), "out_w": gpu_path.raw(out_w), "status": plan.status()}
+    gpu_path.compare(wl, res, disp, o_out, o_w)
+    plan.close()
+
+
+def test_many_calls_reuse_scan_flags():
+    """Sixty dispatches on one plan with changing token counts: every call's scan words carry
+    a fresh stamp, so no call reads a stale prefix."""
+    wl = wlmod.make_workload("dsv3", max_tok=160)
+    plan, (x, w, sc, idx) = _setup(wl)
+    rng = np.random.default_rng(0)
+    ref = {}
+    for i in range(60):
+        n_tok = rng.integers(0, wl.M + 1, size=wl.W).astype(np.int32)
+        if i % 7 == 0:
+            n_tok[:] = wl.M
+        d = plan.dispatch(x, w, sc, idx, n_tok)
+        key = tuple(n_tok.tolist())
+        if i % 10 == 0 or key not in ref:
+            sub = wlmod.Workload(**{**wl.__dict__, "n_tok": n_tok})
+            o = oracle.dispatch(sub.W, sub.E, sub.k, sub.H, sub.elem_bytes, sub.sd, sub.M, sub.x,
+                                sub.weights, sub.scales, sub.indices, sub.n_tok)
+            ref[key] = o
+        o = ref[key]
+        cnt = d.recv_count.cpu().numpy()
+        assert np.array_equal(cnt, o["recv_count"]), i
+        for r in range(wl.W):
+            n = int(cnt[r])
+            assert np.array_equal(d.src_token_pos[r, :n].cpu().numpy(), o["src_pos"][r, :n]), (i, r)
+    assert plan.status() == 0
+    plan.close()
+
+
+def test_cuda_graph_replay_matches_eager():
+    """Dispatch + combine captured once in a CUDA graph and replayed: the per-call stamps live
+    on the device (ticket counter), so replays stay correct and bit-identical to eager calls."""
+    wl = wlmod.make_workload("small", max_tok=96)
+    disp, _, o_out, o_w = _oracle(wl)
+    plan, (x, w, sc, idx) = _setup(wl)
+    out = torch.zeros((wl.W, wl.M, wl.H), dtype=torch.bfloat16, device=DEV)
+    out_w = torch.zeros((wl.W, wl.M, wl.k), dtype=torch.float32, device=DEV)
+    # warm up eagerly on a side stream (graph capture requires a non-default stream)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        d = plan.dispatch(x, w, sc, idx, wl.n_tok, stream=s)
+        eo = harness.expert_torch(wl, d.recv_x, d.recv_idx, d.recv_w, d.recv_scales, d.recv_count)
+        plan.combine(eo, d.recv_w, d.epoch, out=out, out_w=out_w, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    eager = gpu_path.raw(out).copy()
+    assert np.array_equal(eager, o_out)
+    eo_buf = torch.empty((wl.W, wl.W * wl.M, wl.H), dtype=torch.int16, device=DEV)
+    counts = d.recv_count.cpu().tolist()
+    c = torch.from_numpy(wl.expert_scale).to(DEV)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        cs = torch.cuda.current_stream()
+        d = plan.dispatch(x, w, sc, idx, wl.n_tok, stream=cs)
+        # the scalar expert, with the counts known from the eager run (static shapes)
+        for r in range(wl.W):
+            n = counts[r]
+            X = d.recv_x[r, :n].to(torch.float32)
+            IDX = d.recv_idx[r, :n].long()
+            acc = torch.zeros((n, wl.H), dtype=torch.float32, device=DEV)
+            for j in range(wl.k):
+                m = torch.div(IDX[:, j], wl.E, rounding_mode="floor") == r
+                term = torch.mul(torch.mul(d.recv_w[r, :n, j], c[IDX[:, j]])[:, None], X)
+                acc = torch.where(m[:, None], torch.add(acc, term), acc)
+            eo_buf[r, :n] = acc.to(torch.bfloat16).view(torch.int16)
+        plan.combine(eo_buf, d.recv_w, d.epoch, out=out, out_w=out_w, stream=cs)
+    for _ in range(3):
+        out.zero_()
+        out_w.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(gpu_path.raw(out), eager)
+        assert np.array_equal(out_w.cpu().numpy().view(np.uint32), o_w.view(np.uint32))
+    assert plan.status() == 0
+    plan.close()
