@@ -159,7 +159,7 @@ def run_ours(args, rank, world, dist):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     build.build()
-    wl = wlmod.make_workload(WORKLOAD)
+    wl = wlmod.make_workload(WORKLOAD, max_tok=args.tokens_per_rank)
     plan = ep.Plan(wl.W, wl.E, wl.k, wl.H, wl.dtype, wl.sd, wl.M, device=dev)
     x = torch.from_numpy(wl.x.view(np.int16)).to(dev)
     idx = torch.from_numpy(wl.indices).to(dev)
@@ -251,7 +251,8 @@ def run_ours(args, rank, world, dist):
             "vs_baseline": None,
             "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD_DESC, "tokens": wl.N, "token_dest_pairs": P,
+            "config": {"workload": WORKLOAD_DESC.replace("4096", str(wl.M)), "tokens": wl.N,
+                       "token_dest_pairs": P,
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "l2": "inputs larger than L2 (x 470 MB read, 2.5 GB of receive rows "
                              "written then read per step vs 129 MB L2); no flush",
@@ -318,61 +319,66 @@ def measure_e2e(plan, wl, dev, stream, pair_bytes, steps):
 
 # ----------------------------------------------------------------------------- CPU oracle
 
-SAMPLE_TOKENS = 1024  # tokens per rank of the CPU sample (same routing, first tokens of each rank)
-
-
 def _sample(wl, tokens):
     n_tok = np.minimum(wl.n_tok, tokens).astype(np.int32)
     return wlmod.Workload(**{**wl.__dict__, "n_tok": n_tok})
 
 
-def _time_oracle(sub, repeats=1):
+def _time_oracle(sub, min_seconds=0.0, max_repeats=1):
+    """Run the oracle's dispatch + combine on `sub`; median seconds per run."""
     import oracle
     oracle.build()
-    best = None
-    res = None
-    for _ in range(repeats):
+    times, res = [], None
+    t_all = time.perf_counter()
+    while True:
         t = time.perf_counter()
         res = oracle.run_workload(sub)
-        dt = time.perf_counter() - t
-        best = dt if best is None else min(best, dt)
-    disp = res[0]
-    return best, int(disp["recv_count"].sum()), res
+        times.append(time.perf_counter() - t)
+        if len(times) >= max_repeats or time.perf_counter() - t_all >= min_seconds:
+            break
+    return statistics.median(times), int(res[0]["recv_count"].sum()), res, len(times)
 
 
 def cpu_baseline(wl, gpu_out=None):
-    sub = _sample(wl, SAMPLE_TOKENS)
-    dt, P, res = _time_oracle(sub, repeats=3)
-    nb = phase_bytes(sub, P)
+    """The oracle (plain single-threaded C) on the whole workload, repeated for ~10 s."""
+    dt, P, res, runs = _time_oracle(wl, min_seconds=10.0, max_repeats=20)
+    nb = phase_bytes(wl, P)
     info = {"value": round(nb["pair"] / dt / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"first {SAMPLE_TOKENS} tokens of each of the 8 ranks ({sub.N} tokens, "
-                      f"{P} token-destination pairs), dispatch+combine, best of 3, single-threaded C",
-            "seconds": round(dt, 3), "host_cores": os.cpu_count()}
+            "sample": f"the whole workload ({wl.N} tokens, {P} token-destination pairs), "
+                      f"median of {runs} dispatch+combine runs, single-threaded C",
+            "seconds_per_run": round(dt, 3), "host_cores": os.cpu_count()}
     if gpu_out is not None:
-        # the oracle's combined rows of the sampled tokens must equal the GPU's bit for bit
-        o_out = res[2]
         g = gpu_out.view(torch.int16).cpu().numpy().view(np.uint16)
-        ok = all(np.array_equal(g[s, :n], o_out[s, :n]) for s, n in enumerate(sub.n_tok))
-        info["parity_sampled_tokens"] = "bit-exact" if ok else "MISMATCH"
+        o_out = res[2]
+        ok = all(np.array_equal(g[s, :n], o_out[s, :n]) for s, n in enumerate(wl.n_tok))
+        info["parity_combine_output"] = "bit-exact" if ok else "MISMATCH"
     return info
 
 
 def run_reference(args):
+    """The oracle as the reference arm: each step is one dispatch+combine of a sample of the
+    workload (the first T tokens of every rank, T sized so the whole run takes ~2 minutes)."""
     wl = wlmod.make_workload(WORKLOAD)
-    sub = _sample(wl, SAMPLE_TOKENS)
-    for _ in range(max(3, args.warmup)):
+    warm = max(3, args.warmup)
+    probe = _sample(wl, 256)
+    t_probe, _, _, _ = _time_oracle(probe)
+    per_token = t_probe / probe.N
+    budget = 120.0 / (args.steps + warm)
+    T = int(min(wl.M, max(64, budget / per_token / wl.W)))
+    sub = _sample(wl, T)
+    for _ in range(warm):
         _time_oracle(sub)
     times, P = [], 0
     for _ in range(args.steps):
-        dt, P, _ = _time_oracle(sub)
+        dt, P, _, _ = _time_oracle(sub)
         times.append(dt)
     nb = phase_bytes(sub, P)
     ms = 1e3 * sum(times) / len(times)
     v = round(nb["pair"] / (ms * 1e-3) / 1e9, 3)
-    sample = (f"first {SAMPLE_TOKENS} tokens of each of the 8 ranks ({sub.N} tokens, {P} pairs) "
-              "per step, single-threaded C oracle")
+    sample = (f"first {T} tokens of each of the 8 ranks ({sub.N} tokens, {P} pairs) per step, "
+              "single-threaded C oracle")
     return {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": 1,
-            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": round(ms, 3),
+            "steps": args.steps, "warmup": warm, "ms_per_step": round(ms, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
             "config": {"workload": WORKLOAD_DESC, "tokens": sub.N, "token_dest_pairs": P,
@@ -391,6 +397,9 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--tokens-per-rank", type=int, default=4096,
+                    help="tokens per logical rank (4096 = the full workload; smaller values are "
+                         "for profiling captures)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -36,18 +36,21 @@ def _stale() -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    if not force and not _stale():
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
+          defines=(), lib_path: str = LIB, build_dir: str = BUILD_DIR) -> str:
+    """Compile libep.so; `defines` (e.g. ["EP_COMBINE_STAGES=4"]) and a separate lib_path /
+    build_dir let a caller build tuning variants side by side."""
+    if not force and lib_path == LIB and not defines and not _stale():
         return LIB
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
     flags = ["-O3", "-std=c++17", *ARCH, "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE,
-             "-I", CSRC]
+             "-I", CSRC] + [f"-D{d}" for d in defines]
     if ptxas_info:
         flags += ["-Xptxas", "-v"]
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(build_dir, src.replace(".cu", ".o"))
         cmd = [cc, *flags, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -58,13 +61,13 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
 
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [cc, "-shared", *ARCH, "-cudart", "shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

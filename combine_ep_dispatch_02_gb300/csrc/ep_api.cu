@@ -381,10 +381,9 @@ int ep_combine(ep_plan* p, const void* expert_out, const float* weights, void* o
 
     CombineArgs a{};
     a.eo = (const uint16_t*)expert_out; a.w_in = weights; a.fwd = p->fwd;
-    a.out = (uint16_t*)out; a.out_w = out_w; a.H = p->H;
+    a.out = (uint16_t*)out; a.out_w = out_w; a.status = p->status; a.H = p->H;
     a.W = p->W; a.k = p->k; a.F = p->F; a.M = p->M; a.N = p->N;
-    a.chunk_elems = pick_chunk_elems(p, p->N);
-    a.chunks = (int)((p->H + a.chunk_elems - 1) / a.chunk_elems);
+    combine_geometry(a, p->variant, p->num_sms);
     for (int s = 0; s <= p->W; ++s) a.tok_off[s] = p->tok_off[s];
     cudaError_t e = launch_combine(a, p->dtype == EP_FP16, p->num_sms, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "ep_combine: launch");

@@ -7,10 +7,19 @@
 // BF16/FP16.  Optional FP32 weights are communicated and summed separately").  Routing weights
 // are not applied.  The fixed order makes the result independent of the launch shape.
 //
-// HBM-bound: per token, all of its (<= min(W, k)) rows' 16-byte vectors for one step are
-// loaded before any is added -- the pages' bf16 pull combine likewise loads every source a
-// token can have before folding -- then accumulated in registers and stored as one 16-byte
-// packed BF16x8 / FP16x8 vector.  Work units are (token, slice of the row), one warp each.
+// HBM-bound, and bound by how many bytes each SM keeps in flight: at the loaded HBM latency
+// of this part (~2.3 us) an SM needs ~100 KB of reads outstanding to stream at full rate.  A
+// warp owns one work unit (a token, or a 512/1024-element slice of it for small calls) and its
+// lanes own 16-byte columns.  Per step every lane loads U columns from each of the token's nd
+// rows before adding any, with U chosen from nd so that nd*U = 8 loads (4 KB per warp, with
+// 24 warps per SM ~100 KB per SM) are in flight whatever the fan-in -- the pages' bf16 pull combine likewise loads every source a
+// token can have before folding.  Then, column by column, the rows are added in ascending rank
+// order in FP32 registers and the sum leaves as one packed BF16x8 / FP16x8 16-byte store.  The
+// next unit's forward-map row is loaded while the current one is folded.
+//
+// (A TMA variant that staged row slices through shared memory with 1-D bulk copies was
+// measured slower: on this part one CTA's bulk copies each take ~0.3 us, so gathering a
+// token's 3.5 KB row slices that way cannot keep enough bytes in flight.)
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -19,7 +28,13 @@
 namespace ep {
 namespace {
 
-constexpr int kBatch = 8;   // rows whose vectors are in flight together
+#ifndef EP_COMBINE_CTAS_PER_SM
+#define EP_COMBINE_CTAS_PER_SM 2   // 128 registers per thread: the fold loop runs without spills
+#endif
+#ifndef EP_COMBINE_DEPTH
+#define EP_COMBINE_DEPTH 1
+#endif
+constexpr int kDepth = EP_COMBINE_DEPTH;   // columns per row in flight per lane
 
 template <bool FP16>
 __device__ __forceinline__ void add_vec(float (&acc)[8], const uint4& v)
@@ -59,52 +74,117 @@ __device__ __forceinline__ uint4 pack_vec(const float (&acc)[8])
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// Fold one unit of nd <= 8 rows.  Lane d of `src` holds the unit's d-th row; `ro` keeps the
+// rows as 16-byte-vector offsets from eo4 (32 bits: a receive buffer below 64 GB).  Each lane
+// owns columns lane, lane+32, ...; row d's load of the next column is issued as soon as its
+// current column has been taken, so every lane keeps nd loads in flight without a gap.  The
+// column's rows are added in ascending order, one FP32 add each, then packed and stored.
 template <bool FP16>
-__global__ void __launch_bounds__(kCopyThreads) ep_combine_kernel(const CombineArgs a)
+__device__ __forceinline__ void fold_rows(const uint4* __restrict__ eo4, int src, int64_t hv, int v0,
+                                          int nd, int nv, uint4* dst4, int lane)
+{
+    uint32_t ro[8];
+#pragma unroll
+    for (int d = 0; d < 8; ++d)
+        ro[d] = (uint32_t)((int64_t)__shfl_sync(0xffffffffu, src, d) * hv + v0);
+    uint4 b[8][kDepth];
+#pragma unroll
+    for (int t = 0; t < kDepth; ++t)
+#pragma unroll
+        for (int d = 0; d < 8; ++d)
+            if (d < nd && lane + 32 * t < nv) b[d][t] = ld_stream_v4(eo4 + ro[d] + lane + 32 * t);
+    for (int vb = 0; vb < nv; vb += 32 * kDepth) {        // warp-uniform bounds
+#pragma unroll
+        for (int t = 0; t < kDepth; ++t) {
+            const int vcur = vb + 32 * t + lane;
+            const int vnext = vcur + 32 * kDepth;
+            float acc[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+#pragma unroll
+            for (int d = 0; d < 8; ++d) {
+                if (d < nd) {
+                    const uint4 x = b[d][t];
+                    if (vnext < nv) b[d][t] = ld_stream_v4(eo4 + ro[d] + vnext);
+                    if (vcur < nv) add_vec<FP16>(acc, x);
+                }
+            }
+            if (vcur < nv) st_v4(dst4 + vcur, pack_vec<FP16>(acc));
+        }
+    }
+}
+
+// More than 8 rows (W > 8 and k > 8): rows in ascending batches of 8, one column per lane.
+template <bool FP16>
+__device__ __forceinline__ void fold_wide(const uint16_t* eo, int64_t H, int src, int nd,
+                                          int64_t v0_elem, int nv, uint16_t* dst, int lane)
+{
+    for (int vb = 0; vb < nv; vb += 32) {
+        const int v = vb + lane;
+        const bool act = v < nv;
+        float acc[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+        for (int d0 = 0; d0 < nd; d0 += 8) {
+            uint4 buf[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int64_t row = __shfl_sync(0xffffffffu, src, (d0 + q) & 31);
+                if (act && d0 + q < nd) buf[q] = ld_stream_v4(eo + row * H + v0_elem + (int64_t)v * 8);
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                if (act && d0 + q < nd) add_vec<FP16>(acc, buf[q]);
+        }
+        if (act) st_v4(dst + (int64_t)v * 8, pack_vec<FP16>(acc));
+    }
+}
+
+// Forward-map entry of this lane for work unit u (the lane-th row of the unit's token).
+__device__ __forceinline__ int unit_src(const CombineArgs& a, const int* off, uint32_t u, int lane)
+{
+    if (u >= (uint32_t)a.N * (uint32_t)a.chunks) return -1;
+    const int g = (int)(u / (uint32_t)a.chunks);
+    const int s = rank_of_token(off, a.W, g);
+    const int64_t tok = (int64_t)s * a.M + (g - off[s]);
+    return lane < a.F ? __ldg(a.fwd + tok * a.F + lane) : -1;
+}
+
+template <bool FP16, bool WIDE>
+__global__ void __launch_bounds__(kCopyThreads, EP_COMBINE_CTAS_PER_SM) ep_combine_kernel(const CombineArgs a)
 {
     __shared__ int s_off[kMaxRanks + 1];
     if (threadIdx.x <= a.W) s_off[threadIdx.x] = a.tok_off[threadIdx.x];
     __syncthreads();
 
     const int lane = threadIdx.x & 31;
-    const int64_t warps_per_grid = (int64_t)gridDim.x * (kCopyThreads / 32);
-    const int64_t units = (int64_t)a.N * a.chunks;
-    for (int64_t u = (int64_t)blockIdx.x * (kCopyThreads / 32) + (threadIdx.x >> 5); u < units;
-         u += warps_per_grid) {
-        const int g = (int)(u / a.chunks);
-        const int c = (int)(u - (int64_t)g * a.chunks);
-        const int s = rank_of_token(s_off, a.W, g);
-        const int64_t tok = (int64_t)s * a.M + (g - s_off[s]);
-
-        const int src = lane < a.F ? __ldg(a.fwd + tok * a.F + lane) : -1;
+    // units = N * chunks < 2^31 (checked by the host), so unit indices are 32-bit
+    const uint32_t units = (uint32_t)a.N * (uint32_t)a.chunks;
+    const uint32_t step = gridDim.x * (kCopyThreads / 32);
+    uint32_t u = blockIdx.x * (kCopyThreads / 32) + (threadIdx.x >> 5);
+    int src = unit_src(a, s_off, u, lane);
+    for (; u < units; u += step) {
+        const int src_next = unit_src(a, s_off, u + step, lane);   // lands while this unit folds
         const int nd = __popc(__ballot_sync(0xffffffffu, src >= 0));
-
-        const int64_t h0 = (int64_t)c * a.chunk_elems;
-        const int64_t rem = a.H - h0;
-        const int nvec = (int)((rem < a.chunk_elems ? rem : a.chunk_elems) >> 3);
-        uint16_t* dst = a.out + tok * a.H + h0;
-        for (int v0 = 0; v0 < nvec; v0 += 32) {   // warp-uniform bounds
-            const int v = v0 + lane;
-            const bool act = v < nvec;
-            float acc[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-            for (int d0 = 0; d0 < nd; d0 += kBatch) {
-                uint4 buf[kBatch];
-#pragma unroll
-                for (int q = 0; q < kBatch; ++q) {
-                    const int64_t row = __shfl_sync(0xffffffffu, src, (d0 + q) & 31);
-                    if (act && d0 + q < nd)
-                        buf[q] = ld_stream_v4(a.eo + row * a.H + h0 + (int64_t)v * 8);
-                }
-#pragma unroll
-                for (int q = 0; q < kBatch; ++q)
-                    if (act && d0 + q < nd) add_vec<FP16>(acc, buf[q]);
-            }
-            if (act) st_v4(dst + (int64_t)v * 8, pack_vec<FP16>(acc));
+        {
+            const int g = (int)(u / (uint32_t)a.chunks);
+            const int c = (int)(u - (uint32_t)g * (uint32_t)a.chunks);
+            const int s = rank_of_token(s_off, a.W, g);
+            const int64_t tok = (int64_t)s * a.M + (g - s_off[s]);
+            const int hv = (int)(a.H >> 3);
+            const int v0 = c * a.chunk_vecs;
+            const int nv = min(a.chunk_vecs, hv - v0);
+            if (!WIDE || nd <= 8)
+                fold_rows<FP16>(reinterpret_cast<const uint4*>(a.eo), src, hv, v0, nd, nv,
+                                reinterpret_cast<uint4*>(a.out) + tok * hv + v0, lane);  // nd 0: +0
+            else
+                fold_wide<FP16>(a.eo, a.H, src, nd, (int64_t)v0 * 8, nv,
+                                a.out + tok * a.H + (int64_t)v0 * 8, lane);
         }
-
-        if (c == 0 && a.w_in != nullptr && a.out_w != nullptr) {
+        if (a.w_in != nullptr && a.out_w != nullptr && u % (uint32_t)a.chunks == 0) {
+            const int g = (int)(u / (uint32_t)a.chunks);
+            const int s = rank_of_token(s_off, a.W, g);
+            const int64_t tok = (int64_t)s * a.M + (g - s_off[s]);
             for (int e0 = 0; e0 < a.k; e0 += 32) {
                 const int e = e0 + lane;
                 float acc = 0.0f;
@@ -115,31 +195,55 @@ __global__ void __launch_bounds__(kCopyThreads) ep_combine_kernel(const CombineA
                 if (e < a.k) a.out_w[tok * a.k + e] = acc;
             }
         }
+        src = src_next;
     }
 }
 
-template <bool FP16>
+template <bool FP16, bool WIDE>
 cudaError_t launch_t(const CombineArgs& a, int num_sms, cudaStream_t stream)
 {
     const int64_t units = (int64_t)a.N * a.chunks;
     if (units == 0) return cudaSuccess;
     int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ep_combine_kernel<FP16>,
-                                                                  kCopyThreads, 0);
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &per_sm, ep_combine_kernel<FP16, WIDE>, kCopyThreads, 0);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
     const int64_t need = (units + kCopyThreads / 32 - 1) / (kCopyThreads / 32);
     const int64_t cap = (int64_t)per_sm * num_sms;
     const int grid = (int)(need < cap ? need : cap);
-    ep_combine_kernel<FP16><<<grid, kCopyThreads, 0, stream>>>(a);
+    ep_combine_kernel<FP16, WIDE><<<grid, kCopyThreads, 0, stream>>>(a);
     return cudaGetLastError();
 }
 
 }  // namespace
 
+void combine_geometry(CombineArgs& a, int variant, int num_sms)
+{
+    const int hv = (int)(a.H >> 3);
+    int cv = hv;                                           // whole rows
+    if (variant == EP_VARIANT_TILED_512) cv = 64;
+    if (variant == EP_VARIANT_TILED_1024) cv = 128;
+    if (variant == EP_VARIANT_AUTO) {
+        // Small calls split rows into 1024- then 512-element slices so every resident warp
+        // gets work, as the pages' small-batch policy does.
+        const int64_t warps = (int64_t)num_sms * EP_COMBINE_CTAS_PER_SM * (kCopyThreads / 32);
+        if ((int64_t)a.N < warps && hv > 128) {
+            cv = 128;
+            if ((int64_t)a.N * ((hv + cv - 1) / cv) < warps) cv = 64;
+        }
+    }
+    if (cv > hv) cv = hv;
+    a.chunks = (hv + cv - 1) / cv;
+    a.chunk_vecs = cv;
+}
+
 cudaError_t launch_combine(const CombineArgs& a, bool fp16, int num_sms, cudaStream_t stream)
 {
-    return fp16 ? launch_t<true>(a, num_sms, stream) : launch_t<false>(a, num_sms, stream);
+    // a token has at most F = min(W, k) rows; the wide path is only compiled in when F > 8
+    if (a.F > 8)
+        return fp16 ? launch_t<true, true>(a, num_sms, stream) : launch_t<false, true>(a, num_sms, stream);
+    return fp16 ? launch_t<true, false>(a, num_sms, stream) : launch_t<false, false>(a, num_sms, stream);
 }
 
 }  // namespace ep

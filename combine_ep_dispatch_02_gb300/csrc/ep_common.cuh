@@ -69,10 +69,11 @@ struct CombineArgs {
     const int32_t* fwd;
     uint16_t* out;
     float* out_w;
+    int* status;
     int64_t H;
     int W, k, F, M, N;
-    int chunk_elems;      // elements of one work unit's slice of a row (multiple of 8)
-    int chunks;
+    int chunk_vecs;       // 16-byte vectors of one work unit's slice of a row
+    int chunks;           // slices per row
     int tok_off[kMaxRanks + 1];
 };
 
@@ -80,6 +81,8 @@ struct CombineArgs {
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t stream);
 cudaError_t launch_scatter(const ScatterArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_combine(const CombineArgs& a, bool fp16, int num_sms, cudaStream_t stream);
+// choose combine's slice of a row per work unit (a.H and a.N set)
+void combine_geometry(CombineArgs& a, int variant, int num_sms);
 
 // ----------------------------------------------------------------------------- device helpers
 #ifdef __CUDACC__
@@ -122,6 +125,90 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
 __device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v)
 {
     asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
+}
+
+// ---- shared memory, mbarrier and bulk-copy (TMA) primitives
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr)
+{
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
+}
+
+// make barrier initialisation visible to the async (bulk-copy) proxy
+__device__ __forceinline__ void fence_barrier_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// order this thread's generic-proxy shared-memory accesses before later async-proxy ones
+__device__ __forceinline__ void fence_proxy_async_shared()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+    return done != 0;
+}
+
+// Bounded wait for the phase of parity `parity`; false (and a recorded status) on expiry.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* status)
+{
+    for (int it = 0; it < kSpinLimit; ++it)
+        if (mbar_try_wait(bar, parity)) return true;
+    record_status(status, EP_ERR_DEVICE_TIMEOUT);
+    return false;
+}
+
+// 1-D bulk copy global -> shared, completion counted in bytes on an mbarrier.  Both addresses
+// 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
+// 4-byte asynchronous copy global -> shared (for rows too short or unaligned for a bulk copy)
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" :: "r"(dst), "l"(src) : "memory");
+}
+
+// the mbarrier receives one arrival once all of this thread's earlier cp.async copies land
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(bar) : "memory");
 }
 
 __device__ __forceinline__ unsigned lanemask_lt()
