@@ -27,7 +27,7 @@ VARIANTS = {"auto": 0, "whole_row": 1, "tiled_512": 2, "tiled_1024": 3}
 # every entry point include/ep.h declares
 EXPORTS = ("ep_plan_create", "ep_plan_destroy", "ep_plan_set_variant", "ep_plan_device_bytes",
            "ep_dispatch", "ep_dispatch_route", "ep_dispatch_scatter", "ep_combine", "ep_reset",
-           "ep_status", "ep_strerror", "ep_last_error")
+           "ep_status", "ep_strerror", "ep_last_error", "ep_route_noalloc")
 
 
 class EpError(RuntimeError):
@@ -70,6 +70,7 @@ def load_library(path: Optional[str] = None):
         "ep_status": (I, [V, ctypes.POINTER(I)]),
         "ep_strerror": (ctypes.c_char_p, [I]),
         "ep_last_error": (ctypes.c_char_p, []),
+        "ep_route_noalloc": (I, [I, I, I, I, V, V, V, V, V, V, V]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -89,6 +90,21 @@ def plan_device_bytes(W, experts_per_rank, topk, hidden, dtype, scale_dim, max_t
     code = DTYPE_CODES[dtype] if isinstance(dtype, str) else dtype
     return load_library().ep_plan_device_bytes(W, experts_per_rank, topk, hidden, code, scale_dim,
                                                max_tok_per_rank)
+
+
+def route_noalloc(W: int, experts_per_rank: int, topk: int, max_tok_per_rank: int,
+                  indices: torch.Tensor, n_tok: Sequence[int], src_token_pos: torch.Tensor,
+                  recv_count: torch.Tensor, fwd_map: torch.Tensor, device_status: torch.Tensor,
+                  stream=None) -> None:
+    """``ep_route_noalloc``: the routing step into caller-owned tensors, with no device
+    allocation by the library (see include/ep.h).  Shapes: indices [W][M][k] int32,
+    src_token_pos [W][W*M], recv_count [W], fwd_map [W][M][min(W,k)], device_status [1], all
+    int32 on the current device."""
+    arr = np.ascontiguousarray(np.asarray(n_tok, dtype=np.int32).reshape(W))
+    _check(load_library().ep_route_noalloc(
+        W, experts_per_rank, topk, max_tok_per_rank, _ptr(indices),
+        arr.ctypes.data_as(ctypes.c_void_p), _ptr(src_token_pos), _ptr(recv_count), _ptr(fwd_map),
+        _ptr(device_status), _stream(stream)))
 
 
 class _DevPtr:

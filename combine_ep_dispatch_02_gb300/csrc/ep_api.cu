@@ -152,6 +152,11 @@ int pick_chunk_elems(const ep_plan* p, int N)
 
 }  // namespace
 
+namespace ep {
+// lets other translation units of the library report a message through ep_last_error()
+int record_error(int code, const char* msg) { return fail(code, "%s", msg); }
+}  // namespace ep
+
 extern "C" {
 
 const char* ep_last_error(void) { return g_err; }

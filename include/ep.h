@@ -158,6 +158,32 @@ int ep_reset(ep_plan* p, void* stream);
  * EP_ERR_DEVICE_TIMEOUT recorded since the last call) in *device_status, and clear it. */
 int ep_status(ep_plan* p, int* device_status);
 
+/*
+ * Routing without any allocation.  The pages have no counterpart to this call: it exists for
+ * callers that must not call cudaMalloc -- for example a serving runtime whose pool allocator
+ * already owns nearly all of HBM, or a plug-in whose host forbids allocation (which can stall the
+ * device) on its hot path -- and therefore cannot hold an ep_plan.  It runs the same routing
+ * kernel as ep_dispatch_route, for the shape given by its arguments, on memory the caller owns:
+ *   indices        [W][M][k] int32 expert ids                      (input)
+ *   n_tok_host     host [W] tokens per source rank, each 0..M        (input)
+ *   src_token_pos  [W][W*M] int32 reverse map                        (output)
+ *   recv_count     [W] int32 rows received per rank                  (output)
+ *   fwd_map        [W][M][min(W,k)] int32: token (s,t)'s receive rows r*(W*M) + row in
+ *                  ascending rank, then -1                          (output)
+ *   device_status  [1] int32: EP_OK, or EP_ERR_INDEX / EP_ERR_DEVICE_TIMEOUT once the stream
+ *                  reaches the end of the call                       (output)
+ * The kernel's scan words live in one static device array of 16384 64-bit words (128 KB) inside
+ * libep.so, held by every GPU that loads the library until the process exits; a shape needs
+ * 1 + W * ceil(W*M / 256) words and larger shapes fail with EP_ERR_ARG.  The first call on a
+ * device looks up that array's device address (cudaGetSymbolAddress) and should come before any
+ * stream capture.  Each call clears the words it uses on `stream`; all calls share the one
+ * array, so calls that overlap on the GPU (other streams, other threads) race and must be
+ * serialised by the caller.  No call allocates or frees device memory.
+ */
+int ep_route_noalloc(int W, int experts_per_rank, int topk, int max_tok_per_rank,
+                     const int32_t* indices, const int32_t* n_tok_host, int32_t* src_token_pos,
+                     int32_t* recv_count, int32_t* fwd_map, int32_t* device_status, void* stream);
+
 /* Static description of a status code. */
 const char* ep_strerror(int code);
 
