@@ -49,8 +49,11 @@ def _load():
             lib.ep_oracle_dispatch.argtypes = [ctypes.c_int] * 7 + [_p] * 12
             lib.ep_oracle_combine.restype = ctypes.c_int
             lib.ep_oracle_combine.argtypes = [ctypes.c_int] * 5 + [_p] * 6
+            lib.ep_oracle_quantize_e4m3_blockwise.restype = ctypes.c_int
+            lib.ep_oracle_quantize_e4m3_blockwise.argtypes = [ctypes.c_int64, ctypes.c_int, _p, _p, _p]
             for name in ("ep_oracle_bf16_from_f32_array", "ep_oracle_f16_from_f32_array",
-                         "ep_oracle_f32_from_f16_array"):
+                         "ep_oracle_f32_from_f16_array", "ep_oracle_e4m3_from_f32_array",
+                         "ep_oracle_f32_from_e4m3_array"):
                 fn = getattr(lib, name)
                 fn.restype = None
                 fn.argtypes = [_p, _p, ctypes.c_int64]
@@ -139,6 +142,41 @@ def f32_from_f16(a):
     o = np.empty(a.shape, dtype=np.float32)
     _load().ep_oracle_f32_from_f16_array(_ptr(a), _ptr(o), a.size)
     return o
+
+
+def e4m3_from_f32(a):
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    o = np.empty(a.shape, dtype=np.uint8)
+    _load().ep_oracle_e4m3_from_f32_array(_ptr(a), _ptr(o), a.size)
+    return o
+
+
+def f32_from_e4m3(a):
+    a = np.ascontiguousarray(a, dtype=np.uint8)
+    o = np.empty(a.shape, dtype=np.float32)
+    _load().ep_oracle_f32_from_e4m3_array(_ptr(a), _ptr(o), a.size)
+    return o
+
+
+def quantize_e4m3_blockwise(x_bf16):
+    """Block-wise FP8 quantisation of BF16 rows [..., H] (H a multiple of 128): returns
+    (q uint8 [..., H], scales float32 [..., H/128]); see ep_oracle_quantize_e4m3_blockwise."""
+    x = np.ascontiguousarray(x_bf16).view(np.uint16)
+    H = x.shape[-1]
+    rows = x.size // H
+    q = np.empty(x.shape, dtype=np.uint8)
+    sc = np.empty(x.shape[:-1] + (H // 128,), dtype=np.float32)
+    if _load().ep_oracle_quantize_e4m3_blockwise(rows, H, _ptr(x), _ptr(q), _ptr(sc)) != 0:
+        raise ValueError("quantize_e4m3_blockwise: hidden must be a positive multiple of 128")
+    return q, sc
+
+
+def dispatch_quantized(wl):
+    """Quantising dispatch: every source row is quantised block-wise to FP8 once, then the
+    FP8 rows and their scales are dispatched like any FP8 payload."""
+    q, sc = quantize_e4m3_blockwise(wl.x)
+    return dispatch(wl.W, wl.E, wl.k, wl.H, 1, wl.H // 128, wl.M, q, wl.weights, sc,
+                    wl.indices, wl.n_tok)
 
 
 def run_workload(wl, expert_out_fn=None):

@@ -107,6 +107,91 @@ float ep_oracle_f32_from_f16(uint16_t h)
     return bits_f32(sign | ((exp - 15u + 127u) << 23) | (frac << 13));
 }
 
+/* float -> FP8 e4m3fn (OCP: 1 sign, 4 exponent bits with bias 7, 3 fraction bits; no
+ * infinities; largest finite 448; all-ones exponent and fraction is NaN), round to nearest
+ * even, saturating: magnitudes that round above 448 give 448. */
+uint8_t ep_oracle_e4m3_from_f32(float f)
+{
+    uint32_t b = f32_bits(f);
+    uint8_t sign = (uint8_t)((b >> 24) & 0x80u);
+    uint32_t a = b & 0x7FFFFFFFu;
+    if (a > 0x7F800000u) return (uint8_t)(sign | 0x7Fu);              /* NaN */
+    if (a >= 0x43E00000u) return (uint8_t)(sign | 0x7Eu);             /* >= 448 (and Inf): 448 */
+    if (a >= 0x3C800000u) {                                           /* >= 2^-6: normal e4m3 */
+        uint32_t exp = (a >> 23) - 127u + 7u;
+        uint32_t h = (exp << 3) | ((a & 0x7FFFFFu) >> 20);
+        uint32_t rem = a & 0xFFFFFu;                                  /* 20 dropped bits */
+        if (rem > 0x80000u || (rem == 0x80000u && (h & 1u))) h += 1u;
+        if (h > 0x7Eu) h = 0x7Eu;                                     /* 464 > v > 448 rounds up: saturate */
+        return (uint8_t)(sign | h);
+    }
+    /* subnormal e4m3: value / 2^-9 rounded to an integer = m * 2^(E - 150 + 9) with the binary32
+     * significand m and biased exponent E, i.e. m shifted right by 141 - E */
+    uint32_t E = a >> 23;
+    if (E < 117u) return sign;                                        /* below 2^-10: rounds to 0 */
+    uint32_t m = (a & 0x7FFFFFu) | 0x800000u;
+    uint32_t shift = 141u - E;                                        /* 21 .. 24 */
+    uint32_t h = m >> shift;
+    uint32_t rem = m & ((1u << shift) - 1u);
+    uint32_t half = 1u << (shift - 1u);
+    if (rem > half || (rem == half && (h & 1u))) h += 1u;             /* may carry into 0x08 */
+    return (uint8_t)(sign | h);
+}
+
+/* FP8 e4m3fn -> float, exact. */
+float ep_oracle_f32_from_e4m3(uint8_t q)
+{
+    uint32_t sign = ((uint32_t)q & 0x80u) << 24;
+    uint32_t exp = ((uint32_t)q >> 3) & 0xFu;
+    uint32_t frac = (uint32_t)q & 0x7u;
+    if (exp == 0xFu && frac == 0x7u) return bits_f32(sign | 0x7FC00000u);
+    if (exp == 0) {
+        float v = (float)frac * bits_f32(0x3B000000u);                /* frac * 2^-9 */
+        return sign ? -v : v;
+    }
+    return bits_f32(sign | ((exp - 7u + 127u) << 23) | (frac << 20));
+}
+
+/*
+ * Block-wise FP8 quantisation of BF16 rows (the FP8 wire of the MORI-EP tuning matrix, read as
+ * one FP32 scale per 128-element block).  For every block of 128 elements of a row:
+ *   amax  = max |x| (exact, in FP32)
+ *   scale = amax / 448 (FP32 division, round to nearest even), or 1 when amax is 0
+ *   q[i]  = e4m3 RNE saturating of (x[i] / scale) (FP32 division, round to nearest even)
+ * x [rows][H] BF16 bits, q [rows][H], scales [rows][H/128]; H must be a multiple of 128.
+ */
+int ep_oracle_quantize_e4m3_blockwise(int64_t rows, int H, const uint16_t* x, uint8_t* q, float* scales)
+{
+    if (H < 128 || H % 128 != 0 || rows < 0) return EP_ORACLE_ERR_ARG;
+    const int nb = H / 128;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int b = 0; b < nb; ++b) {
+            const uint16_t* xb = x + r * H + b * 128;
+            float amax = 0.0f;
+            for (int i = 0; i < 128; ++i) {
+                float v = ep_oracle_f32_from_bf16(xb[i]);
+                float m = v < 0.0f ? -v : v;
+                if (m > amax) amax = m;
+            }
+            float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+            scales[r * nb + b] = scale;
+            for (int i = 0; i < 128; ++i)
+                q[r * H + b * 128 + i] = ep_oracle_e4m3_from_f32(ep_oracle_f32_from_bf16(xb[i]) / scale);
+        }
+    }
+    return EP_ORACLE_OK;
+}
+
+void ep_oracle_e4m3_from_f32_array(const float* in, uint8_t* out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = ep_oracle_e4m3_from_f32(in[i]);
+}
+
+void ep_oracle_f32_from_e4m3_array(const uint8_t* in, float* out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = ep_oracle_f32_from_e4m3(in[i]);
+}
+
 void ep_oracle_bf16_from_f32_array(const float* in, uint16_t* out, int64_t n)
 {
     for (int64_t i = 0; i < n; ++i) out[i] = ep_oracle_bf16_from_f32(in[i]);

@@ -319,3 +319,87 @@ def test_workload_generator_is_seeded():
             for t in range(int(wl.n_tok[s])):
                 row = wl.indices[s, t]
                 assert len(set(row.tolist())) == wl.k and row.min() >= 0 and row.max() < wl.W * wl.E
+
+
+# ---------------------------------------------------------------- FP8 quantising dispatch (next row F1)
+
+def test_e4m3_rne_matches_torch_cast():
+    rng = np.random.default_rng(12)
+    a = np.concatenate([
+        rng.uniform(-448, 448, 200000).astype(np.float32),
+        (rng.standard_normal(100000) * 2.0 ** -7).astype(np.float32),          # subnormal range
+        np.array([0.0, -0.0, 448.0, -448.0, 2.0 ** -6, 2.0 ** -9, 2.0 ** -10, 1.5 * 2.0 ** -10,
+                  2.0 ** -11, 7 * 2.0 ** -9, 7.5 * 2.0 ** -9, 1.0625, 1.1875, 240.0, 248.0,
+                  440.0, 447.99997], dtype=np.float32),
+    ])
+    a = np.concatenate([a, -a])
+    mine = oracle.e4m3_from_f32(a)
+    ref = torch.from_numpy(a).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(mine, ref)
+    # saturation: everything at or beyond 448 (and infinities) gives +-448; NaN stays NaN
+    big = np.array([448.0, 449.0, 464.0, 465.0, 1e6, np.inf], dtype=np.float32)
+    assert np.all(oracle.e4m3_from_f32(big) == 0x7E) and np.all(oracle.e4m3_from_f32(-big) == 0xFE)
+    assert (oracle.e4m3_from_f32(np.array([np.nan], np.float32))[0] & 0x7F) == 0x7F
+
+
+def test_e4m3_decode_exact_all_codes():
+    codes = np.arange(256, dtype=np.uint8)
+    mine = oracle.f32_from_e4m3(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float32).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(mine), nan)
+    assert np.array_equal(mine[~nan].view(np.uint32), ref[~nan].view(np.uint32))
+
+
+def _bf16(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16) \
+        .view(torch.int16).numpy().view(np.uint16)
+
+
+def test_blockwise_quantiser_properties():
+    rng = np.random.default_rng(3)
+    rows, H = 64, 512
+    xf = rng.standard_normal((rows, H)).astype(np.float32) * np.float32(3.0)
+    xf[5, :128] = 0.0                       # an all-zero block: scale 1, codes 0
+    xf[6, 128:256] *= np.float32(1e-4)      # tiny values: the scale keeps them representable
+    xf[7, 256:384] = -xf[7, 256:384]
+    x = _bf16(xf)
+    q, sc = oracle.quantize_e4m3_blockwise(x)
+    xs = (x.astype(np.uint32) << 16).view(np.float32).reshape(rows, H // 128, 128)
+    amax = np.abs(xs).max(axis=2)
+    assert sc[5, 0] == 1.0 and not (q[5, :128] & 0x7F).any()
+    nz = amax > 0
+    # scale = amax / 448 rounded once in FP32
+    assert np.array_equal(sc[nz], (amax[nz] / np.float32(448.0)).astype(np.float32))
+    # the block maximum lands on +-448 exactly
+    qb = q.reshape(rows, H // 128, 128)
+    assert np.all(((qb & 0x7F) == 0x7E).any(axis=2)[nz])
+    # every code is within half an e4m3 step of x / scale (relative 2^-4, or 2^-10 absolute
+    # in the subnormal range)
+    v = xs.astype(np.float64) / sc[:, :, None].astype(np.float64)
+    deq = oracle.f32_from_e4m3(q).astype(np.float64).reshape(v.shape)
+    assert np.all(np.abs(deq - v) <= np.maximum(np.abs(v) * 2.0 ** -4, 2.0 ** -10) * (1 + 1e-6))
+    # signs survive (a negative value never becomes a positive code)
+    assert np.all((xs < 0) <= ((qb & 0x80) != 0))
+
+
+def test_blockwise_quantiser_scale_one_is_plain_cast():
+    """A block whose maximum is 448 has scale 1, so every code is the plain e4m3 cast of x."""
+    rng = np.random.default_rng(4)
+    xf = rng.uniform(-440, 440, (8, 256)).astype(np.float32)
+    xf[:, 0] = 448.0
+    xf[:, 128] = -448.0
+    x = _bf16(xf)
+    q, sc = oracle.quantize_e4m3_blockwise(x)
+    assert np.all(sc == 1.0)
+    xb = (x.astype(np.uint32) << 16).view(np.float32)
+    ref = torch.from_numpy(xb).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(q, ref)
+
+
+def test_quantised_dispatch_routes_quantised_rows():
+    wl = wlmod.make_workload("dsv3", max_tok=24)
+    disp = oracle.dispatch_quantized(wl)
+    q, sc = oracle.quantize_e4m3_blockwise(wl.x)
+    wq = wlmod.Workload(**{**wl.__dict__, "x": q, "dtype": "fp8", "sd": wl.H // 128, "scales": sc})
+    _check_dispatch(wq, disp)
