@@ -18,8 +18,9 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libep.so")
 
-EP_BF16, EP_FP16, EP_FP8_E4M3 = 0, 1, 2
-DTYPE_CODES = {"bf16": EP_BF16, "fp16": EP_FP16, "fp8": EP_FP8_E4M3}
+EP_BF16, EP_FP16, EP_FP8_E4M3, EP_BF16_TO_FP8_E4M3 = 0, 1, 2, 3
+# "bf16_fp8": BF16 input that dispatch quantises to FP8 e4m3 + one FP32 scale per 128 elements
+DTYPE_CODES = {"bf16": EP_BF16, "fp16": EP_FP16, "fp8": EP_FP8_E4M3, "bf16_fp8": EP_BF16_TO_FP8_E4M3}
 EP_OK, EP_ERR_ARG, EP_ERR_ALLOC, EP_ERR_CUDA, EP_ERR_STATE = 0, -1, -2, -3, -4
 EP_ERR_CAPACITY, EP_ERR_INDEX, EP_ERR_DEVICE_TIMEOUT = -5, -6, -7
 VARIANTS = {"auto": 0, "whole_row": 1, "tiled_512": 2, "tiled_1024": 3}
@@ -152,7 +153,8 @@ class Plan:
     """One expert-parallel Dispatch/Combine problem shape; owns the receive buffers.
 
     ``Plan(W, experts_per_rank, topk, hidden, dtype, scale_dim, max_tok_per_rank)`` maps to
-    ``ep_plan_create``; dtype is "bf16", "fp16" or "fp8" (e4m3)."""
+    ``ep_plan_create``; dtype is "bf16", "fp16", "fp8" (e4m3 with caller scales) or "bf16_fp8"
+    (BF16 input quantised by dispatch to e4m3 with one FP32 scale per 128 elements)."""
 
     def __init__(self, W: int, experts_per_rank: int, topk: int, hidden: int, dtype: str = "bf16",
                  scale_dim: int = 0, max_tok_per_rank: int = 1, device=None):
@@ -166,8 +168,10 @@ class Plan:
             _check(self._lib.ep_plan_create(ctypes.byref(self._h), W, experts_per_rank, topk, hidden,
                                             DTYPE_CODES[dtype], scale_dim, max_tok_per_rank))
         self.rows = W * max_tok_per_rank
+        if dtype == "bf16_fp8":
+            self.sd = hidden // 128
         self.payload_torch_dtype = {"bf16": torch.bfloat16, "fp16": torch.float16,
-                                    "fp8": torch.float8_e4m3fn}[dtype]
+                                    "fp8": torch.float8_e4m3fn, "bf16_fp8": torch.float8_e4m3fn}[dtype]
         self.combine_torch_dtype = torch.float16 if dtype == "fp16" else torch.bfloat16
 
     # -- lifetime
@@ -198,7 +202,7 @@ class Plan:
 
     def _wrap(self, o: DispatchOut) -> Dispatched:
         W, R, k, H, sd, dev = self.W, self.rows, self.k, self.H, self.sd, self.device
-        if self.dtype == "fp8":
+        if self.dtype in ("fp8", "bf16_fp8"):
             rx = _view(o.recv_x, (W, R, H), "|u1", dev).view(torch.float8_e4m3fn)
         else:
             rx = _view(o.recv_x, (W, R, H), "<i2", dev).view(self.payload_torch_dtype)

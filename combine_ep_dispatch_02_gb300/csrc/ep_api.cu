@@ -13,6 +13,7 @@ using namespace ep;
 
 struct ep_plan {
     int W, E, k, H, dtype, sd, M, F, elem_bytes, tiles;
+    bool quantise;       // EP_BF16_TO_FP8_E4M3: BF16 input, FP8 rows + scales on the wire
     int64_t rows;        // W*M receive rows per rank
     int64_t row_bytes;   // H * element size
     int device, num_sms, variant;
@@ -70,10 +71,14 @@ int elem_bytes_of(int dtype)
     switch (dtype) {
     case EP_BF16:
     case EP_FP16: return 2;
-    case EP_FP8_E4M3: return 1;
+    case EP_FP8_E4M3:
+    case EP_BF16_TO_FP8_E4M3: return 1;   // bytes per element of the RECEIVED payload
     default: return 0;
     }
 }
+
+// scale_dim the plan actually uses (the quantising dtype fixes it at hidden / 128)
+int effective_sd(int dtype, int H, int sd) { return dtype == EP_BF16_TO_FP8_E4M3 ? H / 128 : sd; }
 
 int check_shape(int W, int E, int k, int H, int dtype, int sd, int M)
 {
@@ -87,6 +92,11 @@ int check_shape(int W, int E, int k, int H, int dtype, int sd, int M)
         return fail(EP_ERR_ARG, "hidden=%d: hidden * %d bytes must be a positive multiple of 16", H, eb);
     if ((int64_t)H * eb >= (int64_t)1 << 31) return fail(EP_ERR_ARG, "hidden=%d too large", H);
     if (sd < 0 || sd > 65536) return fail(EP_ERR_ARG, "scale_dim=%d outside 0..65536", sd);
+    if (dtype == EP_BF16_TO_FP8_E4M3) {
+        if (H % 128 != 0) return fail(EP_ERR_ARG, "hidden=%d: the quantising dtype needs hidden %% 128 == 0", H);
+        if (sd != 0 && sd != H / 128)
+            return fail(EP_ERR_ARG, "scale_dim=%d: the quantising dtype uses hidden/128 = %d scales", sd, H / 128);
+    }
     if (M < 1) return fail(EP_ERR_ARG, "max_tok_per_rank=%d < 1", M);
     if ((int64_t)W * W * M >= (int64_t)1 << 31)
         return fail(EP_ERR_ARG, "W*W*max_tok_per_rank >= 2^31 overflows the int32 src_token_pos");
@@ -183,7 +193,7 @@ size_t ep_plan_device_bytes(int W, int E, int k, int H, int dtype, int sd, int M
     const int rc = check_shape(W, E, k, H, dtype, sd, M);
     memcpy(g_err, saved, sizeof g_err);
     if (rc != EP_OK) return 0;
-    return layout_of(W, k, H, dtype, sd, M).total;
+    return layout_of(W, k, H, dtype, effective_sd(dtype, H, sd), M).total;
 }
 
 int ep_plan_create(ep_plan** out, int W, int E, int k, int H, int dtype, int sd, int M)
@@ -207,6 +217,9 @@ int ep_plan_create(ep_plan** out, int W, int E, int k, int H, int dtype, int sd,
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
     if (e != cudaSuccess) { delete p; return cuda_fail(e, "ep_plan_create: device query"); }
 
+    sd = effective_sd(dtype, H, sd);
+    p->sd = sd;
+    p->quantise = dtype == EP_BF16_TO_FP8_E4M3;
     const Layout L = layout_of(W, k, H, dtype, sd, M);
     p->bytes = L.total;
     e = cudaMalloc(&p->base, L.total);
@@ -319,9 +332,13 @@ int ep_dispatch_scatter(ep_plan* p, const void* x, const float* weights, const f
     if (!p->routed) return fail(EP_ERR_STATE, "ep_dispatch_scatter without a preceding ep_dispatch_route");
     if (!x || !aligned(x, 16)) return fail(EP_ERR_ARG, "x is NULL or not 16-byte aligned");
     if (weights && !aligned(weights, 4)) return fail(EP_ERR_ARG, "weights not 4-byte aligned");
-    if (p->sd > 0 && (!scales || !aligned(scales, 4)))
-        return fail(EP_ERR_ARG, "scale_dim=%d needs a 4-byte aligned scales array", p->sd);
-    if (p->sd == 0 && scales) return fail(EP_ERR_ARG, "scales given but the plan has scale_dim 0");
+    if (p->quantise) {
+        if (scales) return fail(EP_ERR_ARG, "the quantising dtype computes its scales: pass NULL");
+    } else {
+        if (p->sd > 0 && (!scales || !aligned(scales, 4)))
+            return fail(EP_ERR_ARG, "scale_dim=%d needs a 4-byte aligned scales array", p->sd);
+        if (p->sd == 0 && scales) return fail(EP_ERR_ARG, "scales given but the plan has scale_dim 0");
+    }
     if (indices != p->routed_idx) return fail(EP_ERR_ARG, "indices differ from the routed ones");
     DeviceGuard g(p->device);
     if (!g.ok) return fail(EP_ERR_CUDA, "cannot select the plan's device %d", p->device);
@@ -335,7 +352,8 @@ int ep_dispatch_scatter(ep_plan* p, const void* x, const float* weights, const f
     a.chunk_bytes = ce * p->elem_bytes;
     a.chunks = (int)((p->row_bytes + a.chunk_bytes - 1) / a.chunk_bytes);
     for (int s = 0; s <= p->W; ++s) a.tok_off[s] = p->tok_off[s];
-    cudaError_t e = launch_scatter(a, p->num_sms, (cudaStream_t)stream);
+    cudaError_t e = p->quantise ? launch_scatter_quant(a, p->num_sms, (cudaStream_t)stream)
+                                : launch_scatter(a, p->num_sms, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "ep_dispatch_scatter: launch");
     p->routed = false;
     p->live = true;
@@ -350,9 +368,13 @@ int ep_dispatch(ep_plan* p, const void* x, const float* weights, const float* sc
     // check the payload arguments before the routing kernel starts a new epoch
     if (!x || !aligned(x, 16)) return fail(EP_ERR_ARG, "x is NULL or not 16-byte aligned");
     if (weights && !aligned(weights, 4)) return fail(EP_ERR_ARG, "weights not 4-byte aligned");
-    if (p->sd > 0 && (!scales || !aligned(scales, 4)))
-        return fail(EP_ERR_ARG, "scale_dim=%d needs a 4-byte aligned scales array", p->sd);
-    if (p->sd == 0 && scales) return fail(EP_ERR_ARG, "scales given but the plan has scale_dim 0");
+    if (p->quantise) {
+        if (scales) return fail(EP_ERR_ARG, "the quantising dtype computes its scales: pass NULL");
+    } else {
+        if (p->sd > 0 && (!scales || !aligned(scales, 4)))
+            return fail(EP_ERR_ARG, "scale_dim=%d needs a 4-byte aligned scales array", p->sd);
+        if (p->sd == 0 && scales) return fail(EP_ERR_ARG, "scales given but the plan has scale_dim 0");
+    }
     if (!out) return fail(EP_ERR_ARG, "out is NULL");
     int rc = ep_dispatch_route(p, indices, n_tok_host, stream, nullptr);
     if (rc != EP_OK) return rc;

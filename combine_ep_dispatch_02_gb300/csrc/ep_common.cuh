@@ -80,6 +80,9 @@ struct CombineArgs {
 // Host-side launchers, one per kernel translation unit.
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t stream);
 cudaError_t launch_scatter(const ScatterArgs& a, int num_sms, cudaStream_t stream);
+// BF16 rows in, FP8 e4m3 rows + FP32 scales (one per 128 elements) out.  Here a.row_bytes is
+// the FP8 row (= H), a.chunk_bytes the slice in ELEMENTS (a multiple of 128) and a.sd = H/128.
+cudaError_t launch_scatter_quant(const ScatterArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_combine(const CombineArgs& a, bool fp16, int num_sms, cudaStream_t stream);
 // choose combine's slice of a row per work unit (a.H and a.N set)
 void combine_geometry(CombineArgs& a, int variant, int num_sms);

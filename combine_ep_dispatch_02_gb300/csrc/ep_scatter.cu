@@ -75,7 +75,139 @@ __global__ void __launch_bounds__(kCopyThreads) ep_scatter_kernel(const ScatterA
     }
 }
 
+// ---- quantising scatter: BF16 source rows -> FP8 e4m3 rows + one FP32 scale per 128 elements
+
+constexpr int kQUnroll = 2;   // 32-byte source pieces per lane in flight per step
+
+// Two floats -> two e4m3 codes (round to nearest even, saturating to +-448); lo in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi)
+{
+    unsigned short r;
+    asm("{ .reg .b16 t; cvt.rn.satfinite.e4m3x2.f32 t, %1, %2; mov.b16 %0, t; }"
+        : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Quantise one lane's 16 consecutive BF16 values (two 16-byte vectors) with the block scale:
+// q = e4m3(x / scale), FP32 division rounded to nearest even.
+__device__ __forceinline__ uint4 quantise16(const uint4& a, const uint4& b, float scale)
+{
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t p0 = e4m3x2(__fdiv_rn(bf16_lo(w[2 * i]), scale), __fdiv_rn(bf16_hi(w[2 * i]), scale));
+        const uint32_t p1 =
+            e4m3x2(__fdiv_rn(bf16_lo(w[2 * i + 1]), scale), __fdiv_rn(bf16_hi(w[2 * i + 1]), scale));
+        o[i] = p0 | (p1 << 16);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__device__ __forceinline__ float absmax16(const uint4& a, const uint4& b)
+{
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    float m = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+    return m;
+}
+
+// A lane owns 16 consecutive elements (32 source bytes, 16 code bytes); the 8 lanes of a 128-
+// element block agree on its maximum by shuffles, so each block's scale is computed once per
+// token and its codes are written to every destination row.  Slices are multiples of 128.
+__global__ void __launch_bounds__(kCopyThreads, 3) ep_scatter_quant_kernel(const ScatterArgs a)
+{
+    __shared__ int s_off[kMaxRanks + 1];
+    if (threadIdx.x <= a.W) s_off[threadIdx.x] = a.tok_off[threadIdx.x];
+    __syncthreads();
+
+    const int lane = threadIdx.x & 31;
+    const int64_t warps_per_grid = (int64_t)gridDim.x * (kCopyThreads / 32);
+    const int64_t units = (int64_t)a.N * a.chunks;
+    const int64_t H = a.row_bytes;              // FP8 payload: one byte per element
+    for (int64_t u = (int64_t)blockIdx.x * (kCopyThreads / 32) + (threadIdx.x >> 5); u < units;
+         u += warps_per_grid) {
+        const int g = (int)(u / a.chunks);
+        const int c = (int)(u - (int64_t)g * a.chunks);
+        const int s = rank_of_token(s_off, a.W, g);
+        const int64_t tok = (int64_t)s * a.M + (g - s_off[s]);
+        const int dest = lane < a.F ? __ldg(a.fwd + tok * a.F + lane) : -1;
+        const int nd = __popc(__ballot_sync(0xffffffffu, dest >= 0));
+
+        const int64_t h0 = (int64_t)c * a.chunk_bytes;               // elements
+        const int64_t rem = H - h0;
+        const int npiece = (int)((rem < a.chunk_bytes ? rem : a.chunk_bytes) >> 4);   // 16-element pieces
+        const uint8_t* src = a.x + (tok * H + h0) * 2;
+        for (int p0 = 0; p0 < npiece; p0 += 32 * kQUnroll) {         // warp-uniform bounds
+            uint4 in[kQUnroll][2];
+#pragma unroll
+            for (int q = 0; q < kQUnroll; ++q) {
+                const int p = p0 + q * 32 + lane;
+                if (p < npiece) {
+                    in[q][0] = ld_stream_v4(src + (int64_t)p * 32);
+                    in[q][1] = ld_stream_v4(src + (int64_t)p * 32 + 16);
+                }
+            }
+            uint4 code[kQUnroll];
+            float scale[kQUnroll];
+#pragma unroll
+            for (int q = 0; q < kQUnroll; ++q) {
+                const int p = p0 + q * 32 + lane;
+                float m = p < npiece ? absmax16(in[q][0], in[q][1]) : 0.0f;
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+                scale[q] = m > 0.0f ? __fdiv_rn(m, 448.0f) : 1.0f;
+                if (p < npiece) code[q] = quantise16(in[q][0], in[q][1], scale[q]);
+            }
+            for (int d = 0; d < nd; ++d) {
+                const int64_t row = __shfl_sync(0xffffffffu, dest, d);
+                uint8_t* dst = a.recv_x + row * H + h0;
+                float* dsc = a.recv_scales + row * a.sd + (h0 >> 7);
+#pragma unroll
+                for (int q = 0; q < kQUnroll; ++q) {
+                    const int p = p0 + q * 32 + lane;
+                    if (p < npiece) {
+                        st_v4(dst + (int64_t)p * 16, code[q]);
+                        if ((lane & 7) == 0) dsc[p >> 3] = scale[q];
+                    }
+                }
+            }
+        }
+
+        if (c == 0) {
+            for (int d = 0; d < nd; ++d) {
+                const int64_t row = __shfl_sync(0xffffffffu, dest, d);
+                for (int e = lane; e < a.k; e += 32) {
+                    a.recv_idx[row * a.k + e] = __ldg(a.idx + tok * a.k + e);
+                    if (a.w) a.recv_w[row * a.k + e] = __ldg(a.w + tok * a.k + e);
+                }
+            }
+        }
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_scatter_quant(const ScatterArgs& a, int num_sms, cudaStream_t stream)
+{
+    const int64_t units = (int64_t)a.N * a.chunks;
+    if (units == 0) return cudaSuccess;
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ep_scatter_quant_kernel,
+                                                                  kCopyThreads, 0);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    const int64_t need = (units + kCopyThreads / 32 - 1) / (kCopyThreads / 32);
+    const int64_t cap = (int64_t)per_sm * num_sms;
+    const int grid = (int)(need < cap ? need : cap);
+    ep_scatter_quant_kernel<<<grid, kCopyThreads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_scatter(const ScatterArgs& a, int num_sms, cudaStream_t stream)
 {

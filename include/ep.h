@@ -45,8 +45,20 @@ extern "C" {
 
 typedef struct ep_plan ep_plan; /* opaque; created and owned by the library */
 
-/* payload dtypes (the guide's data_type field) */
-enum ep_dtype { EP_BF16 = 0, EP_FP16 = 1, EP_FP8_E4M3 = 2 };
+/* Payload dtypes (the guide's data_type field).
+ *   EP_BF16, EP_FP16        16-bit payload, moved bit for bit; combine output in the same type.
+ *   EP_FP8_E4M3             FP8 e4m3 payload with caller-supplied FP32 scale rows (scale_dim of
+ *                           them), moved bit for bit; combine takes and returns BF16.
+ *   EP_BF16_TO_FP8_E4M3     BF16 input, quantised by dispatch itself to FP8 e4m3 with one FP32
+ *                           scale per 128 elements (the FP8 wire of the guide's tuning matrix):
+ *                           for each block, scale = max|x| / 448 (1 for an all-zero block) and
+ *                           code = e4m3(x / scale), both FP32 divisions rounded to nearest even,
+ *                           the cast rounding to nearest even and saturating at +-448.  hidden
+ *                           must be a multiple of 128; the plan's scale_dim is hidden / 128
+ *                           (pass 0 or hidden / 128).  Dispatch takes no scales; recv_x holds
+ *                           the codes and recv_scales the scales.  Combine takes and returns
+ *                           BF16 (the expert dequantises). */
+enum ep_dtype { EP_BF16 = 0, EP_FP16 = 1, EP_FP8_E4M3 = 2, EP_BF16_TO_FP8_E4M3 = 3 };
 
 enum ep_status_code {
     EP_OK = 0,
@@ -107,9 +119,11 @@ size_t ep_plan_device_bytes(int W, int experts_per_rank, int topk, int hidden, i
 
 /*
  * Dispatch (guide, dispatch(); gfx1201 PR, Dispatch bullet).
- *   x           [W][M][H] payload elements, 16-byte aligned; rows t >= n_tok[s] are not read
+ *   x           [W][M][H] payload elements (BF16 for EP_BF16_TO_FP8_E4M3), 16-byte aligned;
+ *               rows t >= n_tok[s] are not read
  *   weights     [W][M][k] FP32 or NULL
- *   scales      [W][M][sd] FP32; must be NULL iff sd == 0
+ *   scales      [W][M][sd] FP32; must be NULL iff sd == 0 (always NULL for
+ *               EP_BF16_TO_FP8_E4M3, whose scales dispatch computes)
  *   indices     [W][M][k] int32 expert ids
  *   n_tok_host  host [W]: tokens on each source rank, each 0..M (EP_ERR_CAPACITY if above M)
  *   out         host: receives views of the plan's buffers and the dispatch epoch

@@ -17,8 +17,9 @@ def to_device(wl, dev):
     return x, w, sc, idx
 
 
-def make_plan(wl, dev, variant="auto"):
-    plan = ep.Plan(wl.W, wl.E, wl.k, wl.H, wl.dtype, wl.sd, wl.M, device=dev)
+def make_plan(wl, dev, variant="auto", plan_dtype=None):
+    plan = ep.Plan(wl.W, wl.E, wl.k, wl.H, plan_dtype or wl.dtype, 0 if plan_dtype else wl.sd,
+                   wl.M, device=dev)
     plan.set_variant(variant)
     return plan
 
@@ -33,6 +34,14 @@ def poison(plan, dev):
     plan.reset()
 
 
+def quantised_view(wl, q=None, scales=None):
+    """The workload as the receiving side sees it after a quantising dispatch: FP8 rows and one
+    FP32 scale per 128 elements (q / scales: the oracle's codes, when they are needed)."""
+    from combine_ep_dispatch_02_gb300 import workloads as wlmod
+    return wlmod.Workload(**{**wl.__dict__, "dtype": "fp8", "sd": wl.H // 128,
+                             "x": wl.x if q is None else q, "scales": scales})
+
+
 def raw(t):
     if t is None:
         return None
@@ -43,15 +52,18 @@ def raw(t):
     return t.cpu().numpy()
 
 
-def run(wl, dev, variant="auto", plan=None, do_poison=True):
+def run(wl, dev, variant="auto", plan=None, do_poison=True, quantise=False):
+    """quantise=True: a BF16 workload through the quantising dtype; the expert then sees FP8
+    rows with one scale per 128 elements (dequantising identity)."""
     own = plan is None
     if own:
-        plan = make_plan(wl, dev, variant)
+        plan = make_plan(wl, dev, variant, "bf16_fp8" if quantise else None)
     if do_poison:
         poison(plan, dev)
     x, w, sc, idx = to_device(wl, dev)
     d = plan.dispatch(x, w, sc, idx, wl.n_tok)
-    eo = harness.expert_torch(wl, d.recv_x, d.recv_idx, d.recv_w, d.recv_scales, d.recv_count)
+    wl_e = quantised_view(wl) if quantise else wl
+    eo = harness.expert_torch(wl_e, d.recv_x, d.recv_idx, d.recv_w, d.recv_scales, d.recv_count)
     out, out_w = plan.combine(eo, d.recv_w, d.epoch)
     torch.cuda.synchronize()
     res = {

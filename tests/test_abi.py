@@ -62,7 +62,7 @@ def test_device_bytes_golden(lib):
     ((0, 4, 2, 256, 0, 0, 64), "W"), ((33, 4, 2, 256, 0, 0, 64), "W"),
     ((2, 0, 2, 256, 0, 0, 64), "experts_per_rank"), ((2, 4, 0, 256, 0, 0, 64), "topk"),
     ((2, 4, 65, 256, 0, 0, 64), "topk"), ((2, 4, 2, 4, 0, 0, 64), "hidden"),
-    ((2, 4, 2, 8, 2, 0, 64), "hidden"), ((2, 4, 2, 256, 3, 0, 64), "dtype"),
+    ((2, 4, 2, 8, 2, 0, 64), "hidden"), ((2, 4, 2, 256, 4, 0, 64), "dtype"),
     ((2, 4, 2, 256, 0, -1, 64), "scale_dim"), ((2, 4, 2, 256, 0, 0, 0), "max_tok"),
     ((32, 4, 2, 256, 0, 0, 1 << 21), "2^31"),
 ])
@@ -92,3 +92,15 @@ def test_null_plan_calls_fail_cleanly(lib):
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(RuntimeError):
         ep.load_library(str(tmp_path / "missing" / "libep.so"))
+
+
+def test_quantising_dtype_sizes_and_shape_checks(lib):
+    # BF16 input quantised to FP8 on the wire: 1-byte payload rows and hidden/128 scales per row
+    for sd in (0, 56):
+        assert lib.ep_plan_device_bytes(8, 32, 8, 7168, ep.EP_BF16_TO_FP8_E4M3, sd, 4096) == \
+            _layout_bytes(8, 32, 8, 7168, 1, 56, 4096)
+    h = ctypes.c_void_p()
+    assert lib.ep_plan_create(ctypes.byref(h), 8, 32, 8, 7168 + 64, ep.EP_BF16_TO_FP8_E4M3, 0, 16) == ep.EP_ERR_ARG
+    assert "128" in lib.ep_last_error().decode()
+    assert lib.ep_plan_create(ctypes.byref(h), 8, 32, 8, 7168, ep.EP_BF16_TO_FP8_E4M3, 3, 16) == ep.EP_ERR_ARG
+    assert "scale" in lib.ep_last_error().decode()

@@ -293,3 +293,41 @@ def test_cuda_graph_replay_matches_eager():
         assert np.array_equal(out_w.cpu().numpy().view(np.uint32), o_w.view(np.uint32))
     assert plan.status() == 0
     plan.close()
+
+
+# ---------------------------------------------------------------- quantising FP8 dispatch
+
+def _check_quantised(wl, variant="auto"):
+    disp = oracle.dispatch_quantized(wl)
+    q, sc = oracle.quantize_e4m3_blockwise(wl.x)
+    wq = gpu_path.quantised_view(wl, q, sc)
+    eo = harness.expert_np(wq, disp)
+    o_out, o_w = oracle.combine(wl.W, wl.k, wl.H, False, wl.M, wl.n_tok, disp["slot_of"], eo,
+                                disp["recv_w"])
+    gpu = gpu_path.run(wl, DEV, variant, quantise=True)
+    gpu_path.compare(wq, gpu, disp, o_out, o_w)
+
+
+def test_quantised_dispatch_dsv3_reduced():
+    _check_quantised(wlmod.make_workload("dsv3", max_tok=300))
+
+
+@pytest.mark.parametrize("variant", ["tiled_512", "tiled_1024", "whole_row"])
+def test_quantised_dispatch_small_variants(variant):
+    _check_quantised(wlmod.make_workload("small", max_tok=64), variant)
+
+
+def test_quantised_dispatch_dsv3_full():
+    _check_quantised(wlmod.make_workload("dsv3"))
+
+
+def test_quantised_dispatch_edge_values():
+    wl = wlmod.custom_workload(W=4, E=4, k=3, H=384, M=40, n_tok=[40, 0, 17, 33], seed=9)
+    xf = (wl.x.astype(np.uint32) << 16).view(np.float32).copy()
+    xf[0, 0] = 0.0                                   # all-zero rows and blocks
+    xf[0, 1, 128:256] = 0.0
+    xf[2, 3] *= np.float32(1e-30)                    # values the scale must lift out of underflow
+    xf[2, 4, :128] = np.float32(3e38)                # huge values
+    xf[3, 5, 7] = -0.0
+    wl.x[:] = torch.from_numpy(xf).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    _check_quantised(wl)
