@@ -232,6 +232,8 @@ def run_ours(args, rank, world, dist):
 
     # end to end through the public API: pinned host inputs in, results back to pinned host
     e2e = measure_e2e(plan, wl, dev, stream, nbytes["pair"], steps=max(3, min(args.steps, 20)))
+    quant = measure_quantised_dispatch(ep, wl, dev, stream, x, w, idx, P, peak,
+                                       steps=max(3, min(args.steps, 50)))
     if plan.status() != 0:
         raise RuntimeError("device status after timing: %d" % plan.status())
 
@@ -273,9 +275,41 @@ def run_ours(args, rank, world, dist):
             "e2e": e2e,
             "gpu_launches": 3 * args.steps,
             "cpu_baseline": cpu,
+            "fp8_quantising_dispatch": quant,
         }
     plan.close()
     return result
+
+
+def measure_quantised_dispatch(ep, wl, dev, stream, x, w, idx, P, peak, steps):
+    """Dispatch of the same BF16 tokens through the quantising dtype: FP8 e4m3 rows and one FP32
+    scale per 128 elements are written instead of BF16 rows.  Minimal bytes: read N*(2H + 8k),
+    write P*(H + 4H/128 + 8k + 4)."""
+    plan = ep.Plan(wl.W, wl.E, wl.k, wl.H, "bf16_fp8", 0, wl.M, device=dev)
+    for _ in range(3):
+        plan.dispatch(x, w, None, idx, wl.n_tok, stream=stream)
+    torch.cuda.synchronize(dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for e in ev:
+        e[0].record(stream)
+        plan.dispatch_route(idx, wl.n_tok, stream=stream)
+        e[1].record(stream)
+        plan.dispatch_scatter(x, w, None, idx, stream=stream)
+        e[2].record(stream)
+    torch.cuda.synchronize(dev)
+    if plan.status() != 0:
+        raise RuntimeError("device status after the quantising dispatch: %d" % plan.status())
+    plan.close()
+    route = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
+    scat = sum(e[1].elapsed_time(e[2]) for e in ev) / steps
+    N, H, k = wl.N, wl.H, wl.k
+    nb = N * (2 * H + 8 * k) + P * (H + 4 * (H // 128) + 8 * k + 4)
+    nb_scatter = N * (2 * H + 8 * k) + P * (H + 4 * (H // 128) + 8 * k)
+    return {"dispatch_us": round((route + scat) * 1e3, 2), "route_us": round(route * 1e3, 2),
+            "scatter_us": round(scat * 1e3, 2), "algorithmic_bytes": nb,
+            "dispatch_gbs": round(nb / ((route + scat) * 1e-3) / 1e9, 1),
+            "scatter_frac": round(nb_scatter / (scat * 1e-3) / 1e9 / peak, 4),
+            "dispatch_frac": round(nb / ((route + scat) * 1e-3) / 1e9 / peak, 4)}
 
 
 def measure_e2e(plan, wl, dev, stream, pair_bytes, steps):
