@@ -49,6 +49,8 @@ def _load():
             lib.ep_oracle_dispatch.argtypes = [ctypes.c_int] * 7 + [_p] * 12
             lib.ep_oracle_combine.restype = ctypes.c_int
             lib.ep_oracle_combine.argtypes = [ctypes.c_int] * 5 + [_p] * 6
+            lib.ep_oracle_combine_fp8.restype = ctypes.c_int
+            lib.ep_oracle_combine_fp8.argtypes = [ctypes.c_int] * 4 + [_p] * 7
             lib.ep_oracle_quantize_e4m3_blockwise.restype = ctypes.c_int
             lib.ep_oracle_quantize_e4m3_blockwise.argtypes = [ctypes.c_int64, ctypes.c_int, _p, _p, _p]
             for name in ("ep_oracle_bf16_from_f32_array", "ep_oracle_f16_from_f32_array",
@@ -120,6 +122,23 @@ def combine(W, k, H, out_fp16, M, n_tok, slot_of, expert_out, w_in=None, out=Non
                                _ptr(expert_out), _ptr(w_in), _ptr(out), _ptr(out_w))
     if st != 0:
         raise ValueError("ep_oracle_combine: invalid arguments")
+    return out, out_w
+
+
+def combine_fp8(W, k, H, M, n_tok, slot_of, q, scales, w_in=None):
+    """Combine over an FP8 wire: each row's codes are dequantised as float(q) * scale (one FP32
+    multiply) and added in ascending rank order in FP32; BF16 RNE output.  Returns (out, out_w)."""
+    lib = _load()
+    n_tok = np.ascontiguousarray(n_tok, dtype=np.int32)
+    slot_of = np.ascontiguousarray(slot_of, dtype=np.int32)
+    q = np.ascontiguousarray(q).view(np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.float32)
+    out = np.zeros((W, M, H), dtype=np.uint16)
+    out_w = np.zeros((W, M, k), dtype=np.float32) if w_in is not None else None
+    w_in = None if w_in is None else np.ascontiguousarray(w_in, dtype=np.float32)
+    if lib.ep_oracle_combine_fp8(W, k, H, M, _ptr(n_tok), _ptr(slot_of), _ptr(q), _ptr(scales),
+                                 _ptr(w_in), _ptr(out), _ptr(out_w)) != 0:
+        raise ValueError("ep_oracle_combine_fp8: invalid arguments")
     return out, out_w
 
 

@@ -318,3 +318,51 @@ int ep_oracle_combine(int W, int k, int H, int out_fp16, int M, const int32_t* n
     free(accw);
     return EP_ORACLE_OK;
 }
+
+/* ---- Combine over an FP8 wire ------------------------------------------------------ */
+
+/*
+ * Combine of expert outputs sent as FP8 e4m3 codes with one FP32 scale per 128 elements (the
+ * fp8_blockwise combine of the MORI-EP gfx1250 EPv2 pages).  For each source token and element
+ * h: acc = +0.0f; for each destination rank r holding the token, ascending:
+ *   v = float(q[r][row][h]) * scales[r][row][h / 128]     (one FP32 multiply, rounded)
+ *   acc = acc + v                                         (one FP32 add, rounded)
+ * out = BF16 RNE of acc.  Weights, when given, are summed exactly as in ep_oracle_combine.
+ *   q [W][W*M][H] codes, scales [W][W*M][H/128], out [W][M][H] BF16 bits.
+ */
+int ep_oracle_combine_fp8(int W, int k, int H, int M, const int32_t* n_tok, const int32_t* slot_of,
+                          const uint8_t* q, const float* scales, const float* w_in, uint16_t* out,
+                          float* out_w)
+{
+    if (W < 1 || k < 1 || H < 128 || H % 128 != 0 || M < 1) return EP_ORACLE_ERR_ARG;
+    const int64_t rows = (int64_t)W * M;
+    const int nb = H / 128;
+    float* acc = (float*)malloc((size_t)H * sizeof(float));
+    float* accw = (float*)malloc((size_t)k * sizeof(float));
+    if (!acc || !accw) { free(acc); free(accw); return EP_ORACLE_ERR_ARG; }
+    for (int s = 0; s < W; ++s) {
+        for (int t = 0; t < n_tok[s]; ++t) {
+            const int64_t tok = (int64_t)s * M + t;
+            for (int h = 0; h < H; ++h) acc[h] = 0.0f;
+            for (int j = 0; j < k; ++j) accw[j] = 0.0f;
+            for (int r = 0; r < W; ++r) {
+                const int32_t slot = slot_of[tok * W + r];
+                if (slot < 0) continue;
+                const int64_t row = (int64_t)r * rows + slot;
+                for (int h = 0; h < H; ++h) {
+                    float v = ep_oracle_f32_from_e4m3(q[row * H + h]) * scales[row * nb + h / 128];
+                    acc[h] = acc[h] + v;
+                }
+                if (w_in)
+                    for (int j = 0; j < k; ++j) accw[j] = accw[j] + w_in[row * k + j];
+            }
+            for (int h = 0; h < H; ++h) out[tok * H + h] = ep_oracle_bf16_from_f32(acc[h]);
+            if (w_in && out_w)
+                for (int j = 0; j < k; ++j) out_w[tok * k + j] = accw[j];
+        }
+    }
+    free(acc);
+    free(accw);
+    return EP_ORACLE_OK;
+}
+

@@ -403,3 +403,57 @@ def test_quantised_dispatch_routes_quantised_rows():
     q, sc = oracle.quantize_e4m3_blockwise(wl.x)
     wq = wlmod.Workload(**{**wl.__dict__, "x": q, "dtype": "fp8", "sd": wl.H // 128, "scales": sc})
     _check_dispatch(wq, disp)
+
+
+# ---------------------------------------------------------------- FP8 combine wire (next row F2)
+
+def _fp8_wire_case(seed, W=4, E=4, k=3, H=256, M=12, n_tok=(12, 5, 0, 9)):
+    wl = wlmod.custom_workload(W=W, E=E, k=k, H=H, M=M, n_tok=list(n_tok), seed=seed)
+    disp = _run(wl)
+    q, sc = oracle.quantize_e4m3_blockwise(disp["recv_x"])
+    return wl, disp, q, sc
+
+
+def test_fp8_combine_single_row_is_dequantised_row():
+    """|D| = 1: out = BF16(float(q) * scale), with torch's e4m3 decode and an FP32 multiply."""
+    wl = wlmod.custom_workload(W=3, E=5, k=1, H=256, M=10, n_tok=[10, 4, 7], seed=2)
+    disp = _run(wl)
+    q, sc = oracle.quantize_e4m3_blockwise(disp["recv_x"])
+    out, _ = oracle.combine_fp8(wl.W, wl.k, wl.H, wl.M, wl.n_tok, disp["slot_of"], q, sc)
+    deq = torch.from_numpy(q).view(torch.float8_e4m3fn).to(torch.float32) * \
+        torch.from_numpy(np.repeat(sc, 128, axis=-1))
+    ref = deq.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    for s in range(wl.W):
+        for t in range(int(wl.n_tok[s])):
+            r = int(wl.indices[s, t, 0]) // wl.E
+            assert np.array_equal(out[s, t], ref[r, disp["slot_of"][s, t, r]])
+
+
+def test_fp8_combine_power_of_two_scales_closed_form():
+    """Scales that are powers of two make every product and partial sum exact (codes carry 4
+    significant bits): out = BF16(sum over ranks of float(q) * scale), computed in float64."""
+    wl, disp, q, sc = _fp8_wire_case(5)
+    rng = np.random.default_rng(0)
+    sc = (2.0 ** rng.integers(-6, 6, size=sc.shape)).astype(np.float32)
+    out, _ = oracle.combine_fp8(wl.W, wl.k, wl.H, wl.M, wl.n_tok, disp["slot_of"], q, sc)
+    deq = oracle.f32_from_e4m3(q).astype(np.float64) * np.repeat(sc, 128, axis=-1)
+    for s in range(wl.W):
+        for t in range(int(wl.n_tok[s])):
+            tot = np.zeros(wl.H)
+            for r in range(wl.W):
+                if disp["slot_of"][s, t, r] >= 0:
+                    tot += deq[r, disp["slot_of"][s, t, r]]
+            ref = torch.from_numpy(tot.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy()
+            assert np.array_equal(out[s, t].view(np.int16), ref)
+
+
+def test_fp8_combine_close_to_bf16_combine():
+    """Sanity (not a parity criterion): the FP8 wire moves each term by at most 2^-4 relative,
+    so the FP8 combine stays within that of the BF16 combine of the same rows."""
+    wl, disp, q, sc = _fp8_wire_case(8, W=8, E=2, k=6, H=384, M=20, n_tok=[20] * 8)
+    out8, _ = oracle.combine_fp8(wl.W, wl.k, wl.H, wl.M, wl.n_tok, disp["slot_of"], q, sc)
+    out16, _ = oracle.combine(wl.W, wl.k, wl.H, False, wl.M, wl.n_tok, disp["slot_of"], disp["recv_x"])
+    a = (out8.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    b = (out16.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    amax = np.abs(b).max()
+    assert np.all(np.abs(a - b) <= 2.0 ** -4 * np.abs(b) + 2.0 ** -3 * amax * 2.0 ** -7)
