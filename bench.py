@@ -234,6 +234,8 @@ def run_ours(args, rank, world, dist):
     e2e = measure_e2e(plan, wl, dev, stream, nbytes["pair"], steps=max(3, min(args.steps, 20)))
     quant = measure_quantised_dispatch(ep, wl, dev, stream, x, w, idx, P, peak,
                                        steps=max(3, min(args.steps, 50)))
+    wire = measure_fp8_combine_wire(plan, wl, dev, stream, x, w, idx, P, peak,
+                                    steps=max(3, min(args.steps, 50)))
     if plan.status() != 0:
         raise RuntimeError("device status after timing: %d" % plan.status())
 
@@ -276,6 +278,7 @@ def run_ours(args, rank, world, dist):
             "gpu_launches": 3 * args.steps,
             "cpu_baseline": cpu,
             "fp8_quantising_dispatch": quant,
+            "fp8_combine_wire": wire,
         }
     plan.close()
     return result
@@ -310,6 +313,40 @@ def measure_quantised_dispatch(ep, wl, dev, stream, x, w, idx, P, peak, steps):
             "dispatch_gbs": round(nb / ((route + scat) * 1e-3) / 1e9, 1),
             "scatter_frac": round(nb_scatter / (scat * 1e-3) / 1e9 / peak, 4),
             "dispatch_frac": round(nb / ((route + scat) * 1e-3) / 1e9 / peak, 4)}
+
+
+def measure_fp8_combine_wire(plan, wl, dev, stream, x, w, idx, P, peak, steps):
+    """Combine over the FP8 wire: the received expert rows (identity expert) are quantised once
+    per step, and the gather-reduce reads codes + scales.  Minimal bytes: quantise reads P*2H and
+    writes P*(H + 4H/128); combine reads P*(H + 4H/128 + 4k) + N*4*min(W,k) and writes
+    N*(2H + 4k)."""
+    d = plan.dispatch(x, w, None, idx, wl.n_tok, stream=stream)
+    q, sc = plan.quantize_received(d.recv_x, d.epoch, stream=stream)
+    out = torch.empty((wl.W, wl.M, wl.H), dtype=torch.bfloat16, device=dev)
+    out_w = torch.empty((wl.W, wl.M, wl.k), dtype=torch.float32, device=dev)
+    for _ in range(3):
+        plan.quantize_received(d.recv_x, d.epoch, q=q.view(torch.uint8), scales=sc, stream=stream)
+        plan.combine_fp8(q, sc, d.recv_w, d.epoch, out=out, out_w=out_w, stream=stream)
+    torch.cuda.synchronize(dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for e in ev:
+        e[0].record(stream)
+        plan.quantize_received(d.recv_x, d.epoch, q=q.view(torch.uint8), scales=sc, stream=stream)
+        e[1].record(stream)
+        plan.combine_fp8(q, sc, d.recv_w, d.epoch, out=out, out_w=out_w, stream=stream)
+        e[2].record(stream)
+    torch.cuda.synchronize(dev)
+    if plan.status() != 0:
+        raise RuntimeError("device status after the FP8 combine wire: %d" % plan.status())
+    qt = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
+    ct = sum(e[1].elapsed_time(e[2]) for e in ev) / steps
+    N, H, k, F = wl.N, wl.H, wl.k, min(wl.W, wl.k)
+    qb = P * (2 * H + H + 4 * (H // 128))
+    cb = P * (H + 4 * (H // 128) + 4 * k) + N * 4 * F + N * (2 * H + 4 * k)
+    return {"quantize_us": round(qt * 1e3, 2), "combine_us": round(ct * 1e3, 2),
+            "combine_algorithmic_bytes": cb, "combine_gbs": round(cb / (ct * 1e-3) / 1e9, 1),
+            "combine_frac": round(cb / (ct * 1e-3) / 1e9 / peak, 4),
+            "quantize_frac": round(qb / (qt * 1e-3) / 1e9 / peak, 4)}
 
 
 def measure_e2e(plan, wl, dev, stream, pair_bytes, steps):

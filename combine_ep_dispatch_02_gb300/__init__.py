@@ -28,7 +28,8 @@ VARIANTS = {"auto": 0, "whole_row": 1, "tiled_512": 2, "tiled_1024": 3}
 # every entry point include/ep.h declares
 EXPORTS = ("ep_plan_create", "ep_plan_destroy", "ep_plan_set_variant", "ep_plan_device_bytes",
            "ep_dispatch", "ep_dispatch_route", "ep_dispatch_scatter", "ep_combine", "ep_reset",
-           "ep_status", "ep_strerror", "ep_last_error", "ep_route_noalloc")
+           "ep_status", "ep_strerror", "ep_last_error", "ep_route_noalloc",
+           "ep_quantize_received", "ep_combine_fp8")
 
 
 class EpError(RuntimeError):
@@ -72,6 +73,8 @@ def load_library(path: Optional[str] = None):
         "ep_strerror": (ctypes.c_char_p, [I]),
         "ep_last_error": (ctypes.c_char_p, []),
         "ep_route_noalloc": (I, [I, I, I, I, V, V, V, V, V, V, V]),
+        "ep_quantize_received": (I, [V, V, V, V, U64, V]),
+        "ep_combine_fp8": (I, [V, V, V, V, V, V, U64, V]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -245,6 +248,30 @@ class Plan:
             out_w = torch.zeros((self.W, self.M, self.k), dtype=torch.float32, device=self.device)
         _check(self._lib.ep_combine(self._h, _ptr(expert_out), _ptr(weights), _ptr(out), _ptr(out_w),
                                     ctypes.c_uint64(epoch), _stream(stream)))
+        return out, out_w
+
+    def quantize_received(self, expert_out: torch.Tensor, epoch: int, q: Optional[torch.Tensor] = None,
+                          scales: Optional[torch.Tensor] = None, stream=None):
+        """Quantise the received BF16 expert rows block-wise to e4m3 codes + FP32 scales (the
+        FP8 combine wire); returns (q [W][W*M][H] float8_e4m3fn, scales [W][W*M][H/128])."""
+        if q is None:
+            q = torch.empty((self.W, self.rows, self.H), dtype=torch.uint8, device=self.device)
+        if scales is None:
+            scales = torch.empty((self.W, self.rows, self.H // 128), dtype=torch.float32, device=self.device)
+        _check(self._lib.ep_quantize_received(self._h, _ptr(expert_out), _ptr(q), _ptr(scales),
+                                              ctypes.c_uint64(epoch), _stream(stream)))
+        return q.view(torch.float8_e4m3fn), scales
+
+    def combine_fp8(self, q: torch.Tensor, scales: torch.Tensor, weights: Optional[torch.Tensor],
+                    epoch: int, out: Optional[torch.Tensor] = None, out_w: Optional[torch.Tensor] = None,
+                    want_weights: bool = True, stream=None):
+        """Combine over the FP8 wire; returns (out [W][M][H] BF16, out_w or None)."""
+        if out is None:
+            out = torch.zeros((self.W, self.M, self.H), dtype=torch.bfloat16, device=self.device)
+        if out_w is None and weights is not None and want_weights:
+            out_w = torch.zeros((self.W, self.M, self.k), dtype=torch.float32, device=self.device)
+        _check(self._lib.ep_combine_fp8(self._h, _ptr(q), _ptr(scales), _ptr(weights), _ptr(out),
+                                        _ptr(out_w), ctypes.c_uint64(epoch), _stream(stream)))
         return out, out_w
 
     def reset(self, stream=None):

@@ -15,6 +15,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "ep.h"
@@ -77,6 +78,23 @@ struct CombineArgs {
     int tok_off[kMaxRanks + 1];
 };
 
+// Quantising the received expert rows, and combine over the resulting FP8 wire.
+struct WireArgs {
+    const uint16_t* eo;       // [W][W*M][H] BF16 expert outputs (quantise)
+    uint8_t* q;               // [W][W*M][H] e4m3 codes (quantise: out; combine: in)
+    float* scales;            // [W][W*M][H/128] (quantise: out; combine: in)
+    const int32_t* recv_count;
+    const int32_t* fwd;
+    const float* w_in;
+    uint16_t* out;            // [W][M][H] BF16
+    float* out_w;
+    int64_t H, rows;          // rows = W*M per rank
+    int W, k, F, M, N;
+    int chunk_pieces;         // 16-element pieces of one combine unit's slice
+    int chunks;
+    int tok_off[kMaxRanks + 1];
+};
+
 // Host-side launchers, one per kernel translation unit.
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t stream);
 cudaError_t launch_scatter(const ScatterArgs& a, int num_sms, cudaStream_t stream);
@@ -84,6 +102,8 @@ cudaError_t launch_scatter(const ScatterArgs& a, int num_sms, cudaStream_t strea
 // the FP8 row (= H), a.chunk_bytes the slice in ELEMENTS (a multiple of 128) and a.sd = H/128.
 cudaError_t launch_scatter_quant(const ScatterArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_combine(const CombineArgs& a, bool fp16, int num_sms, cudaStream_t stream);
+cudaError_t launch_quantise_rows(const WireArgs& a, int num_sms, cudaStream_t stream);
+cudaError_t launch_combine_fp8(const WireArgs& a, int num_sms, cudaStream_t stream);
 // choose combine's slice of a row per work unit (a.H and a.N set)
 void combine_geometry(CombineArgs& a, int variant, int num_sms);
 
@@ -212,6 +232,54 @@ __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src)
 __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar)
 {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(bar) : "memory");
+}
+
+// ---- FP8 e4m3 block quantisation (one FP32 scale per 128 elements)
+
+// Two floats -> two e4m3 codes (round to nearest even, saturating to +-448); lo in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi)
+{
+    unsigned short r;
+    asm("{ .reg .b16 t; cvt.rn.satfinite.e4m3x2.f32 t, %1, %2; mov.b16 %0, t; }"
+        : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Quantise one lane's 16 consecutive BF16 values (two 16-byte vectors) with the block scale:
+// q = e4m3(x / scale), FP32 division rounded to nearest even.
+__device__ __forceinline__ uint4 quantise16(const uint4& a, const uint4& b, float scale)
+{
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t p0 = e4m3x2(__fdiv_rn(bf16_lo(w[2 * i]), scale), __fdiv_rn(bf16_hi(w[2 * i]), scale));
+        const uint32_t p1 =
+            e4m3x2(__fdiv_rn(bf16_lo(w[2 * i + 1]), scale), __fdiv_rn(bf16_hi(w[2 * i + 1]), scale));
+        o[i] = p0 | (p1 << 16);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__device__ __forceinline__ float absmax16(const uint4& a, const uint4& b)
+{
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    float m = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+    return m;
+}
+
+// Two e4m3 codes (low byte first) -> two exact floats, via the exact e4m3 -> f16 conversion.
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two_codes)
+{
+    uint32_t h2;
+    asm("{ .reg .b16 c; cvt.u16.u32 c, %1; cvt.rn.f16x2.e4m3x2 %0, c; }" : "=r"(h2) : "r"(two_codes));
+    const __half2 h = *reinterpret_cast<const __half2*>(&h2);
+    return __half22float2(h);
 }
 
 __device__ __forceinline__ unsigned lanemask_lt()

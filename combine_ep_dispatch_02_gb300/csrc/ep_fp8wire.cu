@@ -1,0 +1,237 @@
+// ep_fp8wire.cu -- combine over an FP8 wire.
+//
+// The MORI-EP gfx1250 EPv2 pages send combine contributions at low precision ("fp8 push
+// combine (fp8_blockwise)"; fp4 push combine: producers "load bf16 rows and quantize them",
+// the source dequantises and reduces).  Here the expert-output rows of the live dispatch are
+// quantised block-wise to FP8 e4m3 (one FP32 scale per 128 elements, the same quantiser as the
+// quantising dispatch), and the gather-reduce reads those codes: for every source token, in
+// ascending rank order, v = float(code) * scale (one FP32 multiply) is added in FP32, and the
+// sum is rounded to nearest even into BF16.  The gather then reads H + H/32 bytes per row
+// instead of 2H.
+#include <cuda_bf16.h>
+
+#include "ep_common.cuh"
+
+namespace ep {
+namespace {
+
+// ---- quantise the received expert rows: warp per row, lanes own 16-element pieces
+
+__global__ void __launch_bounds__(kCopyThreads, 3) ep_quantise_rows_kernel(const WireArgs a)
+{
+    __shared__ int s_cnt[kMaxRanks];
+    if (threadIdx.x < a.W) s_cnt[threadIdx.x] = a.recv_count[threadIdx.x];
+    __syncthreads();
+
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = (int64_t)gridDim.x * (kCopyThreads / 32);
+    const int npiece = (int)(a.H >> 4);
+    const int nb = (int)(a.H >> 7);
+    for (int64_t u = (int64_t)blockIdx.x * (kCopyThreads / 32) + (threadIdx.x >> 5);
+         u < (int64_t)a.W * a.rows; u += nwarps) {
+        const int r = (int)(u / a.rows);
+        const int64_t i = u - (int64_t)r * a.rows;
+        if (i >= s_cnt[r]) continue;                 // warp-uniform: only received rows
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(a.eo) + u * a.H * 2;
+        uint8_t* dq = a.q + u * a.H;
+        float* dsc = a.scales + u * nb;
+        for (int p0 = 0; p0 < npiece; p0 += 32) {   // warp-uniform bounds
+            const int p = p0 + lane;
+            uint4 x0 = make_uint4(0, 0, 0, 0), x1 = x0;
+            if (p < npiece) {
+                x0 = ld_stream_v4(src + (int64_t)p * 32);
+                x1 = ld_stream_v4(src + (int64_t)p * 32 + 16);
+            }
+            float m = absmax16(x0, x1);
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            const float scale = m > 0.0f ? __fdiv_rn(m, 448.0f) : 1.0f;
+            if (p < npiece) {
+                st_v4(dq + (int64_t)p * 16, quantise16(x0, x1, scale));
+                if ((lane & 7) == 0) dsc[p >> 3] = scale;
+            }
+        }
+    }
+}
+
+// ---- gather-reduce over the FP8 wire
+
+__device__ __forceinline__ void add_fp8x16(float (&acc)[16], const uint4& c, float scale)
+{
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 lo = e4m3x2_to_float2(w[i] & 0xFFFFu);
+        const float2 hi = e4m3x2_to_float2(w[i] >> 16);
+        acc[4 * i + 0] = __fadd_rn(acc[4 * i + 0], __fmul_rn(lo.x, scale));
+        acc[4 * i + 1] = __fadd_rn(acc[4 * i + 1], __fmul_rn(lo.y, scale));
+        acc[4 * i + 2] = __fadd_rn(acc[4 * i + 2], __fmul_rn(hi.x, scale));
+        acc[4 * i + 3] = __fadd_rn(acc[4 * i + 3], __fmul_rn(hi.y, scale));
+    }
+}
+
+__device__ __forceinline__ void store_bf16x16(uint4* dst, const float (&acc)[16])
+{
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+        w[i] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    st_v4(dst, make_uint4(w[0], w[1], w[2], w[3]));
+    st_v4(dst + 1, make_uint4(w[4], w[5], w[6], w[7]));
+}
+
+// Rolling fold of a unit's nd <= 8 rows (lane d of src holds row d): row d's load of the next
+// piece is issued as soon as its current piece is taken, so every lane keeps the token's rows
+// in flight.
+__device__ __forceinline__ void fold_fp8_rows(const WireArgs& a, int src, int nd, int p0, int np,
+                                              uint4* dst, int lane)
+{
+    const int64_t hp = a.H >> 4;
+    const uint4* q4 = reinterpret_cast<const uint4*>(a.q);
+    // piece offsets of the rows (receive buffer < 64 GB); a piece's scale sits at offset / 8,
+    // since a row has hp = 8 * nb pieces and slices start on multiples of 8 pieces
+    uint32_t ro[8];
+#pragma unroll
+    for (int d = 0; d < 8; ++d) ro[d] = (uint32_t)((int64_t)__shfl_sync(0xffffffffu, src, d) * hp + p0);
+    uint4 b[8];
+    float sc[8];
+#pragma unroll
+    for (int d = 0; d < 8; ++d)
+        if (d < nd && lane < np) {
+            b[d] = ld_stream_v4(q4 + ro[d] + lane);
+            sc[d] = __ldg(a.scales + ((ro[d] + lane) >> 3));
+        }
+    for (int vb = 0; vb < np; vb += 32) {         // warp-uniform bounds
+        const int pc = vb + lane;
+        const int pn = pc + 32;
+        float acc[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+#pragma unroll
+        for (int d = 0; d < 8; ++d) {
+            if (d < nd) {
+                const uint4 x = b[d];
+                const float xs = sc[d];
+                if (pn < np) {
+                    b[d] = ld_stream_v4(q4 + ro[d] + pn);
+                    sc[d] = __ldg(a.scales + ((ro[d] + pn) >> 3));
+                }
+                if (pc < np) add_fp8x16(acc, x, xs);
+            }
+        }
+        if (pc < np) store_bf16x16(dst + (int64_t)pc * 2, acc);
+    }
+}
+
+// More than 8 rows: one piece per lane at a time, rows in ascending batches of 8.
+__device__ __forceinline__ void fold_fp8_wide(const WireArgs& a, int src, int nd, int p0, int np,
+                                              uint4* dst, int lane)
+{
+    const int64_t hp = a.H >> 4;
+    const int64_t nb = a.H >> 7;
+    const uint4* q4 = reinterpret_cast<const uint4*>(a.q);
+    for (int vb = 0; vb < np; vb += 32) {
+        const int pc = vb + lane;
+        const bool act = pc < np;
+        float acc[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+        for (int d0 = 0; d0 < nd; d0 += 8) {
+            uint4 b[8];
+            float sc[8];
+#pragma unroll
+            for (int d = 0; d < 8; ++d) {
+                const int64_t row = __shfl_sync(0xffffffffu, src, (d0 + d) & 31);
+                if (act && d0 + d < nd) {
+                    b[d] = ld_stream_v4(q4 + row * hp + p0 + pc);
+                    sc[d] = __ldg(a.scales + row * nb + ((p0 + pc) >> 3));
+                }
+            }
+#pragma unroll
+            for (int d = 0; d < 8; ++d)
+                if (act && d0 + d < nd) add_fp8x16(acc, b[d], sc[d]);
+        }
+        if (act) store_bf16x16(dst + (int64_t)pc * 2, acc);
+    }
+}
+
+// A warp owns a (token, slice) unit; lanes own 16-element pieces (16 code bytes, 32 output
+// bytes).  Weight rows are summed as in the 16-bit combine.
+template <bool WIDE>
+__global__ void __launch_bounds__(kCopyThreads, 2) ep_combine_fp8_kernel(const WireArgs a)
+{
+    __shared__ int s_off[kMaxRanks + 1];
+    if (threadIdx.x <= a.W) s_off[threadIdx.x] = a.tok_off[threadIdx.x];
+    __syncthreads();
+
+    const int lane = threadIdx.x & 31;
+    const uint32_t units = (uint32_t)a.N * (uint32_t)a.chunks;
+    const uint32_t step = gridDim.x * (kCopyThreads / 32);
+    for (uint32_t u = blockIdx.x * (kCopyThreads / 32) + (threadIdx.x >> 5); u < units; u += step) {
+        const int g = (int)(u / (uint32_t)a.chunks);
+        const int c = (int)(u - (uint32_t)g * (uint32_t)a.chunks);
+        const int s = rank_of_token(s_off, a.W, g);
+        const int64_t tok = (int64_t)s * a.M + (g - s_off[s]);
+        const int src = lane < a.F ? __ldg(a.fwd + tok * a.F + lane) : -1;
+        const int nd = __popc(__ballot_sync(0xffffffffu, src >= 0));
+        const int p0 = c * a.chunk_pieces;
+        const int np = (int)min((int64_t)a.chunk_pieces, (a.H >> 4) - p0);
+        uint4* dst = reinterpret_cast<uint4*>(a.out + tok * a.H) + (int64_t)p0 * 2;
+        if (!WIDE || nd <= 8)
+            fold_fp8_rows(a, src, nd, p0, np, dst, lane);     // nd == 0 stores +0
+        else
+            fold_fp8_wide(a, src, nd, p0, np, dst, lane);
+
+        if (c == 0 && a.w_in != nullptr && a.out_w != nullptr) {
+            for (int e0 = 0; e0 < a.k; e0 += 32) {
+                const int e = e0 + lane;
+                float acc = 0.0f;
+                for (int d = 0; d < nd; ++d) {
+                    const int64_t row = __shfl_sync(0xffffffffu, src, d);
+                    if (e < a.k) acc = __fadd_rn(acc, __ldg(a.w_in + row * a.k + e));
+                }
+                if (e < a.k) a.out_w[tok * a.k + e] = acc;
+            }
+        }
+    }
+}
+
+int grid_for(const void* kernel, int64_t warps_needed, int num_sms)
+{
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kCopyThreads, 0) != cudaSuccess ||
+        per_sm < 1)
+        per_sm = 1;
+    const int64_t need = (warps_needed + kCopyThreads / 32 - 1) / (kCopyThreads / 32);
+    const int64_t cap = (int64_t)per_sm * num_sms;
+    return (int)(need < cap ? need : cap);
+}
+
+}  // namespace
+
+cudaError_t launch_quantise_rows(const WireArgs& a, int num_sms, cudaStream_t stream)
+{
+    const int64_t units = (int64_t)a.W * a.rows;
+    if (units == 0) return cudaSuccess;
+    ep_quantise_rows_kernel<<<grid_for((const void*)ep_quantise_rows_kernel, units, num_sms),
+                              kCopyThreads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine_fp8(const WireArgs& a, int num_sms, cudaStream_t stream)
+{
+    const int64_t units = (int64_t)a.N * a.chunks;
+    if (units == 0) return cudaSuccess;
+    if (a.F > 8)
+        ep_combine_fp8_kernel<true><<<grid_for((const void*)ep_combine_fp8_kernel<true>, units, num_sms),
+                                      kCopyThreads, 0, stream>>>(a);
+    else
+        ep_combine_fp8_kernel<false><<<grid_for((const void*)ep_combine_fp8_kernel<false>, units, num_sms),
+                                       kCopyThreads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace ep

@@ -79,43 +79,6 @@ __global__ void __launch_bounds__(kCopyThreads) ep_scatter_kernel(const ScatterA
 
 constexpr int kQUnroll = 2;   // 32-byte source pieces per lane in flight per step
 
-// Two floats -> two e4m3 codes (round to nearest even, saturating to +-448); lo in the low byte.
-__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi)
-{
-    unsigned short r;
-    asm("{ .reg .b16 t; cvt.rn.satfinite.e4m3x2.f32 t, %1, %2; mov.b16 %0, t; }"
-        : "=h"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-// Quantise one lane's 16 consecutive BF16 values (two 16-byte vectors) with the block scale:
-// q = e4m3(x / scale), FP32 division rounded to nearest even.
-__device__ __forceinline__ uint4 quantise16(const uint4& a, const uint4& b, float scale)
-{
-    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint32_t p0 = e4m3x2(__fdiv_rn(bf16_lo(w[2 * i]), scale), __fdiv_rn(bf16_hi(w[2 * i]), scale));
-        const uint32_t p1 =
-            e4m3x2(__fdiv_rn(bf16_lo(w[2 * i + 1]), scale), __fdiv_rn(bf16_hi(w[2 * i + 1]), scale));
-        o[i] = p0 | (p1 << 16);
-    }
-    return make_uint4(o[0], o[1], o[2], o[3]);
-}
-
-__device__ __forceinline__ float absmax16(const uint4& a, const uint4& b)
-{
-    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-    float m = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
-    return m;
-}
-
 // A lane owns 16 consecutive elements (32 source bytes, 16 code bytes); the 8 lanes of a 128-
 // element block agree on its maximum by shuffles, so each block's scale is computed once per
 // token and its codes are written to every destination row.  Slices are multiples of 128.

@@ -21,7 +21,7 @@ def lib():
 def _declared_functions():
     text = open(os.path.join(ROOT, "include", "ep.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(ep_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(ep_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_exports_every_declared_symbol(lib):

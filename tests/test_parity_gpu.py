@@ -331,3 +331,74 @@ def test_quantised_dispatch_edge_values():
     xf[3, 5, 7] = -0.0
     wl.x[:] = torch.from_numpy(xf).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     _check_quantised(wl)
+
+
+# ---------------------------------------------------------------- combine over an FP8 wire
+
+def _check_fp8_wire(wl, variant="auto"):
+    disp, eo, _, _ = oracle.run_workload(wl, harness.expert_np)
+    q, sc = oracle.quantize_e4m3_blockwise(eo)
+    o_out, o_w = oracle.combine_fp8(wl.W, wl.k, wl.H, wl.M, wl.n_tok, disp["slot_of"], q, sc,
+                                    disp["recv_w"])
+    plan, (x, w, scales, idx) = _setup(wl)
+    plan.set_variant(variant)
+    d = plan.dispatch(x, w, scales, idx, wl.n_tok)
+    eo_g = harness.expert_torch(wl, d.recv_x, d.recv_idx, d.recv_w, d.recv_scales, d.recv_count)
+    qg, scg = plan.quantize_received(eo_g, d.epoch)
+    out, out_w = plan.combine_fp8(qg, scg, d.recv_w, d.epoch)
+    torch.cuda.synchronize()
+    assert plan.status() == 0
+    qg, scg = gpu_path.raw(qg), scg.cpu().numpy()
+    cnt = d.recv_count.cpu().numpy()
+    for r in range(wl.W):
+        n = int(cnt[r])
+        assert np.array_equal(qg[r, :n], q[r, :n]), f"rank {r}: codes"
+        assert np.array_equal(scg[r, :n].view(np.uint32), sc[r, :n].view(np.uint32)), f"rank {r}: scales"
+    out = gpu_path.raw(out)
+    for s in range(wl.W):
+        n = int(wl.n_tok[s])
+        assert gpu_path.nan_aware_equal_bf16(out[s, :n], o_out[s, :n]), f"source rank {s}"
+        if o_w is not None:
+            assert np.array_equal(out_w[s, :n].cpu().numpy().view(np.uint32), o_w[s, :n].view(np.uint32))
+    plan.close()
+
+
+def test_fp8_wire_dsv3_reduced():
+    _check_fp8_wire(wlmod.make_workload("dsv3", max_tok=300))
+
+
+@pytest.mark.parametrize("variant", ["auto", "tiled_512", "whole_row"])
+def test_fp8_wire_small_scalar_expert(variant):
+    _check_fp8_wire(wlmod.make_workload("small", max_tok=64), variant)
+
+
+def test_fp8_wire_fp8_payload():
+    _check_fp8_wire(wlmod.make_workload("fp8", max_tok=256))
+
+
+def test_fp8_wire_wide_fan_in():
+    # min(W, k) = 16 > 8: rows fold in ascending batches of 8
+    _check_fp8_wire(wlmod.custom_workload(W=16, E=2, k=32, H=256, M=40, n_tok=[40] * 8 + [3] * 8, seed=6))
+
+
+def test_fp8_wire_dsv3_full():
+    _check_fp8_wire(wlmod.make_workload("dsv3"))
+
+
+def test_fp8_wire_rejects_fp16_plans_and_stale_epochs():
+    wl = wlmod.make_workload("topk", k=8, max_tok=16)
+    plan, (x, w, sc, idx) = _setup(wl)
+    d = plan.dispatch(x, w, sc, idx, wl.n_tok)
+    with pytest.raises(ep.EpError) as e:
+        plan.quantize_received(d.recv_x, d.epoch)
+    assert e.value.code == ep.EP_ERR_ARG
+    plan.close()
+    wl = wlmod.make_workload("dsv3", max_tok=16)
+    plan, (x, w, sc, idx) = _setup(wl)
+    d = plan.dispatch(x, w, sc, idx, wl.n_tok)
+    q, s = plan.quantize_received(d.recv_x, d.epoch)
+    plan.reset()
+    with pytest.raises(ep.EpError) as e:
+        plan.combine_fp8(q, s, None, d.epoch)
+    assert e.value.code == ep.EP_ERR_STATE
+    plan.close()
