@@ -17,6 +17,8 @@ namespace {
 
 // ---- quantise the received expert rows: warp per row, lanes own 16-element pieces
 
+constexpr int kQuantUnroll = 4;   // 32-byte pieces per lane in flight
+
 __global__ void __launch_bounds__(kCopyThreads, 3) ep_quantise_rows_kernel(const WireArgs a)
 {
     __shared__ int s_cnt[kMaxRanks];
@@ -35,21 +37,29 @@ __global__ void __launch_bounds__(kCopyThreads, 3) ep_quantise_rows_kernel(const
         const uint8_t* src = reinterpret_cast<const uint8_t*>(a.eo) + u * a.H * 2;
         uint8_t* dq = a.q + u * a.H;
         float* dsc = a.scales + u * nb;
-        for (int p0 = 0; p0 < npiece; p0 += 32) {   // warp-uniform bounds
-            const int p = p0 + lane;
-            uint4 x0 = make_uint4(0, 0, 0, 0), x1 = x0;
-            if (p < npiece) {
-                x0 = ld_stream_v4(src + (int64_t)p * 32);
-                x1 = ld_stream_v4(src + (int64_t)p * 32 + 16);
+        for (int p0 = 0; p0 < npiece; p0 += 32 * kQuantUnroll) {   // warp-uniform bounds
+            uint4 x[kQuantUnroll][2];
+#pragma unroll
+            for (int t = 0; t < kQuantUnroll; ++t) {
+                const int p = p0 + 32 * t + lane;
+                x[t][0] = x[t][1] = make_uint4(0, 0, 0, 0);
+                if (p < npiece) {
+                    x[t][0] = ld_stream_v4(src + (int64_t)p * 32);
+                    x[t][1] = ld_stream_v4(src + (int64_t)p * 32 + 16);
+                }
             }
-            float m = absmax16(x0, x1);
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-            const float scale = m > 0.0f ? __fdiv_rn(m, 448.0f) : 1.0f;
-            if (p < npiece) {
-                st_v4(dq + (int64_t)p * 16, quantise16(x0, x1, scale));
-                if ((lane & 7) == 0) dsc[p >> 3] = scale;
+#pragma unroll
+            for (int t = 0; t < kQuantUnroll; ++t) {
+                const int p = p0 + 32 * t + lane;
+                float m = absmax16(x[t][0], x[t][1]);
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+                const float scale = m > 0.0f ? __fdiv_rn(m, 448.0f) : 1.0f;
+                if (p < npiece) {
+                    st_v4(dq + (int64_t)p * 16, quantise16(x[t][0], x[t][1], scale));
+                    if ((lane & 7) == 0) dsc[p >> 3] = scale;
+                }
             }
         }
     }
@@ -83,9 +93,14 @@ __device__ __forceinline__ void store_bf16x16(uint4* dst, const float (&acc)[16]
     st_v4(dst + 1, make_uint4(w[4], w[5], w[6], w[7]));
 }
 
-// Rolling fold of a unit's nd <= 8 rows (lane d of src holds row d): row d's load of the next
-// piece is issued as soon as its current piece is taken, so every lane keeps the token's rows
-// in flight.
+// Rolling fold of a unit's nd <= 8 rows (lane d of src holds row d): row d's loads of the next
+// kWireDepth pieces are in flight while the current ones are folded, so every lane keeps
+// nd * kWireDepth 16-byte loads outstanding.
+#ifndef EP_WIRE_DEPTH
+#define EP_WIRE_DEPTH 1   // 2 spills at the 128-register budget of 2 CTAs per SM
+#endif
+constexpr int kWireDepth = EP_WIRE_DEPTH;
+
 __device__ __forceinline__ void fold_fp8_rows(const WireArgs& a, int src, int nd, int p0, int np,
                                               uint4* dst, int lane)
 {
@@ -96,33 +111,38 @@ __device__ __forceinline__ void fold_fp8_rows(const WireArgs& a, int src, int nd
     uint32_t ro[8];
 #pragma unroll
     for (int d = 0; d < 8; ++d) ro[d] = (uint32_t)((int64_t)__shfl_sync(0xffffffffu, src, d) * hp + p0);
-    uint4 b[8];
-    float sc[8];
+    uint4 b[8][kWireDepth];
+    float sc[8][kWireDepth];
 #pragma unroll
-    for (int d = 0; d < 8; ++d)
-        if (d < nd && lane < np) {
-            b[d] = ld_stream_v4(q4 + ro[d] + lane);
-            sc[d] = __ldg(a.scales + ((ro[d] + lane) >> 3));
-        }
-    for (int vb = 0; vb < np; vb += 32) {         // warp-uniform bounds
-        const int pc = vb + lane;
-        const int pn = pc + 32;
-        float acc[16];
+    for (int t = 0; t < kWireDepth; ++t)
 #pragma unroll
-        for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
-#pragma unroll
-        for (int d = 0; d < 8; ++d) {
-            if (d < nd) {
-                const uint4 x = b[d];
-                const float xs = sc[d];
-                if (pn < np) {
-                    b[d] = ld_stream_v4(q4 + ro[d] + pn);
-                    sc[d] = __ldg(a.scales + ((ro[d] + pn) >> 3));
-                }
-                if (pc < np) add_fp8x16(acc, x, xs);
+        for (int d = 0; d < 8; ++d)
+            if (d < nd && lane + 32 * t < np) {
+                b[d][t] = ld_stream_v4(q4 + ro[d] + lane + 32 * t);
+                sc[d][t] = __ldg(a.scales + ((ro[d] + lane + 32 * t) >> 3));
             }
+    for (int vb = 0; vb < np; vb += 32 * kWireDepth) {    // warp-uniform bounds
+#pragma unroll
+        for (int t = 0; t < kWireDepth; ++t) {
+            const int pc = vb + 32 * t + lane;
+            const int pn = pc + 32 * kWireDepth;
+            float acc[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+#pragma unroll
+            for (int d = 0; d < 8; ++d) {
+                if (d < nd) {
+                    const uint4 x = b[d][t];
+                    const float xs = sc[d][t];
+                    if (pn < np) {
+                        b[d][t] = ld_stream_v4(q4 + ro[d] + pn);
+                        sc[d][t] = __ldg(a.scales + ((ro[d] + pn) >> 3));
+                    }
+                    if (pc < np) add_fp8x16(acc, x, xs);
+                }
+            }
+            if (pc < np) store_bf16x16(dst + (int64_t)pc * 2, acc);
         }
-        if (pc < np) store_bf16x16(dst + (int64_t)pc * 2, acc);
     }
 }
 
