@@ -49,6 +49,10 @@ def _load():
             lib.ep_oracle_dispatch.argtypes = [ctypes.c_int] * 7 + [_p] * 12
             lib.ep_oracle_combine.restype = ctypes.c_int
             lib.ep_oracle_combine.argtypes = [ctypes.c_int] * 5 + [_p] * 6
+            lib.ep_oracle_group_by_expert.restype = ctypes.c_int
+            lib.ep_oracle_group_by_expert.argtypes = [ctypes.c_int] * 6 + [_p] * 9
+            lib.ep_oracle_ungroup_by_expert.restype = ctypes.c_int
+            lib.ep_oracle_ungroup_by_expert.argtypes = [ctypes.c_int] * 5 + [_p] * 5
             lib.ep_oracle_combine_fp8.restype = ctypes.c_int
             lib.ep_oracle_combine_fp8.argtypes = [ctypes.c_int] * 4 + [_p] * 7
             lib.ep_oracle_quantize_e4m3_blockwise.restype = ctypes.c_int
@@ -140,6 +144,42 @@ def combine_fp8(W, k, H, M, n_tok, slot_of, q, scales, w_in=None):
                                  _ptr(w_in), _ptr(out), _ptr(out_w)) != 0:
         raise ValueError("ep_oracle_combine_fp8: invalid arguments")
     return out, out_w
+
+
+def group_by_expert(W, E, k, H, elem_bytes, M, disp):
+    """Expert-grouped view of a dispatch output (see ep_oracle_group_by_expert): returns a dict
+    with packed_x [W][E][W*M][H], packed_count [W][E], packed_src_info [W][E][W*M],
+    layout_range [W][E][W] (int64) and packed_row [W][E][W*M]."""
+    lib = _load()
+    rows = W * M
+    dt = np.uint8 if elem_bytes == 1 else np.uint16
+    out = {"packed_x": np.zeros((W, E, rows, H), dtype=dt),
+           "packed_count": np.zeros((W, E), dtype=np.int32),
+           "packed_src_info": np.full((W, E, rows), -1, dtype=np.int32),
+           "layout_range": np.zeros((W, E, W), dtype=np.int64),
+           "packed_row": np.full((W, E, rows), -1, dtype=np.int32)}
+    st = lib.ep_oracle_group_by_expert(
+        W, E, k, H, elem_bytes, M, _ptr(np.ascontiguousarray(disp["recv_x"])),
+        _ptr(np.ascontiguousarray(disp["recv_idx"])), _ptr(np.ascontiguousarray(disp["recv_count"])),
+        _ptr(np.ascontiguousarray(disp["src_pos"])), _ptr(out["packed_x"]), _ptr(out["packed_count"]),
+        _ptr(out["packed_src_info"]), _ptr(out["layout_range"]), _ptr(out["packed_row"]))
+    if st != 0:
+        raise ValueError("ep_oracle_group_by_expert: invalid arguments")
+    return out
+
+
+def ungroup_by_expert(W, E, H, out_fp16, M, recv_count, grouped, packed_y):
+    """Per received row, the ascending-expert FP32 sum of its local experts' outputs, rounded
+    to BF16 / FP16: returns out [W][W*M][H] (uint16 bits; rows past recv_count are zero)."""
+    lib = _load()
+    out = np.zeros((W, W * M, H), dtype=np.uint16)
+    st = lib.ep_oracle_ungroup_by_expert(
+        W, E, H, 1 if out_fp16 else 0, M, _ptr(np.ascontiguousarray(recv_count, dtype=np.int32)),
+        _ptr(grouped["packed_count"]), _ptr(grouped["packed_row"]),
+        _ptr(np.ascontiguousarray(packed_y).view(np.uint16)), _ptr(out))
+    if st != 0:
+        raise ValueError("ep_oracle_ungroup_by_expert: invalid arguments")
+    return out
 
 
 def bf16_from_f32(a):

@@ -366,3 +366,98 @@ int ep_oracle_combine_fp8(int W, int k, int H, int M, const int32_t* n_tok, cons
     return EP_ORACLE_OK;
 }
 
+
+/* ---- Expert-grouped ("standard MoE") layout ---------------------------------------- */
+
+/*
+ * The dispatch output regrouped by local expert (MORI-EP guide, section 4 "Standard MoE
+ * Compatibility", convert_dispatch_output(): packed_recv_x, packed_recv_count,
+ * packed_recv_src_info, packed_recv_layout_range).  The guide names the outputs only; the
+ * reading taken: on rank r, the list of local expert e (global id r*E + e) holds, in receive-row
+ * order, every received row whose top-k names that expert (once per row, even if named twice);
+ *   packed_x[r][e][slot]        the row's payload (cap = W*M slots per expert)
+ *   packed_count[r][e]          length of the list
+ *   packed_src_info[r][e][slot] the row's source token index within its source rank
+ *   layout_range[r][e][s]       (first slot of source rank s) << 32 | (number of its slots);
+ *                               rows arrive in source-rank order, so each source's slots are
+ *                               contiguous and its first slot is the count of earlier sources
+ *   packed_row[r][e][slot]      the receive row (kept for the inverse below)
+ */
+int ep_oracle_group_by_expert(int W, int E, int k, int H, int elem_bytes, int M, const void* recv_x,
+                              const int32_t* recv_idx, const int32_t* recv_count,
+                              const int32_t* src_pos, void* packed_x, int32_t* packed_count,
+                              int32_t* packed_src_info, int64_t* layout_range, int32_t* packed_row)
+{
+    if (W < 1 || E < 1 || k < 1 || H < 1 || M < 1 || (elem_bytes != 1 && elem_bytes != 2))
+        return EP_ORACLE_ERR_ARG;
+    const int64_t rows = (int64_t)W * M;
+    const size_t row_bytes = (size_t)H * (size_t)elem_bytes;
+    int64_t* per_src = (int64_t*)malloc((size_t)W * sizeof(int64_t));
+    if (!per_src) return EP_ORACLE_ERR_ARG;
+    for (int r = 0; r < W; ++r) {
+        for (int e = 0; e < E; ++e) {
+            const int32_t ge = r * E + e;
+            const int64_t list = (int64_t)r * E + e;
+            int64_t cnt = 0;
+            for (int s = 0; s < W; ++s) per_src[s] = 0;
+            for (int64_t i = 0; i < recv_count[r]; ++i) {
+                const int32_t* ids = recv_idx + ((int64_t)r * rows + i) * k;
+                int named = 0;
+                for (int j = 0; j < k; ++j) named |= ids[j] == ge;
+                if (!named) continue;
+                const int64_t slot = cnt++;
+                memcpy((char*)packed_x + (size_t)(list * rows + slot) * row_bytes,
+                       (const char*)recv_x + (size_t)((int64_t)r * rows + i) * row_bytes, row_bytes);
+                const int32_t pos = src_pos[(int64_t)r * rows + i];
+                packed_src_info[list * rows + slot] = (int32_t)(pos % rows);
+                packed_row[list * rows + slot] = (int32_t)i;
+                per_src[pos / rows] += 1;
+            }
+            packed_count[list] = (int32_t)cnt;
+            int64_t first = 0;
+            for (int s = 0; s < W; ++s) {
+                layout_range[list * W + s] = (first << 32) | per_src[s];
+                first += per_src[s];
+            }
+        }
+    }
+    free(per_src);
+    return EP_ORACLE_OK;
+}
+
+/*
+ * The inverse (guide, convert_combine_input()): the per-rank combine input of every received
+ * row is the sum of its local experts' outputs, taken in ascending expert id, in FP32 from
+ * +0.0f, rounded to nearest even into BF16 (out_fp16 == 0) or FP16.
+ *   packed_y [W][E][W*M][H] 16-bit expert outputs, packed_row / packed_count as written above,
+ *   out [W][W*M][H]; rows at or past recv_count[r] are left untouched.
+ */
+int ep_oracle_ungroup_by_expert(int W, int E, int H, int out_fp16, int M, const int32_t* recv_count,
+                                const int32_t* packed_count, const int32_t* packed_row,
+                                const uint16_t* packed_y, uint16_t* out)
+{
+    if (W < 1 || E < 1 || H < 1 || M < 1) return EP_ORACLE_ERR_ARG;
+    const int64_t rows = (int64_t)W * M;
+    for (int r = 0; r < W; ++r) {
+        const int64_t n = recv_count[r];
+        float* acc = (float*)calloc((size_t)(n > 0 ? n : 1) * (size_t)H, sizeof(float));
+        if (!acc) return EP_ORACLE_ERR_ARG;
+        for (int e = 0; e < E; ++e) {                  /* ascending expert id */
+            const int64_t list = (int64_t)r * E + e;
+            for (int64_t slot = 0; slot < packed_count[list]; ++slot) {
+                const int64_t i = packed_row[list * rows + slot];
+                const uint16_t* y = packed_y + (list * rows + slot) * H;
+                for (int h = 0; h < H; ++h) {
+                    float v = out_fp16 ? ep_oracle_f32_from_f16(y[h]) : ep_oracle_f32_from_bf16(y[h]);
+                    acc[i * H + h] = acc[i * H + h] + v;
+                }
+            }
+        }
+        for (int64_t i = 0; i < n; ++i)
+            for (int h = 0; h < H; ++h)
+                out[((int64_t)r * rows + i) * H + h] =
+                    out_fp16 ? ep_oracle_f16_from_f32(acc[i * H + h]) : ep_oracle_bf16_from_f32(acc[i * H + h]);
+        free(acc);
+    }
+    return EP_ORACLE_OK;
+}

@@ -457,3 +457,65 @@ def test_fp8_combine_close_to_bf16_combine():
     b = (out16.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     amax = np.abs(b).max()
     assert np.all(np.abs(a - b) <= 2.0 ** -4 * np.abs(b) + 2.0 ** -3 * amax * 2.0 ** -7)
+
+
+# ---------------------------------------------------------------- expert-grouped layout (next row F3)
+
+def test_group_by_expert_brute_force():
+    for case in ({"W": 3, "E": 4, "k": 3, "H": 16, "M": 10, "n_tok": [10, 0, 7]},
+                 {"W": 4, "E": 2, "k": 5, "H": 8, "M": 6, "n_tok": [6, 6, 1, 3]},
+                 {"W": 1, "E": 8, "k": 8, "H": 24, "M": 9, "n_tok": [9]}):
+        wl = wlmod.custom_workload(seed=4, **case)
+        wl.indices[0, 0, 1] = wl.indices[0, 0, 0]          # a duplicate id counts once
+        disp = _run(wl)
+        g = oracle.group_by_expert(wl.W, wl.E, wl.k, wl.H, 2, wl.M, disp)
+        for r in range(wl.W):
+            for e in range(wl.E):
+                ge = r * wl.E + e
+                lst = [(s, t) for s in range(wl.W) for t in range(int(wl.n_tok[s]))
+                       if ge in set(int(v) for v in wl.indices[s, t])]
+                n = len(lst)
+                assert g["packed_count"][r, e] == n
+                assert [int(v) for v in g["packed_src_info"][r, e, :n]] == [t for _, t in lst]
+                for slot, (s, t) in enumerate(lst):
+                    assert np.array_equal(g["packed_x"][r, e, slot], wl.x[s, t])
+                    i = g["packed_row"][r, e, slot]
+                    assert disp["src_pos"][r, i] == s * wl.W * wl.M + t
+                first = 0
+                for s in range(wl.W):
+                    c = sum(1 for (ss, _) in lst if ss == s)
+                    assert g["layout_range"][r, e, s] == (first << 32) | c
+                    first += c
+
+
+def test_ungroup_identity_closed_form():
+    """Expert outputs equal to the grouped rows: each received row comes back as m * x, with m its
+    number of distinct local experts (exact before the one rounding)."""
+    wl = wlmod.custom_workload(W=4, E=8, k=6, H=32, M=12, n_tok=[12, 3, 0, 11], seed=8)
+    disp = _run(wl)
+    g = oracle.group_by_expert(wl.W, wl.E, wl.k, wl.H, 2, wl.M, disp)
+    out = oracle.ungroup_by_expert(wl.W, wl.E, wl.H, False, wl.M, disp["recv_count"], g, g["packed_x"])
+    for r in range(wl.W):
+        for i in range(int(disp["recv_count"][r])):
+            m = len({int(v) for v in disp["recv_idx"][r, i] if int(v) // wl.E == r})
+            xf = (disp["recv_x"][r, i].astype(np.uint32) << 16).view(np.float32)
+            exp = torch.from_numpy(xf * np.float32(m)).to(torch.bfloat16).view(torch.int16).numpy()
+            assert np.array_equal(out[r, i].view(np.int16), exp)
+
+
+def test_ungroup_sums_in_ascending_expert_order():
+    """Hand-worked values (tests/golden/combine_order.txt, row 2): experts 0..3 contribute
+    2^-24, 2^-24, 2^-8, 1; the top-k lists them 3, 2, 1, 0.  Ascending expert order gives
+    1 + 2^-7 (0x3F81); top-k order would give 1.0."""
+    W, E, k, H, M = 1, 4, 4, 8, 1
+    x = np.zeros((W, M, H), dtype=np.uint16)
+    idx = np.array([[[3, 2, 1, 0]]], dtype=np.int32)
+    wl = wlmod.Workload("order", W, E, k, H, "bf16", 0, M, np.array([1], np.int32), x, idx, None,
+                        None, "identity")
+    disp = _run(wl)
+    g = oracle.group_by_expert(W, E, k, H, 2, M, disp)
+    y = np.zeros_like(g["packed_x"])
+    for e, v in enumerate((0x3380, 0x3380, 0x3B80, 0x3F80)):
+        y[0, e, 0, :] = v
+    out = oracle.ungroup_by_expert(W, E, H, False, M, disp["recv_count"], g, y)
+    assert np.all(out[0, 0] == 0x3F81)
