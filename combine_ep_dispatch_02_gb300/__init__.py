@@ -29,7 +29,7 @@ VARIANTS = {"auto": 0, "whole_row": 1, "tiled_512": 2, "tiled_1024": 3}
 EXPORTS = ("ep_plan_create", "ep_plan_destroy", "ep_plan_set_variant", "ep_plan_device_bytes",
            "ep_dispatch", "ep_dispatch_route", "ep_dispatch_scatter", "ep_combine", "ep_reset",
            "ep_status", "ep_strerror", "ep_last_error", "ep_route_noalloc",
-           "ep_quantize_received", "ep_combine_fp8")
+           "ep_quantize_received", "ep_combine_fp8", "ep_group_by_expert", "ep_ungroup_by_expert")
 
 
 class EpError(RuntimeError):
@@ -75,6 +75,8 @@ def load_library(path: Optional[str] = None):
         "ep_route_noalloc": (I, [I, I, I, I, V, V, V, V, V, V, V]),
         "ep_quantize_received": (I, [V, V, V, V, U64, V]),
         "ep_combine_fp8": (I, [V, V, V, V, V, V, U64, V]),
+        "ep_group_by_expert": (I, [V, V, V, V, V, U64, V]),
+        "ep_ungroup_by_expert": (I, [V, V, V, U64, V]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -273,6 +275,29 @@ class Plan:
         _check(self._lib.ep_combine_fp8(self._h, _ptr(q), _ptr(scales), _ptr(weights), _ptr(out),
                                         _ptr(out_w), ctypes.c_uint64(epoch), _stream(stream)))
         return out, out_w
+
+    def group_by_expert(self, epoch: int, packed_x: Optional[torch.Tensor] = None, stream=None):
+        """Expert-grouped view of the live dispatch: returns (packed_x [W][E][W*M][H],
+        packed_count [W][E], packed_src_info [W][E][W*M], layout_range [W][E][W] int64)."""
+        W, E, R, H = self.W, self.E, self.rows, self.H
+        if packed_x is None:
+            packed_x = torch.empty((W, E, R, H), dtype=self.payload_torch_dtype, device=self.device)
+        count = torch.empty((W, E), dtype=torch.int32, device=self.device)
+        src_info = torch.empty((W, E, R), dtype=torch.int32, device=self.device)
+        layout = torch.empty((W, E, W), dtype=torch.int64, device=self.device)
+        _check(self._lib.ep_group_by_expert(self._h, _ptr(packed_x), _ptr(count), _ptr(src_info),
+                                            _ptr(layout), ctypes.c_uint64(epoch), _stream(stream)))
+        return packed_x, count, src_info, layout
+
+    def ungroup_by_expert(self, packed_y: torch.Tensor, epoch: int, out: Optional[torch.Tensor] = None,
+                          stream=None) -> torch.Tensor:
+        """Per received row, the ascending-expert sum of its local experts' outputs: the combine
+        input [W][W*M][H] (BF16, FP16 for FP16 plans)."""
+        if out is None:
+            out = torch.empty((self.W, self.rows, self.H), dtype=self.combine_torch_dtype, device=self.device)
+        _check(self._lib.ep_ungroup_by_expert(self._h, _ptr(packed_y), _ptr(out), ctypes.c_uint64(epoch),
+                                              _stream(stream)))
+        return out
 
     def reset(self, stream=None):
         _check(self._lib.ep_reset(self._h, _stream(stream)))

@@ -17,7 +17,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libep.so")
 SOURCES = ("ep_api.cu", "ep_route.cu", "ep_scatter.cu", "ep_combine.cu", "ep_noalloc.cu",
-           "ep_fp8wire.cu")
+           "ep_fp8wire.cu", "ep_grouped.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -27,12 +27,13 @@ struct ep_plan {
     int32_t* src_pos;
     int32_t* fwd;
     int32_t* recv_count;
+    int32_t* expert_map;
     unsigned long long* flags;
     unsigned long long* ticket;
     int* status;
 
     // host state of the live dispatch
-    uint64_t epoch;
+    uint64_t epoch, grouped_epoch;
     bool routed, live, has_w;
     const int32_t* routed_idx;
     int N;
@@ -62,8 +63,8 @@ bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 struct Layout {
-    size_t recv_x, recv_idx, recv_w, recv_scales, src_pos, fwd, recv_count, flags, ticket, status,
-        total;
+    size_t recv_x, recv_idx, recv_w, recv_scales, src_pos, fwd, recv_count, expert_map, flags, ticket,
+        status, total;
 };
 
 int elem_bytes_of(int dtype)
@@ -121,6 +122,7 @@ Layout layout_of(int W, int k, int H, int dtype, int sd, int M)
     put(L.src_pos, (size_t)W * rows * 4);
     put(L.fwd, rows * F * 4);
     put(L.recv_count, (size_t)W * 4);
+    put(L.expert_map, (size_t)W * rows * k * 4);
     put(L.flags, (size_t)tiles * W * 8);
     put(L.ticket, 8);
     put(L.status, 4);
@@ -236,6 +238,7 @@ int ep_plan_create(ep_plan** out, int W, int E, int k, int H, int dtype, int sd,
     p->src_pos = (int32_t*)(b + L.src_pos);
     p->fwd = (int32_t*)(b + L.fwd);
     p->recv_count = (int32_t*)(b + L.recv_count);
+    p->expert_map = (int32_t*)(b + L.expert_map);
     p->flags = (unsigned long long*)(b + L.flags);
     p->ticket = (unsigned long long*)(b + L.ticket);
     p->status = (int*)(b + L.status);
@@ -471,6 +474,48 @@ int ep_combine_fp8(ep_plan* p, const void* expert_q, const float* expert_scales,
     for (int s = 0; s <= p->W; ++s) a.tok_off[s] = p->tok_off[s];
     cudaError_t e = launch_combine_fp8(a, p->num_sms, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "ep_combine_fp8: launch");
+    return EP_OK;
+}
+
+int ep_group_by_expert(ep_plan* p, void* packed_x, int32_t* packed_count, int32_t* packed_src_info,
+                       int64_t* layout_range, uint64_t epoch, void* stream)
+{
+    if (!p) return fail(EP_ERR_ARG, "ep_group_by_expert: plan is NULL");
+    if (!p->live || epoch != p->epoch)
+        return fail(EP_ERR_STATE, "ep_group_by_expert: epoch %llu is not the plan's live dispatch",
+                    (unsigned long long)epoch);
+    if (!packed_x || !aligned(packed_x, 16) || !packed_count || !aligned(packed_count, 4) ||
+        !packed_src_info || !aligned(packed_src_info, 4) || !layout_range || !aligned(layout_range, 8))
+        return fail(EP_ERR_ARG, "ep_group_by_expert: a buffer is NULL or misaligned");
+    DeviceGuard g(p->device);
+    if (!g.ok) return fail(EP_ERR_CUDA, "cannot select the plan's device %d", p->device);
+    GroupArgs a{};
+    a.recv_x = p->recv_x; a.recv_idx = p->recv_idx; a.recv_count = p->recv_count; a.src_pos = p->src_pos;
+    a.map = p->expert_map; a.packed_x = (uint8_t*)packed_x; a.count = packed_count;
+    a.src_info = packed_src_info; a.layout_range = (long long*)layout_range;
+    a.rows = p->rows; a.row_bytes = p->row_bytes; a.W = p->W; a.E = p->E; a.k = p->k;
+    cudaError_t e = launch_group(a, p->num_sms, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "ep_group_by_expert: launch");
+    p->grouped_epoch = epoch;
+    return EP_OK;
+}
+
+int ep_ungroup_by_expert(ep_plan* p, const void* packed_y, void* out, uint64_t epoch, void* stream)
+{
+    if (!p) return fail(EP_ERR_ARG, "ep_ungroup_by_expert: plan is NULL");
+    if (!p->live || epoch != p->epoch || p->grouped_epoch != epoch)
+        return fail(EP_ERR_STATE, "ep_ungroup_by_expert: epoch %llu has no live grouped view",
+                    (unsigned long long)epoch);
+    if (!packed_y || !aligned(packed_y, 16) || !out || !aligned(out, 16))
+        return fail(EP_ERR_ARG, "ep_ungroup_by_expert: a buffer is NULL or not 16-byte aligned");
+    DeviceGuard g(p->device);
+    if (!g.ok) return fail(EP_ERR_CUDA, "cannot select the plan's device %d", p->device);
+    GroupArgs a{};
+    a.recv_idx = p->recv_idx; a.recv_count = p->recv_count; a.map = p->expert_map;
+    a.packed_y = (const uint8_t*)packed_y; a.out = (uint8_t*)out;
+    a.rows = p->rows; a.row_bytes = (int64_t)p->H * 2; a.W = p->W; a.E = p->E; a.k = p->k;
+    cudaError_t e = launch_ungroup(a, p->dtype == EP_FP16, p->num_sms, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "ep_ungroup_by_expert: launch");
     return EP_OK;
 }
 

@@ -9,6 +9,7 @@
 //   fwd          [W][M][F]     forward map, F = min(W, k): the receive rows of token (s,t) as
 //                              r * (W*M) + slot, in ascending destination rank, -1 padded
 //   recv_count   [W]
+//   expert_map   [W][W*M][k]   slot of a received row in its local experts' lists (grouped view)
 //   flags        [tiles][W]    decoupled-lookback scan words of the routing kernel
 //   ticket       u64           monotone tile ticket (never reset; also yields the call stamp)
 //   status       int32         first device-side error
@@ -95,6 +96,24 @@ struct WireArgs {
     int tok_off[kMaxRanks + 1];
 };
 
+// Expert-grouped (3-D) view of the receive buffers, and its inverse.
+struct GroupArgs {
+    const uint8_t* recv_x;       // [W][W*M][row_bytes] received payload
+    const int32_t* recv_idx;     // [W][W*M][k]
+    const int32_t* recv_count;   // [W]
+    const int32_t* src_pos;      // [W][W*M]
+    int32_t* map;                // [W][W*M][k] plan-owned: slot of a row in an expert's list
+    uint8_t* packed_x;           // [W][E][W*M][row_bytes]
+    int32_t* count;              // [W][E]
+    int32_t* src_info;           // [W][E][W*M]
+    long long* layout_range;     // [W][E][W]
+    const uint8_t* packed_y;     // [W][E][W*M][H] 16-bit expert outputs (inverse)
+    uint8_t* out;                // [W][W*M][H] 16-bit combine input (inverse)
+    int64_t rows;                // W*M
+    int64_t row_bytes;           // payload bytes (grouping) / 16-bit row bytes (inverse)
+    int W, E, k;
+};
+
 // Host-side launchers, one per kernel translation unit.
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t stream);
 cudaError_t launch_scatter(const ScatterArgs& a, int num_sms, cudaStream_t stream);
@@ -103,6 +122,8 @@ cudaError_t launch_scatter(const ScatterArgs& a, int num_sms, cudaStream_t strea
 cudaError_t launch_scatter_quant(const ScatterArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_combine(const CombineArgs& a, bool fp16, int num_sms, cudaStream_t stream);
 cudaError_t launch_quantise_rows(const WireArgs& a, int num_sms, cudaStream_t stream);
+cudaError_t launch_group(const GroupArgs& a, int num_sms, cudaStream_t stream);
+cudaError_t launch_ungroup(const GroupArgs& a, bool fp16, int num_sms, cudaStream_t stream);
 cudaError_t launch_combine_fp8(const WireArgs& a, int num_sms, cudaStream_t stream);
 // choose combine's slice of a row per work unit (a.H and a.N set)
 void combine_geometry(CombineArgs& a, int variant, int num_sms);

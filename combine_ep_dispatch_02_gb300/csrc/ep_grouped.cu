@@ -1,0 +1,269 @@
+// ep_grouped.cu -- the expert-grouped ("standard MoE", 3-D) view of a dispatch and its inverse.
+//
+// MORI-EP guide, section 4 "Standard MoE Compatibility": convert_dispatch_output() turns the
+// 2-D receive buffers into packed_recv_x [experts][capacity][H] with packed_recv_count,
+// packed_recv_src_info and packed_recv_layout_range, the layout a grouped GEMM consumes;
+// convert_combine_input() brings expert outputs back to the 2-D combine input.  Readings (the
+// guide names the outputs only): on rank r the list of local expert e holds, in receive-row
+// order, every received row whose top-k names global expert r*E + e (once per row); src_info is
+// the row's source token index; layout_range[s] = (first slot of source rank s) << 32 | count;
+// the capacity is W*M.  The inverse sums a received row's local-expert outputs in ascending
+// expert id in FP32 and rounds once.
+//
+// Kernels:
+//   ep_group_kernel       one CTA per (rank, local expert): block scan over the rank's received
+//                         rows (a row is in the list iff one of its k ids is the expert), writes
+//                         src_info, the count, the layout ranges, and each row's slot into the
+//                         plan's map [W][W*M][k] at the row's first top-k entry naming the expert;
+//   ep_grouped_copy_kernel warp per received row: the row is read once and written to the slot
+//                         of each of its local experts;
+//   ep_ungroup_kernel     warp per received row: its local experts' output rows, ordered by
+//                         expert id, are loaded together and folded in FP32.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "ep_common.cuh"
+
+namespace ep {
+namespace {
+
+// top-k entry j of a received row names a local expert for the first time in the row
+__device__ __forceinline__ bool first_local(const int32_t* ids, int k, int j, int r, int E)
+{
+    const int e = ids[j];
+    if (e < r * E || e >= (r + 1) * E) return false;
+    for (int jj = 0; jj < j; ++jj)
+        if (ids[jj] == e) return false;
+    return true;
+}
+
+__global__ void __launch_bounds__(256) ep_group_kernel(const GroupArgs a)
+{
+    __shared__ int s_warp[8];
+    __shared__ int s_src[kMaxRanks];
+    __shared__ int s_base;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int r = blockIdx.x / a.E;
+    const int e = blockIdx.x - r * a.E;
+    const int32_t ge = r * a.E + e;
+    const int64_t list = (int64_t)r * a.E + e;
+    const int n = a.recv_count[r];
+    if (tid < kMaxRanks) s_src[tid] = 0;
+    if (tid == 0) s_base = 0;
+    __syncthreads();
+    for (int i0 = 0; i0 < n; i0 += 256) {
+        const int i = i0 + tid;
+        int jfirst = -1;
+        if (i < n) {
+            const int32_t* ids = a.recv_idx + ((int64_t)r * a.rows + i) * a.k;
+            for (int j = 0; j < a.k; ++j)
+                if (__ldg(ids + j) == ge) { jfirst = j; break; }
+        }
+        const unsigned bal = __ballot_sync(0xffffffffu, jfirst >= 0);
+        if (lane == 0) s_warp[warp] = __popc(bal);
+        __syncthreads();
+        int before = s_base, total = 0;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+            if (w < warp) before += s_warp[w];
+            total += s_warp[w];
+        }
+        if (jfirst >= 0) {
+            const int slot = before + __popc(bal & lanemask_lt());
+            const int32_t pos = a.src_pos[(int64_t)r * a.rows + i];
+            a.src_info[list * a.rows + slot] = (int32_t)(pos % a.rows);
+            a.map[((int64_t)r * a.rows + i) * a.k + jfirst] = slot;
+            atomicAdd(&s_src[pos / a.rows], 1);
+        }
+        __syncthreads();
+        if (tid == 0) s_base += total;
+        __syncthreads();
+    }
+    if (tid == 0) a.count[list] = s_base;
+    if (tid < a.W) {
+        long long first = 0;
+        for (int s = 0; s < tid; ++s) first += s_src[s];
+        a.layout_range[list * a.W + tid] = (first << 32) | (long long)s_src[tid];
+    }
+}
+
+// lane j of the warp: the packed row (list * rows + slot) its top-k entry j feeds, or -1
+__device__ __forceinline__ int64_t entry_dest(const GroupArgs& a, int r, int64_t i, int j)
+{
+    const int32_t* ids = a.recv_idx + ((int64_t)r * a.rows + i) * a.k;
+    if (j >= a.k || !first_local(ids, a.k, j, r, a.E)) return -1;
+    const int slot = a.map[((int64_t)r * a.rows + i) * a.k + j];
+    return ((int64_t)r * a.E + (ids[j] - r * a.E)) * a.rows + slot;
+}
+
+__global__ void __launch_bounds__(kCopyThreads) ep_grouped_copy_kernel(const GroupArgs a)
+{
+    __shared__ int s_cnt[kMaxRanks];
+    if (threadIdx.x < a.W) s_cnt[threadIdx.x] = a.recv_count[threadIdx.x];
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = (int64_t)gridDim.x * (kCopyThreads / 32);
+    const int nvec = (int)(a.row_bytes >> 4);
+    for (int64_t u = (int64_t)blockIdx.x * (kCopyThreads / 32) + (threadIdx.x >> 5);
+         u < (int64_t)a.W * a.rows; u += nwarps) {
+        const int r = (int)(u / a.rows);
+        const int64_t i = u - (int64_t)r * a.rows;
+        if (i >= s_cnt[r]) continue;                       // warp-uniform
+        const uint8_t* src = a.recv_x + u * a.row_bytes;
+        for (int j0 = 0; j0 < a.k; j0 += 32) {             // up to 64 top-k entries
+            const int64_t dest = entry_dest(a, r, i, j0 + lane);
+            const unsigned has = __ballot_sync(0xffffffffu, dest >= 0);
+            if (!has) continue;
+            for (int v0 = 0; v0 < nvec; v0 += 32 * 4) {
+                uint4 buf[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int v = v0 + q * 32 + lane;
+                    if (v < nvec) buf[q] = ld_stream_v4(src + (int64_t)v * 16);
+                }
+                for (unsigned m = has; m; m &= m - 1) {
+                    const int64_t row = __shfl_sync(0xffffffffu, dest, __ffs(m) - 1);
+                    uint8_t* dst = a.packed_x + row * a.row_bytes;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int v = v0 + q * 32 + lane;
+                        if (v < nvec) st_v4(dst + (int64_t)v * 16, buf[q]);
+                    }
+                }
+            }
+        }
+    }
+}
+
+template <bool FP16>
+__device__ __forceinline__ void add8(float (&acc)[8], const uint4& v)
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float lo, hi;
+        if constexpr (FP16) {
+            const __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
+            lo = __low2float(h);
+            hi = __high2float(h);
+        } else {
+            lo = __uint_as_float(w[i] << 16);
+            hi = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+        acc[2 * i] = __fadd_rn(acc[2 * i], lo);
+        acc[2 * i + 1] = __fadd_rn(acc[2 * i + 1], hi);
+    }
+}
+
+template <bool FP16>
+__device__ __forceinline__ uint4 pack8(const float (&acc)[8])
+{
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if constexpr (FP16) {
+            const __half2 h = __floats2half2_rn(acc[2 * i], acc[2 * i + 1]);
+            w[i] = *reinterpret_cast<const uint32_t*>(&h);
+        } else {
+            const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+            w[i] = *reinterpret_cast<const uint32_t*>(&b);
+        }
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <bool FP16>
+__global__ void __launch_bounds__(kCopyThreads, 2) ep_ungroup_kernel(const GroupArgs a)
+{
+    __shared__ int s_cnt[kMaxRanks];
+    if (threadIdx.x < a.W) s_cnt[threadIdx.x] = a.recv_count[threadIdx.x];
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = (int64_t)gridDim.x * (kCopyThreads / 32);
+    const int hv = (int)(a.row_bytes >> 4);       // 16-byte vectors of a 16-bit row
+    const uint4* y4 = reinterpret_cast<const uint4*>(a.packed_y);
+    for (int64_t u = (int64_t)blockIdx.x * (kCopyThreads / 32) + (threadIdx.x >> 5);
+         u < (int64_t)a.W * a.rows; u += nwarps) {
+        const int r = (int)(u / a.rows);
+        const int64_t i = u - (int64_t)r * a.rows;
+        if (i >= s_cnt[r]) continue;                       // warp-uniform
+        uint4* dst = reinterpret_cast<uint4*>(a.out + u * a.row_bytes);
+        // the row's local experts in ascending id: lane j holds entry j (two passes for k > 32)
+        const int32_t* ids = a.recv_idx + u * a.k;
+        int64_t dest0 = entry_dest(a, r, i, lane), dest1 = entry_dest(a, r, i, lane + 32);
+        const int e0 = dest0 >= 0 ? ids[lane] : 0x7FFFFFFF;
+        const int e1 = dest1 >= 0 ? ids[lane + 32] : 0x7FFFFFFF;
+        const int nd = __popc(__ballot_sync(0xffffffffu, dest0 >= 0)) +
+                       __popc(__ballot_sync(0xffffffffu, dest1 >= 0));
+        // rank of each entry among the valid ones (ids are distinct after first_local)
+        int rank0 = 0, rank1 = 0;
+        for (int j = 0; j < 64; ++j) {
+            const int ej = __shfl_sync(0xffffffffu, j < 32 ? e0 : e1, j & 31);
+            rank0 += ej < e0;
+            rank1 += ej < e1;
+        }
+        for (int vb = 0; vb < hv; vb += 32) {              // warp-uniform bounds
+            const int v = vb + lane;
+            float acc[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+            for (int d0 = 0; d0 < nd; d0 += 8) {
+                uint4 b[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    // the entry of rank d0+q (uniform across the warp)
+                    const int want = d0 + q;
+                    const unsigned m0 = __ballot_sync(0xffffffffu, dest0 >= 0 && rank0 == want);
+                    const unsigned m1 = __ballot_sync(0xffffffffu, dest1 >= 0 && rank1 == want);
+                    int64_t row = -1;
+                    if (m0) row = __shfl_sync(0xffffffffu, dest0, __ffs(m0) - 1);
+                    else if (m1) row = __shfl_sync(0xffffffffu, dest1, __ffs(m1) - 1);
+                    if (row >= 0 && v < hv) b[q] = ld_stream_v4(y4 + row * hv + v);
+                    if (row < 0) b[q] = make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    if (d0 + q < nd) add8<FP16>(acc, b[q]);
+            }
+            if (v < hv) st_v4(dst + v, pack8<FP16>(acc));
+        }
+    }
+}
+
+int grid_of(const void* kernel, int64_t warps, int num_sms)
+{
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kCopyThreads, 0) != cudaSuccess ||
+        per_sm < 1)
+        per_sm = 1;
+    const int64_t need = (warps + kCopyThreads / 32 - 1) / (kCopyThreads / 32);
+    const int64_t cap = (int64_t)per_sm * num_sms;
+    return (int)(need < cap ? need : cap);
+}
+
+}  // namespace
+
+cudaError_t launch_group(const GroupArgs& a, int num_sms, cudaStream_t stream)
+{
+    ep_group_kernel<<<a.W * a.E, 256, 0, stream>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int64_t units = (int64_t)a.W * a.rows;
+    ep_grouped_copy_kernel<<<grid_of((const void*)ep_grouped_copy_kernel, units, num_sms), kCopyThreads,
+                             0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_ungroup(const GroupArgs& a, bool fp16, int num_sms, cudaStream_t stream)
+{
+    const int64_t units = (int64_t)a.W * a.rows;
+    if (fp16)
+        ep_ungroup_kernel<true><<<grid_of((const void*)ep_ungroup_kernel<true>, units, num_sms),
+                                  kCopyThreads, 0, stream>>>(a);
+    else
+        ep_ungroup_kernel<false><<<grid_of((const void*)ep_ungroup_kernel<false>, units, num_sms),
+                                   kCopyThreads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace ep

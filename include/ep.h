@@ -187,6 +187,29 @@ int ep_quantize_received(ep_plan* p, const void* expert_out, void* expert_q, flo
 int ep_combine_fp8(ep_plan* p, const void* expert_q, const float* expert_scales, const float* weights,
                    void* out, float* out_w, uint64_t epoch, void* stream);
 
+/*
+ * Expert-grouped ("standard MoE", 3-D) view of the live dispatch (MORI-EP guide, section 4
+ * "Standard MoE Compatibility", convert_dispatch_output() / convert_combine_input()).  On rank r
+ * the list of local expert e (global id r*E + e) holds, in receive-row order, every received row
+ * whose top-k names that expert, once per row; capacity W*M rows per list.
+ *
+ * ep_group_by_expert writes, all caller-owned:
+ *   packed_x         [W][E][W*M][H] payload rows (the plan's payload type), 16-byte aligned
+ *   packed_count     [W][E] int32 list lengths
+ *   packed_src_info  [W][E][W*M] int32: source token index within its source rank
+ *   layout_range     [W][E][W] int64: (first slot of source rank s) << 32 | (its slot count)
+ * Slots at or past packed_count hold unspecified data.
+ *
+ * ep_ungroup_by_expert is the inverse for expert outputs laid out the same way:
+ *   packed_y         [W][E][W*M][H] 16-bit expert outputs (BF16; FP16 for FP16 plans)
+ *   out              [W][W*M][H] 16-bit: row i of rank r = sum of its local experts' outputs
+ *                    in ascending expert id, FP32 from +0.0f, rounded to nearest even once;
+ *                    the combine input of ep_combine.  Needs ep_group_by_expert on this epoch.
+ */
+int ep_group_by_expert(ep_plan* p, void* packed_x, int32_t* packed_count, int32_t* packed_src_info,
+                       int64_t* layout_range, uint64_t epoch, void* stream);
+int ep_ungroup_by_expert(ep_plan* p, const void* packed_y, void* out, uint64_t epoch, void* stream);
+
 /* End the live dispatch (guide, reset()): its views become invalid and ep_combine on its epoch
  * fails.  No device work is needed: the scan flags carry a per-call stamp. */
 int ep_reset(ep_plan* p, void* stream);

@@ -40,14 +40,15 @@ def _layout_bytes(W, E, k, H, eb, sd, M):
     F = min(W, k)
     tiles = -(-rows // 256)
     parts = [W * rows * H * eb, W * rows * k * 4, W * rows * k * 4, W * rows * sd * 4, W * rows * 4,
-             rows * F * 4, W * 4, tiles * W * 8, 8, 4]
+             rows * F * 4, W * 4, W * rows * k * 4, tiles * W * 8, 8, 4]
     return sum(_align(p) for p in parts)
 
 
 def test_device_bytes_golden(lib):
     # DeepSeek-V3 shape: recv rows 8 * 32768 * 14336 B, index / weight rows 8 MiB each,
-    # src_pos and forward map 1 MiB each, 128 tiles * 8 scan words, three control words
-    assert lib.ep_plan_device_bytes(8, 32, 8, 7168, ep.EP_BF16, 0, 4096) == 3776979712
+    # src_pos and forward map 1 MiB each, the expert-slot map 8 MiB, 128 tiles * 8 scan words,
+    # three control words
+    assert lib.ep_plan_device_bytes(8, 32, 8, 7168, ep.EP_BF16, 0, 4096) == 3785368320
     # FP8 with 56 scales per row
     assert lib.ep_plan_device_bytes(8, 96, 6, 7168, ep.EP_FP8_E4M3, 56, 4096) == \
         _layout_bytes(8, 96, 6, 7168, 1, 56, 4096)

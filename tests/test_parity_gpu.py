@@ -402,3 +402,55 @@ def test_fp8_wire_rejects_fp16_plans_and_stale_epochs():
         plan.combine_fp8(q, s, None, d.epoch)
     assert e.value.code == ep.EP_ERR_STATE
     plan.close()
+
+
+# ---------------------------------------------------------------- expert-grouped layout
+
+def _check_grouped(wl, seed=0):
+    disp = oracle.dispatch(wl.W, wl.E, wl.k, wl.H, wl.elem_bytes, wl.sd, wl.M, wl.x, wl.weights,
+                           wl.scales, wl.indices, wl.n_tok)
+    g = oracle.group_by_expert(wl.W, wl.E, wl.k, wl.H, wl.elem_bytes, wl.M, disp)
+    fp16 = wl.dtype == "fp16"
+    rng = np.random.default_rng(seed)
+    yf = torch.from_numpy(rng.standard_normal(g["packed_x"].shape[:3] + (wl.H,)).astype(np.float32))
+    y = (yf.to(torch.float16) if fp16 else yf.to(torch.bfloat16)).view(torch.int16).numpy().view(np.uint16)
+    o_out = oracle.ungroup_by_expert(wl.W, wl.E, wl.H, fp16, wl.M, disp["recv_count"], g, y)
+
+    plan, (x, w, sc, idx) = _setup(wl)
+    d = plan.dispatch(x, w, sc, idx, wl.n_tok)
+    px, cnt, info, layout = plan.group_by_expert(d.epoch)
+    out = plan.ungroup_by_expert(torch.from_numpy(y.view(np.int16)).to(DEV), d.epoch)
+    torch.cuda.synchronize()
+    assert plan.status() == 0
+    cnt = cnt.cpu().numpy()
+    assert np.array_equal(cnt, g["packed_count"])
+    assert np.array_equal(layout.cpu().numpy(), g["layout_range"])
+    px, info = gpu_path.raw(px), info.cpu().numpy()
+    for r in range(wl.W):
+        for e in range(wl.E):
+            n = int(cnt[r, e])
+            assert np.array_equal(info[r, e, :n], g["packed_src_info"][r, e, :n]), (r, e)
+            assert np.array_equal(px[r, e, :n], g["packed_x"][r, e, :n]), (r, e)
+    out = gpu_path.raw(out)
+    for r in range(wl.W):
+        n = int(disp["recv_count"][r])
+        assert np.array_equal(out[r, :n], o_out[r, :n]), r
+    plan.close()
+
+
+@pytest.mark.parametrize("case", [
+    dict(W=4, E=8, k=6, H=512, M=100, n_tok=[100, 37, 0, 64], dtype="bf16"),
+    dict(W=8, E=4, k=8, H=256, M=40, n_tok=[40, 1, 2, 3, 40, 0, 39, 17], dtype="fp16"),
+    dict(W=4, E=4, k=3, H=256, M=50, n_tok=[50, 7, 0, 31], dtype="fp8", sd=2),
+    dict(W=2, E=32, k=33, H=128, M=70, n_tok=[70, 33], dtype="bf16"),
+], ids=lambda c: f"W{c['W']}E{c['E']}k{c['k']}{c['dtype']}")
+def test_grouped_layout(case):
+    _check_grouped(wlmod.custom_workload(seed=5, **case))
+
+
+def test_grouped_layout_duplicate_ids_and_small_workload():
+    wl = wlmod.custom_workload(W=4, E=8, k=4, H=256, M=30, n_tok=[30, 30, 5, 9], seed=2)
+    wl.indices[0, 3, 2] = wl.indices[0, 3, 0]       # the same expert twice in one top-k row
+    wl.indices[1, 7, 3] = wl.indices[1, 7, 1]
+    _check_grouped(wl)
+    _check_grouped(wlmod.make_workload("small", max_tok=24), seed=1)
