@@ -236,6 +236,7 @@ def run_ours(args, rank, world, dist):
                                        steps=max(3, min(args.steps, 50)))
     wire = measure_fp8_combine_wire(plan, wl, dev, stream, x, w, idx, P, peak,
                                     steps=max(3, min(args.steps, 50)))
+    grouped = measure_grouped(ep, dev, stream, peak, steps=max(3, min(args.steps, 50)))
     if plan.status() != 0:
         raise RuntimeError("device status after timing: %d" % plan.status())
 
@@ -279,6 +280,7 @@ def run_ours(args, rank, world, dist):
             "cpu_baseline": cpu,
             "fp8_quantising_dispatch": quant,
             "fp8_combine_wire": wire,
+            "expert_grouped_layout": grouped,
         }
     plan.close()
     return result
@@ -347,6 +349,45 @@ def measure_fp8_combine_wire(plan, wl, dev, stream, x, w, idx, P, peak, steps):
             "combine_algorithmic_bytes": cb, "combine_gbs": round(cb / (ct * 1e-3) / 1e9, 1),
             "combine_frac": round(cb / (ct * 1e-3) / 1e9 / peak, 4),
             "quantize_frac": round(qb / (qt * 1e-3) / 1e9 / peak, 4)}
+
+
+def measure_grouped(ep, dev, stream, peak, steps):
+    """The expert-grouped (3-D) view and its inverse on the small-batch workload (W=4, 64
+    experts per rank, top-8, hidden 7168 BF16, 256 tokens per rank), the regime a grouped GEMM
+    consumer runs in.  Minimal bytes: grouping reads each received row once and writes one row
+    per (row, local expert) entry; the inverse reads the entries and writes the rows."""
+    wl = wlmod.make_workload("small")
+    plan = ep.Plan(wl.W, wl.E, wl.k, wl.H, "bf16", 0, wl.M, device=dev)
+    x = torch.from_numpy(wl.x.view(np.int16)).to(dev)
+    idx = torch.from_numpy(wl.indices).to(dev)
+    w = torch.from_numpy(wl.weights).to(dev)
+    d = plan.dispatch(x, w, None, idx, wl.n_tok, stream=stream)
+    px, cnt, info, lay = plan.group_by_expert(d.epoch, stream=stream)
+    y = px.view(torch.bfloat16)
+    out = plan.ungroup_by_expert(y, d.epoch, stream=stream)
+    torch.cuda.synchronize(dev)
+    rows = int(d.recv_count.sum())
+    entries = int(cnt.sum())
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for e in ev:
+        e[0].record(stream)
+        plan.group_by_expert(d.epoch, packed_x=px, stream=stream)
+        e[1].record(stream)
+        plan.ungroup_by_expert(y, d.epoch, out=out, stream=stream)
+        e[2].record(stream)
+    torch.cuda.synchronize(dev)
+    if plan.status() != 0:
+        raise RuntimeError("device status after the grouped layout: %d" % plan.status())
+    plan.close()
+    gt = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
+    ut = sum(e[1].elapsed_time(e[2]) for e in ev) / steps
+    rb = 2 * wl.H
+    gb = rows * (rb + 4 * wl.k) + entries * (rb + 4)
+    ub = entries * rb + rows * (rb + 4 * wl.k)
+    return {"workload": "W=4, 64 experts/rank, top-8, hidden 7168 BF16, 256 tokens/rank",
+            "received_rows": rows, "expert_entries": entries,
+            "group_us": round(gt * 1e3, 2), "group_frac": round(gb / (gt * 1e-3) / 1e9 / peak, 4),
+            "ungroup_us": round(ut * 1e3, 2), "ungroup_frac": round(ub / (ut * 1e-3) / 1e9 / peak, 4)}
 
 
 def measure_e2e(plan, wl, dev, stream, pair_bytes, steps):

@@ -33,7 +33,10 @@ constexpr int kCopyThreads = 256;   // scatter / combine CTAs: 8 warps, one work
 constexpr unsigned long long kFlagAggregate = 1ull;   // count = this tile's own total
 constexpr unsigned long long kFlagInclusive = 2ull;   // count = total of tiles 0..this one
 constexpr uint32_t kStampMask = 0x3FFFFFFFu;
-constexpr int kSpinLimit = 1 << 20; // polls before a wait gives up with EP_ERR_DEVICE_TIMEOUT
+#ifndef EP_SPIN_LIMIT
+#define EP_SPIN_LIMIT (1 << 20)
+#endif
+constexpr int kSpinLimit = EP_SPIN_LIMIT;   // polls before a wait gives up with EP_ERR_DEVICE_TIMEOUT
 
 struct RouteArgs {
     const int32_t* idx;

@@ -172,7 +172,7 @@ __device__ __forceinline__ uint4 pack8(const float (&acc)[8])
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-template <bool FP16>
+template <bool FP16, bool WIDE>
 __global__ void __launch_bounds__(kCopyThreads, 2) ep_ungroup_kernel(const GroupArgs a)
 {
     __shared__ int s_cnt[kMaxRanks];
@@ -202,7 +202,41 @@ __global__ void __launch_bounds__(kCopyThreads, 2) ep_ungroup_kernel(const Group
             rank0 += ej < e0;
             rank1 += ej < e1;
         }
-        for (int vb = 0; vb < hv; vb += 32) {              // warp-uniform bounds
+        if (!WIDE || nd <= 8) {
+            // the rows in ascending expert order, once per received row; then a rolling fold:
+            // row d's next column is requested as soon as its current one is taken
+            const uint4* rp[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const unsigned m0 = __ballot_sync(0xffffffffu, dest0 >= 0 && rank0 == q);
+                const unsigned m1 = __ballot_sync(0xffffffffu, dest1 >= 0 && rank1 == q);
+                const int64_t row = m0 ? __shfl_sync(0xffffffffu, dest0, __ffs(m0) - 1)
+                                       : __shfl_sync(0xffffffffu, dest1, m1 ? __ffs(m1) - 1 : 0);
+                rp[q] = y4 + row * hv;
+            }
+            uint4 b[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                if (q < nd && lane < hv) b[q] = ld_stream_v4(rp[q] + lane);
+            for (int vb = 0; vb < hv; vb += 32) {          // warp-uniform bounds
+                const int vc = vb + lane, vn = vc + 32;
+                float acc[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    if (q < nd) {
+                        const uint4 x = b[q];
+                        if (vn < hv) b[q] = ld_stream_v4(rp[q] + vn);
+                        if (vc < hv) add8<FP16>(acc, x);
+                    }
+                }
+                if (vc < hv) st_v4(dst + vc, pack8<FP16>(acc));
+            }
+            continue;
+        }
+        if (!WIDE) continue;
+        for (int vb = 0; vb < hv; vb += 32) {              // more than 8 local experts
             const int v = vb + lane;
             float acc[8];
 #pragma unroll
@@ -254,15 +288,22 @@ cudaError_t launch_group(const GroupArgs& a, int num_sms, cudaStream_t stream)
     return cudaGetLastError();
 }
 
-cudaError_t launch_ungroup(const GroupArgs& a, bool fp16, int num_sms, cudaStream_t stream)
+template <bool FP16, bool WIDE>
+void launch_ungroup_t(const GroupArgs& a, int num_sms, cudaStream_t stream)
 {
     const int64_t units = (int64_t)a.W * a.rows;
+    ep_ungroup_kernel<FP16, WIDE><<<grid_of((const void*)ep_ungroup_kernel<FP16, WIDE>, units, num_sms),
+                                    kCopyThreads, 0, stream>>>(a);
+}
+
+cudaError_t launch_ungroup(const GroupArgs& a, bool fp16, int num_sms, cudaStream_t stream)
+{
+    // a row has at most min(k, E) local experts; the >8 path is only compiled in when needed
+    const bool wide = (a.k < a.E ? a.k : a.E) > 8;
     if (fp16)
-        ep_ungroup_kernel<true><<<grid_of((const void*)ep_ungroup_kernel<true>, units, num_sms),
-                                  kCopyThreads, 0, stream>>>(a);
+        wide ? launch_ungroup_t<true, true>(a, num_sms, stream) : launch_ungroup_t<true, false>(a, num_sms, stream);
     else
-        ep_ungroup_kernel<false><<<grid_of((const void*)ep_ungroup_kernel<false>, units, num_sms),
-                                   kCopyThreads, 0, stream>>>(a);
+        wide ? launch_ungroup_t<false, true>(a, num_sms, stream) : launch_ungroup_t<false, false>(a, num_sms, stream);
     return cudaGetLastError();
 }
 

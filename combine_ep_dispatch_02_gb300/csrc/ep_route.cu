@@ -119,6 +119,10 @@ __global__ void __launch_bounds__(kRouteThreads) ep_route_kernel(const RouteArgs
         s_excl[tid] = 0;
         s_done[tid] = (tile == 0);
         s_incl_at[tid] = INT_MAX;
+#ifdef EP_TEST_WITHHOLD_TILE0
+        // test builds only: tile 0 never publishes, so every other tile's bounded wait runs out
+        if (tile != 0)
+#endif
         st_relaxed_u64(a.flags + (int64_t)tile * a.W + tid,
                        pack_flag(stamp, tile == 0 ? kFlagInclusive : kFlagAggregate, (uint32_t)run));
     }
