@@ -29,8 +29,12 @@ namespace ep {
 namespace {
 
 #ifndef EP_COMBINE_CTAS_PER_SM
-#define EP_COMBINE_CTAS_PER_SM 2   // 128 registers per thread: the fold loop runs without spills
+#define EP_COMBINE_CTAS_PER_SM 2   // >= 100 registers per thread: the fold loop runs without spills
 #endif
+#ifndef EP_COMBINE_THREADS
+#define EP_COMBINE_THREADS 288   // 9 warps: 2 CTAs fill the register file at ~110 registers
+#endif
+constexpr int kCombThreads = EP_COMBINE_THREADS;
 #ifndef EP_COMBINE_DEPTH
 #define EP_COMBINE_DEPTH 1
 #endif
@@ -151,7 +155,7 @@ __device__ __forceinline__ int unit_src(const CombineArgs& a, const int* off, ui
 }
 
 template <bool FP16, bool WIDE>
-__global__ void __launch_bounds__(kCopyThreads, EP_COMBINE_CTAS_PER_SM) ep_combine_kernel(const CombineArgs a)
+__global__ void __launch_bounds__(kCombThreads, EP_COMBINE_CTAS_PER_SM) ep_combine_kernel(const CombineArgs a)
 {
     __shared__ int s_off[kMaxRanks + 1];
     if (threadIdx.x <= a.W) s_off[threadIdx.x] = a.tok_off[threadIdx.x];
@@ -160,8 +164,8 @@ __global__ void __launch_bounds__(kCopyThreads, EP_COMBINE_CTAS_PER_SM) ep_combi
     const int lane = threadIdx.x & 31;
     // units = N * chunks < 2^31 (checked by the host), so unit indices are 32-bit
     const uint32_t units = (uint32_t)a.N * (uint32_t)a.chunks;
-    const uint32_t step = gridDim.x * (kCopyThreads / 32);
-    uint32_t u = blockIdx.x * (kCopyThreads / 32) + (threadIdx.x >> 5);
+    const uint32_t step = gridDim.x * (kCombThreads / 32);
+    uint32_t u = blockIdx.x * (kCombThreads / 32) + (threadIdx.x >> 5);
     int src = unit_src(a, s_off, u, lane);
     for (; u < units; u += step) {
         const int src_next = unit_src(a, s_off, u + step, lane);   // lands while this unit folds
@@ -206,13 +210,13 @@ cudaError_t launch_t(const CombineArgs& a, int num_sms, cudaStream_t stream)
     if (units == 0) return cudaSuccess;
     int per_sm = 0;
     cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &per_sm, ep_combine_kernel<FP16, WIDE>, kCopyThreads, 0);
+        &per_sm, ep_combine_kernel<FP16, WIDE>, kCombThreads, 0);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
-    const int64_t need = (units + kCopyThreads / 32 - 1) / (kCopyThreads / 32);
+    const int64_t need = (units + kCombThreads / 32 - 1) / (kCombThreads / 32);
     const int64_t cap = (int64_t)per_sm * num_sms;
     const int grid = (int)(need < cap ? need : cap);
-    ep_combine_kernel<FP16, WIDE><<<grid, kCopyThreads, 0, stream>>>(a);
+    ep_combine_kernel<FP16, WIDE><<<grid, kCombThreads, 0, stream>>>(a);
     return cudaGetLastError();
 }
 
@@ -227,7 +231,7 @@ void combine_geometry(CombineArgs& a, int variant, int num_sms)
     if (variant == EP_VARIANT_AUTO) {
         // Small calls split rows into 1024- then 512-element slices so every resident warp
         // gets work, as the pages' small-batch policy does.
-        const int64_t warps = (int64_t)num_sms * EP_COMBINE_CTAS_PER_SM * (kCopyThreads / 32);
+        const int64_t warps = (int64_t)num_sms * EP_COMBINE_CTAS_PER_SM * (kCombThreads / 32);
         if ((int64_t)a.N < warps && hv > 128) {
             cv = 128;
             if ((int64_t)a.N * ((hv + cv - 1) / cv) < warps) cv = 64;

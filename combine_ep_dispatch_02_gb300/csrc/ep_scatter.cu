@@ -28,15 +28,23 @@ __global__ void __launch_bounds__(kCopyThreads) ep_scatter_kernel(const ScatterA
     const int lane = threadIdx.x & 31;
     const int64_t warps_per_grid = (int64_t)gridDim.x * (kCopyThreads / 32);
     const int64_t units = (int64_t)a.N * a.chunks;
-    for (int64_t u = (int64_t)blockIdx.x * (kCopyThreads / 32) + (threadIdx.x >> 5); u < units;
-         u += warps_per_grid) {
+    int64_t u = (int64_t)blockIdx.x * (kCopyThreads / 32) + (threadIdx.x >> 5);
+    // destination rows of a unit, compact and ascending in rank; lane d holds the d-th one
+    auto unit_dest = [&](int64_t v) -> int {
+        if (v >= units) return -1;
+        const int gv = (int)(v / a.chunks);
+        const int sv = rank_of_token(s_off, a.W, gv);
+        const int64_t tv = (int64_t)sv * a.M + (gv - s_off[sv]);
+        return lane < a.F ? __ldg(a.fwd + tv * a.F + lane) : -1;
+    };
+    int dest_next = unit_dest(u);
+    for (; u < units; u += warps_per_grid) {
+        const int dest = dest_next;
+        dest_next = unit_dest(u + warps_per_grid);       // lands while this unit is copied
         const int g = (int)(u / a.chunks);
         const int c = (int)(u - (int64_t)g * a.chunks);
         const int s = rank_of_token(s_off, a.W, g);
         const int64_t tok = (int64_t)s * a.M + (g - s_off[s]);
-
-        // destination rows, compact and ascending in rank; lane d holds the d-th one
-        const int dest = lane < a.F ? __ldg(a.fwd + tok * a.F + lane) : -1;
         const int nd = __popc(__ballot_sync(0xffffffffu, dest >= 0));
 
         const int64_t off = (int64_t)c * a.chunk_bytes;
