@@ -237,6 +237,7 @@ def run_ours(args, rank, world, dist):
     wire = measure_fp8_combine_wire(plan, wl, dev, stream, x, w, idx, P, peak,
                                     steps=max(3, min(args.steps, 50)))
     grouped = measure_grouped(ep, dev, stream, peak, steps=max(3, min(args.steps, 50)))
+    latency = measure_small_batch_latency(ep, dev)
     if plan.status() != 0:
         raise RuntimeError("device status after timing: %d" % plan.status())
 
@@ -281,6 +282,7 @@ def run_ours(args, rank, world, dist):
             "fp8_quantising_dispatch": quant,
             "fp8_combine_wire": wire,
             "expert_grouped_layout": grouped,
+            "small_batch_latency_us": latency,
         }
     plan.close()
     return result
@@ -388,6 +390,55 @@ def measure_grouped(ep, dev, stream, peak, steps):
             "received_rows": rows, "expert_entries": entries,
             "group_us": round(gt * 1e3, 2), "group_frac": round(gb / (gt * 1e-3) / 1e9 / peak, 4),
             "ungroup_us": round(ut * 1e3, 2), "ungroup_frac": round(ub / (ut * 1e-3) / 1e9 / peak, 4)}
+
+
+def measure_small_batch_latency(ep, dev, tokens=(8, 128, 256), replays=120):
+    """Dispatch and combine latency at small batches on the DeepSeek-V3 shape (W=8, 32 experts
+    per rank, top-8, hidden 7168 BF16, Zipf routing), as the pages measure it: each call captured
+    in a CUDA graph and replayed; p50 over the replays of the per-replay device time."""
+    res = {}
+    for t in tokens:
+        wl = wlmod.make_workload(WORKLOAD, max_tok=t)
+        plan = ep.Plan(wl.W, wl.E, wl.k, wl.H, "bf16", 0, wl.M, device=dev)
+        x = torch.from_numpy(wl.x.view(np.int16)).to(dev)
+        idx = torch.from_numpy(wl.indices).to(dev)
+        w = torch.from_numpy(wl.weights).to(dev)
+        out = torch.empty((wl.W, wl.M, wl.H), dtype=torch.bfloat16, device=dev)
+        out_w = torch.empty((wl.W, wl.M, wl.k), dtype=torch.float32, device=dev)
+        s = torch.cuda.Stream(dev)
+        with torch.cuda.stream(s):
+            for _ in range(10):                     # eager warm-up
+                d = plan.dispatch(x, w, None, idx, wl.n_tok, stream=s)
+                plan.combine(d.recv_x, d.recv_w, d.epoch, out=out, out_w=out_w, stream=s)
+        torch.cuda.synchronize(dev)
+        gd, gc = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gd, stream=s):
+            d = plan.dispatch(x, w, None, idx, wl.n_tok, stream=s)
+        with torch.cuda.graph(gc, stream=s):
+            plan.combine(d.recv_x, d.recv_w, d.epoch, out=out, out_w=out_w, stream=s)
+        flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+        times = {"dispatch": [], "combine": [], "dispatch_l2_flushed": [], "combine_l2_flushed": []}
+        with torch.cuda.stream(s):                   # replay() launches on the current stream
+            for i in range(replays + 10):
+                for name, g in (("dispatch", gd), ("combine", gc)):
+                    for cold in (False, True):
+                        if cold:
+                            flush.fill_(i & 0xFF)      # evict the working set from L2
+                        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                        a.record(s)
+                        g.replay()
+                        b.record(s)
+                        b.synchronize()
+                        if i >= 10:
+                            times[name + ("_l2_flushed" if cold else "")].append(a.elapsed_time(b) * 1e3)
+        if plan.status() != 0:
+            raise RuntimeError("device status after the latency runs: %d" % plan.status())
+        plan.close()
+        res[f"{t}_tokens_per_rank"] = {k: round(statistics.median(v), 2) for k, v in times.items()}
+    res["method"] = ("CUDA-graph replay of one dispatch (route + scatter) or one combine; p50 of "
+                     f"{replays} replays; hot = back to back, l2_flushed = a 2x-L2 buffer written "
+                     "before each replay")
+    return res
 
 
 def measure_e2e(plan, wl, dev, stream, pair_bytes, steps):

@@ -309,6 +309,7 @@ int ep_dispatch_route(ep_plan* p, const int32_t* indices, const int32_t* n_tok_h
     a.flags = p->flags; a.ticket = p->ticket; a.status = p->status;
     a.rows = p->rows; a.W = p->W; a.E = p->E; a.k = p->k; a.F = p->F; a.M = p->M;
     a.N = off[p->W]; a.tiles = p->tiles;
+    a.vec16 = (p->k % 4 == 0) && aligned(indices, 16);
     for (int s = 0; s <= p->W; ++s) a.tok_off[s] = off[s];
     // the routing kernel always runs all `tiles` CTAs: the ticket arithmetic relies on it
     cudaError_t e = launch_route(a, (cudaStream_t)stream);

@@ -48,6 +48,7 @@ struct RouteArgs {
     int* status;
     int64_t rows;         // W*M
     int W, E, k, F, M, N, tiles;
+    int vec16;            // index rows may be read as 16-byte vectors (k % 4 == 0, idx 16-B aligned)
     int tok_off[kMaxRanks + 1];   // exclusive prefix of per-rank token counts; tok_off[W] = N
 };
 

@@ -118,6 +118,7 @@ extern "C" int ep_route_noalloc(int W, int E, int k, int M, const int32_t* indic
     a.W = W; a.E = E; a.k = k; a.F = W < k ? W : k; a.M = M;
     a.N = a.tok_off[W];
     a.tiles = tiles;
+    a.vec16 = (k % 4 == 0) && ((uintptr_t)indices % 16 == 0);
     e = ep::launch_route(a, s);
     if (e != cudaSuccess) return ep::record_error(EP_ERR_CUDA, cudaGetErrorString(e));
     return EP_OK;

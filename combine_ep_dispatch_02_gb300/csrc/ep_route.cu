@@ -11,10 +11,10 @@
 // prefix sum over tokens of W 0/1 columns, computed here in one pass:
 //   1. one CTA per tile of 256 consecutive tokens takes a tile number from a monotone ticket
 //      (so a CTA only ever waits on tiles whose CTAs are already running);
-//   2. the destination set of each token is the OR over its k slots of (1 << rank); lanes
-//      hold one slot each, in batches of up to 32 slots (k <= 64: "runtime routing loops ...
-//      in wave32-sized batches, including slots 32-63"), OR-reduced with warp shuffles, so a
-//      rank named by several experts counts once;
+//   2. the destination set of each token is the OR over its k slots of (1 << rank), so a rank
+//      named by several experts counts once; each thread loads its token's whole index row
+//      with 16-byte vectors (top-k 1..64: the pages' "runtime routing loops ... including
+//      slots 32-63" become one vector loop per token), so a tile's rows are in flight together;
 //   3. per-rank counts: one ballot per rank gives each token's rank within its warp and the
 //      warp totals; a block scan over the 8 warps gives the tile's own total per rank;
 //   4. decoupled lookback: the tile publishes its totals (status AGGREGATE), then walks back
@@ -38,46 +38,52 @@ __device__ __forceinline__ unsigned long long pack_flag(uint32_t stamp, unsigned
     return ((unsigned long long)stamp << 34) | (st << 32) | (unsigned long long)count;
 }
 
-// Destination-rank masks of the tile's tokens.  KP lanes (a power of two, <= 32) cover the
-// top-k slots of one token; 32/KP tokens per warp pass.
-template <int KP>
-__device__ __forceinline__ void route_masks(const RouteArgs& a, int base, const int* off,
-                                            uint32_t* s_mask, int warp, int lane)
+// Destination-rank mask of one token: OR over its k top-k slots of (1 << rank), so a rank named
+// by several experts counts once.  The thread loads the whole index row at once (16-byte vectors
+// when every row is 16-byte aligned: k % 4 == 0 and a 16-byte aligned array), so a tile's 256 rows are in flight
+// together rather than one slot batch after another; VEC = k / 4 when known at compile time
+// (the pages' dedicated top-k 8 case is VEC = 2), 0 for the runtime loop.
+template <int VEC>
+__device__ __forceinline__ uint32_t token_mask(const RouteArgs& a, const int32_t* row)
 {
-    constexpr int TP = 32 / KP;
-    const int j0 = lane % KP;
-    const int sub = lane / KP;
     const int n_exp = a.W * a.E;
-    for (int pass = 0; pass < KP; ++pass) {
-        const int local = warp * 32 + pass * TP + sub;
-        const int g = base + local;
-        const bool valid = g < a.N;
-        const int32_t* row = nullptr;
-        if (valid) {
-            const int s = rank_of_token(off, a.W, g);
-            row = a.idx + ((int64_t)s * a.M + (g - off[s])) * a.k;
-        }
-        uint32_t m = 0;
-        for (int b = 0; b * KP < a.k; ++b) {      // warp-uniform trip count
-            const int j = b * KP + j0;
-            if (valid && j < a.k) {
-                const int e = __ldg(row + j);
-                if (e >= 0 && e < n_exp)
-                    m |= 1u << (e / a.E);
-                else
-                    record_status(a.status, EP_ERR_INDEX);
-            }
-        }
+    uint32_t m = 0;
+    bool bad = false;
+    auto take = [&](int e) {
+        if (e >= 0 && e < n_exp)
+            m |= 1u << (e / a.E);
+        else
+            bad = true;
+    };
+    if constexpr (VEC > 0) {
+        int4 v[VEC];
 #pragma unroll
-        for (int o = KP / 2; o > 0; o >>= 1) m |= __shfl_xor_sync(0xffffffffu, m, o);
-        if (j0 == 0) s_mask[local] = valid ? m : 0u;
+        for (int q = 0; q < VEC; ++q) v[q] = __ldg(reinterpret_cast<const int4*>(row) + q);
+#pragma unroll
+        for (int q = 0; q < VEC; ++q) {
+            take(v[q].x);
+            take(v[q].y);
+            take(v[q].z);
+            take(v[q].w);
+        }
+    } else if (a.vec16) {
+        for (int q = 0; q < (a.k >> 2); ++q) {
+            const int4 v = __ldg(reinterpret_cast<const int4*>(row) + q);
+            take(v.x);
+            take(v.y);
+            take(v.z);
+            take(v.w);
+        }
+    } else {
+        for (int j = 0; j < a.k; ++j) take(__ldg(row + j));
     }
+    if (bad) record_status(a.status, EP_ERR_INDEX);
+    return m;
 }
 
-template <int KP>
+template <int VEC>
 __global__ void __launch_bounds__(kRouteThreads) ep_route_kernel(const RouteArgs a)
 {
-    __shared__ uint32_t s_mask[kRouteTile];
     __shared__ int s_off[kMaxRanks + 1];
     __shared__ int s_warp[kRouteThreads / 32][kMaxRanks];   // warp totals, then warp prefixes
     __shared__ int s_agg[kMaxRanks];
@@ -95,12 +101,14 @@ __global__ void __launch_bounds__(kRouteThreads) ep_route_kernel(const RouteArgs
     const uint32_t stamp = (uint32_t)((ticket / (unsigned long long)a.tiles + 1ull) & kStampMask);
     const int base = tile * kRouteTile;
 
-    route_masks<KP>(a, base, s_off, s_mask, warp, lane);
-    __syncthreads();
-
     const int g = base + tid;
     const bool valid = g < a.N;
-    const uint32_t mask = valid ? s_mask[tid] : 0u;
+    int s = 0, t = 0;
+    if (valid) {
+        s = rank_of_token(s_off, a.W, g);
+        t = g - s_off[s];
+    }
+    const uint32_t mask = valid ? token_mask<VEC>(a, a.idx + ((int64_t)s * a.M + t) * a.k) : 0u;
     for (int r = 0; r < a.W; ++r) {
         const unsigned bal = __ballot_sync(0xffffffffu, (mask >> r) & 1u);
         if (lane == 0) s_warp[warp][r] = __popc(bal);
@@ -173,11 +181,6 @@ __global__ void __launch_bounds__(kRouteThreads) ep_route_kernel(const RouteArgs
     if (tile == a.tiles - 1 && tid < a.W) a.recv_count[tid] = s_excl[tid] + s_agg[tid];
     // s_excl / s_warp are final: the loop above ended on a barrier (or tile 0 needs no lookback)
 
-    int s = 0, t = 0;
-    if (valid) {
-        s = rank_of_token(s_off, a.W, g);
-        t = g - s_off[s];
-    }
     int32_t* fwd_row = a.fwd + ((int64_t)s * a.M + t) * a.F;
     const unsigned lt = lanemask_lt();
     int j = 0;
@@ -194,10 +197,10 @@ __global__ void __launch_bounds__(kRouteThreads) ep_route_kernel(const RouteArgs
         for (; j < a.F; ++j) fwd_row[j] = -1;
 }
 
-template <int KP>
-cudaError_t launch_kp(const RouteArgs& a, cudaStream_t stream)
+template <int VEC>
+cudaError_t launch_vec(const RouteArgs& a, cudaStream_t stream)
 {
-    ep_route_kernel<KP><<<a.tiles, kRouteThreads, 0, stream>>>(a);
+    ep_route_kernel<VEC><<<a.tiles, kRouteThreads, 0, stream>>>(a);
     return cudaGetLastError();
 }
 
@@ -205,15 +208,14 @@ cudaError_t launch_kp(const RouteArgs& a, cudaStream_t stream)
 
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t stream)
 {
-    // lanes per token: the top-k rounded up to a power of two, capped at one warp; top-k 8
-    // (the pages' specialised case) is one of the compiled widths
-    const int k = a.k < 32 ? a.k : 32;
-    if (k <= 1) return launch_kp<1>(a, stream);
-    if (k <= 2) return launch_kp<2>(a, stream);
-    if (k <= 4) return launch_kp<4>(a, stream);
-    if (k <= 8) return launch_kp<8>(a, stream);
-    if (k <= 16) return launch_kp<16>(a, stream);
-    return launch_kp<32>(a, stream);
+    // compiled row widths: top-k 4, 8 (the pages' specialised case), 16; others loop at run time
+    if (!a.vec16) return launch_vec<0>(a, stream);
+    switch (a.k) {
+    case 4: return launch_vec<1>(a, stream);
+    case 8: return launch_vec<2>(a, stream);
+    case 16: return launch_vec<4>(a, stream);
+    default: return launch_vec<0>(a, stream);
+    }
 }
 
 }  // namespace ep

@@ -454,3 +454,31 @@ def test_grouped_layout_duplicate_ids_and_small_workload():
     wl.indices[1, 7, 3] = wl.indices[1, 7, 1]
     _check_grouped(wl)
     _check_grouped(wlmod.make_workload("small", max_tok=24), seed=1)
+
+
+@pytest.mark.parametrize("k", [4, 16])
+def test_route_compiled_row_widths(k):
+    _check(wlmod.custom_workload(W=8, E=8, k=k, H=256, M=300, n_tok=[300, 299, 0, 1, 256, 257, 2, 300], seed=k))
+
+
+def test_route_with_indices_only_4_byte_aligned():
+    """k % 4 == 0 but the index array starts 4 bytes past a 16-byte boundary: the routing kernel
+    must fall back to scalar loads and route exactly as with an aligned array."""
+    wl = wlmod.make_workload("dsv3", max_tok=200)
+    plan, (x, w, sc, idx) = _setup(wl)
+    d = plan.dispatch_route(idx, wl.n_tok)
+    torch.cuda.synchronize()
+    ref_cnt = d.recv_count.cpu().numpy().copy()
+    ref_pos = d.src_token_pos.cpu().numpy().copy()
+    buf = torch.empty(idx.numel() + 4, dtype=torch.int32, device=DEV)
+    shifted = buf[1:1 + idx.numel()].view(idx.shape)
+    shifted.copy_(idx)
+    assert shifted.data_ptr() % 16 == 4
+    d = plan.dispatch_route(shifted, wl.n_tok)
+    torch.cuda.synchronize()
+    assert plan.status() == 0
+    assert np.array_equal(d.recv_count.cpu().numpy(), ref_cnt)
+    for r in range(wl.W):
+        n = int(ref_cnt[r])
+        assert np.array_equal(d.src_token_pos[r, :n].cpu().numpy(), ref_pos[r, :n])
+    plan.close()
