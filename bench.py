@@ -149,6 +149,22 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": n}
 
 
+# ----------------------------------------------------------------------------- multi-rank
+
+def max_over_ranks(value, dist, device):
+    """The slowest rank's time (replicas: every rank runs the same step on its own GPU)."""
+    if dist is None:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_rank, world, ms_per_step):
+    """Whole-job throughput: every rank's bytes over the slowest rank's time."""
+    return world * bytes_per_rank / (ms_per_step * 1e-3) / 1e9
+
+
 # ----------------------------------------------------------------------------- GPU arm
 
 def run_ours(args, rank, world, dist):
@@ -216,11 +232,7 @@ def run_ours(args, rank, world, dist):
     route = [e[0].elapsed_time(e[1]) for e in evs]
     scat = [e[1].elapsed_time(e[2]) for e in evs]
     comb = [e[2].elapsed_time(e[3]) for e in evs]
-    total_ms = evs[0][0].elapsed_time(evs[-1][3])
-    if dist is not None:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(evs[0][0].elapsed_time(evs[-1][3]), dist, dev)
     ms_step = total_ms / args.steps
     avg = lambda v: sum(v) / len(v)  # noqa: E731
     k_ms = {"route": avg(route), "scatter": avg(scat), "combine": avg(comb)}
@@ -246,7 +258,7 @@ def run_ours(args, rank, world, dist):
         cpu = cpu_baseline(wl, out) if world == 1 else None
         result = {
             "metric": METRIC,
-            "value": round(world * gbs(nbytes["pair"], ms_step), 2),
+            "value": round(whole_job_gbs(nbytes["pair"], world, ms_step), 2),
             "unit": "GB/s",
             "n_gpus": world,
             "steps": args.steps,

@@ -29,6 +29,16 @@ ERR_INDEX = -6
 _p = ctypes.c_void_p
 
 
+def use_library(path):
+    """Point this module at another build of the oracle (the mutation tests compile copies
+    with planted mistakes); None restores the default build."""
+    global _lib
+    with _lock:
+        _lib = None
+    if path is not None:
+        _load(path)
+
+
 def build(force: bool = False) -> str:
     """Compile ep_oracle.c into libep_oracle.so next to it (gcc, no CUDA)."""
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
@@ -39,12 +49,13 @@ def build(force: bool = False) -> str:
     return _LIB
 
 
-def _load():
+def _load(path=None):
     global _lib
     with _lock:
         if _lib is None:
-            build()
-            lib = ctypes.CDLL(_LIB)
+            if path is None:
+                build()
+            lib = ctypes.CDLL(path or _LIB)
             lib.ep_oracle_dispatch.restype = ctypes.c_int
             lib.ep_oracle_dispatch.argtypes = [ctypes.c_int] * 7 + [_p] * 12
             lib.ep_oracle_combine.restype = ctypes.c_int

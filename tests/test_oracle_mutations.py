@@ -1,0 +1,76 @@
+"""The pins catch plausible mistakes: each test plants one mistake in a COPY of the oracle's C
+source (on the CPU), builds it, and checks that the pin aimed at that part of the method fails.
+The oracle itself is never modified."""
+import os
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+import test_oracle as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "ep_oracle.c")
+
+MUTATIONS = {
+    # combine adds ranks in descending order instead of ascending
+    "descending_rank_order": ("for (int r = 0; r < W; ++r) {                 /* ascending destination rank */",
+                              "for (int r = W - 1; r >= 0; --r) {           /* planted */",
+                              pins.test_combine_order_golden),
+    # only the first top-k slot is routed
+    "first_slot_only": ("                in_D[e / E] = 1;", "                if (j == 0) in_D[e / E] = 1;",
+                        None),
+    # reverse map drops the source rank
+    "src_pos_without_rank": ("src_pos[(int64_t)r * rows + slot] = (int32_t)((int64_t)s * rows + t);",
+                             "src_pos[(int64_t)r * rows + slot] = (int32_t)t;",
+                             lambda: pins.test_dispatch_invariants(pins.CASES[0])),
+    # BF16 conversion truncates instead of rounding to nearest even
+    "bf16_truncation": ("    b += 0x7FFFu + kept_lsb;", "    b += 0u * kept_lsb;",
+                        pins.test_bf16_rne_matches_torch_cast),
+    # ties round away from zero instead of to even
+    "bf16_ties_away": ("    b += 0x7FFFu + kept_lsb;", "    b += 0x8000u + 0u * kept_lsb;",
+                       pins.test_bf16_rne_matches_torch_cast),
+    # expert -> rank by modulo instead of contiguous blocks
+    "rank_by_modulo": ("                in_D[e / E] = 1;", "                in_D[e % W] = 1;",
+                       pins.test_brute_force_every_subset),
+    # the weight rows are not summed (last one wins)
+    "weights_overwrite": ("accw[j] = accw[j] + w_in[row * k + j];", "accw[j] = w_in[row * k + j];",
+                          pins.test_combine_weights_dyadic_closed_form),
+    # e4m3 saturation forgotten: values past 448 become NaN
+    "e4m3_no_saturation": ("if (a >= 0x43E00000u) return (uint8_t)(sign | 0x7Eu);",
+                           "if (a >= 0x43F00000u) return (uint8_t)(sign | 0x7Fu);",
+                           pins.test_e4m3_rne_matches_torch_cast),
+    # block scale uses the first element instead of the maximum
+    "scale_not_amax": ("                if (m > amax) amax = m;", "                if (i == 0) amax = m;",
+                       pins.test_blockwise_quantiser_properties),
+    # FP8 wire dequantises with the wrong block's scale
+    "wire_scale_index": ("* scales[row * nb + h / 128];", "* scales[row * nb];",
+                         pins.test_fp8_combine_power_of_two_scales_closed_form),
+    # grouped inverse sums in list order of the last expert only
+    "ungroup_overwrite": ("acc[i * H + h] = acc[i * H + h] + v;", "acc[i * H + h] = v;",
+                          pins.test_ungroup_identity_closed_form),
+}
+
+
+@pytest.fixture(autouse=True)
+def _restore():
+    yield
+    oracle.use_library(None)
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_mistake_is_caught(name, tmp_path):
+    old, new, pin = MUTATIONS[name]
+    src = open(SRC).read()
+    assert src.count(old) >= 1, f"mutation anchor for {name} not found"
+    mutated = src.replace(old, new, 1)
+    c = tmp_path / "mutant.c"
+    c.write_text(mutated)
+    so = tmp_path / "libmutant.so"
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared",
+                           "-o", str(so), str(c)])
+    oracle.use_library(str(so))
+    if pin is None:           # the exactly-once invariant over all cases
+        pin = lambda: [pins.test_dispatch_invariants(c) for c in pins.CASES]  # noqa: E731
+    with pytest.raises((AssertionError, ValueError)):
+        pin()
