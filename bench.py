@@ -174,7 +174,10 @@ def run_ours(args, rank, world, dist):
     local = int(os.environ.get("LOCAL_RANK", "0"))
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    build.build()
+    if local == 0:
+        build.build()           # one build per node; the other ranks wait for it
+    if dist is not None:
+        dist.barrier()
     wl = wlmod.make_workload(WORKLOAD, max_tok=args.tokens_per_rank)
     plan = ep.Plan(wl.W, wl.E, wl.k, wl.H, wl.dtype, wl.sd, wl.M, device=dev)
     x = torch.from_numpy(wl.x.view(np.int16)).to(dev)

@@ -482,3 +482,48 @@ def test_route_with_indices_only_4_byte_aligned():
         n = int(ref_cnt[r])
         assert np.array_equal(d.src_token_pos[r, :n].cpu().numpy(), ref_pos[r, :n])
     plan.close()
+
+
+def test_many_tiles_long_lookback():
+    """W = 32 ranks, 16384 tokens per rank: 2048 routing tiles whose lookback windows cover 8
+    predecessors per step, with tiny rows so the oracle stays fast."""
+    wl = wlmod.custom_workload(W=32, E=2, k=4, H=8, M=16384, n_tok=[16384] * 31 + [1000], seed=12,
+                               with_weights=False)
+    _check(wl)
+
+
+def test_cuda_graph_replay_quantising_dispatch_and_fp8_wire():
+    """The quantising dispatch, the wire quantiser and the FP8 combine captured in one CUDA graph
+    and replayed give the eager results bit for bit."""
+    wl = wlmod.make_workload("dsv3", max_tok=64)
+    plan = gpu_path.make_plan(wl, DEV, plan_dtype="bf16_fp8")
+    x, w, _, idx = gpu_path.to_device(wl, DEV)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        d = plan.dispatch(x, w, None, idx, wl.n_tok, stream=s)
+        y = torch.empty((wl.W, wl.W * wl.M, wl.H), dtype=torch.bfloat16, device=DEV)
+        counts = d.recv_count.cpu().tolist()
+    torch.cuda.synchronize()
+    # dequantising identity expert outside the graph's timed part: a fixed buffer
+    eo = harness.expert_torch(gpu_path.quantised_view(wl), d.recv_x, d.recv_idx, d.recv_w,
+                              d.recv_scales, d.recv_count)
+    y.view(torch.int16).copy_(eo.view(torch.int16))
+    q, sc = plan.quantize_received(y, d.epoch)
+    out, out_w = plan.combine_fp8(q, sc, d.recv_w, d.epoch)
+    torch.cuda.synchronize()
+    eager = (gpu_path.raw(d.recv_x).copy(), gpu_path.raw(out).copy())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        d = plan.dispatch(x, w, None, idx, wl.n_tok, stream=s)
+        plan.quantize_received(y, d.epoch, q=q.view(torch.uint8), scales=sc, stream=s)
+        plan.combine_fp8(q, sc, d.recv_w, d.epoch, out=out, out_w=out_w, stream=s)
+    for _ in range(3):
+        out.zero_()
+        with torch.cuda.stream(s):
+            g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(gpu_path.raw(d.recv_x), eager[0])
+        assert np.array_equal(gpu_path.raw(out), eager[1])
+        assert d.recv_count.cpu().tolist() == counts
+    assert plan.status() == 0
+    plan.close()
