@@ -393,18 +393,34 @@ def measure_grouped(ep, dev, stream, peak, steps):
         plan.ungroup_by_expert(y, d.epoch, out=out, stream=stream)
         e[2].record(stream)
     torch.cuda.synchronize(dev)
+    # unfused (dispatch, then group) against fused (dispatch straight into the grouped view)
+    evf = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for e in evf:
+        e[0].record(stream)
+        d = plan.dispatch(x, w, None, idx, wl.n_tok, stream=stream)
+        plan.group_by_expert(d.epoch, packed_x=px, stream=stream)
+        e[1].record(stream)
+        plan.dispatch_grouped(x, w, None, idx, wl.n_tok, packed_x=px, stream=stream)
+        e[2].record(stream)
+    torch.cuda.synchronize(dev)
     if plan.status() != 0:
         raise RuntimeError("device status after the grouped layout: %d" % plan.status())
     plan.close()
     gt = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
     ut = sum(e[1].elapsed_time(e[2]) for e in ev) / steps
+    unfused = sum(e[0].elapsed_time(e[1]) for e in evf) / steps
+    fused = sum(e[1].elapsed_time(e[2]) for e in evf) / steps
     rb = 2 * wl.H
     gb = rows * (rb + 4 * wl.k) + entries * (rb + 4)
     ub = entries * rb + rows * (rb + 4 * wl.k)
     return {"workload": "W=4, 64 experts/rank, top-8, hidden 7168 BF16, 256 tokens/rank",
             "received_rows": rows, "expert_entries": entries,
             "group_us": round(gt * 1e3, 2), "group_frac": round(gb / (gt * 1e-3) / 1e9 / peak, 4),
-            "ungroup_us": round(ut * 1e3, 2), "ungroup_frac": round(ub / (ut * 1e-3) / 1e9 / peak, 4)}
+            "ungroup_us": round(ut * 1e3, 2), "ungroup_frac": round(ub / (ut * 1e-3) / 1e9 / peak, 4),
+            "dispatch_then_group_us": round(unfused * 1e3, 2),
+            "fused_dispatch_grouped_us": round(fused * 1e3, 2),
+            "fused_frac": round((wl.N * (rb + 8 * wl.k) + entries * rb + rows * (8 * wl.k + 4)) /
+                                (fused * 1e-3) / 1e9 / peak, 4)}
 
 
 def measure_small_batch_latency(ep, dev, tokens=(8, 128, 256), replays=120):

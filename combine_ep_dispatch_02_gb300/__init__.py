@@ -29,7 +29,8 @@ VARIANTS = {"auto": 0, "whole_row": 1, "tiled_512": 2, "tiled_1024": 3}
 EXPORTS = ("ep_plan_create", "ep_plan_destroy", "ep_plan_set_variant", "ep_plan_device_bytes",
            "ep_dispatch", "ep_dispatch_route", "ep_dispatch_scatter", "ep_combine", "ep_reset",
            "ep_status", "ep_strerror", "ep_last_error", "ep_route_noalloc",
-           "ep_quantize_received", "ep_combine_fp8", "ep_group_by_expert", "ep_ungroup_by_expert")
+           "ep_quantize_received", "ep_combine_fp8", "ep_group_by_expert", "ep_ungroup_by_expert",
+           "ep_dispatch_grouped")
 
 
 class EpError(RuntimeError):
@@ -77,6 +78,7 @@ def load_library(path: Optional[str] = None):
         "ep_combine_fp8": (I, [V, V, V, V, V, V, U64, V]),
         "ep_group_by_expert": (I, [V, V, V, V, V, U64, V]),
         "ep_ungroup_by_expert": (I, [V, V, V, U64, V]),
+        "ep_dispatch_grouped": (I, [V, V, V, V, V, V, V, V, V, V, V, ctypes.POINTER(DispatchOut)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -288,6 +290,24 @@ class Plan:
         _check(self._lib.ep_group_by_expert(self._h, _ptr(packed_x), _ptr(count), _ptr(src_info),
                                             _ptr(layout), ctypes.c_uint64(epoch), _stream(stream)))
         return packed_x, count, src_info, layout
+
+    def dispatch_grouped(self, x: torch.Tensor, weights: Optional[torch.Tensor],
+                         scales: Optional[torch.Tensor], indices: torch.Tensor, n_tok: Sequence[int],
+                         packed_x: Optional[torch.Tensor] = None, stream=None):
+        """Dispatch straight into the grouped view: returns (Dispatched, packed_x, packed_count,
+        packed_src_info, layout_range); the Dispatched views' recv_x holds unspecified data."""
+        W, E, R, H = self.W, self.E, self.rows, self.H
+        if packed_x is None:
+            packed_x = torch.empty((W, E, R, H), dtype=self.payload_torch_dtype, device=self.device)
+        count = torch.empty((W, E), dtype=torch.int32, device=self.device)
+        src_info = torch.empty((W, E, R), dtype=torch.int32, device=self.device)
+        layout = torch.empty((W, E, W), dtype=torch.int64, device=self.device)
+        arr, nt = self._n_tok(n_tok)
+        o = DispatchOut()
+        _check(self._lib.ep_dispatch_grouped(self._h, _ptr(x), _ptr(weights), _ptr(scales), _ptr(indices),
+                                             nt, _ptr(packed_x), _ptr(count), _ptr(src_info), _ptr(layout),
+                                             _stream(stream), ctypes.byref(o)))
+        return self._wrap(o), packed_x, count, src_info, layout
 
     def ungroup_by_expert(self, packed_y: torch.Tensor, epoch: int, out: Optional[torch.Tensor] = None,
                           stream=None) -> torch.Tensor:

@@ -501,6 +501,45 @@ int ep_group_by_expert(ep_plan* p, void* packed_x, int32_t* packed_count, int32_
     return EP_OK;
 }
 
+int ep_dispatch_grouped(ep_plan* p, const void* x, const float* weights, const float* scales,
+                        const int32_t* indices, const int32_t* n_tok_host, void* packed_x,
+                        int32_t* packed_count, int32_t* packed_src_info, int64_t* layout_range,
+                        void* stream, ep_dispatch_out* out)
+{
+    if (!p) return fail(EP_ERR_ARG, "ep_dispatch_grouped: plan is NULL");
+    if (p->quantise) return fail(EP_ERR_ARG, "ep_dispatch_grouped: not available for the quantising dtype");
+    if (!x || !aligned(x, 16)) return fail(EP_ERR_ARG, "x is NULL or not 16-byte aligned");
+    if (weights && !aligned(weights, 4)) return fail(EP_ERR_ARG, "weights not 4-byte aligned");
+    if (p->sd > 0 && (!scales || !aligned(scales, 4)))
+        return fail(EP_ERR_ARG, "scale_dim=%d needs a 4-byte aligned scales array", p->sd);
+    if (p->sd == 0 && scales) return fail(EP_ERR_ARG, "scales given but the plan has scale_dim 0");
+    if (!packed_x || !aligned(packed_x, 16) || !packed_count || !aligned(packed_count, 4) ||
+        !packed_src_info || !aligned(packed_src_info, 4) || !layout_range || !aligned(layout_range, 8))
+        return fail(EP_ERR_ARG, "ep_dispatch_grouped: a grouped buffer is NULL or misaligned");
+    if (!out) return fail(EP_ERR_ARG, "out is NULL");
+    int rc = ep_dispatch_route(p, indices, n_tok_host, stream, nullptr);
+    if (rc != EP_OK) return rc;
+    DeviceGuard g(p->device);
+    if (!g.ok) return fail(EP_ERR_CUDA, "cannot select the plan's device %d", p->device);
+    GroupArgs a{};
+    a.recv_count = p->recv_count; a.src_pos = p->src_pos; a.map = p->expert_map;
+    a.packed_x = (uint8_t*)packed_x; a.count = packed_count; a.src_info = packed_src_info;
+    a.layout_range = (long long*)layout_range;
+    a.src_idx = indices; a.x = (const uint8_t*)x; a.w = weights; a.scales = scales; a.fwd = p->fwd;
+    a.recv_idx_out = p->recv_idx; a.recv_w_out = p->recv_w; a.recv_scales_out = p->recv_scales;
+    a.rows = p->rows; a.row_bytes = p->row_bytes;
+    a.W = p->W; a.E = p->E; a.k = p->k; a.M = p->M; a.F = p->F; a.N = p->N; a.sd = p->sd;
+    for (int s = 0; s <= p->W; ++s) a.tok_off[s] = p->tok_off[s];
+    cudaError_t e = launch_group_from_source(a, p->num_sms, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "ep_dispatch_grouped: launch");
+    p->routed = false;
+    p->live = true;
+    p->has_w = weights != nullptr;
+    p->grouped_epoch = p->epoch;
+    fill_out(p, out);
+    return EP_OK;
+}
+
 int ep_ungroup_by_expert(ep_plan* p, const void* packed_y, void* out, uint64_t epoch, void* stream)
 {
     if (!p) return fail(EP_ERR_ARG, "ep_ungroup_by_expert: plan is NULL");

@@ -113,9 +113,19 @@ struct GroupArgs {
     long long* layout_range;     // [W][E][W]
     const uint8_t* packed_y;     // [W][E][W*M][H] 16-bit expert outputs (inverse)
     uint8_t* out;                // [W][W*M][H] 16-bit combine input (inverse)
+    // fused dispatch into the grouped view: the source side
+    const int32_t* src_idx;      // [W][M][k] source index rows (grouping reads these if set)
+    const uint8_t* x;            // [W][M][row_bytes] source payload rows
+    const float* w;              // [W][M][k] or NULL
+    const float* scales;         // [W][M][sd] or NULL
+    const int32_t* fwd;          // [W][M][F]
+    int32_t* recv_idx_out;       // metadata rows of the receive buffers
+    float* recv_w_out;
+    float* recv_scales_out;
     int64_t rows;                // W*M
     int64_t row_bytes;           // payload bytes (grouping) / 16-bit row bytes (inverse)
-    int W, E, k;
+    int W, E, k, M, F, N, sd;
+    int tok_off[kMaxRanks + 1];
 };
 
 // Host-side launchers, one per kernel translation unit.
@@ -128,6 +138,8 @@ cudaError_t launch_combine(const CombineArgs& a, bool fp16, int num_sms, cudaStr
 cudaError_t launch_quantise_rows(const WireArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_group(const GroupArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_ungroup(const GroupArgs& a, bool fp16, int num_sms, cudaStream_t stream);
+// dispatch straight into the grouped view (needs routing done; a.src_idx, a.x, a.fwd set)
+cudaError_t launch_group_from_source(const GroupArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_combine_fp8(const WireArgs& a, int num_sms, cudaStream_t stream);
 // choose combine's slice of a row per work unit (a.H and a.N set)
 void combine_geometry(CombineArgs& a, int variant, int num_sms);

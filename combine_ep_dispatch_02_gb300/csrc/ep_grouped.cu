@@ -55,7 +55,14 @@ __global__ void __launch_bounds__(256) ep_group_kernel(const GroupArgs a)
         const int i = i0 + tid;
         int jfirst = -1;
         if (i < n) {
-            const int32_t* ids = a.recv_idx + ((int64_t)r * a.rows + i) * a.k;
+            const int32_t* ids;
+            if (a.src_idx) {        // fused dispatch: the row's index row is its source's
+                const int32_t pos = a.src_pos[(int64_t)r * a.rows + i];
+                const int64_t s = pos / a.rows;
+                ids = a.src_idx + (s * a.M + (pos - s * a.rows)) * a.k;
+            } else {
+                ids = a.recv_idx + ((int64_t)r * a.rows + i) * a.k;
+            }
             for (int j = 0; j < a.k; ++j)
                 if (__ldg(ids + j) == ge) { jfirst = j; break; }
         }
@@ -264,6 +271,80 @@ __global__ void __launch_bounds__(kCopyThreads, 2) ep_ungroup_kernel(const Group
     }
 }
 
+// Fused dispatch into the grouped view: warp per source token.  Lane j owns top-k slot j: when
+// it is the row's first slot naming its expert e (rank r = e / E), its packed row is
+// (r*E + e - r*E) * rows + slot, the slot being the one ep_group_kernel recorded for the
+// token's receive row on rank r (found in the forward map).  The source row is read once and
+// written to every such packed row; the token's index / weight / scale rows go to its receive
+// rows as in ep_dispatch.  The 2-D payload rows are not written.
+__global__ void __launch_bounds__(kCopyThreads) ep_group_from_source_kernel(const GroupArgs a)
+{
+    __shared__ int s_off[kMaxRanks + 1];
+    if (threadIdx.x <= a.W) s_off[threadIdx.x] = a.tok_off[threadIdx.x];
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = (int64_t)gridDim.x * (kCopyThreads / 32);
+    const int nvec = (int)(a.row_bytes >> 4);
+    for (int64_t g = (int64_t)blockIdx.x * (kCopyThreads / 32) + (threadIdx.x >> 5); g < a.N; g += nwarps) {
+        const int s = rank_of_token(s_off, a.W, (int)g);
+        const int64_t tok = (int64_t)s * a.M + (g - s_off[s]);
+        const int32_t* ids = a.src_idx + tok * a.k;
+        const int fw = lane < a.F ? __ldg(a.fwd + tok * a.F + lane) : -1;   // receive rows, by rank
+        const int nd = __popc(__ballot_sync(0xffffffffu, fw >= 0));
+        // metadata rows to the receive rows, as in ep_dispatch
+        for (int d = 0; d < nd; ++d) {
+            const int64_t row = __shfl_sync(0xffffffffu, fw, d);
+            for (int e = lane; e < a.k; e += 32) {
+                a.recv_idx_out[row * a.k + e] = __ldg(ids + e);
+                if (a.w) a.recv_w_out[row * a.k + e] = __ldg(a.w + tok * a.k + e);
+            }
+            for (int e = lane; e < a.sd; e += 32)
+                a.recv_scales_out[row * a.sd + e] = __ldg(a.scales + tok * a.sd + e);
+        }
+        const uint8_t* src = a.x + tok * a.row_bytes;
+        for (int j0 = 0; j0 < a.k; j0 += 32) {
+            const int j = j0 + lane;
+            int64_t dest = -1;
+            int e = -1, r = -1;
+            if (j < a.k) {
+                e = ids[j];
+                bool first = e >= 0 && e < a.W * a.E;
+                for (int jj = 0; jj < j && first; ++jj) first = ids[jj] != e;
+                if (first) r = e / a.E;
+            }
+            // the token's receive row on rank r: one of the forward-map entries (uniform loop)
+            int64_t rrow = -1;
+            for (int d = 0; d < nd; ++d) {
+                const int64_t row = __shfl_sync(0xffffffffu, fw, d);
+                if (r >= 0 && row / a.rows == r) rrow = row;
+            }
+            if (rrow >= 0) {
+                const int slot = a.map[rrow * a.k + j];
+                dest = ((int64_t)r * a.E + (e - r * a.E)) * a.rows + slot;
+            }
+            const unsigned has = __ballot_sync(0xffffffffu, dest >= 0);
+            if (!has) continue;
+            for (int v0 = 0; v0 < nvec; v0 += 32 * 4) {
+                uint4 buf[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int v = v0 + q * 32 + lane;
+                    if (v < nvec) buf[q] = ld_stream_v4(src + (int64_t)v * 16);
+                }
+                for (unsigned m = has; m; m &= m - 1) {
+                    const int64_t prow = __shfl_sync(0xffffffffu, dest, __ffs(m) - 1);
+                    uint8_t* dst = a.packed_x + prow * a.row_bytes;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int v = v0 + q * 32 + lane;
+                        if (v < nvec) st_v4(dst + (int64_t)v * 16, buf[q]);
+                    }
+                }
+            }
+        }
+    }
+}
+
 int grid_of(const void* kernel, int64_t warps, int num_sms)
 {
     int per_sm = 0;
@@ -276,6 +357,16 @@ int grid_of(const void* kernel, int64_t warps, int num_sms)
 }
 
 }  // namespace
+
+cudaError_t launch_group_from_source(const GroupArgs& a, int num_sms, cudaStream_t stream)
+{
+    ep_group_kernel<<<a.W * a.E, 256, 0, stream>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || a.N == 0) return e;
+    ep_group_from_source_kernel<<<grid_of((const void*)ep_group_from_source_kernel, a.N, num_sms),
+                                  kCopyThreads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_group(const GroupArgs& a, int num_sms, cudaStream_t stream)
 {

@@ -210,6 +210,20 @@ int ep_group_by_expert(ep_plan* p, void* packed_x, int32_t* packed_count, int32_
                        int64_t* layout_range, uint64_t epoch, void* stream);
 int ep_ungroup_by_expert(ep_plan* p, const void* packed_y, void* out, uint64_t epoch, void* stream);
 
+/*
+ * Dispatch straight into the grouped view (guide, section 4, dispatch_standard_moe(): "Combined
+ * dispatch + format conversion in a single launch").  Arguments as ep_dispatch plus the four
+ * grouped buffers of ep_group_by_expert.  Each source row is read once and written to the slot
+ * of every expert it names; the plan's 2-D receive PAYLOAD rows are not written (recv_x holds
+ * unspecified data), while the receive metadata (index, weight, scale rows, src_token_pos,
+ * counts) and the grouped outputs are exactly those of ep_dispatch + ep_group_by_expert, so
+ * ep_ungroup_by_expert and then ep_combine work on the result.  Not for EP_BF16_TO_FP8_E4M3.
+ */
+int ep_dispatch_grouped(ep_plan* p, const void* x, const float* weights, const float* scales,
+                        const int32_t* indices, const int32_t* n_tok_host, void* packed_x,
+                        int32_t* packed_count, int32_t* packed_src_info, int64_t* layout_range,
+                        void* stream, ep_dispatch_out* out);
+
 /* End the live dispatch (guide, reset()): its views become invalid and ep_combine on its epoch
  * fails.  No device work is needed: the scan flags carry a per-call stamp. */
 int ep_reset(ep_plan* p, void* stream);

@@ -406,7 +406,7 @@ def test_fp8_wire_rejects_fp16_plans_and_stale_epochs():
 
 # ---------------------------------------------------------------- expert-grouped layout
 
-def _check_grouped(wl, seed=0):
+def _check_grouped(wl, seed=0, fused=False):
     disp = oracle.dispatch(wl.W, wl.E, wl.k, wl.H, wl.elem_bytes, wl.sd, wl.M, wl.x, wl.weights,
                            wl.scales, wl.indices, wl.n_tok)
     g = oracle.group_by_expert(wl.W, wl.E, wl.k, wl.H, wl.elem_bytes, wl.M, disp)
@@ -417,11 +417,25 @@ def _check_grouped(wl, seed=0):
     o_out = oracle.ungroup_by_expert(wl.W, wl.E, wl.H, fp16, wl.M, disp["recv_count"], g, y)
 
     plan, (x, w, sc, idx) = _setup(wl)
-    d = plan.dispatch(x, w, sc, idx, wl.n_tok)
-    px, cnt, info, layout = plan.group_by_expert(d.epoch)
+    if fused:
+        d, px, cnt, info, layout = plan.dispatch_grouped(x, w, sc, idx, wl.n_tok)
+    else:
+        d = plan.dispatch(x, w, sc, idx, wl.n_tok)
+        px, cnt, info, layout = plan.group_by_expert(d.epoch)
     out = plan.ungroup_by_expert(torch.from_numpy(y.view(np.int16)).to(DEV), d.epoch)
     torch.cuda.synchronize()
     assert plan.status() == 0
+    # the receive metadata is exactly the plain dispatch's (fused: payload rows are not written)
+    dc = d.recv_count.cpu().numpy()
+    assert np.array_equal(dc, disp["recv_count"])
+    for r in range(wl.W):
+        n = int(dc[r])
+        assert np.array_equal(d.src_token_pos[r, :n].cpu().numpy(), disp["src_pos"][r, :n])
+        assert np.array_equal(d.recv_idx[r, :n].cpu().numpy(), disp["recv_idx"][r, :n])
+        if wl.weights is not None:
+            assert np.array_equal(d.recv_w[r, :n].cpu().numpy(), disp["recv_w"][r, :n])
+        if wl.sd:
+            assert np.array_equal(d.recv_scales[r, :n].cpu().numpy(), disp["recv_scales"][r, :n])
     cnt = cnt.cpu().numpy()
     assert np.array_equal(cnt, g["packed_count"])
     assert np.array_equal(layout.cpu().numpy(), g["layout_range"])
@@ -446,6 +460,7 @@ def _check_grouped(wl, seed=0):
 ], ids=lambda c: f"W{c['W']}E{c['E']}k{c['k']}{c['dtype']}")
 def test_grouped_layout(case):
     _check_grouped(wlmod.custom_workload(seed=5, **case))
+    _check_grouped(wlmod.custom_workload(seed=5, **case), fused=True)
 
 
 def test_grouped_layout_duplicate_ids_and_small_workload():
@@ -453,7 +468,9 @@ def test_grouped_layout_duplicate_ids_and_small_workload():
     wl.indices[0, 3, 2] = wl.indices[0, 3, 0]       # the same expert twice in one top-k row
     wl.indices[1, 7, 3] = wl.indices[1, 7, 1]
     _check_grouped(wl)
+    _check_grouped(wl, fused=True)
     _check_grouped(wlmod.make_workload("small", max_tok=24), seed=1)
+    _check_grouped(wlmod.make_workload("small", max_tok=24), seed=1, fused=True)
 
 
 @pytest.mark.parametrize("k", [4, 16])
