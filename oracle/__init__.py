@@ -64,6 +64,16 @@ def _load(path=None):
             lib.ep_oracle_group_by_expert.argtypes = [ctypes.c_int] * 6 + [_p] * 9
             lib.ep_oracle_ungroup_by_expert.restype = ctypes.c_int
             lib.ep_oracle_ungroup_by_expert.argtypes = [ctypes.c_int] * 5 + [_p] * 5
+            lib.ep_oracle_quantize_mxfp4.restype = ctypes.c_int
+            lib.ep_oracle_quantize_mxfp4.argtypes = [ctypes.c_int64, ctypes.c_int, _p, _p, _p]
+            lib.ep_oracle_combine_fp4.restype = ctypes.c_int
+            lib.ep_oracle_combine_fp4.argtypes = [ctypes.c_int] * 4 + [_p] * 7
+            lib.ep_oracle_e2m1_from_f32.restype = ctypes.c_uint8
+            lib.ep_oracle_e2m1_from_f32.argtypes = [ctypes.c_float]
+            lib.ep_oracle_f32_from_e2m1.restype = ctypes.c_float
+            lib.ep_oracle_f32_from_e2m1.argtypes = [ctypes.c_uint8]
+            lib.ep_oracle_f32_from_e8m0.restype = ctypes.c_float
+            lib.ep_oracle_f32_from_e8m0.argtypes = [ctypes.c_uint8]
             lib.ep_oracle_combine_fp8.restype = ctypes.c_int
             lib.ep_oracle_combine_fp8.argtypes = [ctypes.c_int] * 4 + [_p] * 7
             lib.ep_oracle_quantize_e4m3_blockwise.restype = ctypes.c_int
@@ -191,6 +201,47 @@ def ungroup_by_expert(W, E, H, out_fp16, M, recv_count, grouped, packed_y):
     if st != 0:
         raise ValueError("ep_oracle_ungroup_by_expert: invalid arguments")
     return out
+
+
+def e2m1_from_f32(v):
+    return int(_load().ep_oracle_e2m1_from_f32(float(v)))
+
+
+def f32_from_e2m1(c):
+    return float(_load().ep_oracle_f32_from_e2m1(int(c)))
+
+
+def f32_from_e8m0(c):
+    return float(_load().ep_oracle_f32_from_e8m0(int(c)))
+
+
+def quantize_mxfp4(x_bf16):
+    """MX FP4 quantisation of BF16 rows [..., H] (H a multiple of 32): returns (q uint8
+    [..., H/2] packed nibbles, scales uint8 [..., H/32] e8m0 codes)."""
+    x = np.ascontiguousarray(x_bf16).view(np.uint16)
+    H = x.shape[-1]
+    rows = x.size // H
+    q = np.empty(x.shape[:-1] + (H // 2,), dtype=np.uint8)
+    sc = np.empty(x.shape[:-1] + (H // 32,), dtype=np.uint8)
+    if _load().ep_oracle_quantize_mxfp4(rows, H, _ptr(x), _ptr(q), _ptr(sc)) != 0:
+        raise ValueError("quantize_mxfp4: hidden must be a positive multiple of 32")
+    return q, sc
+
+
+def combine_fp4(W, k, H, M, n_tok, slot_of, q, scales, w_in=None):
+    """Combine over the MX FP4 wire (see ep_oracle_combine_fp4): returns (out, out_w)."""
+    lib = _load()
+    n_tok = np.ascontiguousarray(n_tok, dtype=np.int32)
+    slot_of = np.ascontiguousarray(slot_of, dtype=np.int32)
+    q = np.ascontiguousarray(q).view(np.uint8)
+    scales = np.ascontiguousarray(scales).view(np.uint8)
+    out = np.zeros((W, M, H), dtype=np.uint16)
+    out_w = np.zeros((W, M, k), dtype=np.float32) if w_in is not None else None
+    w_in = None if w_in is None else np.ascontiguousarray(w_in, dtype=np.float32)
+    if lib.ep_oracle_combine_fp4(W, k, H, M, _ptr(n_tok), _ptr(slot_of), _ptr(q), _ptr(scales),
+                                 _ptr(w_in), _ptr(out), _ptr(out_w)) != 0:
+        raise ValueError("ep_oracle_combine_fp4: invalid arguments")
+    return out, out_w
 
 
 def bf16_from_f32(a):

@@ -461,3 +461,132 @@ int ep_oracle_ungroup_by_expert(int W, int E, int H, int out_fp16, int M, const 
     }
     return EP_ORACLE_OK;
 }
+
+/* ---- Combine over an FP4 (MX) wire -------------------------------------------------- */
+
+/*
+ * FP4 e2m1 (1 sign, 2 exponent bits with bias 1, 1 fraction bit): magnitudes 0, 0.5, 1, 1.5,
+ * 2, 3, 4, 6.  Round to nearest; a tie goes to the code with a zero fraction bit (even);
+ * magnitudes past 6 saturate to 6; NaN maps to 6 with its sign (the format has no NaN).
+ * Written by comparing against the eight magnitudes, from the definition of the format.
+ */
+uint8_t ep_oracle_e2m1_from_f32(float f)
+{
+    static const float mag[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
+    uint32_t b = f32_bits(f);
+    uint8_t sign = (uint8_t)((b >> 28) & 0x8u);
+    float a = bits_f32(b & 0x7FFFFFFFu);
+    if (!(a <= 6.0f)) return (uint8_t)(sign | 0x7u);            /* > 6, Inf, NaN */
+    int best = 0;
+    for (int c = 1; c < 8; ++c) {
+        float dc = a - mag[c] < 0 ? mag[c] - a : a - mag[c];
+        float db = a - mag[best] < 0 ? mag[best] - a : a - mag[best];
+        if (dc < db || (dc == db && (c & 1) == 0)) best = c;
+    }
+    return (uint8_t)(sign | best);
+}
+
+float ep_oracle_f32_from_e2m1(uint8_t q)
+{
+    static const float mag[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
+    float v = mag[q & 0x7u];
+    return (q & 0x8u) ? -v : v;
+}
+
+/* e8m0 scale code -> 2^(code - 127) (code 255 would be NaN; never produced here) */
+float ep_oracle_f32_from_e8m0(uint8_t c)
+{
+    if (c == 0) return bits_f32(0x00400000u);                   /* 2^-127 */
+    return bits_f32((uint32_t)c << 23);
+}
+
+/*
+ * MX FP4 quantisation of BF16 rows (the "mxfp4" wire of the MORI-EP pages, read as the OCP
+ * microscaling layout): blocks of 32 elements; with amax = max |x| of the block,
+ *   shared exponent e = floor(log2(amax)) - 2   (2 = exponent of e2m1's largest value, 6)
+ *   scale code       = e + 127, clamped to 0..254; an all-zero block uses code 127 (scale 1)
+ *   codes            = e2m1 of (x / 2^e), exact division by a power of two, then RNE above
+ * q [rows][H/2]: element 2i in the low nibble of byte i, 2i+1 in the high nibble;
+ * scales [rows][H/32] e8m0 codes.  H must be a multiple of 32.
+ */
+int ep_oracle_quantize_mxfp4(int64_t rows, int H, const uint16_t* x, uint8_t* q, uint8_t* scales)
+{
+    if (H < 32 || H % 32 != 0 || rows < 0) return EP_ORACLE_ERR_ARG;
+    const int nb = H / 32;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int b = 0; b < nb; ++b) {
+            const uint16_t* xb = x + r * H + b * 32;
+            float amax = 0.0f;
+            for (int i = 0; i < 32; ++i) {
+                float v = ep_oracle_f32_from_bf16(xb[i]);
+                float m = v < 0.0f ? -v : v;
+                if (m > amax) amax = m;
+            }
+            int code = 127;
+            if (amax > 0.0f) {
+                uint32_t ab = f32_bits(amax);
+                int e2 = (int)(ab >> 23) - 127;                 /* floor(log2) of a normal */
+                if ((ab >> 23) == 0) {                          /* subnormal amax */
+                    uint32_t m = ab & 0x7FFFFFu;
+                    e2 = -127;
+                    while (!(m & 0x400000u)) { m <<= 1; --e2; }
+                }
+                code = e2 - 2 + 127;
+                if (code < 0) code = 0;
+                if (code > 254) code = 254;
+            }
+            scales[r * nb + b] = (uint8_t)code;
+            const float s = ep_oracle_f32_from_e8m0((uint8_t)code);
+            for (int i = 0; i < 32; i += 2) {
+                uint8_t lo = ep_oracle_e2m1_from_f32(ep_oracle_f32_from_bf16(xb[i]) / s);
+                uint8_t hi = ep_oracle_e2m1_from_f32(ep_oracle_f32_from_bf16(xb[i + 1]) / s);
+                q[r * (H / 2) + b * 16 + i / 2] = (uint8_t)(lo | (hi << 4));
+            }
+        }
+    }
+    return EP_ORACLE_OK;
+}
+
+/*
+ * Combine over the MX FP4 wire: as ep_oracle_combine_fp8, with each term
+ *   v = float(code) * 2^(scale_code - 127)    (exact: a 2-bit significand times a power of two)
+ * added in ascending rank order in FP32 from +0.0f; BF16 RNE output.
+ *   q [W][W*M][H/2], scales [W][W*M][H/32].
+ */
+int ep_oracle_combine_fp4(int W, int k, int H, int M, const int32_t* n_tok, const int32_t* slot_of,
+                          const uint8_t* q, const uint8_t* scales, const float* w_in, uint16_t* out,
+                          float* out_w)
+{
+    if (W < 1 || k < 1 || H < 32 || H % 32 != 0 || M < 1) return EP_ORACLE_ERR_ARG;
+    const int64_t rows = (int64_t)W * M;
+    const int nb = H / 32;
+    float* acc = (float*)malloc((size_t)H * sizeof(float));
+    float* accw = (float*)malloc((size_t)k * sizeof(float));
+    if (!acc || !accw) { free(acc); free(accw); return EP_ORACLE_ERR_ARG; }
+    for (int s = 0; s < W; ++s) {
+        for (int t = 0; t < n_tok[s]; ++t) {
+            const int64_t tok = (int64_t)s * M + t;
+            for (int h = 0; h < H; ++h) acc[h] = 0.0f;
+            for (int j = 0; j < k; ++j) accw[j] = 0.0f;
+            for (int r = 0; r < W; ++r) {
+                const int32_t slot = slot_of[tok * W + r];
+                if (slot < 0) continue;
+                const int64_t row = (int64_t)r * rows + slot;
+                for (int h = 0; h < H; ++h) {
+                    uint8_t byte = q[row * (H / 2) + h / 2];
+                    uint8_t code = (h & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xFu);
+                    float v = ep_oracle_f32_from_e2m1(code) * ep_oracle_f32_from_e8m0(scales[row * nb + h / 32]);
+                    acc[h] = acc[h] + v;
+                }
+                if (w_in)
+                    for (int j = 0; j < k; ++j) accw[j] = accw[j] + w_in[row * k + j];
+            }
+            for (int h = 0; h < H; ++h) out[tok * H + h] = ep_oracle_bf16_from_f32(acc[h]);
+            if (w_in && out_w)
+                for (int j = 0; j < k; ++j) out_w[tok * k + j] = accw[j];
+        }
+    }
+    free(acc);
+    free(accw);
+    return EP_ORACLE_OK;
+}

@@ -519,3 +519,67 @@ def test_ungroup_sums_in_ascending_expert_order():
         y[0, e, 0, :] = v
     out = oracle.ungroup_by_expert(W, E, H, False, M, disp["recv_count"], g, y)
     assert np.all(out[0, 0] == 0x3F81)
+
+
+# ---------------------------------------------------------------- MX FP4 wire (F2, FP4 form)
+
+_E2M1 = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def _e2m1_brute(v):
+    """Nearest e2m1 magnitude by enumeration in float64; ties to the even code; saturate at 6."""
+    a = min(abs(float(v)), 6.0)
+    d = [abs(a - m) for m in _E2M1]
+    best = min(range(8), key=lambda c: (d[c], c & 1))
+    return best | (8 if np.signbit(v) else 0)
+
+
+def test_e2m1_rne_brute_force():
+    grid = np.concatenate([np.arange(0, 7.01, 0.03125), np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0,
+                                                                 5.99, 6.01, 100.0, 1e-9])])
+    vals = np.concatenate([grid, -grid]).astype(np.float32)
+    for v in vals:
+        assert oracle.e2m1_from_f32(v) == _e2m1_brute(v), v
+    for c in range(16):                         # decode then encode is the identity (but -0)
+        v = oracle.f32_from_e2m1(c)
+        assert oracle.e2m1_from_f32(v) == (c if c != 8 else 8)
+        assert abs(v) == _E2M1[c & 7]
+
+
+def test_mxfp4_quantiser_against_numpy():
+    rng = np.random.default_rng(21)
+    rows, H = 40, 256
+    xf = (rng.standard_normal((rows, H)) * np.exp(rng.uniform(-8, 8, (rows, 1)))).astype(np.float32)
+    xf[3, :32] = 0.0                                   # all-zero block: scale code 127
+    x = _bf16(xf)
+    q, sc = oracle.quantize_mxfp4(x)
+    xs = (x.astype(np.uint32) << 16).view(np.float32).reshape(rows, H // 32, 32).astype(np.float64)
+    amax = np.abs(xs).max(axis=2)
+    exp_code = np.where(amax > 0, np.floor(np.log2(np.where(amax > 0, amax, 1.0))) - 2 + 127, 127)
+    assert np.array_equal(sc.astype(np.int64), np.clip(exp_code, 0, 254).astype(np.int64))
+    scale = 2.0 ** (sc.astype(np.float64) - 127)
+    codes = np.stack([q & 0xF, q >> 4], axis=-1).reshape(rows, H // 32, 32)
+    for r in range(0, rows, 7):
+        for b in range(H // 32):
+            for i in range(32):
+                assert codes[r, b, i] == _e2m1_brute(xs[r, b, i] / scale[r, b]), (r, b, i)
+
+
+def test_fp4_combine_exact_sums():
+    """Dequantised terms are exact (2-bit significands times powers of two) and span a small
+    exponent range here, so the FP32 sum is exact: out = BF16(float64 sum of the terms)."""
+    wl = wlmod.custom_workload(W=4, E=4, k=3, H=64, M=12, n_tok=[12, 5, 0, 9], seed=3)
+    disp = _run(wl)
+    q, sc = oracle.quantize_mxfp4(disp["recv_x"])
+    out, _ = oracle.combine_fp4(wl.W, wl.k, wl.H, wl.M, wl.n_tok, disp["slot_of"], q, sc)
+    codes = np.stack([q & 0xF, q >> 4], axis=-1).reshape(q.shape[:-1] + (wl.H,))
+    mags = np.array(_E2M1 * 2) * np.where(np.arange(16) >= 8, -1.0, 1.0)
+    deq = mags[codes] * np.repeat(2.0 ** (sc.astype(np.float64) - 127), 32, axis=-1)
+    for s in range(wl.W):
+        for t in range(int(wl.n_tok[s])):
+            tot = np.zeros(wl.H)
+            for r in range(wl.W):
+                if disp["slot_of"][s, t, r] >= 0:
+                    tot += deq[r, disp["slot_of"][s, t, r]]
+            ref = torch.from_numpy(tot.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy()
+            assert np.array_equal(out[s, t].view(np.int16), ref)
