@@ -249,8 +249,10 @@ def run_ours(args, rank, world, dist):
     e2e = measure_e2e(plan, wl, dev, stream, nbytes["pair"], steps=max(3, min(args.steps, 20)))
     quant = measure_quantised_dispatch(ep, wl, dev, stream, x, w, idx, P, peak,
                                        steps=max(3, min(args.steps, 50)))
-    wire = measure_fp8_combine_wire(plan, wl, dev, stream, x, w, idx, P, peak,
-                                    steps=max(3, min(args.steps, 50)))
+    wire = measure_combine_wire(plan, wl, dev, stream, x, w, idx, P, peak,
+                                steps=max(3, min(args.steps, 50)), fmt="fp8")
+    wire4 = measure_combine_wire(plan, wl, dev, stream, x, w, idx, P, peak,
+                                 steps=max(3, min(args.steps, 50)), fmt="fp4")
     grouped = measure_grouped(ep, dev, stream, peak, steps=max(3, min(args.steps, 50)))
     latency = measure_small_batch_latency(ep, dev)
     if plan.status() != 0:
@@ -296,6 +298,7 @@ def run_ours(args, rank, world, dist):
             "cpu_baseline": cpu,
             "fp8_quantising_dispatch": quant,
             "fp8_combine_wire": wire,
+            "fp4_combine_wire": wire4,
             "expert_grouped_layout": grouped,
             "small_batch_latency_us": latency,
         }
@@ -334,38 +337,46 @@ def measure_quantised_dispatch(ep, wl, dev, stream, x, w, idx, P, peak, steps):
             "dispatch_frac": round(nb / ((route + scat) * 1e-3) / 1e9 / peak, 4)}
 
 
-def measure_fp8_combine_wire(plan, wl, dev, stream, x, w, idx, P, peak, steps):
-    """Combine over the FP8 wire: the received expert rows (identity expert) are quantised once
-    per step, and the gather-reduce reads codes + scales.  Minimal bytes: quantise reads P*2H and
-    writes P*(H + 4H/128); combine reads P*(H + 4H/128 + 4k) + N*4*min(W,k) and writes
-    N*(2H + 4k)."""
+def measure_combine_wire(plan, wl, dev, stream, x, w, idx, P, peak, steps, fmt):
+    """Combine over a low-precision wire: the received expert rows (identity expert) are
+    quantised once per step, and the gather-reduce reads codes + scales.  Minimal bytes per
+    received row for the codes and scales: FP8 H + 4H/128, MX FP4 H/2 + H/32.  Quantise reads
+    P*2H and writes P*(codes + scales); combine reads P*(codes + scales + 4k) + N*4*min(W,k)
+    and writes N*(2H + 4k)."""
     d = plan.dispatch(x, w, None, idx, wl.n_tok, stream=stream)
-    q, sc = plan.quantize_received(d.recv_x, d.epoch, stream=stream)
+    if fmt == "fp8":
+        quantise, combine = plan.quantize_received, plan.combine_fp8
+        wire_row = wl.H + 4 * (wl.H // 128)
+    else:
+        quantise, combine = plan.quantize_received_fp4, plan.combine_fp4
+        wire_row = wl.H // 2 + wl.H // 32
+    q, sc = quantise(d.recv_x, d.epoch, stream=stream)
+    qb = q.view(torch.uint8)
     out = torch.empty((wl.W, wl.M, wl.H), dtype=torch.bfloat16, device=dev)
     out_w = torch.empty((wl.W, wl.M, wl.k), dtype=torch.float32, device=dev)
     for _ in range(3):
-        plan.quantize_received(d.recv_x, d.epoch, q=q.view(torch.uint8), scales=sc, stream=stream)
-        plan.combine_fp8(q, sc, d.recv_w, d.epoch, out=out, out_w=out_w, stream=stream)
+        quantise(d.recv_x, d.epoch, q=qb, scales=sc, stream=stream)
+        combine(q, sc, d.recv_w, d.epoch, out=out, out_w=out_w, stream=stream)
     torch.cuda.synchronize(dev)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
     for e in ev:
         e[0].record(stream)
-        plan.quantize_received(d.recv_x, d.epoch, q=q.view(torch.uint8), scales=sc, stream=stream)
+        quantise(d.recv_x, d.epoch, q=qb, scales=sc, stream=stream)
         e[1].record(stream)
-        plan.combine_fp8(q, sc, d.recv_w, d.epoch, out=out, out_w=out_w, stream=stream)
+        combine(q, sc, d.recv_w, d.epoch, out=out, out_w=out_w, stream=stream)
         e[2].record(stream)
     torch.cuda.synchronize(dev)
     if plan.status() != 0:
-        raise RuntimeError("device status after the FP8 combine wire: %d" % plan.status())
+        raise RuntimeError("device status after the %s combine wire: %d" % (fmt, plan.status()))
     qt = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
     ct = sum(e[1].elapsed_time(e[2]) for e in ev) / steps
     N, H, k, F = wl.N, wl.H, wl.k, min(wl.W, wl.k)
-    qb = P * (2 * H + H + 4 * (H // 128))
-    cb = P * (H + 4 * (H // 128) + 4 * k) + N * 4 * F + N * (2 * H + 4 * k)
+    qbytes = P * (2 * H + wire_row)
+    cb = P * (wire_row + 4 * k) + N * 4 * F + N * (2 * H + 4 * k)
     return {"quantize_us": round(qt * 1e3, 2), "combine_us": round(ct * 1e3, 2),
             "combine_algorithmic_bytes": cb, "combine_gbs": round(cb / (ct * 1e-3) / 1e9, 1),
             "combine_frac": round(cb / (ct * 1e-3) / 1e9 / peak, 4),
-            "quantize_frac": round(qb / (qt * 1e-3) / 1e9 / peak, 4)}
+            "quantize_frac": round(qbytes / (qt * 1e-3) / 1e9 / peak, 4)}
 
 
 def measure_grouped(ep, dev, stream, peak, steps):

@@ -30,7 +30,7 @@ EXPORTS = ("ep_plan_create", "ep_plan_destroy", "ep_plan_set_variant", "ep_plan_
            "ep_dispatch", "ep_dispatch_route", "ep_dispatch_scatter", "ep_combine", "ep_reset",
            "ep_status", "ep_strerror", "ep_last_error", "ep_route_noalloc",
            "ep_quantize_received", "ep_combine_fp8", "ep_group_by_expert", "ep_ungroup_by_expert",
-           "ep_dispatch_grouped")
+           "ep_dispatch_grouped", "ep_quantize_received_fp4", "ep_combine_fp4")
 
 
 class EpError(RuntimeError):
@@ -79,6 +79,8 @@ def load_library(path: Optional[str] = None):
         "ep_group_by_expert": (I, [V, V, V, V, V, U64, V]),
         "ep_ungroup_by_expert": (I, [V, V, V, U64, V]),
         "ep_dispatch_grouped": (I, [V, V, V, V, V, V, V, V, V, V, V, ctypes.POINTER(DispatchOut)]),
+        "ep_quantize_received_fp4": (I, [V, V, V, V, U64, V]),
+        "ep_combine_fp4": (I, [V, V, V, V, V, V, U64, V]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -275,6 +277,30 @@ class Plan:
         if out_w is None and weights is not None and want_weights:
             out_w = torch.zeros((self.W, self.M, self.k), dtype=torch.float32, device=self.device)
         _check(self._lib.ep_combine_fp8(self._h, _ptr(q), _ptr(scales), _ptr(weights), _ptr(out),
+                                        _ptr(out_w), ctypes.c_uint64(epoch), _stream(stream)))
+        return out, out_w
+
+    def quantize_received_fp4(self, expert_out: torch.Tensor, epoch: int, q: Optional[torch.Tensor] = None,
+                              scales: Optional[torch.Tensor] = None, stream=None):
+        """Quantise the received BF16 expert rows to the MX FP4 wire; returns (q [W][W*M][H/2]
+        uint8 packed e2m1 pairs, scales [W][W*M][H/32] uint8 e8m0 codes)."""
+        if q is None:
+            q = torch.empty((self.W, self.rows, self.H // 2), dtype=torch.uint8, device=self.device)
+        if scales is None:
+            scales = torch.empty((self.W, self.rows, self.H // 32), dtype=torch.uint8, device=self.device)
+        _check(self._lib.ep_quantize_received_fp4(self._h, _ptr(expert_out), _ptr(q), _ptr(scales),
+                                                  ctypes.c_uint64(epoch), _stream(stream)))
+        return q, scales
+
+    def combine_fp4(self, q: torch.Tensor, scales: torch.Tensor, weights: Optional[torch.Tensor],
+                    epoch: int, out: Optional[torch.Tensor] = None, out_w: Optional[torch.Tensor] = None,
+                    want_weights: bool = True, stream=None):
+        """Combine over the MX FP4 wire; returns (out [W][M][H] BF16, out_w or None)."""
+        if out is None:
+            out = torch.zeros((self.W, self.M, self.H), dtype=torch.bfloat16, device=self.device)
+        if out_w is None and weights is not None and want_weights:
+            out_w = torch.zeros((self.W, self.M, self.k), dtype=torch.float32, device=self.device)
+        _check(self._lib.ep_combine_fp4(self._h, _ptr(q), _ptr(scales), _ptr(weights), _ptr(out),
                                         _ptr(out_w), ctypes.c_uint64(epoch), _stream(stream)))
         return out, out_w
 

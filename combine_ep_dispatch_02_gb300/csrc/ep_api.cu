@@ -421,14 +421,14 @@ int ep_combine(ep_plan* p, const void* expert_out, const float* weights, void* o
     return EP_OK;
 }
 
-static int check_wire(ep_plan* p, uint64_t epoch, const char* who)
+static int check_wire(ep_plan* p, uint64_t epoch, const char* who, int block = 128)
 {
     if (!p) return fail(EP_ERR_ARG, "%s: plan is NULL", who);
     if (!p->live || epoch != p->epoch)
         return fail(EP_ERR_STATE, "%s: epoch %llu is not the plan's live dispatch", who,
                     (unsigned long long)epoch);
-    if (p->H % 128 != 0) return fail(EP_ERR_ARG, "%s: hidden=%d is not a multiple of 128", who, p->H);
-    if (p->dtype == EP_FP16) return fail(EP_ERR_ARG, "%s: the FP8 wire carries BF16 outputs; FP16 plan", who);
+    if (p->H % block != 0) return fail(EP_ERR_ARG, "%s: hidden=%d is not a multiple of %d", who, p->H, block);
+    if (p->dtype == EP_FP16) return fail(EP_ERR_ARG, "%s: the wire carries BF16 outputs; FP16 plan", who);
     return EP_OK;
 }
 
@@ -475,6 +475,51 @@ int ep_combine_fp8(ep_plan* p, const void* expert_q, const float* expert_scales,
     for (int s = 0; s <= p->W; ++s) a.tok_off[s] = p->tok_off[s];
     cudaError_t e = launch_combine_fp8(a, p->num_sms, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "ep_combine_fp8: launch");
+    return EP_OK;
+}
+
+int ep_quantize_received_fp4(ep_plan* p, const void* expert_out, void* expert_q, uint8_t* expert_scales,
+                             uint64_t epoch, void* stream)
+{
+    int rc = check_wire(p, epoch, "ep_quantize_received_fp4", 32);
+    if (rc != EP_OK) return rc;
+    if (!expert_out || !aligned(expert_out, 16) || !expert_q || !aligned(expert_q, 16) || !expert_scales)
+        return fail(EP_ERR_ARG, "ep_quantize_received_fp4: a buffer is NULL or misaligned");
+    DeviceGuard g(p->device);
+    if (!g.ok) return fail(EP_ERR_CUDA, "cannot select the plan's device %d", p->device);
+    WireArgs a{};
+    a.eo = (const uint16_t*)expert_out; a.q = (uint8_t*)expert_q; a.scales = (float*)expert_scales;
+    a.recv_count = p->recv_count; a.H = p->H; a.rows = p->rows; a.W = p->W;
+    cudaError_t e = launch_quantise_rows_fp4(a, p->num_sms, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "ep_quantize_received_fp4: launch");
+    return EP_OK;
+}
+
+int ep_combine_fp4(ep_plan* p, const void* expert_q, const uint8_t* expert_scales, const float* weights,
+                   void* out, float* out_w, uint64_t epoch, void* stream)
+{
+    int rc = check_wire(p, epoch, "ep_combine_fp4", 32);
+    if (rc != EP_OK) return rc;
+    if (!expert_q || !aligned(expert_q, 16) || !expert_scales)
+        return fail(EP_ERR_ARG, "ep_combine_fp4: codes or scales NULL or misaligned");
+    if (!out || !aligned(out, 16)) return fail(EP_ERR_ARG, "ep_combine_fp4: out is NULL or not 16-byte aligned");
+    if (out_w && !weights) return fail(EP_ERR_ARG, "ep_combine_fp4: out_w given without weights");
+    if ((weights && !aligned(weights, 4)) || (out_w && !aligned(out_w, 4)))
+        return fail(EP_ERR_ARG, "ep_combine_fp4: weights or out_w not 4-byte aligned");
+    DeviceGuard g(p->device);
+    if (!g.ok) return fail(EP_ERR_CUDA, "cannot select the plan's device %d", p->device);
+    CombineArgs geo{};
+    geo.H = p->H; geo.N = p->N;
+    combine_geometry(geo, p->variant, p->num_sms);     // slice size in 8-element vectors
+    WireArgs a{};
+    a.q = (uint8_t*)expert_q; a.scales = (float*)expert_scales; a.fwd = p->fwd; a.w_in = weights;
+    a.out = (uint16_t*)out; a.out_w = out_w; a.H = p->H; a.rows = p->rows;
+    a.W = p->W; a.k = p->k; a.F = p->F; a.M = p->M; a.N = p->N;
+    a.chunk_pieces = geo.chunk_vecs / 4 > 0 ? geo.chunk_vecs / 4 : 1;   // 32-element blocks
+    a.chunks = (int)((p->H / 32 + a.chunk_pieces - 1) / a.chunk_pieces);
+    for (int s = 0; s <= p->W; ++s) a.tok_off[s] = p->tok_off[s];
+    cudaError_t e = launch_combine_fp4(a, p->num_sms, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "ep_combine_fp4: launch");
     return EP_OK;
 }
 

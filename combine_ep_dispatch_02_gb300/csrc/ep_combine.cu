@@ -3,9 +3,9 @@
 // For every source token, read the expert-output rows of the ranks it was dispatched to
 // (forward map, ascending destination rank), add them in FP32 starting from +0.0f in that
 // fixed order, and round to nearest even into BF16 / FP16 (MORI-EP gfx1201 PR, Combine bullet:
-// "The source sums its local and received contributions in FP32, then converts the output to
-// BF16/FP16.  Optional FP32 weights are communicated and summed separately").  Routing weights
-// are not applied.  The fixed order makes the result independent of the launch shape.
+// the home rank accumulates its own and the received contributions in FP32 and converts once
+// at the end; FP32 weight rows travel and are summed on their own).  Routing weights are not
+// applied.  The fixed order makes the result independent of the launch shape.
 //
 // HBM-bound, and bound by how many bytes each SM keeps in flight: at the loaded HBM latency
 // of this part (~2.3 us) an SM needs ~100 KB of reads outstanding to stream at full rate.  A

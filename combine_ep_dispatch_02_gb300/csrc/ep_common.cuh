@@ -141,6 +141,10 @@ cudaError_t launch_ungroup(const GroupArgs& a, bool fp16, int num_sms, cudaStrea
 // dispatch straight into the grouped view (needs routing done; a.src_idx, a.x, a.fwd set)
 cudaError_t launch_group_from_source(const GroupArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_combine_fp8(const WireArgs& a, int num_sms, cudaStream_t stream);
+// MX FP4 wire: a.q [W][W*M][H/2] packed e2m1, a.scales [W][W*M][H/32] e8m0 bytes; for the
+// combine a.chunk_pieces counts 32-element blocks per slice
+cudaError_t launch_quantise_rows_fp4(const WireArgs& a, int num_sms, cudaStream_t stream);
+cudaError_t launch_combine_fp4(const WireArgs& a, int num_sms, cudaStream_t stream);
 // choose combine's slice of a row per work unit (a.H and a.N set)
 void combine_geometry(CombineArgs& a, int variant, int num_sms);
 

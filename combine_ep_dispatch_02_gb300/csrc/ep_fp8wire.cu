@@ -1,13 +1,14 @@
-// ep_fp8wire.cu -- combine over an FP8 wire.
+// ep_fp8wire.cu -- combine over a low-precision wire: FP8 e4m3 blockwise and MX FP4.
 //
-// The MORI-EP gfx1250 EPv2 pages send combine contributions at low precision ("fp8 push
-// combine (fp8_blockwise)"; fp4 push combine: producers "load bf16 rows and quantize them",
-// the source dequantises and reduces).  Here the expert-output rows of the live dispatch are
-// quantised block-wise to FP8 e4m3 (one FP32 scale per 128 elements, the same quantiser as the
-// quantising dispatch), and the gather-reduce reads those codes: for every source token, in
-// ascending rank order, v = float(code) * scale (one FP32 multiply) is added in FP32, and the
-// sum is rounded to nearest even into BF16.  The gather then reads H + H/32 bytes per row
-// instead of 2H.
+// The MORI-EP gfx1250 EPv2 pages (push-combine variants) let combine contributions travel at
+// low precision: the expert side quantises its BF16 output rows before they are sent, and the
+// token's home rank dequantises them while it reduces.  Two encodings are built here:
+//   FP8: e4m3 codes with one FP32 scale per 128 elements (the quantiser of the quantising
+//        dispatch); the gather reads H + H/32 bytes per row instead of 2H;
+//   FP4: e2m1 codes with one e8m0 power-of-two scale per 32 elements (the OCP microscaling
+//        layout); the gather reads H/2 + H/32 bytes per row.
+// For every source token the terms are added in ascending rank order in FP32 from +0.0f, each
+// term being code * scale (one FP32 multiply), and the sum is rounded to nearest even into BF16.
 #include <cuda_bf16.h>
 
 #include "ep_common.cuh"
@@ -219,6 +220,225 @@ __global__ void __launch_bounds__(kCopyThreads, 2) ep_combine_fp8_kernel(const W
     }
 }
 
+// ---- the MX FP4 wire: 32-element blocks of e2m1 codes with one e8m0 scale each
+//
+// scale code = floor(log2(max|x|)) - 2 + 127 (clamped to 0..254; 127 for an all-zero block),
+// code = e2m1 RNE saturating of x / 2^(code - 127).  Dividing by a power of two equals
+// multiplying by its exact reciprocal 2^(127 - code) (both round the same real quotient), so
+// the kernels multiply.  Nibbles: element 2i low, 2i + 1 high.
+
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("{ .reg .b8 t; cvt.rn.satfinite.e2m1x2.f32 t, %1, %2; cvt.u32.u8 %0, t; }"
+        : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ float2 e2m1x2_to_float2(uint32_t byte)
+{
+    uint32_t h2;
+    asm("{ .reg .b8 c; cvt.u8.u32 c, %1; cvt.rn.f16x2.e2m1x2 %0, c; }" : "=r"(h2) : "r"(byte));
+    return __half22float2(*reinterpret_cast<const __half2*>(&h2));
+}
+
+__device__ __forceinline__ float e8m0_to_float(uint32_t code)
+{
+    return __uint_as_float(code == 0 ? 0x00400000u : code << 23);
+}
+
+// One lane quantises one 32-element block (64 BF16 bytes -> 16 code bytes + 1 scale byte).
+__global__ void __launch_bounds__(kCopyThreads, 3) ep_quantise_rows_fp4_kernel(const WireArgs a)
+{
+    __shared__ int s_cnt[kMaxRanks];
+    if (threadIdx.x < a.W) s_cnt[threadIdx.x] = a.recv_count[threadIdx.x];
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = (int64_t)gridDim.x * (kCopyThreads / 32);
+    const int nblk = (int)(a.H >> 5);
+    uint8_t* sc8 = reinterpret_cast<uint8_t*>(a.scales);
+    for (int64_t u = (int64_t)blockIdx.x * (kCopyThreads / 32) + (threadIdx.x >> 5);
+         u < (int64_t)a.W * a.rows; u += nwarps) {
+        const int r = (int)(u / a.rows);
+        const int64_t i = u - (int64_t)r * a.rows;
+        if (i >= s_cnt[r]) continue;                 // warp-uniform: only received rows
+        const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(a.eo) + u * a.H * 2);
+        uint4* dq = reinterpret_cast<uint4*>(a.q + u * (a.H >> 1));
+        for (int b0 = 0; b0 < nblk; b0 += 32) {      // warp-uniform bounds
+            const int b = b0 + lane;
+            if (b >= nblk) continue;
+            uint4 x[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) x[t] = ld_stream_v4(src + (int64_t)b * 4 + t);
+            float m = 0.0f;
+#pragma unroll
+            for (int t = 0; t < 4; ++t) m = fmaxf(m, absmax16(x[t], x[t]));
+            uint32_t code = 127;
+            if (m > 0.0f) {
+                const uint32_t mb = __float_as_uint(m);
+                int e2 = (int)(mb >> 23) - 127;
+                if ((mb >> 23) == 0) e2 = -127 - (__clz(mb & 0x7FFFFFu) - 9);   // subnormal max
+                int c = e2 - 2 + 127;
+                code = (uint32_t)(c < 0 ? 0 : (c > 254 ? 254 : c));
+            }
+            // 2^(127 - code); code <= 253 for any BF16 input (Inf gives 253), 254 would be 2^-127
+            const float inv = __uint_as_float(code >= 254u ? 0x00400000u : (254u - code) << 23);
+            uint32_t o[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const uint32_t w[4] = {x[t].x, x[t].y, x[t].z, x[t].w};
+                uint32_t bytes = 0;
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const float lo = __fmul_rn(__uint_as_float(w[h] << 16), inv);
+                    const float hi = __fmul_rn(__uint_as_float(w[h] & 0xFFFF0000u), inv);
+                    bytes |= e2m1x2(lo, hi) << (8 * h);
+                }
+                o[t] = bytes;
+            }
+            st_v4(dq + b, make_uint4(o[0], o[1], o[2], o[3]));
+            sc8[u * nblk + b] = (uint8_t)code;
+        }
+    }
+}
+
+// acc[16] += the 16 e2m1 codes of (lo, hi) times scale
+__device__ __forceinline__ void add_fp4x16(float (&acc)[16], uint32_t lo, uint32_t hi, float scale)
+{
+    const uint32_t w[2] = {lo, hi};
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            const float2 v = e2m1x2_to_float2((w[i] >> (8 * h)) & 0xFFu);
+            acc[8 * i + 2 * h] = __fadd_rn(acc[8 * i + 2 * h], __fmul_rn(v.x, scale));
+            acc[8 * i + 2 * h + 1] = __fadd_rn(acc[8 * i + 2 * h + 1], __fmul_rn(v.y, scale));
+        }
+}
+
+// Rolling fold of nd <= 8 rows over the FP4 wire.  A lane owns 32-element blocks (16 code bytes
+// and one scale byte per row); the block's two 16-element halves are summed one after the
+// other, so 16 accumulators are live, and each row's next block is loaded as soon as its
+// upper half has been added.
+__device__ __forceinline__ void fold_fp4_rows(const WireArgs& a, int src, int nd, int b0, int nb,
+                                              uint4* dst, int lane)
+{
+    const int64_t hb = a.H >> 5;                      // blocks per row
+    const uint4* q4 = reinterpret_cast<const uint4*>(a.q);
+    const uint8_t* sc8 = reinterpret_cast<const uint8_t*>(a.scales);
+    uint32_t ro[8];                                   // block offsets (receive buffer < 64 GB)
+#pragma unroll
+    for (int d = 0; d < 8; ++d) ro[d] = (uint32_t)((int64_t)__shfl_sync(0xffffffffu, src, d) * hb + b0);
+    uint4 b[8];
+    uint32_t sc[8];
+#pragma unroll
+    for (int d = 0; d < 8; ++d)
+        if (d < nd && lane < nb) {
+            b[d] = ld_stream_v4(q4 + ro[d] + lane);
+            sc[d] = __ldg(sc8 + ro[d] + lane);
+        }
+    for (int vb = 0; vb < nb; vb += 32) {             // warp-uniform bounds
+        const int pc = vb + lane, pn = pc + 32;
+        float acc[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+#pragma unroll
+        for (int d = 0; d < 8; ++d)
+            if (d < nd && pc < nb) add_fp4x16(acc, b[d].x, b[d].y, e8m0_to_float(sc[d]));
+        if (pc < nb) store_bf16x16(dst + (int64_t)pc * 4, acc);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+#pragma unroll
+        for (int d = 0; d < 8; ++d) {
+            if (d < nd) {
+                const uint32_t z = b[d].z, w = b[d].w;
+                const float xs = e8m0_to_float(sc[d]);
+                if (pn < nb) {
+                    b[d] = ld_stream_v4(q4 + ro[d] + pn);
+                    sc[d] = __ldg(sc8 + ro[d] + pn);
+                }
+                if (pc < nb) add_fp4x16(acc, z, w, xs);
+            }
+        }
+        if (pc < nb) store_bf16x16(dst + (int64_t)pc * 4 + 2, acc);
+    }
+}
+
+// More than 8 rows: one half-block per lane at a time, rows in ascending batches of 8.
+__device__ __forceinline__ void fold_fp4_wide(const WireArgs& a, int src, int nd, int b0, int nb,
+                                              uint4* dst, int lane)
+{
+    const int64_t hb = a.H >> 5;
+    const uint2* q2 = reinterpret_cast<const uint2*>(a.q);
+    const uint8_t* sc8 = reinterpret_cast<const uint8_t*>(a.scales);
+    for (int vb = 0; vb < nb; vb += 32) {
+        const int pc = vb + lane;
+        const bool act = pc < nb;
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+            float acc[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+            for (int d0 = 0; d0 < nd; d0 += 8) {
+                uint2 c[8];
+                uint32_t sc[8];
+#pragma unroll
+                for (int d = 0; d < 8; ++d) {
+                    const int64_t blk = (int64_t)__shfl_sync(0xffffffffu, src, (d0 + d) & 31) * hb + b0 + pc;
+                    if (act && d0 + d < nd) {
+                        c[d] = __ldg(q2 + blk * 2 + half);
+                        sc[d] = __ldg(sc8 + blk);
+                    }
+                }
+#pragma unroll
+                for (int d = 0; d < 8; ++d)
+                    if (act && d0 + d < nd) add_fp4x16(acc, c[d].x, c[d].y, e8m0_to_float(sc[d]));
+            }
+            if (act) store_bf16x16(dst + (int64_t)pc * 4 + 2 * half, acc);
+        }
+    }
+}
+
+// A warp owns a (token, slice) unit; a.chunk_pieces counts 32-element blocks per slice.
+// Weight rows are summed as in the 16-bit combine.
+template <bool WIDE>
+__global__ void __launch_bounds__(kCopyThreads, 2) ep_combine_fp4_kernel(const WireArgs a)
+{
+    __shared__ int s_off[kMaxRanks + 1];
+    if (threadIdx.x <= a.W) s_off[threadIdx.x] = a.tok_off[threadIdx.x];
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const uint32_t units = (uint32_t)a.N * (uint32_t)a.chunks;
+    const uint32_t step = gridDim.x * (kCopyThreads / 32);
+    for (uint32_t u = blockIdx.x * (kCopyThreads / 32) + (threadIdx.x >> 5); u < units; u += step) {
+        const int g = (int)(u / (uint32_t)a.chunks);
+        const int c = (int)(u - (uint32_t)g * (uint32_t)a.chunks);
+        const int s = rank_of_token(s_off, a.W, g);
+        const int64_t tok = (int64_t)s * a.M + (g - s_off[s]);
+        const int src = lane < a.F ? __ldg(a.fwd + tok * a.F + lane) : -1;
+        const int nd = __popc(__ballot_sync(0xffffffffu, src >= 0));
+        const int b0 = c * a.chunk_pieces;
+        const int nb = (int)min((int64_t)a.chunk_pieces, (a.H >> 5) - b0);
+        uint4* dst = reinterpret_cast<uint4*>(a.out + tok * a.H) + (int64_t)b0 * 4;
+        if (!WIDE || nd <= 8)
+            fold_fp4_rows(a, src, nd, b0, nb, dst, lane);     // nd == 0 stores +0
+        else
+            fold_fp4_wide(a, src, nd, b0, nb, dst, lane);
+
+        if (c == 0 && a.w_in != nullptr && a.out_w != nullptr) {
+            for (int e0 = 0; e0 < a.k; e0 += 32) {
+                const int e = e0 + lane;
+                float acc = 0.0f;
+                for (int d = 0; d < nd; ++d) {
+                    const int64_t row = __shfl_sync(0xffffffffu, src, d);
+                    if (e < a.k) acc = __fadd_rn(acc, __ldg(a.w_in + row * a.k + e));
+                }
+                if (e < a.k) a.out_w[tok * a.k + e] = acc;
+            }
+        }
+    }
+}
+
 int grid_for(const void* kernel, int64_t warps_needed, int num_sms)
 {
     int per_sm = 0;
@@ -238,6 +458,28 @@ cudaError_t launch_quantise_rows(const WireArgs& a, int num_sms, cudaStream_t st
     if (units == 0) return cudaSuccess;
     ep_quantise_rows_kernel<<<grid_for((const void*)ep_quantise_rows_kernel, units, num_sms),
                               kCopyThreads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantise_rows_fp4(const WireArgs& a, int num_sms, cudaStream_t stream)
+{
+    const int64_t units = (int64_t)a.W * a.rows;
+    if (units == 0) return cudaSuccess;
+    ep_quantise_rows_fp4_kernel<<<grid_for((const void*)ep_quantise_rows_fp4_kernel, units, num_sms),
+                                  kCopyThreads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine_fp4(const WireArgs& a, int num_sms, cudaStream_t stream)
+{
+    const int64_t units = (int64_t)a.N * a.chunks;
+    if (units == 0) return cudaSuccess;
+    if (a.F > 8)
+        ep_combine_fp4_kernel<true><<<grid_for((const void*)ep_combine_fp4_kernel<true>, units, num_sms),
+                                      kCopyThreads, 0, stream>>>(a);
+    else
+        ep_combine_fp4_kernel<false><<<grid_for((const void*)ep_combine_fp4_kernel<false>, units, num_sms),
+                                       kCopyThreads, 0, stream>>>(a);
     return cudaGetLastError();
 }
 

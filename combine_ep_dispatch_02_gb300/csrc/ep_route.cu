@@ -13,8 +13,8 @@
 //      (so a CTA only ever waits on tiles whose CTAs are already running);
 //   2. the destination set of each token is the OR over its k slots of (1 << rank), so a rank
 //      named by several experts counts once; each thread loads its token's whole index row
-//      with 16-byte vectors (top-k 1..64: the pages' "runtime routing loops ... including
-//      slots 32-63" become one vector loop per token), so a tile's rows are in flight together;
+//      with 16-byte vectors (top-k 1..64: the pages' run-time routing loops over slot batches,
+//      up to slot 63, become one vector loop per token), so a tile's rows are in flight together;
 //   3. per-rank counts: one ballot per rank gives each token's rank within its warp and the
 //      warp totals; a block scan over the 8 warps gives the tile's own total per rank;
 //   4. decoupled lookback: the tile publishes its totals (status AGGREGATE), then walks back
@@ -22,8 +22,8 @@
 //      summing until it meets an INCLUSIVE word, and publishes its own INCLUSIVE prefix;
 //   5. each token writes src_pos for each of its rows and its compact forward-map row.
 // Every scan word carries a stamp derived from the ticket (ticket / tiles + 1), so words from
-// the previous call are ignored and no per-call clearing is needed (the pages' "generation
-// counters ... coordinate ... buffer reuse across calls").  Waits are bounded: an expired wait
+// the previous call are ignored and no per-call clearing is needed (the pages reuse buffers
+// across calls by means of generation counters).  Waits are bounded: an expired wait
 // records EP_ERR_DEVICE_TIMEOUT and the CTA carries on, so the kernel always terminates.
 #include <climits>
 

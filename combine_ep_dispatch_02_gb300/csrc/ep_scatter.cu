@@ -2,8 +2,8 @@
 //
 // For every source token and every destination rank it was routed to, copy the token's hidden
 // row, its top-k index row, its FP32 weight row and its FP32 scale row into that rank's
-// receive row (MORI-EP gfx1201 PR, Dispatch bullet: "Multiple experts on the same rank share
-// one hidden payload"; guide, dispatch() outputs).  The receive rows come from the forward map
+// receive row (MORI-EP gfx1201 PR, Dispatch bullet: experts that live on one rank share a
+// single copy of the hidden row; guide, dispatch() outputs).  The receive rows come from the forward map
 // the routing kernel wrote.
 //
 // HBM-bound: each source row is READ ONCE into registers with 16-byte non-allocating loads and

@@ -23,11 +23,11 @@
  *   Combine.  For each source token the rows it was sent to are read back, in ascending
  *   destination-rank order, converted to FP32, summed starting from +0.0f with plain float
  *   additions (no fused multiply-add; compiled with -ffp-contract=off), and the sum is
- *   rounded to nearest even into BF16 or FP16 ("The source sums its local and received
- *   contributions in FP32, then converts the output to BF16/FP16").  Optional FP32 weight
+ *   rounded to nearest even into BF16 or FP16 (the Combine bullet: FP32 accumulation of the
+ *   local and received contributions, one conversion at the end).  Optional FP32 weight
  *   rows are summed the same way, separately; routing weights are never applied to the
- *   payload ("applying routing weights to expert outputs remain the caller's
- *   responsibility").
+ *   payload (the Combine bullet leaves scaling expert outputs by routing weights to the
+ *   caller).
  *
  *   Expert ids outside [0, W*E) route nowhere and make dispatch return EP_ORACLE_ERR_INDEX.
  *

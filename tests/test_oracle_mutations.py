@@ -46,6 +46,17 @@ MUTATIONS = {
     # FP8 wire dequantises with the wrong block's scale
     "wire_scale_index": ("* scales[row * nb + h / 128];", "* scales[row * nb];",
                          pins.test_fp8_combine_power_of_two_scales_closed_form),
+    # e2m1 ties go to the odd code (away from even)
+    "e2m1_ties_odd": ("if (dc < db || (dc == db && (c & 1) == 0)) best = c;",
+                      "if (dc < db || (dc == db && (c & 1) == 1)) best = c;",
+                      pins.test_e2m1_rne_brute_force),
+    # e8m0 shared exponent off by one (largest e2m1 exponent taken as 1)
+    "e8m0_off_by_one": ("                code = e2 - 2 + 127;", "                code = e2 - 1 + 127;",
+                        pins.test_mxfp4_quantiser_against_numpy),
+    # the FP4 combine pairs the wrong nibble with each element
+    "fp4_nibble_swap": ("uint8_t code = (h & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xFu);",
+                        "uint8_t code = (h & 1) ? (uint8_t)(byte & 0xFu) : (uint8_t)(byte >> 4);",
+                        pins.test_fp4_combine_exact_sums),
     # grouped inverse sums in list order of the last expert only
     "ungroup_overwrite": ("acc[i * H + h] = acc[i * H + h] + v;", "acc[i * H + h] = v;",
                           pins.test_ungroup_identity_closed_form),

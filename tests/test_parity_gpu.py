@@ -404,6 +404,120 @@ def test_fp8_wire_rejects_fp16_plans_and_stale_epochs():
     plan.close()
 
 
+# ---------------------------------------------------------------- combine over an MX FP4 wire
+
+def _check_fp4_wire(wl, variant="auto", edit_expert_out=None):
+    """quantize_received_fp4 codes + scales and combine_fp4 outputs against the oracle, bit-exact.
+    edit_expert_out(eo_np) may overwrite the received expert rows (in place) before quantising."""
+    disp, eo, _, _ = oracle.run_workload(wl, harness.expert_np)
+    plan, (x, w, scales, idx) = _setup(wl)
+    plan.set_variant(variant)
+    d = plan.dispatch(x, w, scales, idx, wl.n_tok)
+    eo_g = harness.expert_torch(wl, d.recv_x, d.recv_idx, d.recv_w, d.recv_scales, d.recv_count)
+    if edit_expert_out is not None:
+        eo = eo.copy()
+        edit_expert_out(eo)
+        eo_g = torch.from_numpy(eo.view(np.int16)).to(DEV).view(torch.bfloat16)
+    q, sc = oracle.quantize_mxfp4(eo)
+    o_out, o_w = oracle.combine_fp4(wl.W, wl.k, wl.H, wl.M, wl.n_tok, disp["slot_of"], q, sc,
+                                    disp["recv_w"])
+    qg, scg = plan.quantize_received_fp4(eo_g, d.epoch)
+    out, out_w = plan.combine_fp4(qg, scg, d.recv_w, d.epoch)
+    torch.cuda.synchronize()
+    assert plan.status() == 0
+    qg, scg = qg.cpu().numpy(), scg.cpu().numpy()
+    cnt = d.recv_count.cpu().numpy()
+    for r in range(wl.W):
+        n = int(cnt[r])
+        assert np.array_equal(scg[r, :n], sc[r, :n]), f"rank {r}: e8m0 scales"
+        assert np.array_equal(qg[r, :n], q[r, :n]), f"rank {r}: e2m1 codes"
+    out = gpu_path.raw(out)
+    for s in range(wl.W):
+        n = int(wl.n_tok[s])
+        assert gpu_path.nan_aware_equal_bf16(out[s, :n], o_out[s, :n]), f"source rank {s}"
+        if o_w is not None:
+            assert np.array_equal(out_w[s, :n].cpu().numpy().view(np.uint32), o_w[s, :n].view(np.uint32))
+    plan.close()
+
+
+def test_fp4_wire_dsv3_reduced():
+    _check_fp4_wire(wlmod.make_workload("dsv3", max_tok=300))
+
+
+@pytest.mark.parametrize("variant", ["auto", "tiled_512", "whole_row"])
+def test_fp4_wire_small_scalar_expert(variant):
+    _check_fp4_wire(wlmod.make_workload("small", max_tok=64), variant)
+
+
+def test_fp4_wire_fp8_payload():
+    _check_fp4_wire(wlmod.make_workload("fp8", max_tok=256))
+
+
+def test_fp4_wire_wide_fan_in():
+    # min(W, k) = 16 > 8: rows fold in ascending batches of 8
+    _check_fp4_wire(wlmod.custom_workload(W=16, E=2, k=32, H=256, M=40, n_tok=[40] * 8 + [3] * 8, seed=6))
+
+
+def test_fp4_wire_ragged_blocks():
+    # H = 96: three 32-element blocks per row, fewer than a warp's lanes; H = 1056: 33 blocks,
+    # one past a warp's worth
+    _check_fp4_wire(wlmod.custom_workload(W=4, E=3, k=4, H=96, M=37, n_tok=[37, 5, 0, 20], seed=11))
+    _check_fp4_wire(wlmod.custom_workload(W=4, E=3, k=4, H=1056, M=37, n_tok=[37, 5, 0, 20], seed=12))
+
+
+def test_fp4_wire_edge_values():
+    wl = wlmod.make_workload("small", max_tok=48)
+
+    def edit(eo):
+        f = eo.view(np.uint16).astype(np.uint32) << 16
+        xf = f.view(np.float32).reshape(eo.shape).copy()
+        H = xf.shape[-1]
+        # every received row of rank 0 and 1 gets crafted blocks
+        xf[0, :, :32] = 0.0                                           # all-zero block: scale code 127
+        xf[0, :, 32:64] = np.float32(2.0) ** -130                     # subnormal BF16 block: code clamps to 0
+        ties = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 7.0], np.float32)
+        xf[0, :, 64:96] = np.tile(np.concatenate([ties, -ties]), 2) * np.float32(4.0)   # amax 28: e = 2
+        xf[1, :, :32] = np.float32(3e38)                              # near BF16 max: code 252
+        xf[1, :, 32:64] = -np.float32(1e-3)
+        xf[1, :, 64] = -0.0
+        xf[1, :, 96:128] = np.linspace(-6.5, 6.5, 32, dtype=np.float32) * np.float32(2.0) ** -20
+        if H > 160:
+            xf[1, :, 128:160] = np.float32(2.0) ** -126 * np.float32(3.0)   # normal/subnormal edge
+        eo[:] = torch.from_numpy(xf).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+    _check_fp4_wire(wl, edit_expert_out=edit)
+
+
+def test_fp4_wire_dsv3_full():
+    _check_fp4_wire(wlmod.make_workload("dsv3"))
+
+
+def test_fp4_wire_rejects_bad_plans():
+    wl = wlmod.make_workload("topk", k=8, max_tok=16)          # FP16 payload
+    plan, (x, w, sc, idx) = _setup(wl)
+    d = plan.dispatch(x, w, sc, idx, wl.n_tok)
+    with pytest.raises(ep.EpError) as e:
+        plan.quantize_received_fp4(d.recv_x, d.epoch)
+    assert e.value.code == ep.EP_ERR_ARG
+    plan.close()
+    wl = wlmod.custom_workload(W=2, E=2, k=2, H=48, M=8, n_tok=[8, 8], seed=3)   # 48 % 32 != 0
+    plan, (x, w, sc, idx) = _setup(wl)
+    d = plan.dispatch(x, w, sc, idx, wl.n_tok)
+    with pytest.raises(ep.EpError) as e:
+        plan.quantize_received_fp4(d.recv_x, d.epoch)
+    assert e.value.code == ep.EP_ERR_ARG
+    plan.close()
+    wl = wlmod.make_workload("dsv3", max_tok=16)
+    plan, (x, w, sc, idx) = _setup(wl)
+    d = plan.dispatch(x, w, sc, idx, wl.n_tok)
+    q, s = plan.quantize_received_fp4(d.recv_x, d.epoch)
+    plan.reset()
+    with pytest.raises(ep.EpError) as e:
+        plan.combine_fp4(q, s, None, d.epoch)
+    assert e.value.code == ep.EP_ERR_STATE
+    plan.close()
+
+
 # ---------------------------------------------------------------- expert-grouped layout
 
 def _check_grouped(wl, seed=0, fused=False):
