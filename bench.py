@@ -77,18 +77,57 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def code_digest(*files) -> str:
+    """sha256 of C/CUDA sources with comments and whitespace removed (string and character
+    literals kept), so an edit that only touches comments leaves it unchanged."""
+    h = hashlib.sha256()
+    for f in files:
+        text = open(f, encoding="utf-8").read()
+        out, i, n = [], 0, len(text)
+        while i < n:
+            c = text[i]
+            if text.startswith("//", i):
+                j = text.find("\n", i)
+                i = n if j < 0 else j
+            elif text.startswith("/*", i):
+                j = text.find("*/", i + 2)
+                i = n if j < 0 else j + 2
+                out.append(" ")
+            elif c in "\"'":
+                j = i + 1
+                while j < n and text[j] != c:
+                    j += 2 if text[j] == "\\" else 1
+                out.append(text[i:j + 1])
+                i = j + 1
+            else:
+                out.append(c)
+                i += 1
+        h.update(" ".join("".join(out).split()).encode())
+    return h.hexdigest()
+
+
+KERNEL_SOURCES = {"scatter": "ep_scatter.cu", "combine": "ep_combine.cu", "route": "ep_route.cu",
+                  "scatter_quant": "ep_scatter.cu", "combine_fp8": "ep_fp8wire.cu",
+                  "quantise_rows": "ep_fp8wire.cu", "combine_fp4": "ep_fp8wire.cu",
+                  "quantise_rows_fp4": "ep_fp8wire.cu", "grouped": "ep_grouped.cu"}
+
+
+def kernel_digest(kernel: str) -> str:
+    """Code digest of a kernel's source file and the shared header it includes."""
+    csrc = os.path.join(ROOT, "combine_ep_dispatch_02_gb300", "csrc")
+    return code_digest(os.path.join(csrc, KERNEL_SOURCES[kernel]), os.path.join(csrc, "ep_common.cuh"))
+
+
 def recorded_traffic(kernel: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on the current
-    source of the kernel's file (a sha256 recorded beside the figure)."""
-    src = {"scatter": "ep_scatter.cu", "combine": "ep_combine.cu", "route": "ep_route.cu"}[kernel]
+    code of the kernel (a code digest recorded beside the figure)."""
     path = os.path.join(ROOT, "profiles", f"ncu_{kernel}_dsv3.md")
     try:
         text = open(path).read()
-        cur = hashlib.sha256(open(os.path.join(ROOT, "combine_ep_dispatch_02_gb300", "csrc", src),
-                                  "rb").read()).hexdigest()
+        cur = kernel_digest(kernel)
     except OSError:
         return None
-    m = re.search(r"traffic_bytes_per_launch:\s*(\d+)\s+source_sha256:\s*([0-9a-f]{64})", text)
+    m = re.search(r"traffic_bytes_per_launch:\s*(\d+)\s+code_digest:\s*([0-9a-f]{64})", text)
     if not m or m.group(2) != cur:
         return None
     return int(m.group(1))
@@ -255,6 +294,7 @@ def run_ours(args, rank, world, dist):
                                  steps=max(3, min(args.steps, 50)), fmt="fp4")
     grouped = measure_grouped(ep, dev, stream, peak, steps=max(3, min(args.steps, 50)))
     latency = measure_small_batch_latency(ep, dev)
+    protocol = measure_graph_protocol(plan, wl, dev, x, w, idx, nbytes, peak)
     if plan.status() != 0:
         raise RuntimeError("device status after timing: %d" % plan.status())
 
@@ -301,6 +341,7 @@ def run_ours(args, rank, world, dist):
             "fp4_combine_wire": wire4,
             "expert_grouped_layout": grouped,
             "small_batch_latency_us": latency,
+            "graph_protocol": protocol,
         }
     plan.close()
     return result
@@ -483,6 +524,62 @@ def measure_small_batch_latency(ep, dev, tokens=(8, 128, 256), replays=120):
     return res
 
 
+def measure_graph_protocol(plan, wl, dev, x, w, idx, nbytes, peak, rounds=3, samples=30):
+    """The pages' timing protocol on the full workload: {dispatch}, {combine} and
+    {dispatch + combine} each captured in a CUDA graph; 10 eager and 10 graph warm-ups; then
+    `rounds` rounds of `samples` replays, each replay preceded by a write of a 2x-L2 buffer (L2
+    flushed); p50 per round and over all samples, the round spread (max / min of the round p50s,
+    to stay <= 1.20), and the hot-L2 p50 (back-to-back replays) beside it."""
+    s = torch.cuda.Stream(dev)
+    out = torch.empty((wl.W, wl.M, wl.H), dtype=torch.bfloat16, device=dev)
+    out_w = torch.empty((wl.W, wl.M, wl.k), dtype=torch.float32, device=dev)
+    with torch.cuda.stream(s):
+        for _ in range(10):
+            d = plan.dispatch(x, w, None, idx, wl.n_tok, stream=s)
+            plan.combine(d.recv_x, d.recv_w, d.epoch, out=out, out_w=out_w, stream=s)
+    torch.cuda.synchronize(dev)
+    graphs = {name: torch.cuda.CUDAGraph() for name in ("dispatch", "combine", "pair")}
+    with torch.cuda.graph(graphs["dispatch"], stream=s):
+        d = plan.dispatch(x, w, None, idx, wl.n_tok, stream=s)
+    with torch.cuda.graph(graphs["combine"], stream=s):
+        plan.combine(d.recv_x, d.recv_w, d.epoch, out=out, out_w=out_w, stream=s)
+    with torch.cuda.graph(graphs["pair"], stream=s):
+        d2 = plan.dispatch(x, w, None, idx, wl.n_tok, stream=s)
+        plan.combine(d2.recv_x, d2.recv_w, d2.epoch, out=out, out_w=out_w, stream=s)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    res = {}
+    with torch.cuda.stream(s):                       # replay() launches on the current stream
+        for name, g in graphs.items():
+            for _ in range(10):
+                g.replay()
+            torch.cuda.synchronize(dev)
+
+            def sample(cold, i):
+                if cold:
+                    flush.fill_(i & 0xFF)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(s)
+                g.replay()
+                b.record(s)
+                b.synchronize()
+                return a.elapsed_time(b) * 1e3
+            per_round = [[sample(True, r * samples + i) for i in range(samples)] for r in range(rounds)]
+            hot = [sample(False, i) for i in range(samples)]
+            p50_rounds = [statistics.median(v) for v in per_round]
+            p50 = statistics.median([t for v in per_round for t in v])
+            gbs = nbytes[name] / (p50 * 1e-6) / 1e9
+            res[name] = {"p50_us": round(p50, 2), "round_p50_us": [round(t, 2) for t in p50_rounds],
+                         "round_spread": round(max(p50_rounds) / min(p50_rounds), 3),
+                         "hot_p50_us": round(statistics.median(hot), 2),
+                         "gbs": round(gbs, 1), "frac": round(gbs / peak, 4)}
+    if plan.status() != 0:
+        raise RuntimeError("device status after the graph protocol: %d" % plan.status())
+    res["method"] = (f"CUDA-graph replay; 10 eager + 10 graph warm-ups; {rounds} rounds x {samples} "
+                     "samples, a 2x-L2 buffer written before each sample; p50; hot = back-to-back "
+                     "replays without the flush")
+    return res
+
+
 def measure_e2e(plan, wl, dev, stream, pair_bytes, steps):
     """Same metric through the public API with host buffers.  Every step copies its inputs
     from pinned host memory (x, indices, weights), dispatches, combines and copies its outputs
@@ -568,6 +665,36 @@ def _time_oracle(sub, min_seconds=0.0, max_repeats=1):
     return statistics.median(times), int(res[0]["recv_count"].sum()), res, len(times)
 
 
+def cpu_all_cores(wl, tokens=256, seconds=6.0):
+    """The oracle on every host core at once: one thread per core, each running its own
+    dispatch+combine of a sample (the first `tokens` tokens of every rank) back to back for
+    ~`seconds`.  The oracle's C calls run without the Python GIL, so the threads run in
+    parallel; the value is the aggregate of all threads (bytes of all runs / wall time)."""
+    import concurrent.futures
+    import oracle
+    oracle.build()
+    sub = _sample(wl, tokens)
+    _, P, _, _ = _time_oracle(sub)
+    cores = os.cpu_count() or 1
+    deadline = time.perf_counter() + seconds
+
+    def worker(_):
+        n = 0
+        while time.perf_counter() < deadline:
+            oracle.run_workload(sub)
+            n += 1
+        return n
+    t0 = time.perf_counter()
+    with concurrent.futures.ThreadPoolExecutor(max_workers=cores) as pool:
+        runs = sum(pool.map(worker, range(cores)))
+    wall = time.perf_counter() - t0
+    nb = phase_bytes(sub, P)
+    return {"value": round(runs * nb["pair"] / wall / 1e9, 3), "unit": "GB/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"first {tokens} tokens of each rank ({sub.N} tokens, {P} pairs); {cores} "
+                      f"threads, {runs} dispatch+combine runs in {wall:.1f} s"}
+
+
 def cpu_baseline(wl, gpu_out=None):
     """The oracle (plain single-threaded C) on the whole workload, repeated for ~10 s."""
     dt, P, res, runs = _time_oracle(wl, min_seconds=10.0, max_repeats=20)
@@ -581,6 +708,7 @@ def cpu_baseline(wl, gpu_out=None):
         o_out = res[2]
         ok = all(np.array_equal(g[s, :n], o_out[s, :n]) for s, n in enumerate(wl.n_tok))
         info["parity_combine_output"] = "bit-exact" if ok else "MISMATCH"
+    info["all_cores"] = cpu_all_cores(wl)
     return info
 
 

@@ -68,6 +68,20 @@ __global__ void __launch_bounds__(kCopyThreads, 3) ep_quantise_rows_kernel(const
 
 // ---- gather-reduce over the FP8 wire
 
+// acc += x * s on an element pair: two scalar FP32 multiplies, then one packed FP32 add.  Each
+// lane rounds exactly as the scalar add.  (A packed multiply followed by a packed add is not
+// used: the two were observed to give fused-multiply-add results, which differ from the
+// oracle's rounded product.)
+__device__ __forceinline__ void mul_add_f32x2(float& a0, float& a1, float x0, float x1, float s)
+{
+    const float p0 = __fmul_rn(x0, s), p1 = __fmul_rn(x1, s);
+    unsigned long long a, pv;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(a0), "f"(a1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(pv) : "f"(p0), "f"(p1));
+    asm("add.rn.f32x2 %0, %0, %1;" : "+l"(a) : "l"(pv));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(a));
+}
+
 __device__ __forceinline__ void add_fp8x16(float (&acc)[16], const uint4& c, float scale)
 {
     const uint32_t w[4] = {c.x, c.y, c.z, c.w};
@@ -75,10 +89,8 @@ __device__ __forceinline__ void add_fp8x16(float (&acc)[16], const uint4& c, flo
     for (int i = 0; i < 4; ++i) {
         const float2 lo = e4m3x2_to_float2(w[i] & 0xFFFFu);
         const float2 hi = e4m3x2_to_float2(w[i] >> 16);
-        acc[4 * i + 0] = __fadd_rn(acc[4 * i + 0], __fmul_rn(lo.x, scale));
-        acc[4 * i + 1] = __fadd_rn(acc[4 * i + 1], __fmul_rn(lo.y, scale));
-        acc[4 * i + 2] = __fadd_rn(acc[4 * i + 2], __fmul_rn(hi.x, scale));
-        acc[4 * i + 3] = __fadd_rn(acc[4 * i + 3], __fmul_rn(hi.y, scale));
+        mul_add_f32x2(acc[4 * i + 0], acc[4 * i + 1], lo.x, lo.y, scale);
+        mul_add_f32x2(acc[4 * i + 2], acc[4 * i + 3], hi.x, hi.y, scale);
     }
 }
 
@@ -235,13 +247,6 @@ __device__ __forceinline__ uint32_t e2m1x2(float lo, float hi)
     return r;
 }
 
-__device__ __forceinline__ float2 e2m1x2_to_float2(uint32_t byte)
-{
-    uint32_t h2;
-    asm("{ .reg .b8 c; cvt.u8.u32 c, %1; cvt.rn.f16x2.e2m1x2 %0, c; }" : "=r"(h2) : "r"(byte));
-    return __half22float2(*reinterpret_cast<const __half2*>(&h2));
-}
-
 __device__ __forceinline__ float e8m0_to_float(uint32_t code)
 {
     return __uint_as_float(code == 0 ? 0x00400000u : code << 23);
@@ -302,18 +307,71 @@ __global__ void __launch_bounds__(kCopyThreads, 3) ep_quantise_rows_fp4_kernel(c
     }
 }
 
-// acc[16] += the 16 e2m1 codes of (lo, hi) times scale
-__device__ __forceinline__ void add_fp4x16(float (&acc)[16], uint32_t lo, uint32_t hi, float scale)
+__device__ __forceinline__ void fma_f32x2(float2& acc, float2 x, unsigned long long ss)
 {
-    const uint32_t w[2] = {lo, hi};
+    unsigned long long a, xv;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(acc.x), "f"(acc.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(xv) : "f"(x.x), "f"(x.y));
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a) : "l"(xv), "l"(ss));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(acc.x), "=f"(acc.y) : "l"(a));
+}
+
+// The four code bytes of w (8 e2m1 codes, element 0 in the low nibble) as four f16x2 pairs.
+__device__ __forceinline__ void e2m1x8_to_half2x4(uint32_t w, uint32_t (&h)[4])
+{
+    asm("{ .reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3; }"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3]) : "r"(w));
+}
+
+// acc[0..7] (element pairs) += the 16 e2m1 codes of (lo, hi) times 2^(code - 127).
+// An e2m1 value has at most two significant bits and the scale is a power of two, so the
+// product is exact in FP32 (down to 2^-128, above FP32's smallest subnormal) unless it
+// overflows; a fused multiply-add therefore rounds exactly as the product followed by an add.
+// Only codes 253 and 254 (an infinite block maximum) can overflow: they take the two-step form.
+__device__ __forceinline__ void add_fp4x16(float2 (&acc)[8], uint32_t lo, uint32_t hi, uint32_t code)
+{
+    const float scale = e8m0_to_float(code);
+    uint32_t hv[8];
+    {
+        uint32_t t[4];
+        e2m1x8_to_half2x4(lo, t);
 #pragma unroll
-    for (int i = 0; i < 2; ++i)
+        for (int i = 0; i < 4; ++i) hv[i] = t[i];
+        e2m1x8_to_half2x4(hi, t);
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-            const float2 v = e2m1x2_to_float2((w[i] >> (8 * h)) & 0xFFu);
-            acc[8 * i + 2 * h] = __fadd_rn(acc[8 * i + 2 * h], __fmul_rn(v.x, scale));
-            acc[8 * i + 2 * h + 1] = __fadd_rn(acc[8 * i + 2 * h + 1], __fmul_rn(v.y, scale));
-        }
+        for (int i = 0; i < 4; ++i) hv[4 + i] = t[i];
+    }
+    if (code < 253u) {
+        unsigned long long ss;
+        asm("mov.b64 %0, {%1, %1};" : "=l"(ss) : "f"(scale));
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            fma_f32x2(acc[i], __half22float2(*reinterpret_cast<const __half2*>(&hv[i])), ss);
+        return;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&hv[i]));
+        acc[i].x = __fadd_rn(acc[i].x, __fmul_rn(v.x, scale));
+        acc[i].y = __fadd_rn(acc[i].y, __fmul_rn(v.y, scale));
+    }
+}
+
+__device__ __forceinline__ void store_bf16x16(uint4* dst, const float2 (&acc)[8])
+{
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const __nv_bfloat162 b = __floats2bfloat162_rn(acc[i].x, acc[i].y);
+        w[i] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    st_v4(dst, make_uint4(w[0], w[1], w[2], w[3]));
+    st_v4(dst + 1, make_uint4(w[4], w[5], w[6], w[7]));
 }
 
 // Rolling fold of nd <= 8 rows over the FP4 wire.  A lane owns 32-element blocks (16 code bytes
@@ -339,20 +397,19 @@ __device__ __forceinline__ void fold_fp4_rows(const WireArgs& a, int src, int nd
         }
     for (int vb = 0; vb < nb; vb += 32) {             // warp-uniform bounds
         const int pc = vb + lane, pn = pc + 32;
-        float acc[16];
+        float2 acc[8];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+        for (int i = 0; i < 8; ++i) acc[i] = make_float2(0.0f, 0.0f);
 #pragma unroll
         for (int d = 0; d < 8; ++d)
-            if (d < nd && pc < nb) add_fp4x16(acc, b[d].x, b[d].y, e8m0_to_float(sc[d]));
+            if (d < nd && pc < nb) add_fp4x16(acc, b[d].x, b[d].y, sc[d]);
         if (pc < nb) store_bf16x16(dst + (int64_t)pc * 4, acc);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+        for (int i = 0; i < 8; ++i) acc[i] = make_float2(0.0f, 0.0f);
 #pragma unroll
         for (int d = 0; d < 8; ++d) {
             if (d < nd) {
-                const uint32_t z = b[d].z, w = b[d].w;
-                const float xs = e8m0_to_float(sc[d]);
+                const uint32_t z = b[d].z, w = b[d].w, xs = sc[d];
                 if (pn < nb) {
                     b[d] = ld_stream_v4(q4 + ro[d] + pn);
                     sc[d] = __ldg(sc8 + ro[d] + pn);
@@ -376,9 +433,9 @@ __device__ __forceinline__ void fold_fp4_wide(const WireArgs& a, int src, int nd
         const bool act = pc < nb;
 #pragma unroll 1
         for (int half = 0; half < 2; ++half) {
-            float acc[16];
+            float2 acc[8];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+            for (int i = 0; i < 8; ++i) acc[i] = make_float2(0.0f, 0.0f);
             for (int d0 = 0; d0 < nd; d0 += 8) {
                 uint2 c[8];
                 uint32_t sc[8];
@@ -392,7 +449,7 @@ __device__ __forceinline__ void fold_fp4_wide(const WireArgs& a, int src, int nd
                 }
 #pragma unroll
                 for (int d = 0; d < 8; ++d)
-                    if (act && d0 + d < nd) add_fp4x16(acc, c[d].x, c[d].y, e8m0_to_float(sc[d]));
+                    if (act && d0 + d < nd) add_fp4x16(acc, c[d].x, c[d].y, sc[d]);
             }
             if (act) store_bf16x16(dst + (int64_t)pc * 4 + 2 * half, acc);
         }
