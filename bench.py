@@ -288,6 +288,8 @@ def run_ours(args, rank, world, dist):
     e2e = measure_e2e(plan, wl, dev, stream, nbytes["pair"], steps=max(3, min(args.steps, 20)))
     quant = measure_quantised_dispatch(ep, wl, dev, stream, x, w, idx, P, peak,
                                        steps=max(3, min(args.steps, 50)))
+    quant4 = measure_quantised_dispatch(ep, wl, dev, stream, x, w, idx, P, peak,
+                                        steps=max(3, min(args.steps, 50)), fmt="fp4")
     wire = measure_combine_wire(plan, wl, dev, stream, x, w, idx, P, peak,
                                 steps=max(3, min(args.steps, 50)), fmt="fp8")
     wire4 = measure_combine_wire(plan, wl, dev, stream, x, w, idx, P, peak,
@@ -337,6 +339,7 @@ def run_ours(args, rank, world, dist):
             "gpu_launches": 3 * args.steps,
             "cpu_baseline": cpu,
             "fp8_quantising_dispatch": quant,
+            "mxfp4_quantising_dispatch": quant4,
             "fp8_combine_wire": wire,
             "fp4_combine_wire": wire4,
             "expert_grouped_layout": grouped,
@@ -347,11 +350,13 @@ def run_ours(args, rank, world, dist):
     return result
 
 
-def measure_quantised_dispatch(ep, wl, dev, stream, x, w, idx, P, peak, steps):
-    """Dispatch of the same BF16 tokens through the quantising dtype: FP8 e4m3 rows and one FP32
-    scale per 128 elements are written instead of BF16 rows.  Minimal bytes: read N*(2H + 8k),
-    write P*(H + 4H/128 + 8k + 4)."""
-    plan = ep.Plan(wl.W, wl.E, wl.k, wl.H, "bf16_fp8", 0, wl.M, device=dev)
+def measure_quantised_dispatch(ep, wl, dev, stream, x, w, idx, P, peak, steps, fmt="fp8"):
+    """Dispatch of the same BF16 tokens through a quantising dtype: FP8 e4m3 rows and one FP32
+    scale per 128 elements (fmt "fp8"), or MX FP4 rows of H/2 code bytes and H/32 scale bytes
+    (fmt "fp4"), are written instead of BF16 rows.  Minimal bytes: read N*(2H + 8k), write
+    P*(wire row + 8k + 4)."""
+    plan = ep.Plan(wl.W, wl.E, wl.k, wl.H, "bf16_fp8" if fmt == "fp8" else "bf16_mxfp4", 0, wl.M,
+                   device=dev)
     for _ in range(3):
         plan.dispatch(x, w, None, idx, wl.n_tok, stream=stream)
     torch.cuda.synchronize(dev)
@@ -369,8 +374,9 @@ def measure_quantised_dispatch(ep, wl, dev, stream, x, w, idx, P, peak, steps):
     route = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
     scat = sum(e[1].elapsed_time(e[2]) for e in ev) / steps
     N, H, k = wl.N, wl.H, wl.k
-    nb = N * (2 * H + 8 * k) + P * (H + 4 * (H // 128) + 8 * k + 4)
-    nb_scatter = N * (2 * H + 8 * k) + P * (H + 4 * (H // 128) + 8 * k)
+    wire_row = H + 4 * (H // 128) if fmt == "fp8" else H // 2 + H // 32
+    nb = N * (2 * H + 8 * k) + P * (wire_row + 8 * k + 4)
+    nb_scatter = N * (2 * H + 8 * k) + P * (wire_row + 8 * k)
     return {"dispatch_us": round((route + scat) * 1e3, 2), "route_us": round(route * 1e3, 2),
             "scatter_us": round(scat * 1e3, 2), "algorithmic_bytes": nb,
             "dispatch_gbs": round(nb / ((route + scat) * 1e-3) / 1e9, 1),

@@ -18,9 +18,11 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libep.so")
 
-EP_BF16, EP_FP16, EP_FP8_E4M3, EP_BF16_TO_FP8_E4M3 = 0, 1, 2, 3
-# "bf16_fp8": BF16 input that dispatch quantises to FP8 e4m3 + one FP32 scale per 128 elements
-DTYPE_CODES = {"bf16": EP_BF16, "fp16": EP_FP16, "fp8": EP_FP8_E4M3, "bf16_fp8": EP_BF16_TO_FP8_E4M3}
+EP_BF16, EP_FP16, EP_FP8_E4M3, EP_BF16_TO_FP8_E4M3, EP_BF16_TO_MXFP4 = 0, 1, 2, 3, 4
+# "bf16_fp8": BF16 input that dispatch quantises to FP8 e4m3 + one FP32 scale per 128 elements;
+# "bf16_mxfp4": BF16 input that dispatch quantises to MX FP4 (e2m1 codes, one e8m0 scale per 32)
+DTYPE_CODES = {"bf16": EP_BF16, "fp16": EP_FP16, "fp8": EP_FP8_E4M3, "bf16_fp8": EP_BF16_TO_FP8_E4M3,
+               "bf16_mxfp4": EP_BF16_TO_MXFP4}
 EP_OK, EP_ERR_ARG, EP_ERR_ALLOC, EP_ERR_CUDA, EP_ERR_STATE = 0, -1, -2, -3, -4
 EP_ERR_CAPACITY, EP_ERR_INDEX, EP_ERR_DEVICE_TIMEOUT = -5, -6, -7
 VARIANTS = {"auto": 0, "whole_row": 1, "tiled_512": 2, "tiled_1024": 3}
@@ -149,10 +151,10 @@ def _stream(stream) -> ctypes.c_void_p:
 class Dispatched:
     """Views of the plan's receive buffers after one dispatch (valid until the next dispatch or
     reset of the plan; the plan must outlive them)."""
-    recv_x: torch.Tensor          # [W][W*M][H] payload dtype
+    recv_x: torch.Tensor          # [W][W*M][H] payload dtype ([W][W*M][H/2] uint8 for MX FP4)
     recv_idx: torch.Tensor        # [W][W*M][k] int32
     recv_w: Optional[torch.Tensor]       # [W][W*M][k] float32
-    recv_scales: Optional[torch.Tensor]  # [W][W*M][sd] float32
+    recv_scales: Optional[torch.Tensor]  # [W][W*M][sd] float32 ([W][W*M][H/32] uint8 for MX FP4)
     recv_count: torch.Tensor      # [W] int32
     src_token_pos: torch.Tensor   # [W][W*M] int32
     epoch: int
@@ -162,8 +164,10 @@ class Plan:
     """One expert-parallel Dispatch/Combine problem shape; owns the receive buffers.
 
     ``Plan(W, experts_per_rank, topk, hidden, dtype, scale_dim, max_tok_per_rank)`` maps to
-    ``ep_plan_create``; dtype is "bf16", "fp16", "fp8" (e4m3 with caller scales) or "bf16_fp8"
-    (BF16 input quantised by dispatch to e4m3 with one FP32 scale per 128 elements)."""
+    ``ep_plan_create``; dtype is "bf16", "fp16", "fp8" (e4m3 with caller scales), "bf16_fp8"
+    (BF16 input quantised by dispatch to e4m3 with one FP32 scale per 128 elements) or
+    "bf16_mxfp4" (BF16 input quantised by dispatch to MX FP4: receive rows of H/2 packed e2m1
+    bytes and H/32 e8m0 scale bytes)."""
 
     def __init__(self, W: int, experts_per_rank: int, topk: int, hidden: int, dtype: str = "bf16",
                  scale_dim: int = 0, max_tok_per_rank: int = 1, device=None):
@@ -177,10 +181,13 @@ class Plan:
             _check(self._lib.ep_plan_create(ctypes.byref(self._h), W, experts_per_rank, topk, hidden,
                                             DTYPE_CODES[dtype], scale_dim, max_tok_per_rank))
         self.rows = W * max_tok_per_rank
-        if dtype == "bf16_fp8":
+        if dtype in ("bf16_fp8", "bf16_mxfp4"):
             self.sd = hidden // 128
         self.payload_torch_dtype = {"bf16": torch.bfloat16, "fp16": torch.float16,
-                                    "fp8": torch.float8_e4m3fn, "bf16_fp8": torch.float8_e4m3fn}[dtype]
+                                    "fp8": torch.float8_e4m3fn, "bf16_fp8": torch.float8_e4m3fn,
+                                    "bf16_mxfp4": torch.uint8}[dtype]
+        # elements of payload_torch_dtype per received row (MX FP4 packs two codes per byte)
+        self.row_elems = hidden // 2 if dtype == "bf16_mxfp4" else hidden
         self.combine_torch_dtype = torch.float16 if dtype == "fp16" else torch.bfloat16
 
     # -- lifetime
@@ -213,11 +220,19 @@ class Plan:
         W, R, k, H, sd, dev = self.W, self.rows, self.k, self.H, self.sd, self.device
         if self.dtype in ("fp8", "bf16_fp8"):
             rx = _view(o.recv_x, (W, R, H), "|u1", dev).view(torch.float8_e4m3fn)
+        elif self.dtype == "bf16_mxfp4":
+            rx = _view(o.recv_x, (W, R, H // 2), "|u1", dev)
         else:
             rx = _view(o.recv_x, (W, R, H), "<i2", dev).view(self.payload_torch_dtype)
+        if not sd:
+            rs = None
+        elif self.dtype == "bf16_mxfp4":                 # H/32 e8m0 scale codes per row
+            rs = _view(o.recv_scales, (W, R, H // 32), "|u1", dev)
+        else:
+            rs = _view(o.recv_scales, (W, R, sd), "<f4", dev)
         return Dispatched(recv_x=rx, recv_idx=_view(o.recv_idx, (W, R, k), "<i4", dev),
                           recv_w=_view(o.recv_w, (W, R, k), "<f4", dev),
-                          recv_scales=_view(o.recv_scales, (W, R, sd), "<f4", dev) if sd else None,
+                          recv_scales=rs,
                           recv_count=_view(o.recv_count, (W,), "<i4", dev),
                           src_token_pos=_view(o.src_token_pos, (W, R), "<i4", dev),
                           epoch=int(o.epoch))
@@ -309,7 +324,8 @@ class Plan:
         packed_count [W][E], packed_src_info [W][E][W*M], layout_range [W][E][W] int64)."""
         W, E, R, H = self.W, self.E, self.rows, self.H
         if packed_x is None:
-            packed_x = torch.empty((W, E, R, H), dtype=self.payload_torch_dtype, device=self.device)
+            packed_x = torch.empty((W, E, R, self.row_elems), dtype=self.payload_torch_dtype,
+                                   device=self.device)
         count = torch.empty((W, E), dtype=torch.int32, device=self.device)
         src_info = torch.empty((W, E, R), dtype=torch.int32, device=self.device)
         layout = torch.empty((W, E, W), dtype=torch.int64, device=self.device)
@@ -324,7 +340,8 @@ class Plan:
         packed_src_info, layout_range); the Dispatched views' recv_x holds unspecified data."""
         W, E, R, H = self.W, self.E, self.rows, self.H
         if packed_x is None:
-            packed_x = torch.empty((W, E, R, H), dtype=self.payload_torch_dtype, device=self.device)
+            packed_x = torch.empty((W, E, R, self.row_elems), dtype=self.payload_torch_dtype,
+                                   device=self.device)
         count = torch.empty((W, E), dtype=torch.int32, device=self.device)
         src_info = torch.empty((W, E, R), dtype=torch.int32, device=self.device)
         layout = torch.empty((W, E, W), dtype=torch.int64, device=self.device)

@@ -13,9 +13,10 @@ using namespace ep;
 
 struct ep_plan {
     int W, E, k, H, dtype, sd, M, F, elem_bytes, tiles;
-    bool quantise;       // EP_BF16_TO_FP8_E4M3: BF16 input, FP8 rows + scales on the wire
+    bool quantise;       // BF16 input quantised by dispatch: FP8 e4m3 or MX FP4 rows + scales
+    bool fp4;            // EP_BF16_TO_MXFP4
     int64_t rows;        // W*M receive rows per rank
-    int64_t row_bytes;   // H * element size
+    int64_t row_bytes;   // received payload bytes per row
     int device, num_sms, variant;
 
     void* base;
@@ -67,19 +68,24 @@ struct Layout {
         status, total;
 };
 
-int elem_bytes_of(int dtype)
+// bytes of one RECEIVED payload row (0 for an unknown dtype)
+int64_t row_bytes_of(int dtype, int64_t H)
 {
     switch (dtype) {
     case EP_BF16:
-    case EP_FP16: return 2;
+    case EP_FP16: return 2 * H;
     case EP_FP8_E4M3:
-    case EP_BF16_TO_FP8_E4M3: return 1;   // bytes per element of the RECEIVED payload
+    case EP_BF16_TO_FP8_E4M3: return H;
+    case EP_BF16_TO_MXFP4: return H / 2;
     default: return 0;
     }
 }
 
-// scale_dim the plan actually uses (the quantising dtype fixes it at hidden / 128)
-int effective_sd(int dtype, int H, int sd) { return dtype == EP_BF16_TO_FP8_E4M3 ? H / 128 : sd; }
+bool quantising(int dtype) { return dtype == EP_BF16_TO_FP8_E4M3 || dtype == EP_BF16_TO_MXFP4; }
+
+// scale_dim the plan actually uses: the quantising dtypes fix it at hidden / 128 (FP32 scales
+// per 128 elements, or the H/32 e8m0 bytes of MX FP4 packed four to a word)
+int effective_sd(int dtype, int H, int sd) { return quantising(dtype) ? H / 128 : sd; }
 
 int check_shape(int W, int E, int k, int H, int dtype, int sd, int M)
 {
@@ -87,13 +93,13 @@ int check_shape(int W, int E, int k, int H, int dtype, int sd, int M)
     if (E < 1) return fail(EP_ERR_ARG, "experts_per_rank=%d < 1", E);
     if ((int64_t)W * E >= (int64_t)1 << 31) return fail(EP_ERR_ARG, "W*experts_per_rank >= 2^31");
     if (k < 1 || k > kMaxTopk) return fail(EP_ERR_ARG, "topk=%d outside 1..%d", k, kMaxTopk);
-    const int eb = elem_bytes_of(dtype);
-    if (eb == 0) return fail(EP_ERR_ARG, "dtype=%d is not an ep_dtype", dtype);
-    if (H < 1 || ((int64_t)H * eb) % 16 != 0)
-        return fail(EP_ERR_ARG, "hidden=%d: hidden * %d bytes must be a positive multiple of 16", H, eb);
-    if ((int64_t)H * eb >= (int64_t)1 << 31) return fail(EP_ERR_ARG, "hidden=%d too large", H);
+    if (row_bytes_of(dtype, 2) == 0) return fail(EP_ERR_ARG, "dtype=%d is not an ep_dtype", dtype);
+    if (H < 1 || row_bytes_of(dtype, H) % 16 != 0 || (dtype == EP_BF16_TO_MXFP4 && H % 2 != 0))
+        return fail(EP_ERR_ARG, "hidden=%d: a received row of %lld bytes is not a positive multiple of 16",
+                    H, (long long)row_bytes_of(dtype, H));
+    if (2 * (int64_t)H >= (int64_t)1 << 31) return fail(EP_ERR_ARG, "hidden=%d too large", H);
     if (sd < 0 || sd > 65536) return fail(EP_ERR_ARG, "scale_dim=%d outside 0..65536", sd);
-    if (dtype == EP_BF16_TO_FP8_E4M3) {
+    if (quantising(dtype)) {
         if (H % 128 != 0) return fail(EP_ERR_ARG, "hidden=%d: the quantising dtype needs hidden %% 128 == 0", H);
         if (sd != 0 && sd != H / 128)
             return fail(EP_ERR_ARG, "scale_dim=%d: the quantising dtype uses hidden/128 = %d scales", sd, H / 128);
@@ -115,7 +121,7 @@ Layout layout_of(int W, int k, int H, int dtype, int sd, int M)
         field = o;
         o += align256(bytes);
     };
-    put(L.recv_x, (size_t)W * rows * H * elem_bytes_of(dtype));
+    put(L.recv_x, (size_t)W * rows * row_bytes_of(dtype, H));
     put(L.recv_idx, (size_t)W * rows * k * 4);
     put(L.recv_w, (size_t)W * rows * k * 4);
     put(L.recv_scales, (size_t)W * rows * sd * 4);
@@ -209,9 +215,9 @@ int ep_plan_create(ep_plan** out, int W, int E, int k, int H, int dtype, int sd,
     if (!p) return fail(EP_ERR_ALLOC, "host allocation of the plan failed");
     p->W = W; p->E = E; p->k = k; p->H = H; p->dtype = dtype; p->sd = sd; p->M = M;
     p->F = W < k ? W : k;
-    p->elem_bytes = elem_bytes_of(dtype);
+    p->elem_bytes = dtype == EP_BF16 || dtype == EP_FP16 ? 2 : 1;   // BF16/FP16, else a byte stream
     p->rows = (int64_t)W * M;
-    p->row_bytes = (int64_t)H * p->elem_bytes;
+    p->row_bytes = row_bytes_of(dtype, H);
     p->tiles = (int)((p->rows + kRouteTile - 1) / kRouteTile);
     p->variant = EP_VARIANT_AUTO;
 
@@ -221,7 +227,8 @@ int ep_plan_create(ep_plan** out, int W, int E, int k, int H, int dtype, int sd,
 
     sd = effective_sd(dtype, H, sd);
     p->sd = sd;
-    p->quantise = dtype == EP_BF16_TO_FP8_E4M3;
+    p->quantise = quantising(dtype);
+    p->fp4 = dtype == EP_BF16_TO_MXFP4;
     const Layout L = layout_of(W, k, H, dtype, sd, M);
     p->bytes = L.total;
     e = cudaMalloc(&p->base, L.total);
@@ -353,11 +360,13 @@ int ep_dispatch_scatter(ep_plan* p, const void* x, const float* weights, const f
     a.row_bytes = p->row_bytes;
     a.W = p->W; a.k = p->k; a.F = p->F; a.M = p->M; a.sd = p->sd; a.N = p->N;
     const int ce = pick_chunk_elems(p, p->N);
-    a.chunk_bytes = ce * p->elem_bytes;
-    a.chunks = (int)((p->row_bytes + a.chunk_bytes - 1) / a.chunk_bytes);
+    // quantising scatters take the slice in elements (their source rows are BF16)
+    a.chunk_bytes = p->quantise ? ce : ce * p->elem_bytes;
+    a.chunks = (int)((p->H + ce - 1) / ce);
     for (int s = 0; s <= p->W; ++s) a.tok_off[s] = p->tok_off[s];
-    cudaError_t e = p->quantise ? launch_scatter_quant(a, p->num_sms, (cudaStream_t)stream)
-                                : launch_scatter(a, p->num_sms, (cudaStream_t)stream);
+    cudaError_t e = p->fp4 ? launch_scatter_quant_fp4(a, p->num_sms, (cudaStream_t)stream)
+                    : p->quantise ? launch_scatter_quant(a, p->num_sms, (cudaStream_t)stream)
+                                  : launch_scatter(a, p->num_sms, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "ep_dispatch_scatter: launch");
     p->routed = false;
     p->live = true;

@@ -134,6 +134,9 @@ cudaError_t launch_scatter(const ScatterArgs& a, int num_sms, cudaStream_t strea
 // BF16 rows in, FP8 e4m3 rows + FP32 scales (one per 128 elements) out.  Here a.row_bytes is
 // the FP8 row (= H), a.chunk_bytes the slice in ELEMENTS (a multiple of 128) and a.sd = H/128.
 cudaError_t launch_scatter_quant(const ScatterArgs& a, int num_sms, cudaStream_t stream);
+// MX FP4 quantising scatter: a.row_bytes = H/2, a.chunk_bytes = slice length in ELEMENTS (a
+// multiple of 32), recv_scales rows hold H/32 e8m0 bytes (sd = H/128 words)
+cudaError_t launch_scatter_quant_fp4(const ScatterArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_combine(const CombineArgs& a, bool fp16, int num_sms, cudaStream_t stream);
 cudaError_t launch_quantise_rows(const WireArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_group(const GroupArgs& a, int num_sms, cudaStream_t stream);
@@ -312,6 +315,53 @@ __device__ __forceinline__ float absmax16(const uint4& a, const uint4& b)
 #pragma unroll
     for (int i = 0; i < 8; ++i) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
     return m;
+}
+
+// ---- MX FP4 (OCP microscaling): 32-element blocks of e2m1 codes sharing one e8m0 scale
+//
+// scale code = floor(log2(max|x|)) - 2 + 127, clamped to 0..254 (127 for an all-zero block);
+// element code = e2m1 of x / 2^(code - 127), nearest with ties to the even code, saturating at
+// +-6.  Dividing by a power of two equals multiplying by its exact reciprocal 2^(127 - code),
+// so the quotient is formed by one multiply.  Nibbles: element 2i low, 2i + 1 high.
+
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("{ .reg .b8 t; cvt.rn.satfinite.e2m1x2.f32 t, %1, %2; cvt.u32.u8 %0, t; }"
+        : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Codes (16 bytes) of the 32 BF16 values in x[0..3]; `code` receives the block's scale code.
+__device__ __forceinline__ uint4 quantise_mxfp4_32(const uint4 (&x)[4], uint32_t& code)
+{
+    float m = 0.0f;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) m = fmaxf(m, absmax16(x[t], x[t]));
+    code = 127;
+    if (m > 0.0f) {
+        const uint32_t mb = __float_as_uint(m);
+        int e2 = (int)(mb >> 23) - 127;
+        if ((mb >> 23) == 0) e2 = -127 - (__clz(mb & 0x7FFFFFu) - 9);   // subnormal maximum
+        const int c = e2 - 2 + 127;
+        code = (uint32_t)(c < 0 ? 0 : (c > 254 ? 254 : c));
+    }
+    // 2^(127 - code); code <= 253 for any BF16 input (Inf gives 253), 254 would be 2^-127
+    const float inv = __uint_as_float(code >= 254u ? 0x00400000u : (254u - code) << 23);
+    uint32_t o[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        const uint32_t w[4] = {x[t].x, x[t].y, x[t].z, x[t].w};
+        uint32_t bytes = 0;
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            const float lo = __fmul_rn(__uint_as_float(w[h] << 16), inv);
+            const float hi = __fmul_rn(__uint_as_float(w[h] & 0xFFFF0000u), inv);
+            bytes |= e2m1x2(lo, hi) << (8 * h);
+        }
+        o[t] = bytes;
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 // Two e4m3 codes (low byte first) -> two exact floats, via the exact e4m3 -> f16 conversion.

@@ -232,20 +232,7 @@ __global__ void __launch_bounds__(kCopyThreads, 2) ep_combine_fp8_kernel(const W
     }
 }
 
-// ---- the MX FP4 wire: 32-element blocks of e2m1 codes with one e8m0 scale each
-//
-// scale code = floor(log2(max|x|)) - 2 + 127 (clamped to 0..254; 127 for an all-zero block),
-// code = e2m1 RNE saturating of x / 2^(code - 127).  Dividing by a power of two equals
-// multiplying by its exact reciprocal 2^(127 - code) (both round the same real quotient), so
-// the kernels multiply.  Nibbles: element 2i low, 2i + 1 high.
-
-__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi)
-{
-    uint32_t r;
-    asm("{ .reg .b8 t; cvt.rn.satfinite.e2m1x2.f32 t, %1, %2; cvt.u32.u8 %0, t; }"
-        : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
-}
+// ---- the MX FP4 wire (quantiser quantise_mxfp4_32 in ep_common.cuh)
 
 __device__ __forceinline__ float e8m0_to_float(uint32_t code)
 {
@@ -275,33 +262,9 @@ __global__ void __launch_bounds__(kCopyThreads, 3) ep_quantise_rows_fp4_kernel(c
             uint4 x[4];
 #pragma unroll
             for (int t = 0; t < 4; ++t) x[t] = ld_stream_v4(src + (int64_t)b * 4 + t);
-            float m = 0.0f;
-#pragma unroll
-            for (int t = 0; t < 4; ++t) m = fmaxf(m, absmax16(x[t], x[t]));
-            uint32_t code = 127;
-            if (m > 0.0f) {
-                const uint32_t mb = __float_as_uint(m);
-                int e2 = (int)(mb >> 23) - 127;
-                if ((mb >> 23) == 0) e2 = -127 - (__clz(mb & 0x7FFFFFu) - 9);   // subnormal max
-                int c = e2 - 2 + 127;
-                code = (uint32_t)(c < 0 ? 0 : (c > 254 ? 254 : c));
-            }
-            // 2^(127 - code); code <= 253 for any BF16 input (Inf gives 253), 254 would be 2^-127
-            const float inv = __uint_as_float(code >= 254u ? 0x00400000u : (254u - code) << 23);
-            uint32_t o[4];
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                const uint32_t w[4] = {x[t].x, x[t].y, x[t].z, x[t].w};
-                uint32_t bytes = 0;
-#pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    const float lo = __fmul_rn(__uint_as_float(w[h] << 16), inv);
-                    const float hi = __fmul_rn(__uint_as_float(w[h] & 0xFFFF0000u), inv);
-                    bytes |= e2m1x2(lo, hi) << (8 * h);
-                }
-                o[t] = bytes;
-            }
-            st_v4(dq + b, make_uint4(o[0], o[1], o[2], o[3]));
+            uint32_t code;
+            const uint4 codes = quantise_mxfp4_32(x, code);
+            st_v4(dq + b, codes);
             sc8[u * nblk + b] = (uint8_t)code;
         }
     }

@@ -162,7 +162,82 @@ __global__ void __launch_bounds__(kCopyThreads, 3) ep_scatter_quant_kernel(const
     }
 }
 
+// MX FP4 quantising scatter.  A lane owns one 32-element block (64 source bytes -> 16 code
+// bytes and one e8m0 scale byte); each block is quantised once per token and written to every
+// destination row.  a.chunk_bytes counts ELEMENTS here (slices are multiples of 128).
+__global__ void __launch_bounds__(kCopyThreads, 3) ep_scatter_quant_fp4_kernel(const ScatterArgs a)
+{
+    __shared__ int s_off[kMaxRanks + 1];
+    if (threadIdx.x <= a.W) s_off[threadIdx.x] = a.tok_off[threadIdx.x];
+    __syncthreads();
+
+    const int lane = threadIdx.x & 31;
+    const int64_t warps_per_grid = (int64_t)gridDim.x * (kCopyThreads / 32);
+    const int64_t units = (int64_t)a.N * a.chunks;
+    const int64_t H = a.row_bytes * 2;           // elements; a received row holds H/2 code bytes
+    const int64_t hb = H >> 5;                    // blocks (and scale bytes) per row
+    uint8_t* sc8 = reinterpret_cast<uint8_t*>(a.recv_scales);
+    for (int64_t u = (int64_t)blockIdx.x * (kCopyThreads / 32) + (threadIdx.x >> 5); u < units;
+         u += warps_per_grid) {
+        const int g = (int)(u / a.chunks);
+        const int c = (int)(u - (int64_t)g * a.chunks);
+        const int s = rank_of_token(s_off, a.W, g);
+        const int64_t tok = (int64_t)s * a.M + (g - s_off[s]);
+        const int dest = lane < a.F ? __ldg(a.fwd + tok * a.F + lane) : -1;
+        const int nd = __popc(__ballot_sync(0xffffffffu, dest >= 0));
+
+        const int64_t h0 = (int64_t)c * a.chunk_bytes;                // elements
+        const int64_t rem = H - h0;
+        const int nblk = (int)((rem < a.chunk_bytes ? rem : a.chunk_bytes) >> 5);
+        const uint4* src = reinterpret_cast<const uint4*>(a.x + (tok * H + h0) * 2);
+        for (int b0 = 0; b0 < nblk; b0 += 32) {                      // warp-uniform bounds
+            const int b = b0 + lane;
+            uint4 codes = make_uint4(0, 0, 0, 0);
+            uint32_t code = 0;
+            if (b < nblk) {
+                uint4 x[4];
+#pragma unroll
+                for (int t = 0; t < 4; ++t) x[t] = ld_stream_v4(src + (int64_t)b * 4 + t);
+                codes = quantise_mxfp4_32(x, code);
+            }
+            for (int d = 0; d < nd; ++d) {
+                const int64_t row = __shfl_sync(0xffffffffu, dest, d);
+                if (b < nblk) {
+                    st_v4(a.recv_x + row * a.row_bytes + (h0 >> 1) + (int64_t)b * 16, codes);
+                    sc8[row * hb + (h0 >> 5) + b] = (uint8_t)code;
+                }
+            }
+        }
+
+        if (c == 0) {
+            for (int d = 0; d < nd; ++d) {
+                const int64_t row = __shfl_sync(0xffffffffu, dest, d);
+                for (int e = lane; e < a.k; e += 32) {
+                    a.recv_idx[row * a.k + e] = __ldg(a.idx + tok * a.k + e);
+                    if (a.w) a.recv_w[row * a.k + e] = __ldg(a.w + tok * a.k + e);
+                }
+            }
+        }
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_scatter_quant_fp4(const ScatterArgs& a, int num_sms, cudaStream_t stream)
+{
+    const int64_t units = (int64_t)a.N * a.chunks;
+    if (units == 0) return cudaSuccess;
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ep_scatter_quant_fp4_kernel,
+                                                                  kCopyThreads, 0);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    const int64_t need = (units + kCopyThreads / 32 - 1) / (kCopyThreads / 32);
+    const int64_t cap = (int64_t)per_sm * num_sms;
+    const int grid = (int)(need < cap ? need : cap);
+    ep_scatter_quant_fp4_kernel<<<grid, kCopyThreads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_scatter_quant(const ScatterArgs& a, int num_sms, cudaStream_t stream)
 {

@@ -57,8 +57,18 @@ typedef struct ep_plan ep_plan; /* opaque; created and owned by the library */
  *                           must be a multiple of 128; the plan's scale_dim is hidden / 128
  *                           (pass 0 or hidden / 128).  Dispatch takes no scales; recv_x holds
  *                           the codes and recv_scales the scales.  Combine takes and returns
- *                           BF16 (the expert dequantises). */
-enum ep_dtype { EP_BF16 = 0, EP_FP16 = 1, EP_FP8_E4M3 = 2, EP_BF16_TO_FP8_E4M3 = 3 };
+ *                           BF16 (the expert dequantises).
+ *   EP_BF16_TO_MXFP4        BF16 input, quantised by dispatch itself to MX FP4 (the pages' FP4
+ *                           dispatch; the OCP microscaling layout): per 32-element block, scale
+ *                           code c = floor(log2 max|x|) - 2 + 127 clamped to 0..254 (127 for an
+ *                           all-zero block) and element codes e2m1(x / 2^(c - 127)), rounded to
+ *                           nearest with ties to the even code, saturating at +-6.  hidden must
+ *                           be a multiple of 128.  recv_x rows hold H/2 bytes, element 2i in the
+ *                           low nibble of byte i; recv_scales rows hold the H/32 scale codes as
+ *                           bytes, i.e. H/128 4-byte words (the plan's scale_dim is hidden / 128;
+ *                           pass 0 or hidden / 128).  Dispatch takes no scales.  Combine takes and
+ *                           returns BF16 (the expert dequantises). */
+enum ep_dtype { EP_BF16 = 0, EP_FP16 = 1, EP_FP8_E4M3 = 2, EP_BF16_TO_FP8_E4M3 = 3, EP_BF16_TO_MXFP4 = 4 };
 
 enum ep_status_code {
     EP_OK = 0,
@@ -79,10 +89,10 @@ enum ep_variant { EP_VARIANT_AUTO = 0, EP_VARIANT_WHOLE_ROW = 1, EP_VARIANT_TILE
 
 /* Views of the plan's receive buffers after a dispatch (guide, dispatch() return values). */
 typedef struct {
-    void* recv_x;           /* [W][W*M][H] payload elements (BF16 / FP16 / FP8 bits)          */
+    void* recv_x;           /* [W][W*M][H] payload (BF16 / FP16 / FP8 bits; MXFP4: H/2 bytes)  */
     int32_t* recv_idx;      /* [W][W*M][k] the token's whole top-k index row                 */
     float* recv_w;          /* [W][W*M][k] FP32 weights, NULL if dispatch got none            */
-    float* recv_scales;     /* [W][W*M][sd] FP32 scales, NULL if sd == 0                      */
+    float* recv_scales;     /* [W][W*M][sd] FP32 scales, NULL if sd == 0 (MXFP4: e8m0 bytes)  */
     int32_t* recv_count;    /* [W] rows received by each rank (guide: recv_num_token)         */
     int32_t* src_token_pos; /* [W][W*M] reverse map: src_rank * (W*M) + src_token             */
     int64_t rows_per_rank;  /* W*M: stride, in rows, between ranks' receive regions           */
@@ -119,11 +129,11 @@ size_t ep_plan_device_bytes(int W, int experts_per_rank, int topk, int hidden, i
 
 /*
  * Dispatch (guide, dispatch(); gfx1201 PR, Dispatch bullet).
- *   x           [W][M][H] payload elements (BF16 for EP_BF16_TO_FP8_E4M3), 16-byte aligned;
+ *   x           [W][M][H] payload elements (BF16 for the quantising dtypes), 16-byte aligned;
  *               rows t >= n_tok[s] are not read
  *   weights     [W][M][k] FP32 or NULL
  *   scales      [W][M][sd] FP32; must be NULL iff sd == 0 (always NULL for
- *               EP_BF16_TO_FP8_E4M3, whose scales dispatch computes)
+ *               EP_BF16_TO_FP8_E4M3 and EP_BF16_TO_MXFP4, whose scales dispatch computes)
  *   indices     [W][M][k] int32 expert ids
  *   n_tok_host  host [W]: tokens on each source rank, each 0..M (EP_ERR_CAPACITY if above M)
  *   out         host: receives views of the plan's buffers and the dispatch epoch
@@ -242,7 +252,7 @@ int ep_ungroup_by_expert(ep_plan* p, const void* packed_y, void* out, uint64_t e
  * of every expert it names; the plan's 2-D receive PAYLOAD rows are not written (recv_x holds
  * unspecified data), while the receive metadata (index, weight, scale rows, src_token_pos,
  * counts) and the grouped outputs are exactly those of ep_dispatch + ep_group_by_expert, so
- * ep_ungroup_by_expert and then ep_combine work on the result.  Not for EP_BF16_TO_FP8_E4M3.
+ * ep_ungroup_by_expert and then ep_combine work on the result.  Not for the quantising dtypes.
  */
 int ep_dispatch_grouped(ep_plan* p, const void* x, const float* weights, const float* scales,
                         const int32_t* indices, const int32_t* n_tok_host, void* packed_x,

@@ -300,6 +300,19 @@ def dispatch_quantized(wl):
                     wl.indices, wl.n_tok)
 
 
+def dispatch_quantized_mxfp4(wl):
+    """Dispatch of BF16 rows quantised to MX FP4 (the pages' FP4 dispatch): every source row is
+    quantised once (quantize_mxfp4), then its H/2 code bytes are dispatched as the payload and
+    its H/32 scale bytes as the scale row (H/128 four-byte words, copied bit for bit).
+    Returns the dispatch dict plus "q" / "sc", the quantised source rows."""
+    q, sc = quantize_mxfp4(wl.x)
+    sc_words = np.ascontiguousarray(sc).view(np.float32)           # [W][M][H/128] byte carriers
+    disp = dispatch(wl.W, wl.E, wl.k, wl.H // 2, 1, wl.H // 128, wl.M, q, wl.weights, sc_words,
+                    wl.indices, wl.n_tok)
+    disp["q"], disp["sc"] = q, sc
+    return disp
+
+
 def run_workload(wl, expert_out_fn=None):
     """Oracle dispatch -> harness expert -> oracle combine for one workload.
 

@@ -57,6 +57,33 @@ def expert_np(wl, disp):
     return out
 
 
+# e2m1 values of the 16 codes (sign in bit 3; code 8 is -0)
+_E2M1 = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0, -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0]
+
+
+def mxfp4_dequant_np(q, sc):
+    """Dequantising expert for MX FP4 receive rows: BF16 bits of e2m1(code) * 2^(c - 127) for
+    q [..., H/2] packed codes and sc [..., H/32] e8m0 bytes.  Each product has at most two
+    significant bits, so it and its BF16 value are exact."""
+    H = q.shape[-1] * 2
+    codes = np.stack([q & 0xF, q >> 4], axis=-1).reshape(q.shape[:-1] + (H,))
+    v = np.array(_E2M1, dtype=np.float32)[codes]
+    bits = np.where(sc == 0, np.uint32(0x00400000), sc.astype(np.uint32) << np.uint32(23))
+    scale = bits.astype(np.uint32).view(np.float32)
+    return _f32_to_bf16_bits(v * np.repeat(scale, 32, axis=-1))
+
+
+def mxfp4_dequant_torch(q, sc):
+    """mxfp4_dequant_np with torch ops on the device: returns int16 BF16 bits [..., H]."""
+    H = q.shape[-1] * 2
+    codes = torch.stack([q & 0xF, q >> 4], dim=-1).reshape(*q.shape[:-1], H).long()
+    v = torch.tensor(_E2M1, dtype=torch.float32, device=q.device)[codes]
+    c = sc.to(torch.int32)
+    bits = torch.where(c == 0, torch.full_like(c, 0x00400000), c << 23)
+    scale = bits.view(torch.float32)
+    return torch.mul(v, scale.repeat_interleave(32, dim=-1)).to(torch.bfloat16).view(torch.int16)
+
+
 def expert_torch(wl, recv_x, recv_idx, recv_w, recv_scales, recv_count):
     """The same expert models on the GPU with torch ops (one op per IEEE step).
 

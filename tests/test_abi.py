@@ -63,7 +63,8 @@ def test_device_bytes_golden(lib):
     ((0, 4, 2, 256, 0, 0, 64), "W"), ((33, 4, 2, 256, 0, 0, 64), "W"),
     ((2, 0, 2, 256, 0, 0, 64), "experts_per_rank"), ((2, 4, 0, 256, 0, 0, 64), "topk"),
     ((2, 4, 65, 256, 0, 0, 64), "topk"), ((2, 4, 2, 4, 0, 0, 64), "hidden"),
-    ((2, 4, 2, 8, 2, 0, 64), "hidden"), ((2, 4, 2, 256, 4, 0, 64), "dtype"),
+    ((2, 4, 2, 8, 2, 0, 64), "hidden"), ((2, 4, 2, 256, 5, 0, 64), "dtype"),
+    ((2, 4, 2, 96, 4, 0, 64), "128"), ((2, 4, 2, 256, 4, 1, 64), "scale_dim"),
     ((2, 4, 2, 256, 0, -1, 64), "scale_dim"), ((2, 4, 2, 256, 0, 0, 0), "max_tok"),
     ((32, 4, 2, 256, 0, 0, 1 << 21), "2^31"),
 ])
@@ -105,3 +106,14 @@ def test_quantising_dtype_sizes_and_shape_checks(lib):
     assert "128" in lib.ep_last_error().decode()
     assert lib.ep_plan_create(ctypes.byref(h), 8, 32, 8, 7168, ep.EP_BF16_TO_FP8_E4M3, 3, 16) == ep.EP_ERR_ARG
     assert "scale" in lib.ep_last_error().decode()
+
+
+def test_mxfp4_dtype_sizes(lib):
+    # BF16 input quantised to MX FP4: H/2 code bytes per received row, and H/32 scale bytes
+    # carried as H/128 four-byte words
+    for sd in (0, 56):
+        assert lib.ep_plan_device_bytes(8, 32, 8, 7168, ep.EP_BF16_TO_MXFP4, sd, 4096) == \
+            _layout_bytes(8, 32, 8, 3584, 1, 56, 4096)
+    # DeepSeek-V3 shape: 8 * 32768 rows of 3584 code bytes, scale rows of 224 bytes
+    assert lib.ep_plan_device_bytes(8, 32, 8, 7168, ep.EP_BF16_TO_MXFP4, 0, 4096) == \
+        8 * 32768 * 3584 + 3 * (8 << 20) + 8 * 32768 * 224 + 2 * (1 << 20) + 256 + 8192 + 256 + 256

@@ -333,6 +333,85 @@ def test_quantised_dispatch_edge_values():
     _check_quantised(wl)
 
 
+# ---------------------------------------------------------------- quantising MX FP4 dispatch
+
+def _check_mxfp4_dispatch(wl, variant="auto"):
+    """Dispatch through the MX FP4 dtype: codes, scale bytes, index / weight rows, reverse map
+    and counts against the oracle (its MX quantiser, then its byte-exact dispatch), bit for bit;
+    then the combine of the dequantised rows (an exact dequantising expert on both sides)."""
+    disp = oracle.dispatch_quantized_mxfp4(wl)
+    eo = harness.mxfp4_dequant_np(disp["recv_x"], disp["recv_scales"].view(np.uint8))
+    o_out, o_w = oracle.combine(wl.W, wl.k, wl.H, False, wl.M, wl.n_tok, disp["slot_of"], eo,
+                                disp["recv_w"])
+    plan = gpu_path.make_plan(wl, DEV, variant, "bf16_mxfp4")
+    gpu_path.poison(plan, DEV)
+    x, w, _, idx = gpu_path.to_device(wl, DEV)
+    d = plan.dispatch(x, w, None, idx, wl.n_tok)
+    assert d.recv_x.shape == (wl.W, wl.W * wl.M, wl.H // 2)
+    assert d.recv_scales.shape == (wl.W, wl.W * wl.M, wl.H // 32)
+    eo_g = harness.mxfp4_dequant_torch(d.recv_x, d.recv_scales)
+    out, out_w = plan.combine(eo_g, d.recv_w, d.epoch)
+    torch.cuda.synchronize()
+    gpu = {"recv_count": d.recv_count.cpu().numpy(), "recv_x": gpu_path.raw(d.recv_x),
+           "recv_idx": gpu_path.raw(d.recv_idx), "recv_w": gpu_path.raw(d.recv_w),
+           "recv_scales": gpu_path.raw(d.recv_scales), "src_pos": gpu_path.raw(d.src_token_pos),
+           "out": gpu_path.raw(out), "out_w": gpu_path.raw(out_w), "status": plan.status()}
+    plan.close()
+    wq = wlmod.Workload(**{**wl.__dict__, "sd": wl.H // 128})   # scale rows are compared
+    gpu_path.compare(wq, gpu, disp, o_out, o_w)
+
+
+def test_mxfp4_dispatch_dsv3_reduced():
+    _check_mxfp4_dispatch(wlmod.make_workload("dsv3", max_tok=300))
+
+
+@pytest.mark.parametrize("variant", ["tiled_512", "tiled_1024", "whole_row"])
+def test_mxfp4_dispatch_small_variants(variant):
+    _check_mxfp4_dispatch(wlmod.make_workload("small", max_tok=64), variant)
+
+
+def test_mxfp4_dispatch_dsv3_full():
+    _check_mxfp4_dispatch(wlmod.make_workload("dsv3"))
+
+
+def test_mxfp4_dispatch_edge_values():
+    wl = wlmod.custom_workload(W=4, E=4, k=3, H=384, M=40, n_tok=[40, 0, 17, 33], seed=9)
+    xf = (wl.x.astype(np.uint32) << 16).view(np.float32).copy()
+    xf[0, 0] = 0.0                                   # all-zero rows and blocks (scale code 127)
+    xf[0, 1, 32:64] = 0.0
+    xf[2, 3] *= np.float32(1e-38)                    # BF16 subnormal blocks: scale code clamps to 0
+    xf[2, 4, :32] = np.float32(3e38)                 # near the BF16 maximum: code 252
+    ties = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 7.0], np.float32) * np.float32(4.0)
+    xf[3, 5, 64:96] = np.tile(np.concatenate([ties, -ties]), 2)   # exact e2m1 ties, amax 28
+    xf[3, 5, 7] = -0.0
+    wl.x[:] = torch.from_numpy(xf).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    _check_mxfp4_dispatch(wl)
+
+
+def test_mxfp4_plan_grouped_view_moves_code_bytes():
+    wl = wlmod.make_workload("small", max_tok=32)
+    disp = oracle.dispatch_quantized_mxfp4(wl)
+    g = oracle.group_by_expert(wl.W, wl.E, wl.k, wl.H // 2, 1, wl.M, disp)
+    plan = gpu_path.make_plan(wl, DEV, "auto", "bf16_mxfp4")
+    x, w, _, idx = gpu_path.to_device(wl, DEV)
+    d = plan.dispatch(x, w, None, idx, wl.n_tok)
+    px, cnt, info, layout = plan.group_by_expert(d.epoch)
+    torch.cuda.synchronize()
+    assert plan.status() == 0
+    cnt, px, info = cnt.cpu().numpy(), px.cpu().numpy(), info.cpu().numpy()
+    assert px.shape == (wl.W, wl.E, wl.W * wl.M, wl.H // 2)
+    assert np.array_equal(cnt, g["packed_count"])
+    assert np.array_equal(layout.cpu().numpy(), g["layout_range"])
+    for r in range(wl.W):
+        for e in range(wl.E):
+            n = int(cnt[r, e])
+            assert np.array_equal(info[r, e, :n], g["packed_src_info"][r, e, :n]), (r, e)
+            assert np.array_equal(px[r, e, :n], g["packed_x"][r, e, :n]), (r, e)
+    with pytest.raises(ep.EpError):
+        plan.dispatch_grouped(x, w, None, idx, wl.n_tok)    # quantising dtypes are not fused
+    plan.close()
+
+
 # ---------------------------------------------------------------- combine over an FP8 wire
 
 def _check_fp8_wire(wl, variant="auto"):
