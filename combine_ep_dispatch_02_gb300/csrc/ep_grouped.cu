@@ -242,31 +242,32 @@ __global__ void __launch_bounds__(kCopyThreads, 2) ep_ungroup_kernel(const Group
             }
             continue;
         }
-        if (!WIDE) continue;
-        for (int vb = 0; vb < hv; vb += 32) {              // more than 8 local experts
-            const int v = vb + lane;
-            float acc[8];
+        if constexpr (WIDE) {
+            for (int vb = 0; vb < hv; vb += 32) {              // more than 8 local experts
+                const int v = vb + lane;
+                float acc[8];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
-            for (int d0 = 0; d0 < nd; d0 += 8) {
-                uint4 b[8];
+                for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+                for (int d0 = 0; d0 < nd; d0 += 8) {
+                    uint4 b[8];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    // the entry of rank d0+q (uniform across the warp)
-                    const int want = d0 + q;
-                    const unsigned m0 = __ballot_sync(0xffffffffu, dest0 >= 0 && rank0 == want);
-                    const unsigned m1 = __ballot_sync(0xffffffffu, dest1 >= 0 && rank1 == want);
-                    int64_t row = -1;
-                    if (m0) row = __shfl_sync(0xffffffffu, dest0, __ffs(m0) - 1);
-                    else if (m1) row = __shfl_sync(0xffffffffu, dest1, __ffs(m1) - 1);
-                    if (row >= 0 && v < hv) b[q] = ld_stream_v4(y4 + row * hv + v);
-                    if (row < 0) b[q] = make_uint4(0, 0, 0, 0);
+                    for (int q = 0; q < 8; ++q) {
+                        // the entry of rank d0+q (uniform across the warp)
+                        const int want = d0 + q;
+                        const unsigned m0 = __ballot_sync(0xffffffffu, dest0 >= 0 && rank0 == want);
+                        const unsigned m1 = __ballot_sync(0xffffffffu, dest1 >= 0 && rank1 == want);
+                        int64_t row = -1;
+                        if (m0) row = __shfl_sync(0xffffffffu, dest0, __ffs(m0) - 1);
+                        else if (m1) row = __shfl_sync(0xffffffffu, dest1, __ffs(m1) - 1);
+                        if (row >= 0 && v < hv) b[q] = ld_stream_v4(y4 + row * hv + v);
+                        if (row < 0) b[q] = make_uint4(0, 0, 0, 0);
+                    }
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        if (d0 + q < nd) add8<FP16>(acc, b[q]);
                 }
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    if (d0 + q < nd) add8<FP16>(acc, b[q]);
+                if (v < hv) st_v4(dst + v, pack8<FP16>(acc));
             }
-            if (v < hv) st_v4(dst + v, pack8<FP16>(acc));
         }
     }
 }
