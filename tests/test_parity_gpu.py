@@ -333,6 +333,38 @@ def test_quantised_dispatch_edge_values():
     _check_quantised(wl)
 
 
+def _e4m3_boundaries():
+    """The positive e4m3fn rounding boundaries below 448: midpoints of consecutive codes, and
+    half the smallest subnormal."""
+    vals = sorted({float(v) for v in torch.arange(0, 127, dtype=torch.uint8).view(torch.float8_e4m3fn).float()})
+    return [(a + b) / 2 for a, b in zip(vals, vals[1:])]
+
+
+def test_quantised_dispatch_at_e4m3_boundaries():
+    # blocks whose quotient x / scale sits exactly on, or one BF16 step around, an e4m3 rounding
+    # boundary, at scales that are and are not powers of two: the quantiser's bracketing must
+    # hand these to the exact division and still match the oracle's FP32 division
+    mids = np.array(_e4m3_boundaries(), dtype=np.float64)          # 126 boundaries
+    cs = [1.0, 1.5, 0.75, 3.0, 2.0 ** -5 * 1.25, 2.0 ** 7 * 1.125, 1.0 / 3.0, 2.0 ** -20 * 1.75]
+    rows = []
+    for c in cs:
+        for nudge in (0, 1, -1):
+            r = np.empty(128, dtype=np.float32)
+            r[0] = 448.0 * c
+            r[1:127] = mids * c
+            r[127] = -mids[63] * c
+            b = torch.from_numpy(r).to(torch.bfloat16).view(torch.int16).numpy()
+            b[1:] = b[1:] + np.int16(nudge) * np.sign(b[1:]).astype(np.int16)   # one BF16 step
+            rows.append(b.view(np.uint16))
+            rows.append((b.view(np.uint16) ^ np.uint16(0x8000)))             # negated row
+    rows = np.stack(rows)
+    W, M = 2, (len(rows) + 1) // 2
+    wl = wlmod.custom_workload(W=W, E=2, k=2, H=128, M=M, n_tok=[M, len(rows) - M], seed=5)
+    wl.x[:] = 0
+    wl.x.reshape(-1, 128)[:len(rows)] = rows
+    _check_quantised(wl)
+
+
 # ---------------------------------------------------------------- quantising MX FP4 dispatch
 
 def _check_mxfp4_dispatch(wl, variant="auto"):
@@ -542,6 +574,10 @@ def test_fp4_wire_ragged_blocks():
     # one past a warp's worth
     _check_fp4_wire(wlmod.custom_workload(W=4, E=3, k=4, H=96, M=37, n_tok=[37, 5, 0, 20], seed=11))
     _check_fp4_wire(wlmod.custom_workload(W=4, E=3, k=4, H=1056, M=37, n_tok=[37, 5, 0, 20], seed=12))
+    # hidden % 128 == 0 takes the shared-memory pipeline: 12 blocks (one partial step) and 36
+    # blocks (a full step of 32 and a partial one)
+    _check_fp4_wire(wlmod.custom_workload(W=4, E=3, k=4, H=384, M=37, n_tok=[37, 5, 0, 20], seed=13))
+    _check_fp4_wire(wlmod.custom_workload(W=4, E=3, k=4, H=1152, M=37, n_tok=[37, 5, 0, 20], seed=14))
 
 
 def test_fp4_wire_edge_values():
