@@ -10,12 +10,12 @@
 // HBM-bound, and bound by how many bytes each SM keeps in flight: at the loaded HBM latency
 // of this part (~2.3 us) an SM needs ~100 KB of reads outstanding to stream at full rate.  A
 // warp owns one work unit (a token, or a 512/1024-element slice of it for small calls) and its
-// lanes own 16-byte columns.  Per step every lane loads U columns from each of the token's nd
-// rows before adding any, with U chosen from nd so that nd*U = 8 loads (4 KB per warp, with
-// 24 warps per SM ~100 KB per SM) are in flight whatever the fan-in -- the pages' bf16 pull combine likewise loads every source a
-// token can have before folding.  Then, column by column, the rows are added in ascending rank
-// order in FP32 registers and the sum leaves as one packed BF16x8 / FP16x8 16-byte store.  The
-// next unit's forward-map row is loaded while the current one is folded.
+// lanes own 16-byte columns.  The token's rows are gathered in a rolling fashion: each row's
+// load of a lane's next column is issued as soon as its current column has been added, so a
+// lane keeps one load per row (nd of them) in flight without a gap.  The column's rows are
+// added in ascending rank order in FP32 registers and the sum leaves as one packed BF16x8 /
+// FP16x8 16-byte store.  Two CTAs of 9 warps per SM fill the register file without spills.
+// The next unit's forward-map row is loaded while the current one is folded.
 //
 // (A TMA variant that staged row slices through shared memory with 1-D bulk copies was
 // measured slower: on this part one CTA's bulk copies each take ~0.3 us, so gathering a
