@@ -692,6 +692,15 @@ def test_grouped_layout(case):
     _check_grouped(wlmod.custom_workload(seed=5, **case), fused=True)
 
 
+def test_grouped_layout_wide_rows():
+    # hidden 2304 (288 16-byte vectors: nine full warp steps of 32 vectors) in BF16 and FP16,
+    # grouped, fused and inverted
+    for dt in ("bf16", "fp16"):
+        wl = wlmod.custom_workload(W=4, E=8, k=6, H=2304, M=40, n_tok=[40, 17, 0, 33], dtype=dt, seed=8)
+        _check_grouped(wl)
+        _check_grouped(wl, fused=True)
+
+
 def test_grouped_layout_duplicate_ids_and_small_workload():
     wl = wlmod.custom_workload(W=4, E=8, k=4, H=256, M=30, n_tok=[30, 30, 5, 9], seed=2)
     wl.indices[0, 3, 2] = wl.indices[0, 3, 0]       # the same expert twice in one top-k row
