@@ -31,6 +31,7 @@ struct ep_plan {
     int32_t* expert_map;
     unsigned long long* flags;
     unsigned long long* ticket;
+    unsigned long long* queues;   // kQueues work queues of two words each, after the ticket
     int* status;
 
     // host state of the live dispatch
@@ -130,7 +131,7 @@ Layout layout_of(int W, int k, int H, int dtype, int sd, int M)
     put(L.recv_count, (size_t)W * 4);
     put(L.expert_map, (size_t)W * rows * k * 4);
     put(L.flags, (size_t)tiles * W * 8);
-    put(L.ticket, 8);
+    put(L.ticket, 8 + kQueues * 16);   // the route ticket, then the copy kernels' work queues
     put(L.status, 4);
     L.total = o;
     return L;
@@ -166,6 +167,15 @@ int pick_chunk_elems(const ep_plan* p, int N)
     if (N >= warps || p->H <= 1024) return p->H;
     if ((int64_t)N * ((p->H + 1023) / 1024) >= warps) return 1024;
     return 512;
+}
+
+// The copy kernels number their work units (tokens x row slices) in 32 bits.
+int check_units(int N, int chunks, const char* who)
+{
+    if ((int64_t)N * chunks >= (int64_t)1 << 31)
+        return fail(EP_ERR_ARG, "%s: %d tokens x %d row slices >= 2^31 work units; use whole rows", who, N,
+                    chunks);
+    return EP_OK;
 }
 
 }  // namespace
@@ -248,6 +258,7 @@ int ep_plan_create(ep_plan** out, int W, int E, int k, int H, int dtype, int sd,
     p->expert_map = (int32_t*)(b + L.expert_map);
     p->flags = (unsigned long long*)(b + L.flags);
     p->ticket = (unsigned long long*)(b + L.ticket);
+    p->queues = p->ticket + 1;
     p->status = (int*)(b + L.status);
     // the control words start at zero once; scan flags are stamped per call after that
     e = cudaMemset(b + L.recv_count, 0, L.total - L.recv_count);
@@ -355,6 +366,7 @@ int ep_dispatch_scatter(ep_plan* p, const void* x, const float* weights, const f
     if (!g.ok) return fail(EP_ERR_CUDA, "cannot select the plan's device %d", p->device);
 
     ScatterArgs a{};
+    a.work.q = p->queues + 2 * kQueueDispatch;
     a.x = (const uint8_t*)x; a.w = weights; a.scales = scales; a.idx = indices; a.fwd = p->fwd;
     a.recv_x = p->recv_x; a.recv_idx = p->recv_idx; a.recv_w = p->recv_w; a.recv_scales = p->recv_scales;
     a.row_bytes = p->row_bytes;
@@ -363,6 +375,7 @@ int ep_dispatch_scatter(ep_plan* p, const void* x, const float* weights, const f
     // quantising scatters take the slice in elements (their source rows are BF16)
     a.chunk_bytes = p->quantise ? ce : ce * p->elem_bytes;
     a.chunks = (int)((p->H + ce - 1) / ce);
+    if (int rc = check_units(a.N, a.chunks, "ep_dispatch_scatter")) return rc;
     for (int s = 0; s <= p->W; ++s) a.tok_off[s] = p->tok_off[s];
     cudaError_t e = p->fp4 ? launch_scatter_quant_fp4(a, p->num_sms, (cudaStream_t)stream)
                     : p->quantise ? launch_scatter_quant(a, p->num_sms, (cudaStream_t)stream)
@@ -424,6 +437,7 @@ int ep_combine(ep_plan* p, const void* expert_out, const float* weights, void* o
     a.out = (uint16_t*)out; a.out_w = out_w; a.status = p->status; a.H = p->H;
     a.W = p->W; a.k = p->k; a.F = p->F; a.M = p->M; a.N = p->N;
     combine_geometry(a, p->variant, p->num_sms);
+    if (int rc = check_units(a.N, a.chunks, "ep_combine")) return rc;
     for (int s = 0; s <= p->W; ++s) a.tok_off[s] = p->tok_off[s];
     cudaError_t e = launch_combine(a, p->dtype == EP_FP16, p->num_sms, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "ep_combine: launch");
@@ -481,6 +495,7 @@ int ep_combine_fp8(ep_plan* p, const void* expert_q, const float* expert_scales,
     a.W = p->W; a.k = p->k; a.F = p->F; a.M = p->M; a.N = p->N;
     a.chunk_pieces = geo.chunk_vecs / 2;
     a.chunks = (int)((p->H / 16 + a.chunk_pieces - 1) / a.chunk_pieces);
+    if (int rc2 = check_units(a.N, a.chunks, "ep_combine_fp8")) return rc2;
     for (int s = 0; s <= p->W; ++s) a.tok_off[s] = p->tok_off[s];
     cudaError_t e = launch_combine_fp8(a, p->num_sms, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "ep_combine_fp8: launch");
@@ -526,6 +541,7 @@ int ep_combine_fp4(ep_plan* p, const void* expert_q, const uint8_t* expert_scale
     a.W = p->W; a.k = p->k; a.F = p->F; a.M = p->M; a.N = p->N;
     a.chunk_pieces = geo.chunk_vecs / 4 > 0 ? geo.chunk_vecs / 4 : 1;   // 32-element blocks
     a.chunks = (int)((p->H / 32 + a.chunk_pieces - 1) / a.chunk_pieces);
+    if (int rc2 = check_units(a.N, a.chunks, "ep_combine_fp4")) return rc2;
     for (int s = 0; s <= p->W; ++s) a.tok_off[s] = p->tok_off[s];
     cudaError_t e = launch_combine_fp4(a, p->num_sms, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "ep_combine_fp4: launch");

@@ -11,7 +11,8 @@
 //   recv_count   [W]
 //   expert_map   [W][W*M][k]   slot of a received row in its local experts' lists (grouped view)
 //   flags        [tiles][W]    decoupled-lookback scan words of the routing kernel
-//   ticket       u64           monotone tile ticket (never reset; also yields the call stamp)
+//   ticket       u64           monotone tile ticket (never reset; also yields the call stamp),
+//                              followed in its 256-byte block by the work queues, kQueues x 2 u64
 //   status       int32         first device-side error
 #pragma once
 
@@ -38,6 +39,43 @@ constexpr uint32_t kStampMask = 0x3FFFFFFFu;
 #endif
 constexpr int kSpinLimit = EP_SPIN_LIMIT;   // polls before a wait gives up with EP_ERR_DEVICE_TIMEOUT
 
+// Work queues of the persistent copy kernels (see WorkSplit): launches that share a queue must
+// run one after the other, as the calls on one plan do.
+constexpr int kQueueDispatch = 0;   // payload scatters (BF16 / FP8 / MX FP4 rows)
+constexpr int kQueues = 1;
+
+// ---- work split of a persistent copy kernel
+//
+// A token costs one read of its row and one write per destination rank, so a plain round-robin
+// split of the units over the grid's G warps leaves a tail in which a few warps still copy
+// expensive tokens while the rest of the GPU idles.  The split here is round-robin for all but
+// the last two rounds' worth of units (warp w takes w, w + G, ... below static_end, with no
+// atomics), and the rest are drawn one at a time, in ascending order, from a per-plan queue
+// word q[0]: a warp whose units were cheap draws more of them.  Calls with fewer than four
+// rounds of units are split round-robin only: there the queue word, polled by every warp of the
+// grid, costs more than the imbalance it removes.  Once the queue is in use,
+// each CTA counts itself in q[1] when all its warps are done, and the last CTA returns both
+// words to zero, so the next launch on the same queue (stream-ordered after this one, or a
+// CUDA-graph replay) starts from zero without a memset.  The launcher fills the split in the
+// kernel's arguments, so the kernel reads it from the parameter bank rather than registers.
+struct WorkSplit {
+    unsigned long long* q;   // two words, zero between launches
+    uint32_t units;          // < 2^31 (checked by the host before every launch)
+    uint32_t warps;          // warps of the grid
+    uint32_t static_end;     // units below this are split round-robin
+};
+
+inline WorkSplit make_work_split(unsigned long long* q, int64_t units, int64_t warps)
+{
+    WorkSplit s;
+    s.q = q;
+    s.units = (uint32_t)units;
+    s.warps = (uint32_t)warps;
+    const int64_t rounds = units / warps;
+    s.static_end = (uint32_t)(rounds >= 4 ? (rounds - 2) * warps : units);
+    return s;
+}
+
 struct RouteArgs {
     const int32_t* idx;
     int32_t* fwd;
@@ -62,6 +100,7 @@ struct ScatterArgs {
     int32_t* recv_idx;
     float* recv_w;
     float* recv_scales;
+    WorkSplit work;       // q set by the caller, the rest by the launcher
     int64_t row_bytes;    // H * element size, a multiple of 16
     int W, k, F, M, sd, N;
     int chunk_bytes;      // bytes of one work unit's slice of a row (multiple of 16)
@@ -157,6 +196,43 @@ void combine_geometry(CombineArgs& a, int variant, int num_sms);
 __device__ __forceinline__ void record_status(int* status, int code)
 {
     if (*reinterpret_cast<volatile int*>(status) == 0) atomicCAS(status, 0, code);
+}
+
+// This warp's first unit, or s.units if it has none.
+__device__ __forceinline__ uint32_t work_first(const WorkSplit& s)
+{
+    const uint32_t w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    return w < s.static_end ? w : s.units;
+}
+
+// The unit after u, or s.units when the work is done (warp-uniform).
+__device__ __forceinline__ uint32_t work_next(const WorkSplit& s, uint32_t u, int lane)
+{
+    if (u + s.warps < s.static_end) return u + s.warps;
+    if (s.static_end >= s.units) return s.units;
+    unsigned long long t = ~0ull;
+    if (lane == 0) {
+        unsigned long long seen;   // an exhausted queue is seen by a plain read, without an atomic
+        asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(seen) : "l"(s.q) : "memory");
+        if (seen < s.units - s.static_end) t = atomicAdd(s.q, 1ull);
+    }
+    t = __shfl_sync(0xffffffffu, t, 0);
+    return t < s.units - s.static_end ? s.static_end + (uint32_t)t : s.units;
+}
+
+// Called by every thread of the CTA after its last unit: resets the queue once the grid is done.
+__device__ __forceinline__ void work_retire(const WorkSplit& s)
+{
+    if (s.static_end >= s.units) return;   // the queue was not used
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();   // this CTA's draws are ordered before its retirement
+        if (atomicAdd(s.q + 1, 1ull) == (unsigned long long)gridDim.x - 1) {   // the last CTA
+            __threadfence();
+            atomicExch(s.q, 0ull);
+            atomicExch(s.q + 1, 0ull);
+        }
+    }
 }
 
 // Source rank of flattened token g (tokens of rank 0 first, then rank 1, ...); off in shared.
@@ -292,18 +368,45 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi)
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// x / s from y = RN(1/s) without a division: q0 = RN(x * y) lies within one ulp of x / s, so the
+// residual x - q0 * s is exact in one fma, and RN(q0 + residual * y) is the correctly rounded
+// quotient (P. Markstein, "Computation of elementary functions on the IBM RISC System/6000
+// processor", IBM J. Res. Develop. 34(1), 1990).  Used only for 2^-60 <= s <= 2^126: below that
+// the residual of a BF16 dividend can underflow.  A zero quotient takes the sign of x, as the
+// division's does.  Over that scale range the e4m3 code of this quotient equals the code of the
+// IEEE quotient for every BF16 x with |x| <= 448 s (checked exhaustively against the division).
+__device__ __forceinline__ float div_by_scale(float x, float s, float y)
+{
+    const float q0 = __fmul_rn(x, y);
+    const float r = __fmaf_rn(-q0, s, x);
+    const float q1 = __fmaf_rn(r, y, q0);
+    return __uint_as_float(__float_as_uint(q1) | (__float_as_uint(x) & 0x80000000u));
+}
+
 // Quantise one lane's 16 consecutive BF16 values (two 16-byte vectors) with the block scale:
-// q = e4m3(x / scale), FP32 division rounded to nearest even.
+// q = e4m3(x / scale), the FP32 quotient rounded to nearest even.
 __device__ __forceinline__ uint4 quantise16(const uint4& a, const uint4& b, float scale)
 {
     const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
     uint32_t o[4];
+    if (scale >= 0x1p-60f && scale <= 0x1p126f) {
+        const float y = __frcp_rn(scale);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint32_t p0 = e4m3x2(__fdiv_rn(bf16_lo(w[2 * i]), scale), __fdiv_rn(bf16_hi(w[2 * i]), scale));
-        const uint32_t p1 =
-            e4m3x2(__fdiv_rn(bf16_lo(w[2 * i + 1]), scale), __fdiv_rn(bf16_hi(w[2 * i + 1]), scale));
-        o[i] = p0 | (p1 << 16);
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t p0 = e4m3x2(div_by_scale(bf16_lo(w[2 * i]), scale, y),
+                                       div_by_scale(bf16_hi(w[2 * i]), scale, y));
+            const uint32_t p1 = e4m3x2(div_by_scale(bf16_lo(w[2 * i + 1]), scale, y),
+                                       div_by_scale(bf16_hi(w[2 * i + 1]), scale, y));
+            o[i] = p0 | (p1 << 16);
+        }
+    } else {   // tiny or infinite block scales: IEEE division
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t p0 = e4m3x2(__fdiv_rn(bf16_lo(w[2 * i]), scale), __fdiv_rn(bf16_hi(w[2 * i]), scale));
+            const uint32_t p1 =
+                e4m3x2(__fdiv_rn(bf16_lo(w[2 * i + 1]), scale), __fdiv_rn(bf16_hi(w[2 * i + 1]), scale));
+            o[i] = p0 | (p1 << 16);
+        }
     }
     return make_uint4(o[0], o[1], o[2], o[3]);
 }

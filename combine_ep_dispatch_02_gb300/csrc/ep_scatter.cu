@@ -11,7 +11,9 @@
 // N*row + P*row bytes (N tokens, P token-destination pairs).  Work units are (token, slice of
 // the row): whole rows for large token counts, 512- or 1024-element slices for small ones (the
 // pages' small-batch launch policy), one warp per unit, a persistent grid sized from the
-// occupancy of this kernel times the SM count.
+// occupancy of this kernel times the SM count.  The last rounds of units are drawn from the
+// plan's dispatch work queue (work_split), so tokens with many destination ranks do not leave
+// a tail of busy warps.
 #include "ep_common.cuh"
 
 namespace ep {
@@ -26,9 +28,7 @@ __global__ void __launch_bounds__(kCopyThreads) ep_scatter_kernel(const ScatterA
     __syncthreads();
 
     const int lane = threadIdx.x & 31;
-    const int64_t warps_per_grid = (int64_t)gridDim.x * (kCopyThreads / 32);
     const int64_t units = (int64_t)a.N * a.chunks;
-    int64_t u = (int64_t)blockIdx.x * (kCopyThreads / 32) + (threadIdx.x >> 5);
     // destination rows of a unit, compact and ascending in rank; lane d holds the d-th one
     auto unit_dest = [&](int64_t v) -> int {
         if (v >= units) return -1;
@@ -37,10 +37,14 @@ __global__ void __launch_bounds__(kCopyThreads) ep_scatter_kernel(const ScatterA
         const int64_t tv = (int64_t)sv * a.M + (gv - s_off[sv]);
         return lane < a.F ? __ldg(a.fwd + tv * a.F + lane) : -1;
     };
-    int dest_next = unit_dest(u);
-    for (; u < units; u += warps_per_grid) {
+    const WorkSplit& ws = a.work;
+    uint32_t u_next = work_first(ws);
+    int dest_next = unit_dest(u_next);
+    while (u_next < units) {
+        const uint32_t u = u_next;
         const int dest = dest_next;
-        dest_next = unit_dest(u + warps_per_grid);       // lands while this unit is copied
+        u_next = work_next(ws, u, lane);                 // the next unit's forward-map row
+        dest_next = unit_dest(u_next);                   // lands while this unit is copied
         const int g = (int)(u / a.chunks);
         const int c = (int)(u - (int64_t)g * a.chunks);
         const int s = rank_of_token(s_off, a.W, g);
@@ -81,6 +85,7 @@ __global__ void __launch_bounds__(kCopyThreads) ep_scatter_kernel(const ScatterA
             }
         }
     }
+    work_retire(ws);
 }
 
 // ---- quantising scatter: BF16 source rows -> FP8 e4m3 rows + one FP32 scale per 128 elements
@@ -97,11 +102,10 @@ __global__ void __launch_bounds__(kCopyThreads, 3) ep_scatter_quant_kernel(const
     __syncthreads();
 
     const int lane = threadIdx.x & 31;
-    const int64_t warps_per_grid = (int64_t)gridDim.x * (kCopyThreads / 32);
     const int64_t units = (int64_t)a.N * a.chunks;
     const int64_t H = a.row_bytes;              // FP8 payload: one byte per element
-    for (int64_t u = (int64_t)blockIdx.x * (kCopyThreads / 32) + (threadIdx.x >> 5); u < units;
-         u += warps_per_grid) {
+    const WorkSplit& ws = a.work;
+    for (uint32_t u = work_first(ws); u < units; u = work_next(ws, u, lane)) {
         const int g = (int)(u / a.chunks);
         const int c = (int)(u - (int64_t)g * a.chunks);
         const int s = rank_of_token(s_off, a.W, g);
@@ -160,6 +164,7 @@ __global__ void __launch_bounds__(kCopyThreads, 3) ep_scatter_quant_kernel(const
             }
         }
     }
+    work_retire(ws);
 }
 
 // MX FP4 quantising scatter.  A lane owns one 32-element block (64 source bytes -> 16 code
@@ -172,13 +177,12 @@ __global__ void __launch_bounds__(kCopyThreads, 3) ep_scatter_quant_fp4_kernel(c
     __syncthreads();
 
     const int lane = threadIdx.x & 31;
-    const int64_t warps_per_grid = (int64_t)gridDim.x * (kCopyThreads / 32);
     const int64_t units = (int64_t)a.N * a.chunks;
     const int64_t H = a.row_bytes * 2;           // elements; a received row holds H/2 code bytes
     const int64_t hb = H >> 5;                    // blocks (and scale bytes) per row
     uint8_t* sc8 = reinterpret_cast<uint8_t*>(a.recv_scales);
-    for (int64_t u = (int64_t)blockIdx.x * (kCopyThreads / 32) + (threadIdx.x >> 5); u < units;
-         u += warps_per_grid) {
+    const WorkSplit& ws = a.work;
+    for (uint32_t u = work_first(ws); u < units; u = work_next(ws, u, lane)) {
         const int g = (int)(u / a.chunks);
         const int c = (int)(u - (int64_t)g * a.chunks);
         const int s = rank_of_token(s_off, a.W, g);
@@ -219,6 +223,7 @@ __global__ void __launch_bounds__(kCopyThreads, 3) ep_scatter_quant_fp4_kernel(c
             }
         }
     }
+    work_retire(ws);
 }
 
 }  // namespace
@@ -235,7 +240,9 @@ cudaError_t launch_scatter_quant_fp4(const ScatterArgs& a, int num_sms, cudaStre
     const int64_t need = (units + kCopyThreads / 32 - 1) / (kCopyThreads / 32);
     const int64_t cap = (int64_t)per_sm * num_sms;
     const int grid = (int)(need < cap ? need : cap);
-    ep_scatter_quant_fp4_kernel<<<grid, kCopyThreads, 0, stream>>>(a);
+    ScatterArgs b = a;
+    b.work = make_work_split(a.work.q, units, (int64_t)grid * (kCopyThreads / 32));
+    ep_scatter_quant_fp4_kernel<<<grid, kCopyThreads, 0, stream>>>(b);
     return cudaGetLastError();
 }
 
@@ -251,7 +258,9 @@ cudaError_t launch_scatter_quant(const ScatterArgs& a, int num_sms, cudaStream_t
     const int64_t need = (units + kCopyThreads / 32 - 1) / (kCopyThreads / 32);
     const int64_t cap = (int64_t)per_sm * num_sms;
     const int grid = (int)(need < cap ? need : cap);
-    ep_scatter_quant_kernel<<<grid, kCopyThreads, 0, stream>>>(a);
+    ScatterArgs b = a;
+    b.work = make_work_split(a.work.q, units, (int64_t)grid * (kCopyThreads / 32));
+    ep_scatter_quant_kernel<<<grid, kCopyThreads, 0, stream>>>(b);
     return cudaGetLastError();
 }
 
@@ -267,7 +276,9 @@ cudaError_t launch_scatter(const ScatterArgs& a, int num_sms, cudaStream_t strea
     const int64_t need = (units + kCopyThreads / 32 - 1) / (kCopyThreads / 32);
     const int64_t cap = (int64_t)per_sm * num_sms;
     const int grid = (int)(need < cap ? need : cap);
-    ep_scatter_kernel<<<grid, kCopyThreads, 0, stream>>>(a);
+    ScatterArgs b = a;
+    b.work = make_work_split(a.work.q, units, (int64_t)grid * (kCopyThreads / 32));
+    ep_scatter_kernel<<<grid, kCopyThreads, 0, stream>>>(b);
     return cudaGetLastError();
 }
 

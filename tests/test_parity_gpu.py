@@ -295,6 +295,50 @@ def test_cuda_graph_replay_matches_eager():
     plan.close()
 
 
+def test_scatter_work_queue_reuse_and_graph_replay():
+    """Dispatches with more than four rounds of work units per warp (2400 tokens cut into
+    512-element slices), so the scatter draws its last units from the plan's work queue.  They
+    run three times in a row on one plan and are replayed three times from a CUDA graph, with
+    the receive rows poisoned before each: a queue left short of zero would skip units."""
+    wl = wlmod.make_workload("dsv3", max_tok=300)
+    disp, _, o_out, o_w = _oracle(wl)
+    plan = gpu_path.make_plan(wl, DEV, "tiled_512")
+    for _ in range(3):
+        gpu_path.compare(wl, gpu_path.run(wl, DEV, "tiled_512", plan=plan), disp, o_out, o_w)
+    x, w, sc, idx = gpu_path.to_device(wl, DEV)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        plan.dispatch(x, w, sc, idx, wl.n_tok, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        d = plan.dispatch(x, w, sc, idx, wl.n_tok, stream=torch.cuda.current_stream())
+    for _ in range(3):
+        d.recv_x.view(torch.uint8).fill_(0xFF)
+        g.replay()
+        torch.cuda.synchronize()
+        rx = gpu_path.raw(d.recv_x)
+        for r in range(wl.W):
+            n = int(disp["recv_count"][r])
+            assert np.array_equal(rx[r, :n], disp["recv_x"][r, :n]), f"rank {r}"
+    assert plan.status() == 0
+    plan.close()
+
+    # the quantising scatters share the queue
+    dq = oracle.dispatch_quantized(wl)
+    q, qs = oracle.quantize_e4m3_blockwise(wl.x)
+    wq = gpu_path.quantised_view(wl, q, qs)
+    eo = harness.expert_np(wq, dq)
+    qo, qw = oracle.combine(wl.W, wl.k, wl.H, False, wl.M, wl.n_tok, dq["slot_of"], eo, dq["recv_w"])
+    plan = gpu_path.make_plan(wl, DEV, "tiled_512", "bf16_fp8")
+    for _ in range(2):
+        gpu_path.compare(wq, gpu_path.run(wl, DEV, plan=plan, quantise=True), dq, qo, qw)
+    plan.close()
+    _check_mxfp4_dispatch(wl, "tiled_512", repeats=2)
+
+
 # ---------------------------------------------------------------- quantising FP8 dispatch
 
 def _check_quantised(wl, variant="auto"):
@@ -365,32 +409,92 @@ def test_quantised_dispatch_at_e4m3_boundaries():
     _check_quantised(wl)
 
 
+def _quantiser_class_blocks():
+    """128-element BF16 blocks covering the FP8 quantiser's inputs class by class.
+
+    A block's scale depends only on its maximum m, and the code of x depends only on x and m.
+    Scaling both by a power of two leaves the code unchanged while no intermediate under- or
+    overflows, so every significand of m (7 fraction bits) at a few exponents, with every BF16 x
+    of either sign whose exponent lies within 24 of m's, covers the normal range; anything
+    smaller quantises to +-0.  The exponents span subnormal maxima, the scale 2^-60 below which
+    the quantiser divides (m near 2^-51), ordinary values and the BF16 maximum.  Each block
+    holds m once, at a position that moves from block to block, and 127 values of magnitude
+    <= m."""
+    blocks = []
+    frac = np.arange(128, dtype=np.uint32)
+    for e_m in (0, 1, 58, 75, 76, 77, 100, 127, 140, 200, 254):
+        for f_m in range(128):
+            if e_m == 0 and f_m == 0:
+                continue
+            m_bits = (e_m << 7) | f_m
+            e = np.arange(max(0, e_m - 24), e_m + 1, dtype=np.uint32)
+            xs = ((e[:, None] << 7) | frac[None, :]).ravel()
+            xs = xs[xs <= m_bits]
+            xs = np.concatenate([xs, xs | 0x8000]).astype(np.uint16)
+            nb = -(-len(xs) // 127)
+            pad = np.zeros(nb * 127, dtype=np.uint16)
+            pad[:len(xs)] = xs
+            for chunk in pad.reshape(nb, 127):
+                i = len(blocks)
+                blocks.append(np.insert(chunk, i % 128, np.uint16(m_bits ^ (0x8000 if i & 1 else 0))))
+    return np.stack(blocks).astype(np.uint16)
+
+
+def test_fp8_quantisers_over_every_input_class():
+    """Both FP8 quantisers (inside the quantising dispatch, and on received expert rows for the
+    FP8 wire) against the oracle's division, code for code, on _quantiser_class_blocks()."""
+    H = 7168
+    blocks = _quantiser_class_blocks()
+    M = -(-len(blocks) * 128 // H)
+    rows = np.zeros((M * H // 128, 128), dtype=np.uint16)
+    rows[:len(blocks)] = blocks
+    rows = rows.reshape(1, M, H)
+
+    wl = wlmod.custom_workload(W=1, E=1, k=1, H=H, M=M, n_tok=[M], seed=11)
+    wl.x[:] = rows
+    _check_quantised(wl)
+
+    q, sc = oracle.quantize_e4m3_blockwise(rows)
+    plan = ep.Plan(1, 1, 1, H, "bf16", 0, M, device=DEV)
+    x, w, _, idx = gpu_path.to_device(wl, DEV)
+    d = plan.dispatch(x, w, None, idx, [M])
+    eo = torch.from_numpy(rows.view(np.int16)).to(DEV).view(torch.bfloat16)
+    qg, scg = plan.quantize_received(eo, d.epoch)
+    torch.cuda.synchronize()
+    assert plan.status() == 0
+    assert np.array_equal(gpu_path.raw(qg)[0, :M], q[0])
+    assert np.array_equal(scg.cpu().numpy()[0, :M].view(np.uint32), sc[0].view(np.uint32))
+    plan.close()
+
+
 # ---------------------------------------------------------------- quantising MX FP4 dispatch
 
-def _check_mxfp4_dispatch(wl, variant="auto"):
+def _check_mxfp4_dispatch(wl, variant="auto", repeats=1):
     """Dispatch through the MX FP4 dtype: codes, scale bytes, index / weight rows, reverse map
     and counts against the oracle (its MX quantiser, then its byte-exact dispatch), bit for bit;
-    then the combine of the dequantised rows (an exact dequantising expert on both sides)."""
+    then the combine of the dequantised rows (an exact dequantising expert on both sides).
+    repeats > 1 dispatches again on the same plan, receive rows poisoned before each call."""
     disp = oracle.dispatch_quantized_mxfp4(wl)
     eo = harness.mxfp4_dequant_np(disp["recv_x"], disp["recv_scales"].view(np.uint8))
     o_out, o_w = oracle.combine(wl.W, wl.k, wl.H, False, wl.M, wl.n_tok, disp["slot_of"], eo,
                                 disp["recv_w"])
     plan = gpu_path.make_plan(wl, DEV, variant, "bf16_mxfp4")
-    gpu_path.poison(plan, DEV)
     x, w, _, idx = gpu_path.to_device(wl, DEV)
-    d = plan.dispatch(x, w, None, idx, wl.n_tok)
-    assert d.recv_x.shape == (wl.W, wl.W * wl.M, wl.H // 2)
-    assert d.recv_scales.shape == (wl.W, wl.W * wl.M, wl.H // 32)
-    eo_g = harness.mxfp4_dequant_torch(d.recv_x, d.recv_scales)
-    out, out_w = plan.combine(eo_g, d.recv_w, d.epoch)
-    torch.cuda.synchronize()
-    gpu = {"recv_count": d.recv_count.cpu().numpy(), "recv_x": gpu_path.raw(d.recv_x),
-           "recv_idx": gpu_path.raw(d.recv_idx), "recv_w": gpu_path.raw(d.recv_w),
-           "recv_scales": gpu_path.raw(d.recv_scales), "src_pos": gpu_path.raw(d.src_token_pos),
-           "out": gpu_path.raw(out), "out_w": gpu_path.raw(out_w), "status": plan.status()}
-    plan.close()
     wq = wlmod.Workload(**{**wl.__dict__, "sd": wl.H // 128})   # scale rows are compared
-    gpu_path.compare(wq, gpu, disp, o_out, o_w)
+    for _ in range(repeats):
+        gpu_path.poison(plan, DEV)
+        d = plan.dispatch(x, w, None, idx, wl.n_tok)
+        assert d.recv_x.shape == (wl.W, wl.W * wl.M, wl.H // 2)
+        assert d.recv_scales.shape == (wl.W, wl.W * wl.M, wl.H // 32)
+        eo_g = harness.mxfp4_dequant_torch(d.recv_x, d.recv_scales)
+        out, out_w = plan.combine(eo_g, d.recv_w, d.epoch)
+        torch.cuda.synchronize()
+        gpu = {"recv_count": d.recv_count.cpu().numpy(), "recv_x": gpu_path.raw(d.recv_x),
+               "recv_idx": gpu_path.raw(d.recv_idx), "recv_w": gpu_path.raw(d.recv_w),
+               "recv_scales": gpu_path.raw(d.recv_scales), "src_pos": gpu_path.raw(d.src_token_pos),
+               "out": gpu_path.raw(out), "out_w": gpu_path.raw(out_w), "status": plan.status()}
+        gpu_path.compare(wq, gpu, disp, o_out, o_w)
+    plan.close()
 
 
 def test_mxfp4_dispatch_dsv3_reduced():
