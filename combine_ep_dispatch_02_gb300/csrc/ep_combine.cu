@@ -11,11 +11,13 @@
 // of this part (~2.3 us) an SM needs ~100 KB of reads outstanding to stream at full rate.  A
 // warp owns one work unit (a token, or a 512/1024-element slice of it for small calls) and its
 // lanes own 16-byte columns.  The token's rows are gathered in a rolling fashion: each row's
-// load of a lane's next column is issued as soon as its current column has been added, so a
-// lane keeps one load per row (nd of them) in flight without a gap.  The column's rows are
-// added in ascending rank order in FP32 registers and the sum leaves as one packed BF16x8 /
-// FP16x8 16-byte store.  Two CTAs of 9 warps per SM fill the register file without spills.
-// The next unit's forward-map row is loaded while the current one is folded.
+// load of a lane's column two steps ahead is issued as soon as its current column has been
+// added, so a lane keeps two loads per row (2 nd of them) in flight without a gap.  The
+// column's rows are added in ascending rank order in FP32 registers and the sum leaves as one
+// packed BF16x8 / FP16x8 16-byte store.  Two CTAs of 6 warps per SM hold the 2 x 8 row
+// vectors per lane in registers without spills; 18 warps at one load per row in flight kept
+// fewer bytes outstanding and ran 3 % slower.  The next unit's forward-map row is loaded
+// while the current one is folded.
 //
 // (A TMA variant that staged row slices through shared memory with 1-D bulk copies was
 // measured slower: on this part one CTA's bulk copies each take ~0.3 us, so gathering a
@@ -29,14 +31,14 @@ namespace ep {
 namespace {
 
 #ifndef EP_COMBINE_CTAS_PER_SM
-#define EP_COMBINE_CTAS_PER_SM 2   // >= 100 registers per thread: the fold loop runs without spills
+#define EP_COMBINE_CTAS_PER_SM 2   // ~160 registers per thread: the fold loop runs without spills
 #endif
 #ifndef EP_COMBINE_THREADS
-#define EP_COMBINE_THREADS 288   // 9 warps: 2 CTAs fill the register file at ~110 registers
+#define EP_COMBINE_THREADS 192   // 6 warps: 2 CTAs fill the register file at ~160 registers
 #endif
 constexpr int kCombThreads = EP_COMBINE_THREADS;
 #ifndef EP_COMBINE_DEPTH
-#define EP_COMBINE_DEPTH 1
+#define EP_COMBINE_DEPTH 2
 #endif
 constexpr int kDepth = EP_COMBINE_DEPTH;   // columns per row in flight per lane
 
@@ -230,11 +232,11 @@ void combine_geometry(CombineArgs& a, int variant, int num_sms)
     if (variant == EP_VARIANT_TILED_1024) cv = 128;
     if (variant == EP_VARIANT_AUTO) {
         // Small calls split rows into 1024- then 512-element slices so every resident warp
-        // gets work, as the pages' small-batch policy does.
+        // gets at least two units, as the pages' small-batch policy does.
         const int64_t warps = (int64_t)num_sms * EP_COMBINE_CTAS_PER_SM * (kCombThreads / 32);
-        if ((int64_t)a.N < warps && hv > 128) {
+        if ((int64_t)a.N < 2 * warps && hv > 128) {
             cv = 128;
-            if ((int64_t)a.N * ((hv + cv - 1) / cv) < warps) cv = 64;
+            if ((int64_t)a.N * ((hv + cv - 1) / cv) < 2 * warps) cv = 64;
         }
     }
     if (cv > hv) cv = hv;
