@@ -18,7 +18,8 @@
 //   ep_grouped_copy_kernel warp per received row: the row is read once and written to the slot
 //                         of each of its local experts;
 //   ep_ungroup_kernel     warp per received row: its local experts' output rows, ordered by
-//                         expert id, are loaded together and folded in FP32.
+//                         expert id, are loaded together and folded in FP32, with 8 loads per
+//                         lane in flight however many local experts the row has.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -179,8 +180,52 @@ __device__ __forceinline__ uint4 pack8(const float (&acc)[8])
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// Rolling fold of nd <= R rows of hv 16-byte vectors into dst: each lane keeps the next D columns
+// of every row in flight, R * D = 8 loads, so a row with few local experts still keeps as many
+// bytes outstanding as one with many.  Each column's rows are added in ascending order.
+// Entries are found by their rank among the row's valid entries (rank0 / rank1 of lane j belong
+// to top-k entries j and j + 32, whose packed rows are dest0 / dest1).
+template <bool FP16, int R, int D>
+__device__ __forceinline__ void fold_rd(const uint4* y4, int64_t dest0, int64_t dest1, int rank0, int rank1,
+                                        int nd, int hv, uint4* dst, int lane)
+{
+    const uint4* rp[R];
+#pragma unroll
+    for (int q = 0; q < R; ++q) {
+        const unsigned m0 = __ballot_sync(0xffffffffu, dest0 >= 0 && rank0 == q);
+        const unsigned m1 = __ballot_sync(0xffffffffu, dest1 >= 0 && rank1 == q);
+        const int64_t row = m0 ? __shfl_sync(0xffffffffu, dest0, __ffs(m0) - 1)
+                               : __shfl_sync(0xffffffffu, dest1, m1 ? __ffs(m1) - 1 : 0);
+        rp[q] = y4 + row * hv;
+    }
+    uint4 b[R][D];
+#pragma unroll
+    for (int t = 0; t < D; ++t)
+#pragma unroll
+        for (int q = 0; q < R; ++q)
+            if (q < nd && lane + 32 * t < hv) b[q][t] = ld_stream_v4(rp[q] + lane + 32 * t);
+    for (int vb = 0; vb < hv; vb += 32 * D) {              // warp-uniform bounds
+#pragma unroll
+        for (int t = 0; t < D; ++t) {
+            const int vc = vb + 32 * t + lane, vn = vc + 32 * D;
+            float acc[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+#pragma unroll
+            for (int q = 0; q < R; ++q) {
+                if (q < nd) {
+                    const uint4 x = b[q][t];
+                    if (vn < hv) b[q][t] = ld_stream_v4(rp[q] + vn);
+                    if (vc < hv) add8<FP16>(acc, x);
+                }
+            }
+            if (vc < hv) st_v4(dst + vc, pack8<FP16>(acc));
+        }
+    }
+}
+
 template <bool FP16, bool WIDE>
-__global__ void __launch_bounds__(kCopyThreads, 2) ep_ungroup_kernel(const GroupArgs a)
+__global__ void __launch_bounds__(kCopyThreads, 1) ep_ungroup_kernel(const GroupArgs a)
 {
     __shared__ int s_cnt[kMaxRanks];
     if (threadIdx.x < a.W) s_cnt[threadIdx.x] = a.recv_count[threadIdx.x];
@@ -204,42 +249,22 @@ __global__ void __launch_bounds__(kCopyThreads, 2) ep_ungroup_kernel(const Group
                        __popc(__ballot_sync(0xffffffffu, dest1 >= 0));
         // rank of each entry among the valid ones (ids are distinct after first_local)
         int rank0 = 0, rank1 = 0;
-        for (int j = 0; j < 64; ++j) {
+        for (int j = 0; j < a.k; ++j) {
             const int ej = __shfl_sync(0xffffffffu, j < 32 ? e0 : e1, j & 31);
             rank0 += ej < e0;
             rank1 += ej < e1;
         }
         if (!WIDE || nd <= 8) {
             // the rows in ascending expert order, once per received row; then a rolling fold:
-            // row d's next column is requested as soon as its current one is taken
-            const uint4* rp[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const unsigned m0 = __ballot_sync(0xffffffffu, dest0 >= 0 && rank0 == q);
-                const unsigned m1 = __ballot_sync(0xffffffffu, dest1 >= 0 && rank1 == q);
-                const int64_t row = m0 ? __shfl_sync(0xffffffffu, dest0, __ffs(m0) - 1)
-                                       : __shfl_sync(0xffffffffu, dest1, m1 ? __ffs(m1) - 1 : 0);
-                rp[q] = y4 + row * hv;
-            }
-            uint4 b[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-                if (q < nd && lane < hv) b[q] = ld_stream_v4(rp[q] + lane);
-            for (int vb = 0; vb < hv; vb += 32) {          // warp-uniform bounds
-                const int vc = vb + lane, vn = vc + 32;
-                float acc[8];
-#pragma unroll
-                for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    if (q < nd) {
-                        const uint4 x = b[q];
-                        if (vn < hv) b[q] = ld_stream_v4(rp[q] + vn);
-                        if (vc < hv) add8<FP16>(acc, x);
-                    }
-                }
-                if (vc < hv) st_v4(dst + vc, pack8<FP16>(acc));
-            }
+            // row d's next columns are requested as soon as its current one is taken
+            if (nd <= 1)
+                fold_rd<FP16, 1, 8>(y4, dest0, dest1, rank0, rank1, nd, hv, dst, lane);
+            else if (nd == 2)
+                fold_rd<FP16, 2, 4>(y4, dest0, dest1, rank0, rank1, nd, hv, dst, lane);
+            else if (nd <= 4)
+                fold_rd<FP16, 4, 2>(y4, dest0, dest1, rank0, rank1, nd, hv, dst, lane);
+            else
+                fold_rd<FP16, 8, 1>(y4, dest0, dest1, rank0, rank1, nd, hv, dst, lane);
             continue;
         }
         if constexpr (WIDE) {
