@@ -28,16 +28,6 @@
 namespace ep {
 namespace {
 
-// top-k entry j of a received row names a local expert for the first time in the row
-__device__ __forceinline__ bool first_local(const int32_t* ids, int k, int j, int r, int E)
-{
-    const int e = ids[j];
-    if (e < r * E || e >= (r + 1) * E) return false;
-    for (int jj = 0; jj < j; ++jj)
-        if (ids[jj] == e) return false;
-    return true;
-}
-
 __global__ void __launch_bounds__(256) ep_group_kernel(const GroupArgs a)
 {
     __shared__ int s_warp[8];
@@ -95,31 +85,82 @@ __global__ void __launch_bounds__(256) ep_group_kernel(const GroupArgs a)
     }
 }
 
-// lane j of the warp: the packed row (list * rows + slot) its top-k entry j feeds, or -1
-__device__ __forceinline__ int64_t entry_dest(const GroupArgs& a, int r, int64_t i, int j)
+// A received row's top-k entries as the lanes hold them: lane j has entry j and entry j + 32
+// (top-k up to 64), each with the row's slot in that expert's list from the plan's map (only
+// meaningful where the entry is the row's first naming a local expert).  Loading them is two
+// independent loads per lane, so a warp can fetch the next row's entries before it copies or
+// folds the current one; resolving them is shuffles only.
+struct RowEntries {
+    int id0, id1, slot0, slot1;
+};
+
+__device__ __forceinline__ RowEntries load_entries(const GroupArgs& a, int64_t u, int lane)
 {
-    const int32_t* ids = a.recv_idx + ((int64_t)r * a.rows + i) * a.k;
-    if (j >= a.k || !first_local(ids, a.k, j, r, a.E)) return -1;
-    const int slot = a.map[((int64_t)r * a.rows + i) * a.k + j];
-    return ((int64_t)r * a.E + (ids[j] - r * a.E)) * a.rows + slot;
+    const int32_t* ids = a.recv_idx + u * a.k;
+    const int32_t* mp = a.map + u * a.k;
+    RowEntries e;
+    e.id0 = lane < a.k ? __ldg(ids + lane) : -1;
+    e.id1 = lane + 32 < a.k ? __ldg(ids + lane + 32) : -1;
+    e.slot0 = lane < a.k ? __ldg(mp + lane) : 0;
+    e.slot1 = lane + 32 < a.k ? __ldg(mp + lane + 32) : 0;
+    return e;
+}
+
+// The packed rows (list * rows + slot) entries j and j + 32 feed, -1 where the entry names no
+// local expert of rank r or repeats an earlier entry of the row (a row joins an expert's list
+// once, at its first top-k entry naming the expert).
+__device__ __forceinline__ void resolve_entries(const GroupArgs& a, int r, const RowEntries& e, int lane,
+                                                int64_t& dest0, int64_t& dest1)
+{
+    const int lo = r * a.E, hi = lo + a.E;
+    bool ok0 = lane < a.k && e.id0 >= lo && e.id0 < hi;
+    bool ok1 = lane + 32 < a.k && e.id1 >= lo && e.id1 < hi;
+    for (int jj = 0; jj < a.k; ++jj) {                    // warp-uniform loop
+        const int x = __shfl_sync(0xffffffffu, jj < 32 ? e.id0 : e.id1, jj & 31);
+        if (jj < lane && x == e.id0) ok0 = false;
+        if (jj < lane + 32 && x == e.id1) ok1 = false;
+    }
+    dest0 = ok0 ? ((int64_t)r * a.E + (e.id0 - lo)) * a.rows + e.slot0 : -1;
+    dest1 = ok1 ? ((int64_t)r * a.E + (e.id1 - lo)) * a.rows + e.slot1 : -1;
+}
+
+// Received rows only, flattened across ranks: row g is row g - off[r] of rank r.
+__device__ __forceinline__ int64_t received_row(const int* off, int W, int64_t rows, int g)
+{
+    const int r = rank_of_token(off, W, g);
+    return (int64_t)r * rows + (g - off[r]);
 }
 
 __global__ void __launch_bounds__(kCopyThreads) ep_grouped_copy_kernel(const GroupArgs a)
 {
-    __shared__ int s_cnt[kMaxRanks];
-    if (threadIdx.x < a.W) s_cnt[threadIdx.x] = a.recv_count[threadIdx.x];
+    __shared__ int s_off[kMaxRanks + 1];
+    if (threadIdx.x == 0) {
+        int run = 0;
+        for (int r = 0; r < a.W; ++r) {
+            s_off[r] = run;
+            run += a.recv_count[r];
+        }
+        s_off[a.W] = run;
+    }
     __syncthreads();
     const int lane = threadIdx.x & 31;
-    const int64_t nwarps = (int64_t)gridDim.x * (kCopyThreads / 32);
+    const int nwarps = gridDim.x * (kCopyThreads / 32);
+    const int total = s_off[a.W];
     const int nvec = (int)(a.row_bytes >> 4);
-    for (int64_t u = (int64_t)blockIdx.x * (kCopyThreads / 32) + (threadIdx.x >> 5);
-         u < (int64_t)a.W * a.rows; u += nwarps) {
+    int g = blockIdx.x * (kCopyThreads / 32) + (threadIdx.x >> 5);
+    RowEntries next{};
+    if (g < total) next = load_entries(a, received_row(s_off, a.W, a.rows, g), lane);
+    for (; g < total; g += nwarps) {
+        const int64_t u = received_row(s_off, a.W, a.rows, g);
         const int r = (int)(u / a.rows);
-        const int64_t i = u - (int64_t)r * a.rows;
-        if (i >= s_cnt[r]) continue;                       // warp-uniform
+        const RowEntries cur = next;
+        if (g + nwarps < total)                            // lands while this row is copied
+            next = load_entries(a, received_row(s_off, a.W, a.rows, g + nwarps), lane);
+        int64_t dest0, dest1;
+        resolve_entries(a, r, cur, lane, dest0, dest1);
         const uint8_t* src = a.recv_x + u * a.row_bytes;
-        for (int j0 = 0; j0 < a.k; j0 += 32) {             // up to 64 top-k entries
-            const int64_t dest = entry_dest(a, r, i, j0 + lane);
+        for (int half = 0; half < 2; ++half) {             // entries j < 32, then j >= 32
+            const int64_t dest = half ? dest1 : dest0;
             const unsigned has = __ballot_sync(0xffffffffu, dest >= 0);
             if (!has) continue;
             for (int v0 = 0; v0 < nvec; v0 += 32 * 4) {
@@ -227,27 +268,39 @@ __device__ __forceinline__ void fold_rd(const uint4* y4, int64_t dest0, int64_t 
 template <bool FP16, bool WIDE>
 __global__ void __launch_bounds__(kCopyThreads, 1) ep_ungroup_kernel(const GroupArgs a)
 {
-    __shared__ int s_cnt[kMaxRanks];
-    if (threadIdx.x < a.W) s_cnt[threadIdx.x] = a.recv_count[threadIdx.x];
+    __shared__ int s_off[kMaxRanks + 1];
+    if (threadIdx.x == 0) {
+        int run = 0;
+        for (int r = 0; r < a.W; ++r) {
+            s_off[r] = run;
+            run += a.recv_count[r];
+        }
+        s_off[a.W] = run;
+    }
     __syncthreads();
     const int lane = threadIdx.x & 31;
-    const int64_t nwarps = (int64_t)gridDim.x * (kCopyThreads / 32);
+    const int nwarps = gridDim.x * (kCopyThreads / 32);
+    const int total = s_off[a.W];
     const int hv = (int)(a.row_bytes >> 4);       // 16-byte vectors of a 16-bit row
     const uint4* y4 = reinterpret_cast<const uint4*>(a.packed_y);
-    for (int64_t u = (int64_t)blockIdx.x * (kCopyThreads / 32) + (threadIdx.x >> 5);
-         u < (int64_t)a.W * a.rows; u += nwarps) {
+    int g = blockIdx.x * (kCopyThreads / 32) + (threadIdx.x >> 5);
+    RowEntries next{};
+    if (g < total) next = load_entries(a, received_row(s_off, a.W, a.rows, g), lane);
+    for (; g < total; g += nwarps) {
+        const int64_t u = received_row(s_off, a.W, a.rows, g);
         const int r = (int)(u / a.rows);
-        const int64_t i = u - (int64_t)r * a.rows;
-        if (i >= s_cnt[r]) continue;                       // warp-uniform
+        const RowEntries cur = next;
+        if (g + nwarps < total)                            // lands while this row is folded
+            next = load_entries(a, received_row(s_off, a.W, a.rows, g + nwarps), lane);
         uint4* dst = reinterpret_cast<uint4*>(a.out + u * a.row_bytes);
-        // the row's local experts in ascending id: lane j holds entry j (two passes for k > 32)
-        const int32_t* ids = a.recv_idx + u * a.k;
-        int64_t dest0 = entry_dest(a, r, i, lane), dest1 = entry_dest(a, r, i, lane + 32);
-        const int e0 = dest0 >= 0 ? ids[lane] : 0x7FFFFFFF;
-        const int e1 = dest1 >= 0 ? ids[lane + 32] : 0x7FFFFFFF;
+        // the row's local experts in ascending id: lane j holds entry j (and j + 32 for k > 32)
+        int64_t dest0, dest1;
+        resolve_entries(a, r, cur, lane, dest0, dest1);
+        const int e0 = dest0 >= 0 ? cur.id0 : 0x7FFFFFFF;
+        const int e1 = dest1 >= 0 ? cur.id1 : 0x7FFFFFFF;
         const int nd = __popc(__ballot_sync(0xffffffffu, dest0 >= 0)) +
                        __popc(__ballot_sync(0xffffffffu, dest1 >= 0));
-        // rank of each entry among the valid ones (ids are distinct after first_local)
+        // rank of each entry among the valid ones (their ids are distinct)
         int rank0 = 0, rank1 = 0;
         for (int j = 0; j < a.k; ++j) {
             const int ej = __shfl_sync(0xffffffffu, j < 32 ? e0 : e1, j & 31);
