@@ -295,6 +295,8 @@ def run_ours(args, rank, world, dist):
     wire4 = measure_combine_wire(plan, wl, dev, stream, x, w, idx, P, peak,
                                  steps=max(3, min(args.steps, 50)), fmt="fp4")
     grouped = measure_grouped(ep, dev, stream, peak, steps=max(3, min(args.steps, 50)))
+    grouped_large = measure_grouped(ep, dev, stream, peak, steps=max(3, min(args.steps, 20)),
+                                    workload="dsv3", max_tok=min(1024, wl.M))
     latency = measure_small_batch_latency(ep, dev)
     protocol = measure_graph_protocol(plan, wl, dev, x, w, idx, nbytes, peak)
     if plan.status() != 0:
@@ -343,6 +345,7 @@ def run_ours(args, rank, world, dist):
             "fp8_combine_wire": wire,
             "fp4_combine_wire": wire4,
             "expert_grouped_layout": grouped,
+            "expert_grouped_layout_dsv3": grouped_large,
             "small_batch_latency_us": latency,
             "graph_protocol": protocol,
         }
@@ -426,12 +429,14 @@ def measure_combine_wire(plan, wl, dev, stream, x, w, idx, P, peak, steps, fmt):
             "quantize_frac": round(qbytes / (qt * 1e-3) / 1e9 / peak, 4)}
 
 
-def measure_grouped(ep, dev, stream, peak, steps):
-    """The expert-grouped (3-D) view and its inverse on the small-batch workload (W=4, 64
-    experts per rank, top-8, hidden 7168 BF16, 256 tokens per rank), the regime a grouped GEMM
-    consumer runs in.  Minimal bytes: grouping reads each received row once and writes one row
-    per (row, local expert) entry; the inverse reads the entries and writes the rows."""
-    wl = wlmod.make_workload("small")
+def measure_grouped(ep, dev, stream, peak, steps, workload="small", max_tok=None):
+    """The expert-grouped (3-D) view and its inverse: by default on the small-batch workload (W=4,
+    64 experts per rank, top-8, hidden 7168 BF16, 256 tokens per rank), the regime a grouped GEMM
+    consumer runs in; workload="dsv3", max_tok=1024 measures the DeepSeek-V3 shape at 1024
+    tokens per rank, whose grouped view holds 30 GB.  Minimal bytes: grouping reads each
+    received row once and writes one row per (row, local expert) entry; the inverse reads the
+    entries and writes the rows."""
+    wl = wlmod.make_workload(workload, max_tok=max_tok)
     plan = ep.Plan(wl.W, wl.E, wl.k, wl.H, "bf16", 0, wl.M, device=dev)
     x = torch.from_numpy(wl.x.view(np.int16)).to(dev)
     idx = torch.from_numpy(wl.indices).to(dev)
@@ -471,7 +476,11 @@ def measure_grouped(ep, dev, stream, peak, steps):
     rb = 2 * wl.H
     gb = rows * (rb + 4 * wl.k) + entries * (rb + 4)
     ub = entries * rb + rows * (rb + 4 * wl.k)
-    return {"workload": "W=4, 64 experts/rank, top-8, hidden 7168 BF16, 256 tokens/rank",
+    desc = ("W=4, 64 experts/rank, top-8, hidden 7168 BF16, 256 tokens/rank" if workload == "small" else
+            f"W={wl.W}, {wl.E} experts/rank, top-{wl.k}, hidden {wl.H} BF16, {wl.M} tokens/rank, Zipf(1.2)")
+    del px, y, out
+    torch.cuda.empty_cache()
+    return {"workload": desc,
             "received_rows": rows, "expert_entries": entries,
             "group_us": round(gt * 1e3, 2), "group_frac": round(gb / (gt * 1e-3) / 1e9 / peak, 4),
             "ungroup_us": round(ut * 1e3, 2), "ungroup_frac": round(ub / (ut * 1e-3) / 1e9 / peak, 4),
