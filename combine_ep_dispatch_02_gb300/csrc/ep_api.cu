@@ -561,6 +561,7 @@ int ep_group_by_expert(ep_plan* p, void* packed_x, int32_t* packed_count, int32_
     DeviceGuard g(p->device);
     if (!g.ok) return fail(EP_ERR_CUDA, "cannot select the plan's device %d", p->device);
     GroupArgs a{};
+    a.work.q = p->queues + 2 * kQueueGroup;
     a.recv_x = p->recv_x; a.recv_idx = p->recv_idx; a.recv_count = p->recv_count; a.src_pos = p->src_pos;
     a.map = p->expert_map; a.packed_x = (uint8_t*)packed_x; a.count = packed_count;
     a.src_info = packed_src_info; a.layout_range = (long long*)layout_range;

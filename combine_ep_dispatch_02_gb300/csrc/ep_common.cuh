@@ -42,7 +42,8 @@ constexpr int kSpinLimit = EP_SPIN_LIMIT;   // polls before a wait gives up with
 // Work queues of the persistent copy kernels (see WorkSplit): launches that share a queue must
 // run one after the other, as the calls on one plan do.
 constexpr int kQueueDispatch = 0;   // payload scatters (BF16 / FP8 / MX FP4 rows)
-constexpr int kQueues = 1;
+constexpr int kQueueGroup = 1;      // copy of received rows into the expert-grouped view
+constexpr int kQueues = 2;
 
 // ---- work split of a persistent copy kernel
 //
@@ -57,7 +58,8 @@ constexpr int kQueues = 1;
 // each CTA counts itself in q[1] when all its warps are done, and the last CTA returns both
 // words to zero, so the next launch on the same queue (stream-ordered after this one, or a
 // CUDA-graph replay) starts from zero without a memset.  The launcher fills the split in the
-// kernel's arguments, so the kernel reads it from the parameter bank rather than registers.
+// kernel's arguments, so the kernel reads it from the parameter bank rather than registers; a
+// kernel whose unit count only the device knows builds the split itself.
 struct WorkSplit {
     unsigned long long* q;   // two words, zero between launches
     uint32_t units;          // < 2^31 (checked by the host before every launch)
@@ -65,6 +67,9 @@ struct WorkSplit {
     uint32_t static_end;     // units below this are split round-robin
 };
 
+#ifdef __CUDACC__
+__host__ __device__
+#endif
 inline WorkSplit make_work_split(unsigned long long* q, int64_t units, int64_t warps)
 {
     WorkSplit s;
@@ -161,6 +166,7 @@ struct GroupArgs {
     int32_t* recv_idx_out;       // metadata rows of the receive buffers
     float* recv_w_out;
     float* recv_scales_out;
+    WorkSplit work;              // grouped copy: q set by the caller, the rest by the launcher
     int64_t rows;                // W*M
     int64_t row_bytes;           // payload bytes (grouping) / 16-bit row bytes (inverse)
     int W, E, k, M, F, N, sd;

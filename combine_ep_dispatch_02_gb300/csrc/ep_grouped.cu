@@ -131,6 +131,9 @@ __device__ __forceinline__ int64_t received_row(const int* off, int W, int64_t r
     return (int64_t)r * rows + (g - off[r]);
 }
 
+// Rows are split over warps as the payload scatter's units are (WorkSplit): the last rounds come
+// from the plan's grouping queue (a.work.q), since a row costs one read and one write per local
+// expert.  The unit count, the rows received by all ranks, is known on the device only.
 __global__ void __launch_bounds__(kCopyThreads) ep_grouped_copy_kernel(const GroupArgs a)
 {
     __shared__ int s_off[kMaxRanks + 1];
@@ -144,18 +147,20 @@ __global__ void __launch_bounds__(kCopyThreads) ep_grouped_copy_kernel(const Gro
     }
     __syncthreads();
     const int lane = threadIdx.x & 31;
-    const int nwarps = gridDim.x * (kCopyThreads / 32);
-    const int total = s_off[a.W];
+    const WorkSplit ws = make_work_split(a.work.q, s_off[a.W], (int64_t)gridDim.x * (kCopyThreads / 32));
+    const uint32_t total = ws.units;
     const int nvec = (int)(a.row_bytes >> 4);
-    int g = blockIdx.x * (kCopyThreads / 32) + (threadIdx.x >> 5);
+    uint32_t g_next = work_first(ws);
     RowEntries next{};
-    if (g < total) next = load_entries(a, received_row(s_off, a.W, a.rows, g), lane);
-    for (; g < total; g += nwarps) {
-        const int64_t u = received_row(s_off, a.W, a.rows, g);
+    if (g_next < total) next = load_entries(a, received_row(s_off, a.W, a.rows, (int)g_next), lane);
+    while (g_next < total) {
+        const uint32_t g = g_next;
+        const int64_t u = received_row(s_off, a.W, a.rows, (int)g);
         const int r = (int)(u / a.rows);
         const RowEntries cur = next;
-        if (g + nwarps < total)                            // lands while this row is copied
-            next = load_entries(a, received_row(s_off, a.W, a.rows, g + nwarps), lane);
+        g_next = work_next(ws, g, lane);
+        if (g_next < total)                                // lands while this row is copied
+            next = load_entries(a, received_row(s_off, a.W, a.rows, (int)g_next), lane);
         int64_t dest0, dest1;
         resolve_entries(a, r, cur, lane, dest0, dest1);
         const uint8_t* src = a.recv_x + u * a.row_bytes;
@@ -182,6 +187,7 @@ __global__ void __launch_bounds__(kCopyThreads) ep_grouped_copy_kernel(const Gro
             }
         }
     }
+    work_retire(ws);
 }
 
 template <bool FP16>

@@ -739,7 +739,9 @@ def test_fp4_wire_rejects_bad_plans():
 
 # ---------------------------------------------------------------- expert-grouped layout
 
-def _check_grouped(wl, seed=0, fused=False):
+def _check_grouped(wl, seed=0, fused=False, repeats=1):
+    """repeats > 1 groups again on the same plan into a packed buffer filled with 0xFF bytes, so
+    rows a call fails to write show."""
     disp = oracle.dispatch(wl.W, wl.E, wl.k, wl.H, wl.elem_bytes, wl.sd, wl.M, wl.x, wl.weights,
                            wl.scales, wl.indices, wl.n_tok)
     g = oracle.group_by_expert(wl.W, wl.E, wl.k, wl.H, wl.elem_bytes, wl.M, disp)
@@ -750,11 +752,21 @@ def _check_grouped(wl, seed=0, fused=False):
     o_out = oracle.ungroup_by_expert(wl.W, wl.E, wl.H, fp16, wl.M, disp["recv_count"], g, y)
 
     plan, (x, w, sc, idx) = _setup(wl)
+    for rep in range(repeats):
+        _check_grouped_once(wl, plan, x, w, sc, idx, disp, g, y, o_out, fused, rep > 0)
+    plan.close()
+
+
+def _check_grouped_once(wl, plan, x, w, sc, idx, disp, g, y, o_out, fused, poisoned):
+    px = None
+    if poisoned:
+        px = torch.empty((wl.W, wl.E, wl.W * wl.M, plan.row_elems), dtype=plan.payload_torch_dtype, device=DEV)
+        px.view(torch.uint8).fill_(0xFF)
     if fused:
-        d, px, cnt, info, layout = plan.dispatch_grouped(x, w, sc, idx, wl.n_tok)
+        d, px, cnt, info, layout = plan.dispatch_grouped(x, w, sc, idx, wl.n_tok, packed_x=px)
     else:
         d = plan.dispatch(x, w, sc, idx, wl.n_tok)
-        px, cnt, info, layout = plan.group_by_expert(d.epoch)
+        px, cnt, info, layout = plan.group_by_expert(d.epoch, packed_x=px)
     out = plan.ungroup_by_expert(torch.from_numpy(y.view(np.int16)).to(DEV), d.epoch)
     torch.cuda.synchronize()
     assert plan.status() == 0
@@ -782,7 +794,6 @@ def _check_grouped(wl, seed=0, fused=False):
     for r in range(wl.W):
         n = int(disp["recv_count"][r])
         assert np.array_equal(out[r, :n], o_out[r, :n]), r
-    plan.close()
 
 
 @pytest.mark.parametrize("case", [
@@ -794,6 +805,15 @@ def _check_grouped(wl, seed=0, fused=False):
 def test_grouped_layout(case):
     _check_grouped(wlmod.custom_workload(seed=5, **case))
     _check_grouped(wlmod.custom_workload(seed=5, **case), fused=True)
+
+
+def test_grouped_layout_work_queue():
+    """About 54 000 received rows, more than four rounds per warp of the grouped copy, so its
+    last rows come from the plan's grouping queue; grouped twice on one plan, the second time
+    into a poisoned buffer, and through the fused dispatch twice."""
+    wl = wlmod.custom_workload(W=8, E=4, k=4, H=64, M=2048, n_tok=[2048] * 8, seed=12)
+    _check_grouped(wl, repeats=2)
+    _check_grouped(wl, fused=True, repeats=2)
 
 
 def test_grouped_layout_wide_rows():
