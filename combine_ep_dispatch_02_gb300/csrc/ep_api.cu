@@ -562,6 +562,7 @@ int ep_group_by_expert(ep_plan* p, void* packed_x, int32_t* packed_count, int32_
     if (!g.ok) return fail(EP_ERR_CUDA, "cannot select the plan's device %d", p->device);
     GroupArgs a{};
     a.work.q = p->queues + 2 * kQueueGroup;
+    a.vec16 = p->k % 4 == 0;   // receive index rows: 256-byte-aligned buffer, 4k-byte rows
     a.recv_x = p->recv_x; a.recv_idx = p->recv_idx; a.recv_count = p->recv_count; a.src_pos = p->src_pos;
     a.map = p->expert_map; a.packed_x = (uint8_t*)packed_x; a.count = packed_count;
     a.src_info = packed_src_info; a.layout_range = (long long*)layout_range;
@@ -597,6 +598,7 @@ int ep_dispatch_grouped(ep_plan* p, const void* x, const float* weights, const f
     a.packed_x = (uint8_t*)packed_x; a.count = packed_count; a.src_info = packed_src_info;
     a.layout_range = (long long*)layout_range;
     a.src_idx = indices; a.x = (const uint8_t*)x; a.w = weights; a.scales = scales; a.fwd = p->fwd;
+    a.vec16 = (p->k % 4 == 0) && aligned(indices, 16);
     a.recv_idx_out = p->recv_idx; a.recv_w_out = p->recv_w; a.recv_scales_out = p->recv_scales;
     a.rows = p->rows; a.row_bytes = p->row_bytes;
     a.W = p->W; a.E = p->E; a.k = p->k; a.M = p->M; a.F = p->F; a.N = p->N; a.sd = p->sd;

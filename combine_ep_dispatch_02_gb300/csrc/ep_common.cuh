@@ -167,6 +167,7 @@ struct GroupArgs {
     float* recv_w_out;
     float* recv_scales_out;
     WorkSplit work;              // grouped copy: q set by the caller, the rest by the launcher
+    int vec16;                   // the index rows grouping reads are 16-byte aligned (k % 4 == 0)
     int64_t rows;                // W*M
     int64_t row_bytes;           // payload bytes (grouping) / 16-bit row bytes (inverse)
     int W, E, k, M, F, N, sd;

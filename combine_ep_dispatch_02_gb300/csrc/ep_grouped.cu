@@ -12,9 +12,10 @@
 //
 // Kernels:
 //   ep_group_kernel       one CTA per (rank, local expert): block scan over the rank's received
-//                         rows (a row is in the list iff one of its k ids is the expert), writes
-//                         src_info, the count, the layout ranges, and each row's slot into the
-//                         plan's map [W][W*M][k] at the row's first top-k entry naming the expert;
+//                         rows, 1024 per step (a row is in the list iff one of its k ids is the
+//                         expert); writes src_info, the count, the layout ranges, and each row's
+//                         slot into the plan's map [W][W*M][k] at the row's first top-k entry
+//                         naming the expert;
 //   ep_grouped_copy_kernel warp per received row: the row is read once and written to the slot
 //                         of each of its local experts;
 //   ep_ungroup_kernel     warp per received row: its local experts' output rows, ordered by
@@ -28,9 +29,42 @@
 namespace ep {
 namespace {
 
+// One CTA per (rank, local expert): the rank's received rows are taken 1024 at a time, four per
+// thread (rows i0 + q*256 + tid, q = 0..3, so each batch is coalesced), and the rows naming the
+// expert get consecutive slots in row order: a row's slot is the count of hits in earlier
+// batches of the chunk, then in earlier warps of its batch, then in earlier lanes.
+constexpr int kGroupRowsPerThread = 4;
+
+// First top-k entry of a row naming expert ge, or -1.  VEC = k / 4 reads the row as 16-byte
+// vectors (rows 16-byte aligned), VEC = 0 loops over the k ids; no early exit, so the loads of
+// a row are in flight together.
+template <int VEC>
+__device__ __forceinline__ int first_entry(const int32_t* ids, int k, int32_t ge)
+{
+    int jf = -1;
+    if constexpr (VEC > 0) {
+        int4 v[VEC];
+#pragma unroll
+        for (int q = 0; q < VEC; ++q) v[q] = __ldg(reinterpret_cast<const int4*>(ids) + q);
+#pragma unroll
+        for (int q = VEC - 1; q >= 0; --q) {
+            if (v[q].w == ge) jf = 4 * q + 3;
+            if (v[q].z == ge) jf = 4 * q + 2;
+            if (v[q].y == ge) jf = 4 * q + 1;
+            if (v[q].x == ge) jf = 4 * q;
+        }
+    } else {
+        for (int j = k - 1; j >= 0; --j)
+            if (__ldg(ids + j) == ge) jf = j;
+    }
+    return jf;
+}
+
+template <int VEC>
 __global__ void __launch_bounds__(256) ep_group_kernel(const GroupArgs a)
 {
-    __shared__ int s_warp[8];
+    constexpr int Q = kGroupRowsPerThread;
+    __shared__ int s_warp[Q][8];
     __shared__ int s_src[kMaxRanks];
     __shared__ int s_base;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -42,36 +76,56 @@ __global__ void __launch_bounds__(256) ep_group_kernel(const GroupArgs a)
     if (tid < kMaxRanks) s_src[tid] = 0;
     if (tid == 0) s_base = 0;
     __syncthreads();
-    for (int i0 = 0; i0 < n; i0 += 256) {
-        const int i = i0 + tid;
-        int jfirst = -1;
-        if (i < n) {
-            const int32_t* ids;
-            if (a.src_idx) {        // fused dispatch: the row's index row is its source's
-                const int32_t pos = a.src_pos[(int64_t)r * a.rows + i];
-                const int64_t s = pos / a.rows;
-                ids = a.src_idx + (s * a.M + (pos - s * a.rows)) * a.k;
-            } else {
-                ids = a.recv_idx + ((int64_t)r * a.rows + i) * a.k;
-            }
-            for (int j = 0; j < a.k; ++j)
-                if (__ldg(ids + j) == ge) { jfirst = j; break; }
-        }
-        const unsigned bal = __ballot_sync(0xffffffffu, jfirst >= 0);
-        if (lane == 0) s_warp[warp] = __popc(bal);
-        __syncthreads();
-        int before = s_base, total = 0;
+    for (int i0 = 0; i0 < n; i0 += 256 * Q) {
+        int jfirst[Q], pos[Q];
 #pragma unroll
-        for (int w = 0; w < 8; ++w) {
-            if (w < warp) before += s_warp[w];
-            total += s_warp[w];
+        for (int q = 0; q < Q; ++q) {
+            const int i = i0 + q * 256 + tid;
+            pos[q] = i < n ? __ldg(a.src_pos + (int64_t)r * a.rows + i) : 0;
         }
-        if (jfirst >= 0) {
-            const int slot = before + __popc(bal & lanemask_lt());
-            const int32_t pos = a.src_pos[(int64_t)r * a.rows + i];
-            a.src_info[list * a.rows + slot] = (int32_t)(pos % a.rows);
-            a.map[((int64_t)r * a.rows + i) * a.k + jfirst] = slot;
-            atomicAdd(&s_src[pos / a.rows], 1);
+#pragma unroll
+        for (int q = 0; q < Q; ++q) {
+            const int i = i0 + q * 256 + tid;
+            jfirst[q] = -1;
+            if (i < n) {
+                const int32_t* ids;
+                if (a.src_idx) {    // fused dispatch: the row's index row is its source's
+                    const int64_t s = pos[q] / a.rows;
+                    ids = a.src_idx + (s * a.M + (pos[q] - s * a.rows)) * a.k;
+                } else {
+                    ids = a.recv_idx + ((int64_t)r * a.rows + i) * a.k;
+                }
+                jfirst[q] = first_entry<VEC>(ids, a.k, ge);
+            }
+        }
+        unsigned bal[Q];
+#pragma unroll
+        for (int q = 0; q < Q; ++q) {
+            bal[q] = __ballot_sync(0xffffffffu, jfirst[q] >= 0);
+            if (lane == 0) s_warp[q][warp] = __popc(bal[q]);
+        }
+        __syncthreads();
+        int run = s_base, total = 0;
+        int before[Q];
+#pragma unroll
+        for (int q = 0; q < Q; ++q) {
+            before[q] = run;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) {
+                if (w < warp) before[q] += s_warp[q][w];
+                run += s_warp[q][w];
+                total += s_warp[q][w];
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < Q; ++q) {
+            if (jfirst[q] >= 0) {
+                const int i = i0 + q * 256 + tid;
+                const int slot = before[q] + __popc(bal[q] & lanemask_lt());
+                a.src_info[list * a.rows + slot] = (int32_t)(pos[q] % a.rows);
+                a.map[((int64_t)r * a.rows + i) * a.k + jfirst[q]] = slot;
+                atomicAdd(&s_src[pos[q] / a.rows], 1);
+            }
         }
         __syncthreads();
         if (tid == 0) s_base += total;
@@ -443,9 +497,23 @@ int grid_of(const void* kernel, int64_t warps, int num_sms)
 
 }  // namespace
 
+// compiled index-row widths: top-k 4, 8 (the pages' specialised case), 16; others loop
+static void launch_group_scan(const GroupArgs& a, cudaStream_t stream)
+{
+    const int grid = a.W * a.E;
+    if (!a.vec16 || (a.k != 4 && a.k != 8 && a.k != 16))
+        ep_group_kernel<0><<<grid, 256, 0, stream>>>(a);
+    else if (a.k == 4)
+        ep_group_kernel<1><<<grid, 256, 0, stream>>>(a);
+    else if (a.k == 8)
+        ep_group_kernel<2><<<grid, 256, 0, stream>>>(a);
+    else
+        ep_group_kernel<4><<<grid, 256, 0, stream>>>(a);
+}
+
 cudaError_t launch_group_from_source(const GroupArgs& a, int num_sms, cudaStream_t stream)
 {
-    ep_group_kernel<<<a.W * a.E, 256, 0, stream>>>(a);
+    launch_group_scan(a, stream);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || a.N == 0) return e;
     ep_group_from_source_kernel<<<grid_of((const void*)ep_group_from_source_kernel, a.N, num_sms),
@@ -455,7 +523,7 @@ cudaError_t launch_group_from_source(const GroupArgs& a, int num_sms, cudaStream
 
 cudaError_t launch_group(const GroupArgs& a, int num_sms, cudaStream_t stream)
 {
-    ep_group_kernel<<<a.W * a.E, 256, 0, stream>>>(a);
+    launch_group_scan(a, stream);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int64_t units = (int64_t)a.W * a.rows;
