@@ -490,10 +490,12 @@ def measure_grouped(ep, dev, stream, peak, steps, workload="small", max_tok=None
                                 (fused * 1e-3) / 1e9 / peak, 4)}
 
 
-def measure_small_batch_latency(ep, dev, tokens=(8, 128, 256), replays=120):
-    """Dispatch and combine latency at small batches on the DeepSeek-V3 shape (W=8, 32 experts
-    per rank, top-8, hidden 7168 BF16, Zipf routing), as the pages measure it: each call captured
-    in a CUDA graph and replayed; p50 over the replays of the per-replay device time."""
+def measure_small_batch_latency(ep, dev, tokens=(8, 128, 256, 1024, 2048), replays=120):
+    """Dispatch and combine latency at small and mid-size batches on the DeepSeek-V3 shape (W=8,
+    32 experts per rank, top-8, hidden 7168 BF16, Zipf routing), as the pages measure it: each
+    call captured in a CUDA graph and replayed; p50 over the replays of the per-replay device
+    time.  From 1024 tokens per rank on, the entries also give the effective GB/s of the L2-
+    flushed times (the dispatch and combine minimal bytes of phase_bytes)."""
     res = {}
     for t in tokens:
         wl = wlmod.make_workload(WORKLOAD, max_tok=t)
@@ -531,8 +533,16 @@ def measure_small_batch_latency(ep, dev, tokens=(8, 128, 256), replays=120):
                             times[name + ("_l2_flushed" if cold else "")].append(a.elapsed_time(b) * 1e3)
         if plan.status() != 0:
             raise RuntimeError("device status after the latency runs: %d" % plan.status())
+        entry = {k: round(statistics.median(v), 2) for k, v in times.items()}
+        if t >= 1024:
+            nb = phase_bytes(wl, int(d.recv_count.sum().item()))
+            peak = hbm_peak()[0]
+            for ph in ("dispatch", "combine"):
+                gbs = nb[ph] / (entry[ph + "_l2_flushed"] * 1e-6) / 1e9
+                entry[ph + "_gbs"] = round(gbs, 1)
+                entry[ph + "_frac"] = round(gbs / peak, 4)
         plan.close()
-        res[f"{t}_tokens_per_rank"] = {k: round(statistics.median(v), 2) for k, v in times.items()}
+        res[f"{t}_tokens_per_rank"] = entry
     res["method"] = ("CUDA-graph replay of one dispatch (route + scatter) or one combine; p50 of "
                      f"{replays} replays; hot = back to back, l2_flushed = a 2x-L2 buffer written "
                      "before each replay")

@@ -160,11 +160,12 @@ int pick_chunk_elems(const ep_plan* p, int N)
     case EP_VARIANT_TILED_1024: return p->H < 1024 ? p->H : 1024;
     default: break;
     }
-    // Whole rows once there are enough tokens to give every resident warp a few rows;
-    // otherwise split rows so small calls still spread over all SMs (the pages use 512- or
-    // 1024-element tiles up to 256 tokens per source rank).
+    // Whole rows once there are enough tokens to give every resident warp four rows, so the
+    // scatter's work queue can even out tokens of different destination counts; otherwise
+    // split rows into 1024-element slices, and into 512-element ones when even those leave
+    // warps idle (the pages use 512- or 1024-element tiles up to 256 tokens per source rank).
     const int64_t warps = (int64_t)p->num_sms * 32;
-    if (N >= warps || p->H <= 1024) return p->H;
+    if (N >= 4 * warps || p->H <= 1024) return p->H;
     if ((int64_t)N * ((p->H + 1023) / 1024) >= warps) return 1024;
     return 512;
 }

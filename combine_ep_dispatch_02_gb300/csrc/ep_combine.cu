@@ -231,10 +231,11 @@ void combine_geometry(CombineArgs& a, int variant, int num_sms)
     if (variant == EP_VARIANT_TILED_512) cv = 64;
     if (variant == EP_VARIANT_TILED_1024) cv = 128;
     if (variant == EP_VARIANT_AUTO) {
-        // Small calls split rows into 1024- then 512-element slices so every resident warp
-        // gets at least two units, as the pages' small-batch policy does.
+        // Calls with fewer than four whole rows per resident warp split rows into 1024-element
+        // slices, and into 512-element ones when that still leaves fewer than two units per
+        // warp, as the pages' small-batch policy does.
         const int64_t warps = (int64_t)num_sms * EP_COMBINE_CTAS_PER_SM * (kCombThreads / 32);
-        if ((int64_t)a.N < 2 * warps && hv > 128) {
+        if ((int64_t)a.N < 4 * warps && hv > 128) {
             cv = 128;
             if ((int64_t)a.N * ((hv + cv - 1) / cv) < 2 * warps) cv = 64;
         }
