@@ -339,6 +339,16 @@ def test_scatter_work_queue_reuse_and_graph_replay():
     _check_mxfp4_dispatch(wl, "tiled_512", repeats=2)
 
 
+def test_mid_size_sliced_rows_with_work_queue():
+    """1024 tokens per rank of the DeepSeek-V3 shape: the AUTO variant cuts rows into 1024-element
+    slices (fewer than four whole rows per resident warp) and the scatters draw their last slices
+    from the work queue; BF16, FP8 and MX FP4 dispatch and the combine against the oracle."""
+    wl = wlmod.make_workload("dsv3", max_tok=1024)
+    _check(wl)
+    _check_quantised(wl)
+    _check_mxfp4_dispatch(wl)
+
+
 # ---------------------------------------------------------------- quantising FP8 dispatch
 
 def _check_quantised(wl, variant="auto"):
