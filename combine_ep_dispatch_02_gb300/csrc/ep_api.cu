@@ -603,6 +603,11 @@ int ep_dispatch_grouped(ep_plan* p, const void* x, const float* weights, const f
     a.recv_idx_out = p->recv_idx; a.recv_w_out = p->recv_w; a.recv_scales_out = p->recv_scales;
     a.rows = p->rows; a.row_bytes = p->row_bytes;
     a.W = p->W; a.E = p->E; a.k = p->k; a.M = p->M; a.F = p->F; a.N = p->N; a.sd = p->sd;
+    const int ce = pick_chunk_elems(p, p->N);          // rows sliced as the payload scatter's
+    a.chunk_bytes = ce * p->elem_bytes;
+    a.chunks = (int)((p->H + ce - 1) / ce);
+    if (int rc2 = check_units(a.N, a.chunks, "ep_dispatch_grouped")) return rc2;
+    a.work.q = p->queues + 2 * kQueueGroup;
     for (int s = 0; s <= p->W; ++s) a.tok_off[s] = p->tok_off[s];
     cudaError_t e = launch_group_from_source(a, p->num_sms, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "ep_dispatch_grouped: launch");

@@ -166,11 +166,12 @@ struct GroupArgs {
     int32_t* recv_idx_out;       // metadata rows of the receive buffers
     float* recv_w_out;
     float* recv_scales_out;
-    WorkSplit work;              // grouped copy: q set by the caller, the rest by the launcher
+    WorkSplit work;              // grouped copy / fused dispatch: q set by the caller
     int vec16;                   // the index rows grouping reads are 16-byte aligned (k % 4 == 0)
     int64_t rows;                // W*M
     int64_t row_bytes;           // payload bytes (grouping) / 16-bit row bytes (inverse)
     int W, E, k, M, F, N, sd;
+    int chunk_bytes, chunks;     // fused dispatch: work unit = (token, slice of chunk_bytes)
     int tok_off[kMaxRanks + 1];
 };
 

@@ -422,16 +422,19 @@ __global__ void __launch_bounds__(kCopyThreads) ep_group_from_source_kernel(cons
     if (threadIdx.x <= a.W) s_off[threadIdx.x] = a.tok_off[threadIdx.x];
     __syncthreads();
     const int lane = threadIdx.x & 31;
-    const int64_t nwarps = (int64_t)gridDim.x * (kCopyThreads / 32);
-    const int nvec = (int)(a.row_bytes >> 4);
-    for (int64_t g = (int64_t)blockIdx.x * (kCopyThreads / 32) + (threadIdx.x >> 5); g < a.N; g += nwarps) {
-        const int s = rank_of_token(s_off, a.W, (int)g);
+    const WorkSplit& ws = a.work;
+    for (uint32_t u = work_first(ws); u < ws.units; u = work_next(ws, u, lane)) {
+        const int g = (int)(u / (uint32_t)a.chunks);
+        const int c = (int)(u - (uint32_t)g * (uint32_t)a.chunks);
+        const int64_t off = (int64_t)c * a.chunk_bytes;      // this unit's slice of the row
+        const int nvec = (int)(min((int64_t)a.chunk_bytes, a.row_bytes - off) >> 4);
+        const int s = rank_of_token(s_off, a.W, g);
         const int64_t tok = (int64_t)s * a.M + (g - s_off[s]);
         const int32_t* ids = a.src_idx + tok * a.k;
         const int fw = lane < a.F ? __ldg(a.fwd + tok * a.F + lane) : -1;   // receive rows, by rank
         const int nd = __popc(__ballot_sync(0xffffffffu, fw >= 0));
-        // metadata rows to the receive rows, as in ep_dispatch
-        for (int d = 0; d < nd; ++d) {
+        // metadata rows to the receive rows, as in ep_dispatch (with the first slice)
+        for (int d = 0; d < (c == 0 ? nd : 0); ++d) {
             const int64_t row = __shfl_sync(0xffffffffu, fw, d);
             for (int e = lane; e < a.k; e += 32) {
                 a.recv_idx_out[row * a.k + e] = __ldg(ids + e);
@@ -440,7 +443,7 @@ __global__ void __launch_bounds__(kCopyThreads) ep_group_from_source_kernel(cons
             for (int e = lane; e < a.sd; e += 32)
                 a.recv_scales_out[row * a.sd + e] = __ldg(a.scales + tok * a.sd + e);
         }
-        const uint8_t* src = a.x + tok * a.row_bytes;
+        const uint8_t* src = a.x + tok * a.row_bytes + off;
         for (int j0 = 0; j0 < a.k; j0 += 32) {
             const int j = j0 + lane;
             int64_t dest = -1;
@@ -472,7 +475,7 @@ __global__ void __launch_bounds__(kCopyThreads) ep_group_from_source_kernel(cons
                 }
                 for (unsigned m = has; m; m &= m - 1) {
                     const int64_t prow = __shfl_sync(0xffffffffu, dest, __ffs(m) - 1);
-                    uint8_t* dst = a.packed_x + prow * a.row_bytes;
+                    uint8_t* dst = a.packed_x + prow * a.row_bytes + off;
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const int v = v0 + q * 32 + lane;
@@ -482,6 +485,7 @@ __global__ void __launch_bounds__(kCopyThreads) ep_group_from_source_kernel(cons
             }
         }
     }
+    work_retire(ws);
 }
 
 int grid_of(const void* kernel, int64_t warps, int num_sms)
@@ -516,8 +520,11 @@ cudaError_t launch_group_from_source(const GroupArgs& a, int num_sms, cudaStream
     launch_group_scan(a, stream);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || a.N == 0) return e;
-    ep_group_from_source_kernel<<<grid_of((const void*)ep_group_from_source_kernel, a.N, num_sms),
-                                  kCopyThreads, 0, stream>>>(a);
+    const int64_t units = (int64_t)a.N * a.chunks;
+    const int grid = grid_of((const void*)ep_group_from_source_kernel, units, num_sms);
+    GroupArgs b = a;
+    b.work = make_work_split(a.work.q, units, (int64_t)grid * (kCopyThreads / 32));
+    ep_group_from_source_kernel<<<grid, kCopyThreads, 0, stream>>>(b);
     return cudaGetLastError();
 }
 

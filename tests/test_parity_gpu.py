@@ -824,6 +824,10 @@ def test_grouped_layout_work_queue():
     wl = wlmod.custom_workload(W=8, E=4, k=4, H=64, M=2048, n_tok=[2048] * 8, seed=12)
     _check_grouped(wl, repeats=2)
     _check_grouped(wl, fused=True, repeats=2)
+    # rows of 4096 elements cut into 1024-element slices (fewer than four rows per warp), more than
+    # four rounds of slices: the fused dispatch draws its last slices from the queue
+    wl = wlmod.custom_workload(W=8, E=4, k=4, H=4096, M=1024, n_tok=[1024] * 8, seed=13)
+    _check_grouped(wl, fused=True, repeats=2)
 
 
 def test_grouped_layout_wide_rows():
