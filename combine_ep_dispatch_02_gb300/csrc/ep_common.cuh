@@ -28,7 +28,7 @@ constexpr int kMaxRanks = 32;       // destination sets are uint32 bit masks
 constexpr int kMaxTopk = 64;        // two 32-slot batches
 constexpr int kRouteTile = 256;     // tokens per routing CTA, one per thread
 constexpr int kRouteThreads = 256;
-constexpr int kCopyThreads = 256;   // scatter / combine CTAs: 8 warps, one work unit per warp
+constexpr int kCopyThreads = 256;   // scatter, wire and grouped-view CTAs: 8 warps, a work unit per warp
 
 // Scan flag word: [63:34] call stamp (30 bits) | [33:32] status | [31:0] count.
 constexpr unsigned long long kFlagAggregate = 1ull;   // count = this tile's own total
@@ -54,10 +54,10 @@ constexpr int kQueues = 2;
 // atomics), and the rest are drawn one at a time, in ascending order, from a per-plan queue
 // word q[0]: a warp whose units were cheap draws more of them.  Calls with fewer than four
 // rounds of units are split round-robin only: there the queue word, polled by every warp of the
-// grid, costs more than the imbalance it removes.  Once the queue is in use,
-// each CTA counts itself in q[1] when all its warps are done, and the last CTA returns both
-// words to zero, so the next launch on the same queue (stream-ordered after this one, or a
-// CUDA-graph replay) starts from zero without a memset.  The launcher fills the split in the
+// grid, costs more than the imbalance it removes.  Once the queue is in use, each CTA counts
+// itself in q[1] when all its warps are done, and the last CTA returns both words to zero, so
+// the next launch on the same queue (stream-ordered after this one, or a CUDA-graph replay)
+// starts from zero without a memset.  The launcher fills the split in the
 // kernel's arguments, so the kernel reads it from the parameter bank rather than registers; a
 // kernel whose unit count only the device knows builds the split itself.
 struct WorkSplit {
@@ -276,90 +276,6 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
 __device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v)
 {
     asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
-}
-
-// ---- shared memory, mbarrier and bulk-copy (TMA) primitives
-
-__device__ __forceinline__ uint32_t smem_addr(const void* p)
-{
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr)
-{
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-    return v;
-}
-
-__device__ __forceinline__ float ld_shared_f32(uint32_t addr)
-{
-    float v;
-    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
-    return v;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
-}
-
-// make barrier initialisation visible to the async (bulk-copy) proxy
-__device__ __forceinline__ void fence_barrier_init()
-{
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-// order this thread's generic-proxy shared-memory accesses before later async-proxy ones
-__device__ __forceinline__ void fence_proxy_async_shared()
-{
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
-{
-    uint32_t done;
-    asm volatile("{\n\t.reg .pred p;\n\t"
-                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-                 "selp.u32 %0, 1, 0, p;\n\t}"
-                 : "=r"(done) : "r"(bar), "r"(parity) : "memory");
-    return done != 0;
-}
-
-// Bounded wait for the phase of parity `parity`; false (and a recorded status) on expiry.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* status)
-{
-    for (int it = 0; it < kSpinLimit; ++it)
-        if (mbar_try_wait(bar, parity)) return true;
-    record_status(status, EP_ERR_DEVICE_TIMEOUT);
-    return false;
-}
-
-// 1-D bulk copy global -> shared, completion counted in bytes on an mbarrier.  Both addresses
-// 16-byte aligned, size a multiple of 16.
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                 :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
-}
-
-// 4-byte asynchronous copy global -> shared (for rows too short or unaligned for a bulk copy)
-__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src)
-{
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" :: "r"(dst), "l"(src) : "memory");
-}
-
-// the mbarrier receives one arrival once all of this thread's earlier cp.async copies land
-__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar)
-{
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(bar) : "memory");
 }
 
 // ---- FP8 e4m3 block quantisation (one FP32 scale per 128 elements)
