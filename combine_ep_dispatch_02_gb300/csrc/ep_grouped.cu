@@ -19,8 +19,8 @@
 //   ep_grouped_copy_kernel warp per received row: the row is read once and written to the slot
 //                         of each of its local experts;
 //   ep_ungroup_kernel     warp per received row: its local experts' output rows, ordered by
-//                         expert id, are loaded together and folded in FP32, with 8 loads per
-//                         lane in flight however many local experts the row has.
+//                         expert id, are loaded together and folded in FP32, with 4 to 8 loads
+//                         per lane in flight however many local experts the row has.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -282,8 +282,10 @@ __device__ __forceinline__ uint4 pack8(const float (&acc)[8])
 }
 
 // Rolling fold of nd <= R rows of hv 16-byte vectors into dst: each lane keeps the next D columns
-// of every row in flight, R * D = 8 loads, so a row with few local experts still keeps as many
-// bytes outstanding as one with many.  Each column's rows are added in ascending order.
+// of every row in flight, R * D = 4 loads for rows of up to four local experts and 8 above, so a
+// row with few local experts still keeps as many bytes outstanding as one with many.  Each
+// column's rows are added in ascending order.  (Eight columns ahead for a single-expert row needs
+// about 200 registers; four fit two 8-warp CTAs per SM, which hides more latency.)
 // Entries are found by their rank among the row's valid entries (rank0 / rank1 of lane j belong
 // to top-k entries j and j + 32, whose packed rows are dest0 / dest1).
 template <bool FP16, int R, int D>
@@ -326,7 +328,7 @@ __device__ __forceinline__ void fold_rd(const uint4* y4, int64_t dest0, int64_t 
 }
 
 template <bool FP16, bool WIDE>
-__global__ void __launch_bounds__(kCopyThreads, 1) ep_ungroup_kernel(const GroupArgs a)
+__global__ void __launch_bounds__(kCopyThreads, 2) ep_ungroup_kernel(const GroupArgs a)
 {
     __shared__ int s_off[kMaxRanks + 1];
     if (threadIdx.x == 0) {
@@ -371,11 +373,11 @@ __global__ void __launch_bounds__(kCopyThreads, 1) ep_ungroup_kernel(const Group
             // the rows in ascending expert order, once per received row; then a rolling fold:
             // row d's next columns are requested as soon as its current one is taken
             if (nd <= 1)
-                fold_rd<FP16, 1, 8>(y4, dest0, dest1, rank0, rank1, nd, hv, dst, lane);
+                fold_rd<FP16, 1, 4>(y4, dest0, dest1, rank0, rank1, nd, hv, dst, lane);
             else if (nd == 2)
-                fold_rd<FP16, 2, 4>(y4, dest0, dest1, rank0, rank1, nd, hv, dst, lane);
+                fold_rd<FP16, 2, 2>(y4, dest0, dest1, rank0, rank1, nd, hv, dst, lane);
             else if (nd <= 4)
-                fold_rd<FP16, 4, 2>(y4, dest0, dest1, rank0, rank1, nd, hv, dst, lane);
+                fold_rd<FP16, 4, 1>(y4, dest0, dest1, rank0, rank1, nd, hv, dst, lane);
             else
                 fold_rd<FP16, 8, 1>(y4, dest0, dest1, rank0, rank1, nd, hv, dst, lane);
             continue;
