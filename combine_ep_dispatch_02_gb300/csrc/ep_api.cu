@@ -29,6 +29,8 @@ struct ep_plan {
     int32_t* fwd;
     int32_t* recv_count;
     int32_t* expert_map;
+    int32_t* scan_cnt;            // two-pass grouping scan counts, or NULL
+    int scan_chunks;
     unsigned long long* flags;
     unsigned long long* ticket;
     unsigned long long* queues;   // kQueues work queues of two words each, after the ticket
@@ -65,9 +67,19 @@ bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 struct Layout {
-    size_t recv_x, recv_idx, recv_w, recv_scales, src_pos, fwd, recv_count, expert_map, flags, ticket,
-        status, total;
+    size_t recv_x, recv_idx, recv_w, recv_scales, src_pos, fwd, scan_cnt, recv_count, expert_map, flags,
+        ticket, status, total;
 };
+
+// 1024-row chunks of a rank's receive capacity when the grouping scan runs in two passes (three
+// chunks or more, per-chunk counts within kScanMaxBytes), else 0
+int64_t scan_chunks_of(int W, int E, int64_t rows)
+{
+    const int64_t chunks = (rows + kScanChunk - 1) / kScanChunk;
+    if (chunks < kScanMinChunks) return 0;
+    const int64_t bytes = (int64_t)W * E * chunks * W * 4;
+    return bytes <= kScanMaxBytes ? chunks : 0;
+}
 
 // bytes of one RECEIVED payload row (0 for an unknown dtype)
 int64_t row_bytes_of(int dtype, int64_t H)
@@ -111,7 +123,7 @@ int check_shape(int W, int E, int k, int H, int dtype, int sd, int M)
     return EP_OK;
 }
 
-Layout layout_of(int W, int k, int H, int dtype, int sd, int M)
+Layout layout_of(int W, int E, int k, int H, int dtype, int sd, int M)
 {
     Layout L{};
     const size_t rows = (size_t)W * M;
@@ -128,6 +140,7 @@ Layout layout_of(int W, int k, int H, int dtype, int sd, int M)
     put(L.recv_scales, (size_t)W * rows * sd * 4);
     put(L.src_pos, (size_t)W * rows * 4);
     put(L.fwd, rows * F * 4);
+    put(L.scan_cnt, (size_t)W * E * scan_chunks_of(W, E, (int64_t)rows) * W * 4);
     put(L.recv_count, (size_t)W * 4);
     put(L.expert_map, (size_t)W * rows * k * 4);
     put(L.flags, (size_t)tiles * W * 8);
@@ -212,7 +225,7 @@ size_t ep_plan_device_bytes(int W, int E, int k, int H, int dtype, int sd, int M
     const int rc = check_shape(W, E, k, H, dtype, sd, M);
     memcpy(g_err, saved, sizeof g_err);
     if (rc != EP_OK) return 0;
-    return layout_of(W, k, H, dtype, effective_sd(dtype, H, sd), M).total;
+    return layout_of(W, E, k, H, dtype, effective_sd(dtype, H, sd), M).total;
 }
 
 int ep_plan_create(ep_plan** out, int W, int E, int k, int H, int dtype, int sd, int M)
@@ -240,7 +253,7 @@ int ep_plan_create(ep_plan** out, int W, int E, int k, int H, int dtype, int sd,
     p->sd = sd;
     p->quantise = quantising(dtype);
     p->fp4 = dtype == EP_BF16_TO_MXFP4;
-    const Layout L = layout_of(W, k, H, dtype, sd, M);
+    const Layout L = layout_of(W, E, k, H, dtype, sd, M);
     p->bytes = L.total;
     e = cudaMalloc(&p->base, L.total);
     if (e != cudaSuccess) {
@@ -257,6 +270,8 @@ int ep_plan_create(ep_plan** out, int W, int E, int k, int H, int dtype, int sd,
     p->fwd = (int32_t*)(b + L.fwd);
     p->recv_count = (int32_t*)(b + L.recv_count);
     p->expert_map = (int32_t*)(b + L.expert_map);
+    p->scan_chunks = (int)scan_chunks_of(W, E, p->rows);
+    p->scan_cnt = p->scan_chunks ? (int32_t*)(b + L.scan_cnt) : nullptr;
     p->flags = (unsigned long long*)(b + L.flags);
     p->ticket = (unsigned long long*)(b + L.ticket);
     p->queues = p->ticket + 1;
@@ -568,6 +583,7 @@ int ep_group_by_expert(ep_plan* p, void* packed_x, int32_t* packed_count, int32_
     a.map = p->expert_map; a.packed_x = (uint8_t*)packed_x; a.count = packed_count;
     a.src_info = packed_src_info; a.layout_range = (long long*)layout_range;
     a.rows = p->rows; a.row_bytes = p->row_bytes; a.W = p->W; a.E = p->E; a.k = p->k;
+    a.scan_cnt = p->scan_cnt; a.scan_chunks = p->scan_chunks;
     cudaError_t e = launch_group(a, p->num_sms, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "ep_group_by_expert: launch");
     p->grouped_epoch = epoch;
@@ -603,6 +619,7 @@ int ep_dispatch_grouped(ep_plan* p, const void* x, const float* weights, const f
     a.recv_idx_out = p->recv_idx; a.recv_w_out = p->recv_w; a.recv_scales_out = p->recv_scales;
     a.rows = p->rows; a.row_bytes = p->row_bytes;
     a.W = p->W; a.E = p->E; a.k = p->k; a.M = p->M; a.F = p->F; a.N = p->N; a.sd = p->sd;
+    a.scan_cnt = p->scan_cnt; a.scan_chunks = p->scan_chunks;
     const int ce = pick_chunk_elems(p, p->N);          // rows sliced as the payload scatter's
     a.chunk_bytes = ce * p->elem_bytes;
     a.chunks = (int)((p->H + ce - 1) / ce);

@@ -8,6 +8,8 @@
 //   src_pos      [W][W*M]      reverse map: src_rank * (W*M) + src_token
 //   fwd          [W][M][F]     forward map, F = min(W, k): the receive rows of token (s,t) as
 //                              r * (W*M) + slot, in ascending destination rank, -1 padded
+//   scan_cnt     [W*E][chunks][W]  grouping scan: hits of a 1024-row chunk per source rank,
+//                              present when a rank's capacity spans kScanMinChunks chunks or more
 //   recv_count   [W]
 //   expert_map   [W][W*M][k]   slot of a received row in its local experts' lists (grouped view)
 //   flags        [tiles][W]    decoupled-lookback scan words of the routing kernel
@@ -29,6 +31,9 @@ constexpr int kMaxTopk = 64;        // two 32-slot batches
 constexpr int kRouteTile = 256;     // tokens per routing CTA, one per thread
 constexpr int kRouteThreads = 256;
 constexpr int kCopyThreads = 256;   // scatter, wire and grouped-view CTAs: 8 warps, a work unit per warp
+constexpr int kScanChunk = 1024;    // received rows per step of the grouping scan (4 per thread)
+constexpr int kScanMinChunks = 3;   // capacities of this many chunks or more are scanned in two passes
+constexpr long long kScanMaxBytes = 64ll << 20;   // ... when their per-chunk counts fit in this
 
 // Scan flag word: [63:34] call stamp (30 bits) | [33:32] status | [31:0] count.
 constexpr unsigned long long kFlagAggregate = 1ull;   // count = this tile's own total
@@ -168,6 +173,8 @@ struct GroupArgs {
     float* recv_scales_out;
     WorkSplit work;              // grouped copy / fused dispatch: q set by the caller
     int vec16;                   // the index rows grouping reads are 16-byte aligned (k % 4 == 0)
+    int32_t* scan_cnt;           // [W*E][scan_chunks][W] plan-owned, or NULL: one-pass scan
+    int scan_chunks;             // ceil(W*M / kScanChunk) when scan_cnt is set, else 0
     int64_t rows;                // W*M
     int64_t row_bytes;           // payload bytes (grouping) / 16-bit row bytes (inverse)
     int W, E, k, M, F, N, sd;

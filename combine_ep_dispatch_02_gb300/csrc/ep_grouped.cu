@@ -16,6 +16,10 @@
 //                         expert); writes src_info, the count, the layout ranges, and each row's
 //                         slot into the plan's map [W][W*M][k] at the row's first top-k entry
 //                         naming the expert;
+//   ep_group_count_kernel / ep_group_assign_kernel  the same scan in two passes over
+//                         (rank, local expert, 1024-row chunk) CTAs, for capacities of three
+//                         chunks or more: per-chunk hits by source rank, then slots from the
+//                         hits of earlier chunks;
 //   ep_grouped_copy_kernel warp per received row: the row is read once and written to the slot
 //                         of each of its local experts;
 //   ep_ungroup_kernel     warp per received row: its local experts' output rows, ordered by
@@ -60,6 +64,77 @@ __device__ __forceinline__ int first_entry(const int32_t* ids, int k, int32_t ge
     return jf;
 }
 
+static_assert(kScanChunk == 256 * kGroupRowsPerThread, "a scan step is 256 threads x 4 rows");
+
+// The rows i0 + q*256 + tid (q < 4) of rank r: pos = the row's src_pos entry and jfirst = its
+// first top-k entry naming global expert ge, or -1 (also for rows i >= n).
+template <int VEC>
+__device__ __forceinline__ void load_chunk(const GroupArgs& a, int r, int n, int i0, int32_t ge, int tid,
+                                           int (&pos)[kGroupRowsPerThread], int (&jfirst)[kGroupRowsPerThread])
+{
+#pragma unroll
+    for (int q = 0; q < kGroupRowsPerThread; ++q) {
+        const int i = i0 + q * 256 + tid;
+        pos[q] = i < n ? __ldg(a.src_pos + (int64_t)r * a.rows + i) : 0;
+    }
+#pragma unroll
+    for (int q = 0; q < kGroupRowsPerThread; ++q) {
+        const int i = i0 + q * 256 + tid;
+        jfirst[q] = -1;
+        if (i < n) {
+            const int32_t* ids;
+            if (a.src_idx) {    // fused dispatch: the row's index row is its source's
+                const int64_t s = pos[q] / a.rows;
+                ids = a.src_idx + (s * a.M + (pos[q] - s * a.rows)) * a.k;
+            } else {
+                ids = a.recv_idx + ((int64_t)r * a.rows + i) * a.k;
+            }
+            jfirst[q] = first_entry<VEC>(ids, a.k, ge);
+        }
+    }
+}
+
+// Slots of one chunk's hits, base + the hits before the row in the chunk (rows in order of
+// (q, warp, lane)): writes src_info and the row's map entry.  Leaves the chunk's hit count in
+// *total; s_warp is the CTA's [4][8] scratch; one __syncthreads inside.
+__device__ __forceinline__ void assign_chunk(const GroupArgs& a, int r, int64_t list, int i0, int base,
+                                             const int (&pos)[kGroupRowsPerThread],
+                                             const int (&jfirst)[kGroupRowsPerThread],
+                                             int (*s_warp)[8], int tid, int* total)
+{
+    constexpr int Q = kGroupRowsPerThread;
+    const int lane = tid & 31, warp = tid >> 5;
+    unsigned bal[Q];
+#pragma unroll
+    for (int q = 0; q < Q; ++q) {
+        bal[q] = __ballot_sync(0xffffffffu, jfirst[q] >= 0);
+        if (lane == 0) s_warp[q][warp] = __popc(bal[q]);
+    }
+    __syncthreads();
+    int run = base, tot = 0;
+    int before[Q];
+#pragma unroll
+    for (int q = 0; q < Q; ++q) {
+        before[q] = run;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+            if (w < warp) before[q] += s_warp[q][w];
+            run += s_warp[q][w];
+            tot += s_warp[q][w];
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < Q; ++q) {
+        if (jfirst[q] >= 0) {
+            const int i = i0 + q * 256 + tid;
+            const int slot = before[q] + __popc(bal[q] & lanemask_lt());
+            a.src_info[list * a.rows + slot] = (int32_t)(pos[q] % a.rows);
+            a.map[((int64_t)r * a.rows + i) * a.k + jfirst[q]] = slot;
+        }
+    }
+    *total = tot;
+}
+
 template <int VEC>
 __global__ void __launch_bounds__(256) ep_group_kernel(const GroupArgs a)
 {
@@ -67,7 +142,7 @@ __global__ void __launch_bounds__(256) ep_group_kernel(const GroupArgs a)
     __shared__ int s_warp[Q][8];
     __shared__ int s_src[kMaxRanks];
     __shared__ int s_base;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x;
     const int r = blockIdx.x / a.E;
     const int e = blockIdx.x - r * a.E;
     const int32_t ge = r * a.E + e;
@@ -76,57 +151,14 @@ __global__ void __launch_bounds__(256) ep_group_kernel(const GroupArgs a)
     if (tid < kMaxRanks) s_src[tid] = 0;
     if (tid == 0) s_base = 0;
     __syncthreads();
-    for (int i0 = 0; i0 < n; i0 += 256 * Q) {
+    for (int i0 = 0; i0 < n; i0 += kScanChunk) {
         int jfirst[Q], pos[Q];
+        load_chunk<VEC>(a, r, n, i0, ge, tid, pos, jfirst);
+        int total;
+        assign_chunk(a, r, list, i0, s_base, pos, jfirst, s_warp, tid, &total);
 #pragma unroll
-        for (int q = 0; q < Q; ++q) {
-            const int i = i0 + q * 256 + tid;
-            pos[q] = i < n ? __ldg(a.src_pos + (int64_t)r * a.rows + i) : 0;
-        }
-#pragma unroll
-        for (int q = 0; q < Q; ++q) {
-            const int i = i0 + q * 256 + tid;
-            jfirst[q] = -1;
-            if (i < n) {
-                const int32_t* ids;
-                if (a.src_idx) {    // fused dispatch: the row's index row is its source's
-                    const int64_t s = pos[q] / a.rows;
-                    ids = a.src_idx + (s * a.M + (pos[q] - s * a.rows)) * a.k;
-                } else {
-                    ids = a.recv_idx + ((int64_t)r * a.rows + i) * a.k;
-                }
-                jfirst[q] = first_entry<VEC>(ids, a.k, ge);
-            }
-        }
-        unsigned bal[Q];
-#pragma unroll
-        for (int q = 0; q < Q; ++q) {
-            bal[q] = __ballot_sync(0xffffffffu, jfirst[q] >= 0);
-            if (lane == 0) s_warp[q][warp] = __popc(bal[q]);
-        }
-        __syncthreads();
-        int run = s_base, total = 0;
-        int before[Q];
-#pragma unroll
-        for (int q = 0; q < Q; ++q) {
-            before[q] = run;
-#pragma unroll
-            for (int w = 0; w < 8; ++w) {
-                if (w < warp) before[q] += s_warp[q][w];
-                run += s_warp[q][w];
-                total += s_warp[q][w];
-            }
-        }
-#pragma unroll
-        for (int q = 0; q < Q; ++q) {
-            if (jfirst[q] >= 0) {
-                const int i = i0 + q * 256 + tid;
-                const int slot = before[q] + __popc(bal[q] & lanemask_lt());
-                a.src_info[list * a.rows + slot] = (int32_t)(pos[q] % a.rows);
-                a.map[((int64_t)r * a.rows + i) * a.k + jfirst[q]] = slot;
-                atomicAdd(&s_src[pos[q] / a.rows], 1);
-            }
-        }
+        for (int q = 0; q < Q; ++q)
+            if (jfirst[q] >= 0) atomicAdd(&s_src[pos[q] / a.rows], 1);
         __syncthreads();
         if (tid == 0) s_base += total;
         __syncthreads();
@@ -136,6 +168,83 @@ __global__ void __launch_bounds__(256) ep_group_kernel(const GroupArgs a)
         long long first = 0;
         for (int s = 0; s < tid; ++s) first += s_src[s];
         a.layout_range[list * a.W + tid] = (first << 32) | (long long)s_src[tid];
+    }
+}
+
+// Two-pass scan, pass 1: grid (W*E lists) x (chunk strides); CTA (list, y) takes chunks y,
+// y + gridDim.y, ... below the rank's received rows and stores each chunk's hits per source
+// rank in scan_cnt[list][c][s].  Nothing else is written, and no CTA waits on another.
+template <int VEC>
+__global__ void __launch_bounds__(256) ep_group_count_kernel(const GroupArgs a)
+{
+    constexpr int Q = kGroupRowsPerThread;
+    __shared__ int s_src[kMaxRanks];
+    const int tid = threadIdx.x;
+    const int r = blockIdx.x / a.E;
+    const int e = blockIdx.x - r * a.E;
+    const int32_t ge = r * a.E + e;
+    const int64_t list = (int64_t)r * a.E + e;
+    const int n = a.recv_count[r];
+    for (int c = blockIdx.y; (int64_t)c * kScanChunk < n; c += gridDim.y) {
+        if (tid < kMaxRanks) s_src[tid] = 0;
+        __syncthreads();
+        int jfirst[Q], pos[Q];
+        load_chunk<VEC>(a, r, n, c * kScanChunk, ge, tid, pos, jfirst);
+#pragma unroll
+        for (int q = 0; q < Q; ++q)
+            if (jfirst[q] >= 0) atomicAdd(&s_src[pos[q] / a.rows], 1);
+        __syncthreads();
+        if (tid < a.W) a.scan_cnt[(list * a.scan_chunks + c) * a.W + tid] = s_src[tid];
+        __syncthreads();
+    }
+}
+
+// Pass 2, the same grid: chunk c's base is the sum of scan_cnt over chunks 0..c-1 (all sources),
+// and its rows get slots as in the one-pass scan.  The y = 0 CTA of each list also sums every
+// chunk's counts per source into the count and the layout ranges (zeros for a rank that
+// received nothing).  Pass 1 has finished before any of this runs (stream order).
+template <int VEC>
+__global__ void __launch_bounds__(256) ep_group_assign_kernel(const GroupArgs a)
+{
+    constexpr int Q = kGroupRowsPerThread;
+    __shared__ int s_warp[Q][8];
+    __shared__ int s_part[8];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int r = blockIdx.x / a.E;
+    const int e = blockIdx.x - r * a.E;
+    const int32_t ge = r * a.E + e;
+    const int64_t list = (int64_t)r * a.E + e;
+    const int n = a.recv_count[r];
+    const int active = (int)(((int64_t)n + kScanChunk - 1) / kScanChunk);
+    const int32_t* cnt = a.scan_cnt + list * a.scan_chunks * a.W;
+    if (blockIdx.y == 0 && warp == 0) {       // lane s: source rank s (W <= 32)
+        int tot = 0;
+        if (lane < a.W)
+            for (int c = 0; c < active; ++c) tot += cnt[c * a.W + lane];
+        int incl = tot;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl += v;
+        }
+        if (lane < a.W) a.layout_range[list * a.W + lane] = ((long long)(incl - tot) << 32) | (long long)tot;
+        if (lane == 31) a.count[list] = incl;
+    }
+    for (int c = blockIdx.y; c < active; c += gridDim.y) {
+        int part = 0;
+        for (int v = tid; v < c * a.W; v += 256) part += cnt[v];
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) part += __shfl_xor_sync(0xffffffffu, part, d);
+        if (lane == 0) s_part[warp] = part;
+        int jfirst[Q], pos[Q];
+        load_chunk<VEC>(a, r, n, c * kScanChunk, ge, tid, pos, jfirst);
+        __syncthreads();
+        int base = 0;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) base += s_part[w];
+        int total;
+        assign_chunk(a, r, list, c * kScanChunk, base, pos, jfirst, s_warp, tid, &total);
+        __syncthreads();                      // s_part and s_warp are reused by the next chunk
     }
 }
 
@@ -503,23 +612,39 @@ int grid_of(const void* kernel, int64_t warps, int num_sms)
 
 }  // namespace
 
-// compiled index-row widths: top-k 4, 8 (the pages' specialised case), 16; others loop
-static void launch_group_scan(const GroupArgs& a, cudaStream_t stream)
+template <int VEC>
+static void launch_group_scan_t(const GroupArgs& a, int num_sms, cudaStream_t stream)
 {
-    const int grid = a.W * a.E;
+    if (!a.scan_cnt) {
+        ep_group_kernel<VEC><<<a.W * a.E, 256, 0, stream>>>(a);
+        return;
+    }
+    // about 16 CTAs per SM in all; a CTA takes every gridDim.y-th chunk of its list
+    const int per = 16 * num_sms / (a.W * a.E);
+    int gy = per > 1 ? per : 1;
+    if (gy > a.scan_chunks) gy = a.scan_chunks;
+    if (gy > 65535) gy = 65535;
+    const dim3 grid(a.W * a.E, gy);
+    ep_group_count_kernel<VEC><<<grid, 256, 0, stream>>>(a);
+    ep_group_assign_kernel<VEC><<<grid, 256, 0, stream>>>(a);
+}
+
+// compiled index-row widths: top-k 4, 8 (the pages' specialised case), 16; others loop
+static void launch_group_scan(const GroupArgs& a, int num_sms, cudaStream_t stream)
+{
     if (!a.vec16 || (a.k != 4 && a.k != 8 && a.k != 16))
-        ep_group_kernel<0><<<grid, 256, 0, stream>>>(a);
+        launch_group_scan_t<0>(a, num_sms, stream);
     else if (a.k == 4)
-        ep_group_kernel<1><<<grid, 256, 0, stream>>>(a);
+        launch_group_scan_t<1>(a, num_sms, stream);
     else if (a.k == 8)
-        ep_group_kernel<2><<<grid, 256, 0, stream>>>(a);
+        launch_group_scan_t<2>(a, num_sms, stream);
     else
-        ep_group_kernel<4><<<grid, 256, 0, stream>>>(a);
+        launch_group_scan_t<4>(a, num_sms, stream);
 }
 
 cudaError_t launch_group_from_source(const GroupArgs& a, int num_sms, cudaStream_t stream)
 {
-    launch_group_scan(a, stream);
+    launch_group_scan(a, num_sms, stream);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || a.N == 0) return e;
     const int64_t units = (int64_t)a.N * a.chunks;
@@ -532,7 +657,7 @@ cudaError_t launch_group_from_source(const GroupArgs& a, int num_sms, cudaStream
 
 cudaError_t launch_group(const GroupArgs& a, int num_sms, cudaStream_t stream)
 {
-    launch_group_scan(a, stream);
+    launch_group_scan(a, num_sms, stream);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int64_t units = (int64_t)a.W * a.rows;

@@ -35,25 +35,33 @@ def _align(v):
     return (v + 255) // 256 * 256
 
 
+def _scan_bytes(W, E, M):
+    # grouping scan counts [W*E][chunks][W] int32, for three or more 1024-row chunks of capacity,
+    # up to 64 MiB
+    chunks = -(-(W * M) // 1024)
+    b = W * E * chunks * W * 4
+    return b if chunks >= 3 and b <= 64 << 20 else 0
+
+
 def _layout_bytes(W, E, k, H, eb, sd, M):
     rows = W * M
     F = min(W, k)
     tiles = -(-rows // 256)
     parts = [W * rows * H * eb, W * rows * k * 4, W * rows * k * 4, W * rows * sd * 4, W * rows * 4,
-             rows * F * 4, W * 4, W * rows * k * 4, tiles * W * 8, 8, 4]
+             rows * F * 4, _scan_bytes(W, E, M), W * 4, W * rows * k * 4, tiles * W * 8, 8, 4]
     return sum(_align(p) for p in parts)
 
 
 def test_device_bytes_golden(lib):
     # DeepSeek-V3 shape: recv rows 8 * 32768 * 14336 B, index / weight rows 8 MiB each,
-    # src_pos and forward map 1 MiB each, the expert-slot map 8 MiB, 128 tiles * 8 scan words,
-    # three control words
-    assert lib.ep_plan_device_bytes(8, 32, 8, 7168, ep.EP_BF16, 0, 4096) == 3785368320
+    # src_pos and forward map 1 MiB each, grouping scan counts 256 lists * 32 chunks * 8 sources
+    # * 4 B, the expert-slot map 8 MiB, 128 tiles * 8 scan words, three control words
+    assert lib.ep_plan_device_bytes(8, 32, 8, 7168, ep.EP_BF16, 0, 4096) == 3785630464
     # FP8 with 56 scales per row
     assert lib.ep_plan_device_bytes(8, 96, 6, 7168, ep.EP_FP8_E4M3, 56, 4096) == \
         _layout_bytes(8, 96, 6, 7168, 1, 56, 4096)
     for shape in [(2, 4, 2, 256, 0, 0, 64), (4, 64, 64, 2048, 1, 0, 512), (1, 1, 1, 8, 0, 0, 1),
-                  (32, 8, 64, 16, 2, 3, 100)]:
+                  (32, 8, 64, 16, 2, 3, 100), (2, 1 << 20, 2, 16, 0, 0, 4096)]:
         W, E, k, H, dt, sd, M = shape
         eb = 1 if dt == ep.EP_FP8_E4M3 else 2
         assert lib.ep_plan_device_bytes(*shape) == _layout_bytes(W, E, k, H, eb, sd, M), shape
@@ -114,6 +122,8 @@ def test_mxfp4_dtype_sizes(lib):
     for sd in (0, 56):
         assert lib.ep_plan_device_bytes(8, 32, 8, 7168, ep.EP_BF16_TO_MXFP4, sd, 4096) == \
             _layout_bytes(8, 32, 8, 3584, 1, 56, 4096)
-    # DeepSeek-V3 shape: 8 * 32768 rows of 3584 code bytes, scale rows of 224 bytes
+    # DeepSeek-V3 shape: 8 * 32768 rows of 3584 code bytes, scale rows of 224 bytes, and the
+    # grouping scan's 256 * 32 * 8 counts
     assert lib.ep_plan_device_bytes(8, 32, 8, 7168, ep.EP_BF16_TO_MXFP4, 0, 4096) == \
-        8 * 32768 * 3584 + 3 * (8 << 20) + 8 * 32768 * 224 + 2 * (1 << 20) + 256 + 8192 + 256 + 256
+        8 * 32768 * 3584 + 3 * (8 << 20) + 8 * 32768 * 224 + 2 * (1 << 20) + 256 * 32 * 8 * 4 + \
+        256 + 8192 + 256 + 256

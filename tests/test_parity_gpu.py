@@ -830,6 +830,54 @@ def test_grouped_layout_work_queue():
     _check_grouped(wl, fused=True, repeats=2)
 
 
+def _chunk_edge_workload(k):
+    """Receive capacity 4 * 1100 rows, five 1024-row chunks, so grouping scans in two passes.
+    Rank 0 receives all 3300 tokens (a ragged last chunk, up to three local experts a row),
+    rank 1 exactly 2048 (two full chunks; sources 2 and 3 send it nothing; its expert 2 gets
+    no row), rank 2 1025 (source 0 sends it nothing, source 2 has no tokens) and rank 3
+    nothing.  Some rows name the same expert twice."""
+    W, E, M = 4, 3, 1100
+    wl = wlmod.custom_workload(W=W, E=E, k=k, H=64, M=M, n_tok=[M, M, 0, M], seed=21)
+    g = 0
+    for s in (0, 1, 3):
+        for t in range(M):
+            row = [g % 3]                                        # rank 0
+            if g < 2048:
+                row.append(E + (g // 7) % 2)                     # rank 1, experts 0 and 1
+            elif g < 2048 + 1025:
+                row.append(2 * E + g % 3)                        # rank 2
+            else:
+                row.append((g + 1) % 3)                          # rank 0 again
+            row.append(row[0] if g % 5 == 0 else (g + 2) % 3)    # a repeat, or rank 0
+            wl.indices[s, t] = [row[j % 3] for j in range(k)]
+            g += 1
+    return wl
+
+
+@pytest.mark.parametrize("k", [3, 8])
+def test_grouped_layout_chunked_scan(k):
+    """The two-pass grouping scan at its chunk edges: empty ranks and sources, a rank whose
+    rows end exactly on a chunk boundary and one a row past it, repeated ids; the one-row
+    index loop (top-k 3) and the 16-byte-vector one (top-k 8)."""
+    wl = _chunk_edge_workload(k)
+    disp = oracle.dispatch(wl.W, wl.E, wl.k, wl.H, wl.elem_bytes, wl.sd, wl.M, wl.x, wl.weights,
+                           wl.scales, wl.indices, wl.n_tok)
+    assert list(disp["recv_count"]) == [3300, 2048, 1025, 0]
+    _check_grouped(wl, repeats=2)
+    _check_grouped(wl, fused=True, repeats=2)
+
+
+def test_grouped_layout_chunk_strides():
+    """More chunks than the scan grid's chunk stride: 512 lists take every fourth chunk of the
+    12 (about 5 with rows), and 2500 lists one CTA per list for every chunk."""
+    wl = wlmod.custom_workload(W=8, E=64, k=4, H=16, M=1536, n_tok=[1536] * 8, seed=22)
+    _check_grouped(wl, repeats=2)
+    _check_grouped(wl, fused=True)
+    wl = wlmod.custom_workload(W=2, E=1250, k=2, H=8, M=1536, n_tok=[1536, 1500], seed=23)
+    _check_grouped(wl)
+    _check_grouped(wl, fused=True)
+
+
 def test_grouped_layout_wide_rows():
     # hidden 2304 (288 16-byte vectors: nine full warp steps of 32 vectors) in BF16 and FP16,
     # grouped, fused and inverted
