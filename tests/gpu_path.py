@@ -96,7 +96,7 @@ def compare(wl, gpu, orc, o_out, o_w):
         g_pos = gpu["src_pos"][r, :n]
         o_pos = orc["src_pos"][r, :n]
         # compare through src_token_pos: the multiset of (source position, row content) must
-        # agree; this build's scan also fixes the order, so the rows line up one to one
+        # agree; the routing kernel's scan also fixes the order, so the rows line up one to one
         gi = np.argsort(g_pos, kind="stable")
         oi = np.argsort(o_pos, kind="stable")
         assert np.array_equal(g_pos[gi], o_pos[oi]), f"rank {r}: reverse map differs"
