@@ -61,10 +61,19 @@ def test_device_bytes_golden(lib):
     assert lib.ep_plan_device_bytes(8, 96, 6, 7168, ep.EP_FP8_E4M3, 56, 4096) == \
         _layout_bytes(8, 96, 6, 7168, 1, 56, 4096)
     for shape in [(2, 4, 2, 256, 0, 0, 64), (4, 64, 64, 2048, 1, 0, 512), (1, 1, 1, 8, 0, 0, 1),
-                  (32, 8, 64, 16, 2, 3, 100), (2, 1 << 20, 2, 16, 0, 0, 4096)]:
+                  (32, 8, 64, 16, 2, 3, 100), (2, 1 << 20, 2, 16, 0, 0, 4096),
+                  # grouping scan counts: 2048 rows are two chunks (none), 2049 three; at W=2 and
+                  # three chunks, 1398101 experts per rank need 67108848 B (kept) and one more
+                  # 67108896 B, past 64 MiB (none)
+                  (1, 1, 1, 8, 0, 0, 2048), (1, 1, 1, 8, 0, 0, 2049),
+                  (2, 1398101, 2, 8, 0, 0, 1536), (2, 1398102, 2, 8, 0, 0, 1536)]:
         W, E, k, H, dt, sd, M = shape
         eb = 1 if dt == ep.EP_FP8_E4M3 else 2
         assert lib.ep_plan_device_bytes(*shape) == _layout_bytes(W, E, k, H, eb, sd, M), shape
+    assert _scan_bytes(1, 1, 2048) == 0 and _scan_bytes(1, 1, 2049) == 12
+    assert _scan_bytes(2, 1398101, 1536) == 67108848 and _scan_bytes(2, 1398102, 1536) == 0
+    big = lib.ep_plan_device_bytes(2, 1398101, 2, 8, 0, 0, 1536)
+    assert big - lib.ep_plan_device_bytes(2, 1398102, 2, 8, 0, 0, 1536) == _align(67108848)
 
 
 @pytest.mark.parametrize("shape,why", [
