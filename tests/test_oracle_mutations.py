@@ -60,6 +60,20 @@ MUTATIONS = {
     # grouped inverse sums in list order of the last expert only
     "ungroup_overwrite": ("acc[i * H + h] = acc[i * H + h] + v;", "acc[i * H + h] = v;",
                           pins.test_ungroup_identity_closed_form),
+    # grouping: a source's first slot taken after its own rows (inclusive prefix)
+    "layout_first_inclusive": ("                layout_range[list * W + s] = (first << 32) | per_src[s];\n"
+                               "                first += per_src[s];",
+                               "                first += per_src[s];\n"
+                               "                layout_range[list * W + s] = (first << 32) | per_src[s];",
+                               pins.test_group_by_expert_brute_force),
+    # grouping: src_info keeps the source rank (the packed reverse-map entry, not the token)
+    "src_info_with_rank": ("packed_src_info[list * rows + slot] = (int32_t)(pos % rows);",
+                           "packed_src_info[list * rows + slot] = (int32_t)pos;",
+                           pins.test_group_by_expert_brute_force),
+    # grouping: only the last top-k entry is looked at
+    "group_last_entry_only": ("for (int j = 0; j < k; ++j) named |= ids[j] == ge;",
+                              "for (int j = 0; j < k; ++j) named = ids[j] == ge;",
+                              pins.test_group_by_expert_brute_force),
 }
 
 
