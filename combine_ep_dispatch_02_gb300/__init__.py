@@ -113,10 +113,12 @@ def route_noalloc(W: int, experts_per_rank: int, topk: int, max_tok_per_rank: in
     src_token_pos [W][W*M], recv_count [W], fwd_map [W][M][min(W,k)], device_status [1], all
     int32 on the current device."""
     arr = np.ascontiguousarray(np.asarray(n_tok, dtype=np.int32).reshape(W))
+    M, F = max_tok_per_rank, min(W, topk)
     _check(load_library().ep_route_noalloc(
-        W, experts_per_rank, topk, max_tok_per_rank, _ptr(indices),
-        arr.ctypes.data_as(ctypes.c_void_p), _ptr(src_token_pos), _ptr(recv_count), _ptr(fwd_map),
-        _ptr(device_status), _stream(stream)))
+        W, experts_per_rank, topk, max_tok_per_rank, _buf(indices, 4 * W * M * topk, "indices", 4),
+        arr.ctypes.data_as(ctypes.c_void_p), _buf(src_token_pos, 4 * W * W * M, "src_token_pos", 4),
+        _buf(recv_count, 4 * W, "recv_count", 4), _buf(fwd_map, 4 * W * M * F, "fwd_map", 4),
+        _buf(device_status, 4, "device_status", 4), _stream(stream)))
 
 
 class _DevPtr:
@@ -139,6 +141,24 @@ def _ptr(t: Optional[torch.Tensor]):
     if not t.is_cuda or not t.is_contiguous():
         raise ValueError("arguments must be contiguous CUDA tensors")
     return ctypes.c_void_p(t.data_ptr())
+
+
+def _buf(t: Optional[torch.Tensor], nbytes: int, what: str, itemsize: Optional[int] = None,
+         device: Optional[torch.device] = None):
+    """_ptr after the host checks the C ABI leaves to its caller: the tensor holds at least the
+    nbytes the call reads or writes, has itemsize-byte elements where the ABI fixes the type, and
+    lives on the plan's device.  A failed check raises EpError(EP_ERR_ARG) before any launch."""
+    if t is None:
+        return None
+    p = _ptr(t)
+    if device is not None and t.device != device:
+        raise EpError(EP_ERR_ARG, f"{what} is on {t.device}, the plan on {device}")
+    if itemsize is not None and t.element_size() != itemsize:
+        raise EpError(EP_ERR_ARG, f"{what} has {t.element_size()}-byte elements, the call takes {itemsize}")
+    have = t.numel() * t.element_size()
+    if have < nbytes:
+        raise EpError(EP_ERR_ARG, f"{what} holds {have} bytes, the call needs {nbytes}")
+    return p
 
 
 def _stream(stream) -> ctypes.c_void_p:
@@ -189,6 +209,9 @@ class Plan:
         # elements of payload_torch_dtype per received row (MX FP4 packs two codes per byte)
         self.row_elems = hidden // 2 if dtype == "bf16_mxfp4" else hidden
         self.combine_torch_dtype = torch.float16 if dtype == "fp16" else torch.bfloat16
+        self._in_bytes = 1 if dtype == "fp8" else 2            # bytes of one caller x element
+        self._row_bytes = {"bf16": 2 * hidden, "fp16": 2 * hidden, "fp8": hidden, "bf16_fp8": hidden,
+                           "bf16_mxfp4": hidden // 2}[dtype]   # bytes of one received payload row
 
     # -- lifetime
     def close(self):
@@ -212,6 +235,24 @@ class Plan:
         _check(self._lib.ep_plan_set_variant(self._h, VARIANTS[variant]))
 
     # -- calls
+    def _arg(self, t, nbytes, what, itemsize=None):
+        return _buf(t, nbytes, what, itemsize, self.device)
+
+    def _source_args(self, x, weights, scales, indices):
+        """Pointers of dispatch's [W][M][...] inputs, checked against the plan's shape."""
+        W, M, k, H = self.W, self.M, self.k, self.H
+        sd = 0 if self.dtype in ("bf16_fp8", "bf16_mxfp4") else self.sd
+        return (self._arg(x, W * M * H * self._in_bytes, "x", self._in_bytes),
+                self._arg(weights, 4 * W * M * k, "weights", 4),
+                self._arg(scales, 4 * W * M * sd, "scales", 4),
+                self._arg(indices, 4 * W * M * k, "indices", 4))
+
+    def _combine_outs(self, weights, out, out_w):
+        """Pointers of a combine's received weights [W][W*M][k] and outputs [W][M][H], [W][M][k]."""
+        W, M, k = self.W, self.M, self.k
+        return (self._arg(weights, 4 * W * self.rows * k, "weights", 4),
+                self._arg(out, 2 * W * M * self.H, "out", 2), self._arg(out_w, 4 * W * M * k, "out_w", 4))
+
     def _n_tok(self, n_tok: Sequence[int]):
         arr = np.ascontiguousarray(np.asarray(n_tok, dtype=np.int32).reshape(self.W))
         return arr, arr.ctypes.data_as(ctypes.c_void_p)
@@ -243,19 +284,20 @@ class Plan:
         indices [W][M][k] int32, n_tok: W host ints."""
         arr, nt = self._n_tok(n_tok)
         o = DispatchOut()
-        _check(self._lib.ep_dispatch(self._h, _ptr(x), _ptr(weights), _ptr(scales), _ptr(indices),
+        _check(self._lib.ep_dispatch(self._h, *self._source_args(x, weights, scales, indices),
                                      nt, _stream(stream), ctypes.byref(o)))
         return self._wrap(o)
 
     def dispatch_route(self, indices: torch.Tensor, n_tok: Sequence[int], stream=None) -> Dispatched:
         arr, nt = self._n_tok(n_tok)
         o = DispatchOut()
-        _check(self._lib.ep_dispatch_route(self._h, _ptr(indices), nt, _stream(stream), ctypes.byref(o)))
+        idx = self._arg(indices, 4 * self.W * self.M * self.k, "indices", 4)
+        _check(self._lib.ep_dispatch_route(self._h, idx, nt, _stream(stream), ctypes.byref(o)))
         return self._wrap(o)
 
     def dispatch_scatter(self, x, weights, scales, indices, stream=None):
-        _check(self._lib.ep_dispatch_scatter(self._h, _ptr(x), _ptr(weights), _ptr(scales),
-                                             _ptr(indices), _stream(stream)))
+        _check(self._lib.ep_dispatch_scatter(self._h, *self._source_args(x, weights, scales, indices),
+                                             _stream(stream)))
 
     def combine(self, expert_out: torch.Tensor, weights: Optional[torch.Tensor], epoch: int,
                 out: Optional[torch.Tensor] = None, out_w: Optional[torch.Tensor] = None,
@@ -267,8 +309,9 @@ class Plan:
                               device=self.device)
         if out_w is None and weights is not None and want_weights:
             out_w = torch.zeros((self.W, self.M, self.k), dtype=torch.float32, device=self.device)
-        _check(self._lib.ep_combine(self._h, _ptr(expert_out), _ptr(weights), _ptr(out), _ptr(out_w),
-                                    ctypes.c_uint64(epoch), _stream(stream)))
+        _check(self._lib.ep_combine(self._h, self._arg(expert_out, 2 * self.W * self.rows * self.H, "expert_out", 2),
+                                    *self._combine_outs(weights, out, out_w), ctypes.c_uint64(epoch),
+                                    _stream(stream)))
         return out, out_w
 
     def quantize_received(self, expert_out: torch.Tensor, epoch: int, q: Optional[torch.Tensor] = None,
@@ -279,7 +322,9 @@ class Plan:
             q = torch.empty((self.W, self.rows, self.H), dtype=torch.uint8, device=self.device)
         if scales is None:
             scales = torch.empty((self.W, self.rows, self.H // 128), dtype=torch.float32, device=self.device)
-        _check(self._lib.ep_quantize_received(self._h, _ptr(expert_out), _ptr(q), _ptr(scales),
+        n = self.W * self.rows * self.H
+        _check(self._lib.ep_quantize_received(self._h, self._arg(expert_out, 2 * n, "expert_out", 2),
+                                              self._arg(q, n, "q", 1), self._arg(scales, 4 * (n // 128), "scales", 4),
                                               ctypes.c_uint64(epoch), _stream(stream)))
         return q.view(torch.float8_e4m3fn), scales
 
@@ -291,8 +336,10 @@ class Plan:
             out = torch.zeros((self.W, self.M, self.H), dtype=torch.bfloat16, device=self.device)
         if out_w is None and weights is not None and want_weights:
             out_w = torch.zeros((self.W, self.M, self.k), dtype=torch.float32, device=self.device)
-        _check(self._lib.ep_combine_fp8(self._h, _ptr(q), _ptr(scales), _ptr(weights), _ptr(out),
-                                        _ptr(out_w), ctypes.c_uint64(epoch), _stream(stream)))
+        n = self.W * self.rows * self.H
+        _check(self._lib.ep_combine_fp8(self._h, self._arg(q, n, "q", 1), self._arg(scales, 4 * (n // 128), "scales", 4),
+                                        *self._combine_outs(weights, out, out_w), ctypes.c_uint64(epoch),
+                                        _stream(stream)))
         return out, out_w
 
     def quantize_received_fp4(self, expert_out: torch.Tensor, epoch: int, q: Optional[torch.Tensor] = None,
@@ -303,7 +350,9 @@ class Plan:
             q = torch.empty((self.W, self.rows, self.H // 2), dtype=torch.uint8, device=self.device)
         if scales is None:
             scales = torch.empty((self.W, self.rows, self.H // 32), dtype=torch.uint8, device=self.device)
-        _check(self._lib.ep_quantize_received_fp4(self._h, _ptr(expert_out), _ptr(q), _ptr(scales),
+        n = self.W * self.rows * self.H
+        _check(self._lib.ep_quantize_received_fp4(self._h, self._arg(expert_out, 2 * n, "expert_out", 2),
+                                                  self._arg(q, n // 2, "q", 1), self._arg(scales, n // 32, "scales", 1),
                                                   ctypes.c_uint64(epoch), _stream(stream)))
         return q, scales
 
@@ -315,8 +364,10 @@ class Plan:
             out = torch.zeros((self.W, self.M, self.H), dtype=torch.bfloat16, device=self.device)
         if out_w is None and weights is not None and want_weights:
             out_w = torch.zeros((self.W, self.M, self.k), dtype=torch.float32, device=self.device)
-        _check(self._lib.ep_combine_fp4(self._h, _ptr(q), _ptr(scales), _ptr(weights), _ptr(out),
-                                        _ptr(out_w), ctypes.c_uint64(epoch), _stream(stream)))
+        n = self.W * self.rows * self.H
+        _check(self._lib.ep_combine_fp4(self._h, self._arg(q, n // 2, "q", 1), self._arg(scales, n // 32, "scales", 1),
+                                        *self._combine_outs(weights, out, out_w), ctypes.c_uint64(epoch),
+                                        _stream(stream)))
         return out, out_w
 
     def group_by_expert(self, epoch: int, packed_x: Optional[torch.Tensor] = None, stream=None):
@@ -329,8 +380,9 @@ class Plan:
         count = torch.empty((W, E), dtype=torch.int32, device=self.device)
         src_info = torch.empty((W, E, R), dtype=torch.int32, device=self.device)
         layout = torch.empty((W, E, W), dtype=torch.int64, device=self.device)
-        _check(self._lib.ep_group_by_expert(self._h, _ptr(packed_x), _ptr(count), _ptr(src_info),
-                                            _ptr(layout), ctypes.c_uint64(epoch), _stream(stream)))
+        _check(self._lib.ep_group_by_expert(self._h, self._arg(packed_x, W * E * R * self._row_bytes, "packed_x"),
+                                            _ptr(count), _ptr(src_info), _ptr(layout), ctypes.c_uint64(epoch),
+                                            _stream(stream)))
         return packed_x, count, src_info, layout
 
     def dispatch_grouped(self, x: torch.Tensor, weights: Optional[torch.Tensor],
@@ -347,9 +399,10 @@ class Plan:
         layout = torch.empty((W, E, W), dtype=torch.int64, device=self.device)
         arr, nt = self._n_tok(n_tok)
         o = DispatchOut()
-        _check(self._lib.ep_dispatch_grouped(self._h, _ptr(x), _ptr(weights), _ptr(scales), _ptr(indices),
-                                             nt, _ptr(packed_x), _ptr(count), _ptr(src_info), _ptr(layout),
-                                             _stream(stream), ctypes.byref(o)))
+        _check(self._lib.ep_dispatch_grouped(self._h, *self._source_args(x, weights, scales, indices), nt,
+                                             self._arg(packed_x, W * E * R * self._row_bytes, "packed_x"),
+                                             _ptr(count), _ptr(src_info), _ptr(layout), _stream(stream),
+                                             ctypes.byref(o)))
         return self._wrap(o), packed_x, count, src_info, layout
 
     def ungroup_by_expert(self, packed_y: torch.Tensor, epoch: int, out: Optional[torch.Tensor] = None,
@@ -358,7 +411,9 @@ class Plan:
         input [W][W*M][H] (BF16, FP16 for FP16 plans)."""
         if out is None:
             out = torch.empty((self.W, self.rows, self.H), dtype=self.combine_torch_dtype, device=self.device)
-        _check(self._lib.ep_ungroup_by_expert(self._h, _ptr(packed_y), _ptr(out), ctypes.c_uint64(epoch),
+        n = self.W * self.rows * self.H
+        _check(self._lib.ep_ungroup_by_expert(self._h, self._arg(packed_y, 2 * self.E * n, "packed_y", 2),
+                                              self._arg(out, 2 * n, "out", 2), ctypes.c_uint64(epoch),
                                               _stream(stream)))
         return out
 

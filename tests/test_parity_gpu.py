@@ -184,12 +184,23 @@ def test_host_errors_before_launch():
     with pytest.raises(ep.EpError) as e:   # scales on a plan without scale_dim
         plan.dispatch(x, w, torch.zeros(4, device=DEV), idx, [1, 1])
     assert e.value.code == ep.EP_ERR_ARG
-    with pytest.raises(ep.EpError) as e:   # misaligned x
-        plan.dispatch(x.view(-1)[1:], w, None, idx, [1, 1])
-    assert e.value.code == ep.EP_ERR_ARG
+    with pytest.raises(ep.EpError) as e:   # misaligned x (full size, 2 bytes past a 16-byte boundary)
+        xs = torch.empty(x.numel() + 8, dtype=x.dtype, device=DEV)[1:1 + x.numel()].view(x.shape)
+        plan.dispatch(xs, w, None, idx, [1, 1])
+    assert e.value.code == ep.EP_ERR_ARG and "aligned" in str(e.value)
     with pytest.raises(ep.EpError) as e:   # combine before any dispatch
-        plan.combine(x, None, 1)
+        plan.combine(torch.zeros((2, 32, 64), dtype=torch.bfloat16, device=DEV), None, 1)
     assert e.value.code == ep.EP_ERR_STATE
+    # the binding checks buffer sizes and element widths against the plan before any launch
+    with pytest.raises(ep.EpError) as e:   # x one element short
+        plan.dispatch(x.view(-1)[1:], w, None, idx, [1, 1])
+    assert e.value.code == ep.EP_ERR_ARG and "x holds" in str(e.value)
+    with pytest.raises(ep.EpError) as e:   # int64 indices
+        plan.dispatch(x, w, None, idx.long(), [1, 1])
+    assert e.value.code == ep.EP_ERR_ARG and "indices" in str(e.value)
+    with pytest.raises(ep.EpError) as e:   # expert_out of [W][M][H] instead of [W][W*M][H]
+        plan.combine(x, None, 1)
+    assert e.value.code == ep.EP_ERR_ARG and "expert_out" in str(e.value)
     d = plan.dispatch(x, w, None, idx, wl.n_tok)
     with pytest.raises(ep.EpError) as e:   # out_w without weights
         plan.combine(d.recv_x, None, d.epoch, out_w=torch.zeros((2, 16, 2), device=DEV))

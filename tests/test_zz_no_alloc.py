@@ -89,9 +89,9 @@ def test_noalloc_rejects_shapes_beyond_its_scratch():
     dev = torch.device("cuda", 0)
     W, M = 32, 8192          # 1 + 32 * 1024 scan words > 16384
     i32 = dict(dtype=torch.int32, device=dev)
-    with pytest.raises(ep.EpError) as e:
-        ep.route_noalloc(W, 2, 4, M, torch.zeros((W, 1, 4), **i32), [0] * W,
-                         torch.zeros(1, **i32), torch.zeros(W, **i32), torch.zeros(1, **i32),
+    with pytest.raises(ep.EpError) as e:     # full-size buffers (40 MB), so only the shape is wrong
+        ep.route_noalloc(W, 2, 4, M, torch.zeros((W, M, 4), **i32), [0] * W,
+                         torch.zeros((W, W * M), **i32), torch.zeros(W, **i32), torch.zeros((W, M, 4), **i32),
                          torch.zeros(1, **i32))
     assert e.value.code == ep.EP_ERR_ARG
     assert "static scratch" in str(e.value)
