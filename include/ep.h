@@ -101,7 +101,9 @@ typedef struct {
 
 /*
  * Create a plan: validate the shape and allocate, once, every device buffer the calls use
- * (receive rows, index/weight/scale rows, reverse and forward maps, scan flags, status word).
+ * (receive rows, index/weight/scale rows, reverse and forward maps, scan flags, status word,
+ * and for the grouped view the expert-slot map and, from three 1024-row chunks of capacity, the
+ * grouping scan's per-chunk counts).
  * Follows the guide's EpDispatchCombineConfig (section 2, "Configuration") with the receive
  * capacity of W*M rows per rank.
  *   W                 1..32 logical ranks
