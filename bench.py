@@ -109,7 +109,7 @@ def code_digest(*files) -> str:
 KERNEL_SOURCES = {"scatter": "ep_scatter.cu", "combine": "ep_combine.cu", "route": "ep_route.cu",
                   "scatter_quant": "ep_scatter.cu", "combine_fp8": "ep_fp8wire.cu",
                   "quantise_rows": "ep_fp8wire.cu", "combine_fp4": "ep_fp8wire.cu",
-                  "quantise_rows_fp4": "ep_fp8wire.cu", "grouped": "ep_grouped.cu"}
+                  "quantise_rows_fp4": "ep_fp8wire.cu"}
 
 
 def kernel_digest(kernel: str) -> str:
