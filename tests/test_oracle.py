@@ -461,31 +461,50 @@ def test_fp8_combine_close_to_bf16_combine():
 
 # ---------------------------------------------------------------- expert-grouped layout (next row F3)
 
+def _check_grouping_brute_force(wl):
+    disp = _run(wl)
+    g = oracle.group_by_expert(wl.W, wl.E, wl.k, wl.H, 2, wl.M, disp)
+    for r in range(wl.W):
+        for e in range(wl.E):
+            ge = r * wl.E + e
+            lst = [(s, t) for s in range(wl.W) for t in range(int(wl.n_tok[s]))
+                   if ge in set(int(v) for v in wl.indices[s, t])]
+            n = len(lst)
+            assert g["packed_count"][r, e] == n
+            assert [int(v) for v in g["packed_src_info"][r, e, :n]] == [t for _, t in lst]
+            for slot, (s, t) in enumerate(lst):
+                assert np.array_equal(g["packed_x"][r, e, slot], wl.x[s, t])
+                i = g["packed_row"][r, e, slot]
+                assert disp["src_pos"][r, i] == s * wl.W * wl.M + t
+            first = 0
+            for s in range(wl.W):
+                c = sum(1 for (ss, _) in lst if ss == s)
+                assert g["layout_range"][r, e, s] == (first << 32) | c
+                first += c
+
+
 def test_group_by_expert_brute_force():
     for case in ({"W": 3, "E": 4, "k": 3, "H": 16, "M": 10, "n_tok": [10, 0, 7]},
                  {"W": 4, "E": 2, "k": 5, "H": 8, "M": 6, "n_tok": [6, 6, 1, 3]},
                  {"W": 1, "E": 8, "k": 8, "H": 24, "M": 9, "n_tok": [9]}):
         wl = wlmod.custom_workload(seed=4, **case)
         wl.indices[0, 0, 1] = wl.indices[0, 0, 0]          # a duplicate id counts once
-        disp = _run(wl)
-        g = oracle.group_by_expert(wl.W, wl.E, wl.k, wl.H, 2, wl.M, disp)
-        for r in range(wl.W):
-            for e in range(wl.E):
-                ge = r * wl.E + e
-                lst = [(s, t) for s in range(wl.W) for t in range(int(wl.n_tok[s]))
-                       if ge in set(int(v) for v in wl.indices[s, t])]
-                n = len(lst)
-                assert g["packed_count"][r, e] == n
-                assert [int(v) for v in g["packed_src_info"][r, e, :n]] == [t for _, t in lst]
-                for slot, (s, t) in enumerate(lst):
-                    assert np.array_equal(g["packed_x"][r, e, slot], wl.x[s, t])
-                    i = g["packed_row"][r, e, slot]
-                    assert disp["src_pos"][r, i] == s * wl.W * wl.M + t
-                first = 0
-                for s in range(wl.W):
-                    c = sum(1 for (ss, _) in lst if ss == s)
-                    assert g["layout_range"][r, e, s] == (first << 32) | c
-                    first += c
+        _check_grouping_brute_force(wl)
+
+
+def test_group_by_expert_brute_force_random_shapes():
+    """40 seeded small shapes: 1-6 ranks, 1-5 experts per rank, top-1..6 (at most W*E), empty
+    ranks, and repeated ids in about a tenth of the rows."""
+    rng = np.random.default_rng(2024)
+    for case in range(40):
+        W, E, M = int(rng.integers(1, 7)), int(rng.integers(1, 6)), int(rng.integers(1, 13))
+        k = min(int(rng.integers(1, 7)), W * E)            # top-k picks distinct experts
+        n_tok = [int(v) for v in rng.integers(0, M + 1, size=W)]
+        wl = wlmod.custom_workload(W=W, E=E, k=k, H=8, M=M, n_tok=n_tok, seed=100 + case)
+        if k > 1:
+            dup = rng.random((W, M)) < 0.1
+            wl.indices[:, :, 1] = np.where(dup, wl.indices[:, :, 0], wl.indices[:, :, 1])
+        _check_grouping_brute_force(wl)
 
 
 def test_ungroup_identity_closed_form():
