@@ -397,6 +397,63 @@ def test_blockwise_quantiser_scale_one_is_plain_cast():
     assert np.array_equal(q, ref)
 
 
+def _discriminating_blocks(n_max=300, seed=9):
+    """BF16 blocks whose codes tell the IEEE quotient x / scale apart from x * (1 / scale).
+
+    For seeded random block maxima (BF16 normals from 2^-31 to 2^31), every positive BF16 x no
+    larger than the maximum is divided by scale = RN(amax / 448) two ways with torch on the CPU:
+    the correctly rounded FP32 quotient, and the product with the rounded reciprocal.  Where the
+    two land on different sides of an e4m3 rounding boundary, x goes into the block.  Returns
+    (blocks [n][128] float32 holding BF16 values, count of such x)."""
+    bits = np.arange(0x0001, 0x7F80, dtype=np.uint32)
+    allx = (bits << 16).view(np.float32)
+    rng = np.random.default_rng(seed)
+    blocks, hits = [], 0
+    for amax_bits in rng.integers(0x3000, 0x4F00, n_max):
+        amax = (np.uint32(amax_bits) << np.uint32(16)).view(np.float32)
+        s = torch.tensor(amax, dtype=torch.float32) / torch.tensor(448.0, dtype=torch.float32)
+        xs = torch.from_numpy(allx[allx <= amax])
+        c_div = (xs / s).to(torch.float8_e4m3fn).view(torch.uint8)
+        c_mul = (xs * (torch.tensor(1.0, dtype=torch.float32) / s)).to(torch.float8_e4m3fn).view(torch.uint8)
+        sel = xs[c_div != c_mul].numpy()[:63]
+        if len(sel) == 0:
+            continue
+        hits += 2 * len(sel)
+        blk = rng.uniform(-1.0, 1.0, 128).astype(np.float32) * amax
+        blk[0] = amax
+        blk[1:1 + len(sel)] = sel
+        blk[64:64 + len(sel)] = -sel
+        blocks.append(blk)
+    return np.stack(blocks), hits
+
+
+def test_blockwise_quantiser_codes_are_the_ieee_quotient_cast():
+    """Exact pin of the per-element quotient (reading of the guide's fp8_direct_cast): every code
+    equals torch's e4m3fn cast of the correctly rounded FP32 quotient x / scale, with scale the
+    FP32 quotient amax / 448.  The blocks hold random values and, above all, values whose
+    quotient sits so close to an e4m3 rounding boundary that x * RN(1 / scale) rounds to the
+    other code, so a reciprocal-multiply quotient fails here."""
+    blocks, hits = _discriminating_blocks()
+    assert hits >= 100
+    x = _bf16(blocks)                       # one 128-element block per row
+    q, sc = oracle.quantize_e4m3_blockwise(x)
+    xs = torch.from_numpy((x.astype(np.uint32) << 16).view(np.float32)).reshape(x.shape[0], -1, 128)
+    amax = xs.abs().amax(dim=2)
+    scale = torch.where(amax > 0, amax / torch.tensor(448.0), torch.ones_like(amax))
+    assert np.array_equal(sc.view(np.uint32), scale.numpy().view(np.uint32))
+    ref = (xs / scale[:, :, None]).to(torch.float8_e4m3fn).view(torch.uint8).reshape(x.shape).numpy()
+    assert np.array_equal(q, ref)
+    # random rows as well, across many binades
+    rng = np.random.default_rng(31)
+    xf = (rng.standard_normal((32, 512)) * np.exp(rng.uniform(-20, 20, (32, 1)))).astype(np.float32)
+    x = _bf16(xf)
+    q, sc = oracle.quantize_e4m3_blockwise(x)
+    xs = torch.from_numpy((x.astype(np.uint32) << 16).view(np.float32)).reshape(32, 4, 128)
+    scale = xs.abs().amax(dim=2) / torch.tensor(448.0)
+    ref = (xs / scale[:, :, None]).to(torch.float8_e4m3fn).view(torch.uint8).reshape(32, 512).numpy()
+    assert np.array_equal(q, ref)
+
+
 def test_quantised_dispatch_routes_quantised_rows():
     wl = wlmod.make_workload("dsv3", max_tok=24)
     disp = oracle.dispatch_quantized(wl)
@@ -582,6 +639,47 @@ def test_mxfp4_quantiser_against_numpy():
         for b in range(H // 32):
             for i in range(32):
                 assert codes[r, b, i] == _e2m1_brute(xs[r, b, i] / scale[r, b]), (r, b, i)
+
+
+def test_e8m0_decode_every_code():
+    """Every scale code c in 0..254 decodes to 2^(c - 127) exactly, including code 0, the FP32
+    subnormal 2^-127."""
+    for c in range(255):
+        v = np.float32(oracle.f32_from_e8m0(c))
+        assert v == np.float32(2.0 ** (c - 127)), c
+    assert np.float32(oracle.f32_from_e8m0(0)).view(np.uint32) == 0x00400000
+
+
+def test_mxfp4_quantiser_tiny_blocks_take_scale_code_zero():
+    """Blocks whose maximum is a BF16 subnormal give a scale code below 0, clamped to 0 (scale
+    2^-127), and their codes are the brute-force e2m1 encoding of x / 2^-127; decoding them
+    through the FP4 combine of one row gives BF16(e2m1 value * 2^-127)."""
+    xf = np.zeros((2, 64), dtype=np.float32)
+    xf[0, :32] = np.float32(2.0 ** -133) * np.arange(-16, 16, dtype=np.float32)   # subnormal BF16
+    xf[0, 32:] = np.float32(2.0 ** -126) * np.linspace(-6, 6, 32, dtype=np.float32)
+    xf[1, :32] = np.float32(2.0 ** -128)
+    xf[1, 32:] = np.float32(-(2.0 ** -127)) * np.float32(3.0)
+    x = _bf16(xf)
+    q, sc = oracle.quantize_mxfp4(x)
+    xs = (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64).reshape(2, 2, 32)
+    amax = np.abs(xs).max(axis=2)
+    exp_code = np.clip(np.floor(np.log2(amax)) - 2 + 127, 0, 254)
+    assert np.array_equal(sc.astype(np.int64), exp_code.astype(np.int64))
+    assert (sc == 0).sum() >= 2
+    codes = np.stack([q & 0xF, q >> 4], axis=-1).reshape(2, 2, 32)
+    scale = 2.0 ** (sc.astype(np.float64) - 127)
+    for r in range(2):
+        for b in range(2):
+            for i in range(32):
+                assert codes[r, b, i] == _e2m1_brute(xs[r, b, i] / scale[r, b]), (r, b, i)
+    # the combine of a single row dequantises with the code-0 scale
+    wl = wlmod.custom_workload(W=1, E=1, k=1, H=64, M=2, n_tok=[2], seed=0)
+    slot_of = np.array([[[0]], [[1]]], dtype=np.int32)
+    out, _ = oracle.combine_fp4(1, 1, 64, 2, wl.n_tok, slot_of, q[None], sc[None])
+    mags = np.array(_E2M1 * 2) * np.where(np.arange(16) >= 8, -1.0, 1.0)
+    deq = 0.0 + mags[codes.reshape(2, 64)] * np.repeat(scale.reshape(2, 2), 32, axis=-1)   # the sum starts at +0
+    ref = torch.from_numpy(deq.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy()
+    assert np.array_equal(out[0].view(np.int16), ref)
 
 
 def test_fp4_combine_exact_sums():

@@ -53,6 +53,16 @@ MUTATIONS = {
     # e8m0 shared exponent off by one (largest e2m1 exponent taken as 1)
     "e8m0_off_by_one": ("                code = e2 - 2 + 127;", "                code = e2 - 1 + 127;",
                         pins.test_mxfp4_quantiser_against_numpy),
+    # FP8 quotient formed as x times the rounded reciprocal of the scale, not the IEEE quotient
+    "fp8_reciprocal_multiply": ("q[r * H + b * 128 + i] = ep_oracle_e4m3_from_f32(ep_oracle_f32_from_bf16(xb[i]) / scale);",
+                                "q[r * H + b * 128 + i] = ep_oracle_e4m3_from_f32(ep_oracle_f32_from_bf16(xb[i]) * (1.0f / scale));",
+                                pins.test_blockwise_quantiser_codes_are_the_ieee_quotient_cast),
+    # e8m0 code 0 decoded as zero instead of the subnormal 2^-127
+    "e8m0_code_zero_as_zero": ("if (c == 0) return bits_f32(0x00400000u);", "if (c == 0) return 0.0f;",
+                               pins.test_e8m0_decode_every_code),
+    # e8m0 code 0 decoded as 2^-126 (the exponent field read as if it were normal)
+    "e8m0_code_zero_normal": ("if (c == 0) return bits_f32(0x00400000u);", "if (c == 0) return bits_f32(0x00800000u);",
+                              pins.test_mxfp4_quantiser_tiny_blocks_take_scale_code_zero),
     # the FP4 combine pairs the wrong nibble with each element
     "fp4_nibble_swap": ("uint8_t code = (h & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xFu);",
                         "uint8_t code = (h & 1) ? (uint8_t)(byte & 0xFu) : (uint8_t)(byte >> 4);",
