@@ -120,6 +120,14 @@ int check_shape(int W, int E, int k, int H, int dtype, int sd, int M)
     if (M < 1) return fail(EP_ERR_ARG, "max_tok_per_rank=%d < 1", M);
     if ((int64_t)W * W * M >= (int64_t)1 << 31)
         return fail(EP_ERR_ARG, "W*W*max_tok_per_rank >= 2^31 overflows the int32 src_token_pos");
+    // The combine kernels address a token's rows in 32-bit counts of 16-byte vectors of the
+    // 16-bit expert outputs [W][W*M][H] (FP8 wire: 16-byte pieces of 16 codes; MX FP4: 32-element
+    // blocks), so that buffer must stay below 2^32 vectors = 64 GiB: W*W*M*H < 2^35.
+    if ((int64_t)W * W * M * H >= (int64_t)1 << 35)
+        return fail(EP_ERR_ARG,
+                    "W*W*max_tok_per_rank*hidden >= 2^35: the 16-bit expert outputs combine reads "
+                    "([W][W*M][H], %lld bytes) reach 64 GiB, past its 32-bit row offsets",
+                    (long long)((int64_t)W * W * M * H * 2));
     return EP_OK;
 }
 

@@ -81,7 +81,8 @@ __device__ __forceinline__ uint4 pack_vec(const float (&acc)[8])
 }
 
 // Fold one unit of nd <= 8 rows.  Lane d of `src` holds the unit's d-th row; `ro` keeps the
-// rows as 16-byte-vector offsets from eo4 (32 bits: a receive buffer below 64 GB).  Each lane
+// rows as 16-byte-vector offsets from eo4 (32 bits: ep_plan_create rejects shapes whose expert
+// outputs [W][W*M][H] reach 64 GiB, 2^32 vectors).  Each lane
 // owns columns lane, lane+32, ...; row d's load of the next column is issued as soon as its
 // current column has been taken, so every lane keeps nd loads in flight without a gap.  The
 // column's rows are added in ascending order, one FP32 add each, then packed and stored.

@@ -119,7 +119,8 @@ __device__ __forceinline__ void fold_fp8_rows(const WireArgs& a, int src, int nd
 {
     const int64_t hp = a.H >> 4;
     const uint4* q4 = reinterpret_cast<const uint4*>(a.q);
-    // piece offsets of the rows (receive buffer < 64 GB); a piece's scale sits at offset / 8,
+    // piece offsets of the rows (32 bits: the plan's shape keeps W*W*M*H below 2^35, so the wire's
+    // W*W*M*H/16 pieces stay below 2^31); a piece's scale sits at offset / 8,
     // since a row has hp = 8 * nb pieces and slices start on multiples of 8 pieces
     uint32_t ro[8];
 #pragma unroll
@@ -347,7 +348,7 @@ __device__ __forceinline__ void fold_fp4_rows(const WireArgs& a, int src, int nd
     const int64_t hb = a.H >> 5;                      // blocks per row
     const uint4* q4 = reinterpret_cast<const uint4*>(a.q);
     const uint8_t* sc8 = reinterpret_cast<const uint8_t*>(a.scales);
-    uint32_t ro[8];                                   // block offsets (receive buffer < 64 GB)
+    uint32_t ro[8];                                   // block offsets (W*W*M*H/32 < 2^30)
 #pragma unroll
     for (int d = 0; d < 8; ++d) ro[d] = (uint32_t)((int64_t)__shfl_sync(0xffffffffu, src, d) * hb + b0);
     uint4 b[8];

@@ -84,6 +84,11 @@ def test_device_bytes_golden(lib):
     ((2, 4, 2, 96, 4, 0, 64), "128"), ((2, 4, 2, 256, 4, 1, 64), "scale_dim"),
     ((2, 4, 2, 256, 0, -1, 64), "scale_dim"), ((2, 4, 2, 256, 0, 0, 0), "max_tok"),
     ((32, 4, 2, 256, 0, 0, 1 << 21), "2^31"),
+    # the combine's 16-bit expert outputs [W][W*M][H] reach 64 GiB (W*W*M*H = 2^35)
+    ((32, 8, 8, 8192, 0, 0, 4096), "64 GiB"), ((32, 8, 8, 4096, 0, 0, 8192), "64 GiB"),
+    ((32, 8, 8, 4096, 1, 0, 8192), "64 GiB"), ((32, 8, 8, 8192, 2, 0, 4096), "64 GiB"),
+    ((32, 8, 8, 8192, 3, 0, 4096), "64 GiB"), ((32, 8, 8, 8192, 4, 0, 4096), "64 GiB"),
+    ((16, 8, 8, 7168, 0, 0, 18725), "64 GiB"),
 ])
 def test_invalid_shapes_rejected_on_host(lib, shape, why):
     h = ctypes.c_void_p(123)
@@ -92,6 +97,19 @@ def test_invalid_shapes_rejected_on_host(lib, shape, why):
     assert h.value is None
     assert why in lib.ep_last_error().decode()
     assert lib.ep_plan_device_bytes(*shape) == 0
+
+
+def test_combine_offset_limit_boundary(lib):
+    """The largest accepted shapes sit one unit below W*W*M*H = 2^35 (64 GiB of 16-bit expert
+    outputs): one vector of hidden, or one token per rank, less than the rejected shapes."""
+    for dt in (ep.EP_BF16, ep.EP_FP16, ep.EP_FP8_E4M3, ep.EP_BF16_TO_FP8_E4M3, ep.EP_BF16_TO_MXFP4):
+        H = 8192 - 128                       # W*W*M*H = 2^35 - 2^29 at W=32, M=4096
+        assert lib.ep_plan_device_bytes(32, 8, 8, H, dt, 0, 4096) > 0, dt
+        assert lib.ep_plan_device_bytes(32, 8, 8, 8192, dt, 0, 4096) == 0, dt
+    # W=16, H=7168: 2^35 / (256 * 7168) = 18724.57 tokens per rank
+    assert lib.ep_plan_device_bytes(16, 8, 8, 7168, ep.EP_BF16, 0, 18724) > 0
+    assert lib.ep_plan_device_bytes(16, 8, 8, 7168, ep.EP_BF16, 0, 18725) == 0
+    assert 16 * 16 * 18724 * 7168 < 2 ** 35 <= 16 * 16 * 18725 * 7168
 
 
 def test_null_plan_calls_fail_cleanly(lib):
