@@ -112,20 +112,36 @@ typedef struct {
  *   hidden            >= 1, hidden * element size a multiple of 16 bytes
  *   dtype             enum ep_dtype
  *   scale_dim         0..65536 FP32 scales per token row
- *   max_tok_per_rank  >= 1, W*W*max_tok_per_rank < 2^31 (int32 reverse map)
+ *   max_tok_per_rank  >= 1, W*W*max_tok_per_rank < 2^31 (int32 reverse map), and
+ *                     W*W*max_tok_per_rank*hidden < 2^35: the 16-bit expert outputs that combine
+ *                     reads, [W][W*M][H], stay below 64 GiB, the reach of its 32-bit row offsets
  * The plan belongs to the CUDA device current at creation.  Returns EP_OK and *out, or an error
- * with *out = NULL.
+ * with *out = NULL.  A shape outside these limits is EP_ERR_ARG before any CUDA call (the
+ * staging PR's caller contract, "refactor(EPv2): replace per-module __device__ staging with
+ * shared buffer", section "Caller contract": a host error naming the argument, never a memory
+ * fault or a short buffer).
  */
 int ep_plan_create(ep_plan** out, int W, int experts_per_rank, int topk, int hidden, int dtype,
                    int scale_dim, int max_tok_per_rank);
 
-/* Wait for the device, then free the plan and its buffers.  NULL is a no-op. */
+/* Wait for the device, then free the plan and its buffers.  NULL is a no-op.  Synchronising
+ * first follows the fix to close() recorded on the gfx1250 EPv2 PR page ("gfx1250 EPv2: EP4
+ * topk-9 geometry; selfFirst follows MORI_EP_TOKOFF_EXT", the aiter commits that reference it):
+ * a launch still in flight must not read buffers that have been freed.  Returns EP_ERR_CUDA if
+ * the synchronisation or the free fails (the plan is released either way). */
 int ep_plan_destroy(ep_plan* p);
 
-/* Select the work split (enum ep_variant) of later ep_dispatch / ep_combine calls. */
+/* Select the work split (enum ep_variant) of later ep_dispatch / ep_combine calls: the whole-row
+ * or 512- / 1024-element hidden tiles of the gfx1201 PR ("How the gfx1201 kernels work", "Wave32
+ * and launch policy").  Results do not depend on it.  EP_ERR_ARG for a NULL plan or an unknown
+ * variant. */
 int ep_plan_set_variant(ep_plan* p, int variant);
 
-/* Device bytes ep_plan_create allocates for this shape, 0 for an invalid shape. */
+/* Device bytes ep_plan_create allocates for this shape, 0 for an invalid shape; host-only, no
+ * CUDA call.  The counterpart of the staging PR's ep_staging_bytes() ("refactor(EPv2): replace
+ * per-module __device__ staging with shared buffer", sections "Memory" and "Test plan"): the one
+ * function that sizes the device buffers, pinned by golden sizes so that it cannot drift from
+ * the layout the kernels index. */
 size_t ep_plan_device_bytes(int W, int experts_per_rank, int topk, int hidden, int dtype,
                             int scale_dim, int max_tok_per_rank);
 
@@ -266,7 +282,11 @@ int ep_dispatch_grouped(ep_plan* p, const void* x, const float* weights, const f
 int ep_reset(ep_plan* p, void* stream);
 
 /* Wait for the device, store the plan's device status word (EP_OK or the first EP_ERR_INDEX /
- * EP_ERR_DEVICE_TIMEOUT recorded since the last call) in *device_status, and clear it. */
+ * EP_ERR_DEVICE_TIMEOUT recorded since the last call) in *device_status, and clear it.  Device
+ * problems are recorded rather than trapped, as the staging PR's caller contract asks of the
+ * host and device checks ("refactor(EPv2): replace per-module __device__ staging with shared
+ * buffer", section "Caller contract").  EP_ERR_ARG for NULL arguments, EP_ERR_CUDA if the
+ * synchronisation or the copy fails. */
 int ep_status(ep_plan* p, int* device_status);
 
 /*
@@ -287,7 +307,10 @@ int ep_status(ep_plan* p, int* device_status);
  * libep.so, held by every GPU that loads the library until the process exits; a shape needs
  * 1 + W * ceil(W*M / 256) words and larger shapes fail with EP_ERR_ARG.  The first call on a
  * device looks up that array's device address (cudaGetSymbolAddress) and should come before any
- * stream capture.  Each call clears the words it uses on `stream`; all calls share the one
+ * stream capture; the address is kept for the life of the process, so the entry point must not
+ * be called on a device after cudaDeviceReset of that device.  The call runs on the current
+ * device, and every pointer argument must be memory usable there (EP_ERR_ARG for another GPU's
+ * device memory or for pageable host memory).  Each call clears the words it uses on `stream`; all calls share the one
  * array, so calls that overlap on the GPU (other streams, other threads) race and must be
  * serialised by the caller.  No call allocates or frees device memory.
  */
@@ -295,10 +318,15 @@ int ep_route_noalloc(int W, int experts_per_rank, int topk, int max_tok_per_rank
                      const int32_t* indices, const int32_t* n_tok_host, int32_t* src_token_pos,
                      int32_t* recv_count, int32_t* fwd_map, int32_t* device_status, void* stream);
 
-/* Static description of a status code. */
+/* Static description of a status code ("unknown status" for any other value); never NULL.
+ * With ep_last_error, the host side of the staging PR's caller contract ("refactor(EPv2):
+ * replace per-module __device__ staging with shared buffer", section "Caller contract"): a
+ * rejected call reports an error that names the argument. */
 const char* ep_strerror(int code);
 
-/* Message of the last failed call on the calling host thread ("" if none). */
+/* Message of the last failed call on the calling host thread ("" if none), naming the argument
+ * or limit at fault (same contract as ep_strerror).  The string is thread-local and stays valid
+ * until that thread's next failing call. */
 const char* ep_last_error(void);
 
 #ifdef __cplusplus
