@@ -111,14 +111,19 @@ def route_noalloc(W: int, experts_per_rank: int, topk: int, max_tok_per_rank: in
     """``ep_route_noalloc``: the routing step into caller-owned tensors, with no device
     allocation by the library (see include/ep.h).  Shapes: indices [W][M][k] int32,
     src_token_pos [W][W*M], recv_count [W], fwd_map [W][M][min(W,k)], device_status [1], all
-    int32 on the current device."""
+    int32 on indices' device, where the call runs."""
     arr = np.ascontiguousarray(np.asarray(n_tok, dtype=np.int32).reshape(W))
     M, F = max_tok_per_rank, min(W, topk)
-    _check(load_library().ep_route_noalloc(
-        W, experts_per_rank, topk, max_tok_per_rank, _buf(indices, 4 * W * M * topk, "indices", 4),
-        arr.ctypes.data_as(ctypes.c_void_p), _buf(src_token_pos, 4 * W * W * M, "src_token_pos", 4),
-        _buf(recv_count, 4 * W, "recv_count", 4), _buf(fwd_map, 4 * W * M * F, "fwd_map", 4),
-        _buf(device_status, 4, "device_status", 4), _stream(stream)))
+    dev = indices.device
+    if dev.type != "cuda":
+        raise EpError(EP_ERR_ARG, f"indices is on {dev}, not a CUDA device")
+    with torch.cuda.device(dev):
+        _check(load_library().ep_route_noalloc(
+            W, experts_per_rank, topk, max_tok_per_rank, _buf(indices, 4 * W * M * topk, "indices", 4, dev),
+            arr.ctypes.data_as(ctypes.c_void_p),
+            _buf(src_token_pos, 4 * W * W * M, "src_token_pos", 4, dev),
+            _buf(recv_count, 4 * W, "recv_count", 4, dev), _buf(fwd_map, 4 * W * M * F, "fwd_map", 4, dev),
+            _buf(device_status, 4, "device_status", 4, dev), _stream(stream)))
 
 
 class _DevPtr:

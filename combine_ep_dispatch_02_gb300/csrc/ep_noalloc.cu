@@ -14,7 +14,10 @@
 // holds its kNoAllocScratchWords * 8 bytes until the process exits.  Host code only knows the
 // array's name as a host-side stand-in, so the first call on each device looks up its device
 // address with cudaGetSymbolAddress (with that device current) and caches it; that first call
-// should be made before any stream capture begins.
+// should be made before any stream capture begins.  The cached address belongs to the device's
+// primary context: after cudaDeviceReset on that device it is stale, so a process that resets a
+// device must not call this entry point on it again.  Every pointer argument is checked to be
+// device memory usable from the current device before anything is enqueued.
 #include <cstdio>
 #include <mutex>
 
@@ -59,6 +62,32 @@ int scratch_of_current_device(unsigned long long** out)
 
 bool aligned4(const void* p) { return ((uintptr_t)p & 3u) == 0; }
 
+// The kernel runs on the current device and dereferences every pointer there, so each must be
+// memory that device can use: device memory of another GPU, or pageable host memory the
+// runtime does not know, is rejected on the host rather than left to fault on the device.
+int check_on_device(const void* p, const char* what, int dev)
+{
+    cudaPointerAttributes at{};
+    cudaError_t e = cudaPointerGetAttributes(&at, p);
+    char msg[256];
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        snprintf(msg, sizeof msg, "ep_route_noalloc: %s: cudaPointerGetAttributes failed: %s", what,
+                 cudaGetErrorString(e));
+        return ep::record_error(EP_ERR_ARG, msg);
+    }
+    if (at.type == cudaMemoryTypeUnregistered) {
+        snprintf(msg, sizeof msg, "ep_route_noalloc: %s is pageable host memory, not device memory", what);
+        return ep::record_error(EP_ERR_ARG, msg);
+    }
+    if (at.type == cudaMemoryTypeDevice && at.device != dev) {
+        snprintf(msg, sizeof msg, "ep_route_noalloc: %s is on device %d, the call runs on device %d", what,
+                 at.device, dev);
+        return ep::record_error(EP_ERR_ARG, msg);
+    }
+    return EP_OK;
+}
+
 }  // namespace
 
 extern "C" int ep_route_noalloc(int W, int E, int k, int M, const int32_t* indices,
@@ -98,6 +127,12 @@ extern "C" int ep_route_noalloc(int W, int E, int k, int M, const int32_t* indic
     unsigned long long* scratch = nullptr;
     int rc = scratch_of_current_device(&scratch);
     if (rc != EP_OK) return rc;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ep::record_error(EP_ERR_CUDA, "ep_route_noalloc: cudaGetDevice");
+    const void* ptrs[5] = {indices, src_token_pos, recv_count, fwd_map, device_status};
+    const char* names[5] = {"indices", "src_token_pos", "recv_count", "fwd_map", "device_status"};
+    for (int i = 0; i < 5; ++i)
+        if ((rc = check_on_device(ptrs[i], names[i], dev)) != EP_OK) return rc;
 
     // The array keeps the previous call's words: the ticket must restart at 0 and the scan
     // words must read "not published" for this call's stamp, so both are cleared first.  The

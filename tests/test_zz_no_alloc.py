@@ -4,7 +4,7 @@ ep_route_noalloc exists for callers that must not call cudaMalloc -- a serving r
 pool allocator already owns nearly all of HBM, or a plug-in whose host forbids allocation on the
 hot path -- and so cannot create an ep_plan.  Whatever memory it is given, it must route exactly
 as ep_dispatch_route does: the same receive counts, the same reverse map, and a forward map that
-points back at each token.  Its scratch is one static array shared by every call, so two calls
+points back at each token; and all three must equal the oracle's, bit for bit.  Its scratch is one static array shared by every call, so two calls
 in a row with different shapes check that each call starts from clean scan words.
 
 This file is collected last on purpose (it adds no coverage the others depend on).
@@ -14,6 +14,7 @@ import pytest
 import torch
 
 import combine_ep_dispatch_02_gb300 as ep
+import oracle
 from combine_ep_dispatch_02_gb300 import workloads as wlmod
 
 pytestmark = pytest.mark.gpu
@@ -52,14 +53,25 @@ def _without_alloc(wl, dev):
     return cnt.cpu().numpy(), pos.cpu().numpy(), fwd.cpu().numpy(), int(status.item())
 
 
+def _oracle_routing(wl):
+    """The oracle's dispatch of the same routing (the payload does not affect routing, so a
+    hidden of 8 zero elements stands in for the workload's rows)."""
+    x = np.zeros((wl.W, wl.M, 8), dtype=np.uint16)
+    d = oracle.dispatch(wl.W, wl.E, wl.k, 8, 2, 0, wl.M, x, None, None, wl.indices, wl.n_tok)
+    return d["recv_count"], d["src_pos"], d["slot_of"]
+
+
 def _check_same_routing(wl, dev):
     ref_cnt, ref_pos = _with_plan(wl, dev)
     cnt, pos, fwd, status = _without_alloc(wl, dev)
+    o_cnt, o_pos, o_slot = _oracle_routing(wl)
     assert status == ep.EP_OK
     assert np.array_equal(cnt, ref_cnt)
+    assert np.array_equal(cnt, o_cnt)                          # bit-exact against the oracle
     for r in range(wl.W):
         n = int(cnt[r])
         assert np.array_equal(pos[r, :n], ref_pos[r, :n]), f"rank {r}"
+        assert np.array_equal(pos[r, :n], o_pos[r, :n]), f"rank {r} against the oracle"
     rows = wl.W * wl.M
     for s in range(wl.W):
         n = int(wl.n_tok[s])
@@ -75,6 +87,8 @@ def _check_same_routing(wl, dev):
         r_idx, slot = np.divmod(f[valid], rows)
         tok = np.repeat(np.arange(n), nvalid)
         assert np.array_equal(pos[r_idx, slot], s * rows + tok)
+        # the forward map's rows are the oracle's slots, rank by rank
+        assert np.array_equal(slot, o_slot[s, tok, r_idx])
 
 
 def test_noalloc_routing_matches_plan_routing_two_calls_in_a_row():
