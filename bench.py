@@ -18,10 +18,8 @@ the host cores instead (rank 0 only).
 from __future__ import annotations
 
 import argparse
-import hashlib
 import json
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -77,60 +75,27 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def code_digest(*files) -> str:
-    """sha256 of C/CUDA sources with comments and whitespace removed (string and character
-    literals kept), so an edit that only touches comments leaves it unchanged."""
-    h = hashlib.sha256()
-    for f in files:
-        text = open(f, encoding="utf-8").read()
-        out, i, n = [], 0, len(text)
-        while i < n:
-            c = text[i]
-            if text.startswith("//", i):
-                j = text.find("\n", i)
-                i = n if j < 0 else j
-            elif text.startswith("/*", i):
-                j = text.find("*/", i + 2)
-                i = n if j < 0 else j + 2
-                out.append(" ")
-            elif c in "\"'":
-                j = i + 1
-                while j < n and text[j] != c:
-                    j += 2 if text[j] == "\\" else 1
-                out.append(text[i:j + 1])
-                i = j + 1
-            else:
-                out.append(c)
-                i += 1
-        h.update(" ".join("".join(out).split()).encode())
-    return h.hexdigest()
+from combine_ep_dispatch_02_gb300.profile_case import TRAFFIC_FILE, kernel_digest  # noqa: E402
 
 
-KERNEL_SOURCES = {"scatter": "ep_scatter.cu", "combine": "ep_combine.cu", "route": "ep_route.cu",
-                  "scatter_quant": "ep_scatter.cu", "combine_fp8": "ep_fp8wire.cu",
-                  "quantise_rows": "ep_fp8wire.cu", "combine_fp4": "ep_fp8wire.cu",
-                  "quantise_rows_fp4": "ep_fp8wire.cu"}
-
-
-def kernel_digest(kernel: str) -> str:
-    """Code digest of a kernel's source file and the shared header it includes."""
-    csrc = os.path.join(ROOT, "combine_ep_dispatch_02_gb300", "csrc")
-    return code_digest(os.path.join(csrc, KERNEL_SOURCES[kernel]), os.path.join(csrc, "ep_common.cuh"))
-
-
-def recorded_traffic(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current
-    code of the kernel (a code digest recorded beside the figure)."""
-    path = os.path.join(ROOT, "profiles", f"ncu_{kernel}_dsv3.md")
+def recorded_traffic(kernel: str, algorithmic_bytes: int):
+    """DRAM bytes of one full-size launch of `kernel`, from the ncu capture recorded in
+    profiles/dram_traffic.json, if that capture was taken on the current code of the kernel (the
+    code digest recorded beside the figure).  The capture runs a smaller case of the same
+    workload; its traffic per algorithmic byte is applied to this launch's algorithmic bytes.
+    Returns (bytes, note) or (None, reason)."""
     try:
-        text = open(path).read()
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)["kernels"][kernel]
         cur = kernel_digest(kernel)
-    except OSError:
-        return None
-    m = re.search(r"traffic_bytes_per_launch:\s*(\d+)\s+code_digest:\s*([0-9a-f]{64})", text)
-    if not m or m.group(2) != cur:
-        return None
-    return int(m.group(1))
+    except (OSError, KeyError, ValueError):
+        return None, "no recorded capture"
+    if rec.get("code_digest") != cur:
+        return None, "kernel changed since the recorded capture"
+    ratio = rec["dram_bytes_per_launch"] / rec["algorithmic_bytes_per_launch"]
+    return int(round(ratio * algorithmic_bytes)), (
+        f"ncu dram__bytes_read.sum + dram__bytes_write.sum of {rec['case']}, "
+        f"{ratio:.4f} x algorithmic bytes, scaled to this launch's algorithmic bytes")
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -302,6 +267,7 @@ def run_ours(args, rank, world, dist):
     if plan.status() != 0:
         raise RuntimeError("device status after timing: %d" % plan.status())
 
+    traffic, traffic_note = recorded_traffic(dom, nbytes[dom])
     result = None
     if rank == 0:
         cpu = cpu_baseline(wl, out) if world == 1 else None
@@ -335,7 +301,8 @@ def run_ours(args, rank, world, dist):
             "algorithmic_bytes": nbytes,
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
                          "peak": peak, "peak_source": f"hbm_gbs of {peak_src}", "unit": "GB/s",
-                         "frac": round(achieved / peak, 4), "traffic": recorded_traffic(dom)},
+                         "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "traffic_source": traffic_note},
             "clocks": sampler.summary(t0, t_extra),
             "e2e": e2e,
             "gpu_launches": 3 * args.steps,

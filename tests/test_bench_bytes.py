@@ -59,3 +59,40 @@ def test_phase_bytes_deepseek_v3_full_size():
     assert got["combine"] == (173981 + 32768) * (14336 + 32) + 32768 * 4 * 8 == 2971618208
     assert got["scatter"] == 2977185600
     assert got["route"] == 32768 * 32 + 173981 * 4 == 1744500
+
+
+def test_profile_case_kernel_bytes_agree_with_the_bench():
+    """The profiling driver's per-kernel algorithmic bytes are the bench's (route, scatter and
+    combine at the full DeepSeek-V3 size), so a recorded traffic ratio scales consistently."""
+    from combine_ep_dispatch_02_gb300 import profile_case
+    wl = types.SimpleNamespace(N=32768, H=7168, elem_bytes=2, k=8, sd=0, W=8, weights=True)
+    got = bench.phase_bytes(wl, 173981)
+    for phase in ("route", "scatter", "combine"):
+        assert profile_case.kernel_bytes(phase, 32768, 173981, 8, 7168, 8) == got[phase], phase
+
+
+def test_recorded_traffic_scales_and_expires(tmp_path, monkeypatch):
+    """A capture entered by profile_case.record gives bench.recorded_traffic its DRAM bytes per
+    algorithmic byte, applied to the full launch; a code digest that no longer matches voids it."""
+    from combine_ep_dispatch_02_gb300 import profile_case
+    path = tmp_path / "dram_traffic.json"
+    monkeypatch.setattr(profile_case, "TRAFFIC_FILE", str(path))
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(path))
+    csv_path = tmp_path / "ncu.csv"
+    hdr = '"ID","Process ID","Process Name","Host Name","Kernel Name","Context","Stream","Block Size",' \
+          '"Grid Size","Device","CC","Section Name","Metric Name","Metric Unit","Metric Value"\n'
+    rows = []
+    for i, (r, w) in enumerate([(100.0, 300.0), (110.0, 290.0)]):
+        for name, v in (("dram__bytes_read.sum", r), ("dram__bytes_write.sum", w)):
+            rows.append(f'"{i}","1","python3","h","ep_combine_kernel","1","7","(192, 1, 1)","(304, 1, 1)",'
+                        f'"0","10.3","Command line profiler metrics","{name}","Mbyte","{v}"\n')
+    csv_path.write_text("==PROF== noise\n" + hdr + "".join(rows))
+    line = {"tokens_per_rank": 1024, "tokens": 8192, "token_dest_pairs": 43601,
+            "kernel_algorithmic_bytes": 500_000_000}
+    rec = profile_case.record("combine", line, str(csv_path), "ncu ... (test)")
+    assert rec["dram_bytes_per_launch"] == 400_000_000 and rec["captured_launches"] == 2
+    assert rec["traffic_over_algorithmic"] == 0.8
+    traffic, note = bench.recorded_traffic("combine", 2_000_000_000)
+    assert traffic == 1_600_000_000 and "0.8000" in note
+    monkeypatch.setattr(bench, "kernel_digest", lambda k: "0" * 64)
+    assert bench.recorded_traffic("combine", 2_000_000_000)[0] is None
