@@ -164,6 +164,13 @@ def max_over_ranks(value, dist, device):
     return float(t.item())
 
 
+def run_config(wl, P, world):
+    """The `config` of the JSON line, the same keys and values for both arms on one workload."""
+    return {"workload": WORKLOAD_DESC.replace("4096", str(wl.M)), "tokens": int(wl.N),
+            "token_dest_pairs": int(P),
+            "parallelism": f"replicas x{world}" if world > 1 else "none: W logical ranks on one device"}
+
+
 def whole_job_gbs(bytes_per_rank, world, ms_per_step):
     """Whole-job throughput: every rank's bytes over the slowest rank's time."""
     return world * bytes_per_rank / (ms_per_step * 1e-3) / 1e9
@@ -220,6 +227,9 @@ def run_ours(args, rank, world, dist):
         dist.barrier()
     torch.cuda.synchronize(dev)
     t0 = time.time()
+    # one untimed step primes the stream, so the first timed step's events do not wait for the
+    # host to issue its launches (the events bracket exactly the K timed steps)
+    step()
     for i in range(args.steps):
         step(evs[i])
     torch.cuda.synchronize(dev)
@@ -243,6 +253,8 @@ def run_ours(args, rank, world, dist):
     ms_step = total_ms / args.steps
     avg = lambda v: sum(v) / len(v)  # noqa: E731
     k_ms = {"route": avg(route), "scatter": avg(scat), "combine": avg(comb)}
+    k_med = {"route": statistics.median(route), "scatter": statistics.median(scat),
+             "combine": statistics.median(comb)}
     disp_ms = k_ms["route"] + k_ms["scatter"]
     peak, peak_src = hbm_peak()
     gbs = lambda b, ms: b / (ms * 1e-3) / 1e9  # noqa: E731
@@ -262,8 +274,9 @@ def run_ours(args, rank, world, dist):
     grouped = measure_grouped(ep, dev, stream, peak, steps=max(3, min(args.steps, 50)))
     grouped_large = measure_grouped(ep, dev, stream, peak, steps=max(3, min(args.steps, 20)),
                                     workload="dsv3", max_tok=min(1024, wl.M))
-    latency = measure_small_batch_latency(ep, dev)
+    latency = measure_small_batch_latency(ep, dev, full=(plan, wl, x, w, idx))
     protocol = measure_graph_protocol(plan, wl, dev, x, w, idx, nbytes, peak)
+    other = measure_workloads(ep, dev, peak)
     if plan.status() != 0:
         raise RuntimeError("device status after timing: %d" % plan.status())
 
@@ -284,16 +297,15 @@ def run_ours(args, rank, world, dist):
             "vs_baseline": None,
             "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD_DESC.replace("4096", str(wl.M)), "tokens": wl.N,
-                       "token_dest_pairs": P,
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                       "l2": "inputs larger than L2 (x 470 MB read, 2.5 GB of receive rows "
-                             "written then read per step vs 129 MB L2); no flush",
-                       "variant": "auto"},
+            "config": run_config(wl, P, world),
+            "l2": "inputs larger than L2 (x 470 MB read, 2.5 GB of receive rows written then "
+                  "read per step vs 129 MB L2); no flush",
+            "variant": "auto",
             "pair_us": round(ms_step * 1e3, 2),
             "dispatch_us": round(disp_ms * 1e3, 2),
             "combine_us": round(k_ms["combine"] * 1e3, 2),
             "kernel_us": {k: round(v * 1e3, 2) for k, v in k_ms.items()},
+            "kernel_us_median": {k: round(v * 1e3, 2) for k, v in k_med.items()},
             "dispatch_gbs": round(gbs(nbytes["dispatch"], disp_ms), 1),
             "combine_gbs": round(gbs(nbytes["combine"], k_ms["combine"]), 1),
             "dispatch_frac": round(gbs(nbytes["dispatch"], disp_ms) / peak, 4),
@@ -315,6 +327,7 @@ def run_ours(args, rank, world, dist):
             "expert_grouped_layout_dsv3": grouped_large,
             "small_batch_latency_us": latency,
             "graph_protocol": protocol,
+            "workloads": other,
         }
     plan.close()
     return result
@@ -457,13 +470,57 @@ def measure_grouped(ep, dev, stream, peak, steps, workload="small", max_tok=None
                                 (fused * 1e-3) / 1e9 / peak, 4)}
 
 
-def measure_small_batch_latency(ep, dev, tokens=(8, 128, 256, 1024, 2048), replays=120):
+def _replay_times(graphs, s, flush, replays, warm=10):
+    """Per-replay device times (µs) of each captured graph, back to back ("hot") and with a
+    2x-L2 buffer written before each replay ("l2_flushed"), in the order hot, flushed per round."""
+    times = {name: {"hot": [], "l2_flushed": []} for name in graphs}
+    with torch.cuda.stream(s):                       # replay() launches on the current stream
+        for i in range(replays + warm):
+            for name, g in graphs.items():
+                for cold in (False, True):
+                    if cold:
+                        flush.fill_(i & 0xFF)        # evict the working set from L2
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(s)
+                    g.replay()
+                    b.record(s)
+                    b.synchronize()
+                    if i >= warm:
+                        times[name]["l2_flushed" if cold else "hot"].append(a.elapsed_time(b) * 1e3)
+    return times
+
+
+def _capture_pair(plan, x, w, sc, idx, n_tok, out, out_w, s, expert_out=None):
+    """Dispatch and combine of one call, each captured in its own CUDA graph after 10 eager
+    warm-ups on stream s; returns ({"dispatch": g, "combine": g}, the dispatch views)."""
+    with torch.cuda.stream(s):
+        for _ in range(10):
+            d = plan.dispatch(x, w, sc, idx, n_tok, stream=s)
+            plan.combine(d.recv_x if expert_out is None else expert_out, d.recv_w, d.epoch, out=out,
+                         out_w=out_w, stream=s)
+    torch.cuda.synchronize()
+    gd, gc = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gd, stream=s):
+        d = plan.dispatch(x, w, sc, idx, n_tok, stream=s)
+    with torch.cuda.graph(gc, stream=s):
+        plan.combine(d.recv_x if expert_out is None else expert_out, d.recv_w, d.epoch, out=out,
+                     out_w=out_w, stream=s)
+    return {"dispatch": gd, "combine": gc}, d
+
+
+def measure_small_batch_latency(ep, dev, full=None, tokens=(8, 128, 256, 1024, 2048), replays=120):
     """Dispatch and combine latency at small and mid-size batches on the DeepSeek-V3 shape (W=8,
     32 experts per rank, top-8, hidden 7168 BF16, Zipf routing), as the pages measure it: each
     call captured in a CUDA graph and replayed; p50 over the replays of the per-replay device
-    time.  From 1024 tokens per rank on, the entries also give the effective GB/s of the L2-
-    flushed times (the dispatch and combine minimal bytes of phase_bytes)."""
+    time.  Each token count runs twice: on a plan sized for it (max_tok_per_rank = the count),
+    and, when `full` = (plan, workload, x, w, idx) is given, as a call of that many tokens per
+    rank on the full-size plan of 4096 tokens per rank, as a serving loop sized for its largest
+    batch would call it.  From 1024 tokens per rank on, the entries also give the effective GB/s
+    of the L2-flushed times (the dispatch and combine minimal bytes of phase_bytes)."""
     res = {}
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    peak = hbm_peak()[0]
+    s = torch.cuda.Stream(dev)
     for t in tokens:
         wl = wlmod.make_workload(WORKLOAD, max_tok=t)
         plan = ep.Plan(wl.W, wl.E, wl.k, wl.H, "bf16", 0, wl.M, device=dev)
@@ -472,72 +529,59 @@ def measure_small_batch_latency(ep, dev, tokens=(8, 128, 256, 1024, 2048), repla
         w = torch.from_numpy(wl.weights).to(dev)
         out = torch.empty((wl.W, wl.M, wl.H), dtype=torch.bfloat16, device=dev)
         out_w = torch.empty((wl.W, wl.M, wl.k), dtype=torch.float32, device=dev)
-        s = torch.cuda.Stream(dev)
-        with torch.cuda.stream(s):
-            for _ in range(10):                     # eager warm-up
-                d = plan.dispatch(x, w, None, idx, wl.n_tok, stream=s)
-                plan.combine(d.recv_x, d.recv_w, d.epoch, out=out, out_w=out_w, stream=s)
-        torch.cuda.synchronize(dev)
-        gd, gc = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gd, stream=s):
-            d = plan.dispatch(x, w, None, idx, wl.n_tok, stream=s)
-        with torch.cuda.graph(gc, stream=s):
-            plan.combine(d.recv_x, d.recv_w, d.epoch, out=out, out_w=out_w, stream=s)
-        flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
-        times = {"dispatch": [], "combine": [], "dispatch_l2_flushed": [], "combine_l2_flushed": []}
-        with torch.cuda.stream(s):                   # replay() launches on the current stream
-            for i in range(replays + 10):
-                for name, g in (("dispatch", gd), ("combine", gc)):
-                    for cold in (False, True):
-                        if cold:
-                            flush.fill_(i & 0xFF)      # evict the working set from L2
-                        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                        a.record(s)
-                        g.replay()
-                        b.record(s)
-                        b.synchronize()
-                        if i >= 10:
-                            times[name + ("_l2_flushed" if cold else "")].append(a.elapsed_time(b) * 1e3)
+        graphs, d = _capture_pair(plan, x, w, None, idx, wl.n_tok, out, out_w, s)
+        times = _replay_times(graphs, s, flush, replays)
         if plan.status() != 0:
             raise RuntimeError("device status after the latency runs: %d" % plan.status())
-        entry = {k: round(statistics.median(v), 2) for k, v in times.items()}
+        entry = {}
+        for ph in ("dispatch", "combine"):
+            entry[ph] = round(statistics.median(times[ph]["hot"]), 2)
+            entry[ph + "_l2_flushed"] = round(statistics.median(times[ph]["l2_flushed"]), 2)
         if t >= 1024:
             nb = phase_bytes(wl, int(d.recv_count.sum().item()))
-            peak = hbm_peak()[0]
             for ph in ("dispatch", "combine"):
                 gbs = nb[ph] / (entry[ph + "_l2_flushed"] * 1e-6) / 1e9
                 entry[ph + "_gbs"] = round(gbs, 1)
                 entry[ph + "_frac"] = round(gbs / peak, 4)
         plan.close()
+        del graphs
+        if full is not None:
+            fplan, fwl, fx, fw, fidx = full
+            out = torch.empty((fwl.W, fwl.M, fwl.H), dtype=torch.bfloat16, device=dev)
+            out_w = torch.empty((fwl.W, fwl.M, fwl.k), dtype=torch.float32, device=dev)
+            graphs, _ = _capture_pair(fplan, fx, fw, None, fidx, [t] * fwl.W, out, out_w, s)
+            times = _replay_times(graphs, s, flush, replays)
+            if fplan.status() != 0:
+                raise RuntimeError("device status after the full-plan latency runs: %d" % fplan.status())
+            for ph in ("dispatch", "combine"):
+                entry[ph + "_on_full_plan"] = round(statistics.median(times[ph]["hot"]), 2)
+                entry[ph + "_l2_flushed_on_full_plan"] = round(statistics.median(times[ph]["l2_flushed"]), 2)
+            del graphs
         res[f"{t}_tokens_per_rank"] = entry
     res["method"] = ("CUDA-graph replay of one dispatch (route + scatter) or one combine; p50 of "
                      f"{replays} replays; hot = back to back, l2_flushed = a 2x-L2 buffer written "
-                     "before each replay")
+                     "before each replay; *_on_full_plan = the same call on the plan sized for "
+                     "4096 tokens per rank")
     return res
 
 
-def measure_graph_protocol(plan, wl, dev, x, w, idx, nbytes, peak, rounds=3, samples=30):
-    """The pages' timing protocol on the full workload: {dispatch}, {combine} and
-    {dispatch + combine} each captured in a CUDA graph; 10 eager and 10 graph warm-ups; then
-    `rounds` rounds of `samples` replays, each replay preceded by a write of a 2x-L2 buffer (L2
-    flushed); p50 per round and over all samples, the round spread (max / min of the round p50s,
-    to stay <= 1.20), and the hot-L2 p50 (back-to-back replays) beside it."""
+def graph_protocol(plan, wl, dev, x, w, sc, idx, nbytes, peak, expert_out=None, rounds=3, samples=30):
+    """The pages' timing protocol: {dispatch}, {combine} and {dispatch + combine} each captured
+    in a CUDA graph; 10 eager and 10 graph warm-ups; then `rounds` rounds of `samples` replays,
+    each replay preceded by a write of a 2x-L2 buffer (L2 flushed); p50 per round and over all
+    samples, the round spread (max / min of the round p50s, to stay <= 1.20), and the hot-L2
+    p50 (back-to-back replays) beside it.  Combine reads `expert_out` ([W][W*M][H] 16-bit), or
+    the dispatch's own receive rows (identity expert, in place) when it is None."""
     s = torch.cuda.Stream(dev)
-    out = torch.empty((wl.W, wl.M, wl.H), dtype=torch.bfloat16, device=dev)
-    out_w = torch.empty((wl.W, wl.M, wl.k), dtype=torch.float32, device=dev)
-    with torch.cuda.stream(s):
-        for _ in range(10):
-            d = plan.dispatch(x, w, None, idx, wl.n_tok, stream=s)
-            plan.combine(d.recv_x, d.recv_w, d.epoch, out=out, out_w=out_w, stream=s)
-    torch.cuda.synchronize(dev)
-    graphs = {name: torch.cuda.CUDAGraph() for name in ("dispatch", "combine", "pair")}
-    with torch.cuda.graph(graphs["dispatch"], stream=s):
-        d = plan.dispatch(x, w, None, idx, wl.n_tok, stream=s)
-    with torch.cuda.graph(graphs["combine"], stream=s):
-        plan.combine(d.recv_x, d.recv_w, d.epoch, out=out, out_w=out_w, stream=s)
+    out = torch.empty((wl.W, wl.M, wl.H), dtype=torch.bfloat16 if wl.dtype != "fp16" else torch.float16,
+                      device=dev)
+    out_w = torch.empty((wl.W, wl.M, wl.k), dtype=torch.float32, device=dev) if w is not None else None
+    graphs, d = _capture_pair(plan, x, w, sc, idx, wl.n_tok, out, out_w, s, expert_out)
+    graphs["pair"] = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graphs["pair"], stream=s):
-        d2 = plan.dispatch(x, w, None, idx, wl.n_tok, stream=s)
-        plan.combine(d2.recv_x, d2.recv_w, d2.epoch, out=out, out_w=out_w, stream=s)
+        d2 = plan.dispatch(x, w, sc, idx, wl.n_tok, stream=s)
+        plan.combine(d2.recv_x if expert_out is None else expert_out, d2.recv_w, d2.epoch, out=out,
+                     out_w=out_w, stream=s)
     flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
     res = {}
     with torch.cuda.stream(s):                       # replay() launches on the current stream
@@ -569,6 +613,64 @@ def measure_graph_protocol(plan, wl, dev, x, w, idx, nbytes, peak, rounds=3, sam
     res["method"] = (f"CUDA-graph replay; 10 eager + 10 graph warm-ups; {rounds} rounds x {samples} "
                      "samples, a 2x-L2 buffer written before each sample; p50; hot = back-to-back "
                      "replays without the flush")
+    return res
+
+
+def measure_graph_protocol(plan, wl, dev, x, w, idx, nbytes, peak):
+    """The pages' timing protocol on the full DeepSeek-V3 workload (identity expert)."""
+    return graph_protocol(plan, wl, dev, x, w, None, idx, nbytes, peak)
+
+
+WORKLOAD_CASES = (
+    ("small", {}, "W=4, 64 experts/rank (256), top-8, hidden 7168 BF16, 256 tokens/rank, uniform "
+                  "routing, FP32 softmax weights; combine reads the received rows in place (the "
+                  "per-expert-scalar expert is caller code, outside the timed calls)"),
+    *[(f"topk_k{k}", {"k": k}, f"W=4, 64 experts/rank (256), top-{k}, hidden 2048 FP16, 512 "
+                                "tokens/rank, uniform routing, FP32 weights, identity expert")
+      for k in wlmod.TOPK_SWEEP],
+    ("fp8", {}, "W=8, 96 experts/rank (768), top-6, hidden 7168 FP8 e4m3 + 56 FP32 block scales, "
+                "ragged tokens/rank U[16,4096], FP32 softmax weights; combine reads BF16 expert "
+                "outputs [W][W*M][H] (the dequantising expert is caller code)"),
+)
+
+
+def measure_workloads(ep, dev, peak, rounds=3, samples=20):
+    """Dispatch, combine and the pair on the other workloads of the pages' configurations, under
+    the pages' protocol (graph_protocol, L2 flushed before every sample: the small and top-k
+    workloads fit in L2), with per-phase µs, effective GB/s of the minimal bytes and fraction
+    of the measured HBM peak."""
+    res = {}
+    for key, kw, desc in WORKLOAD_CASES:
+        name = key.split("_")[0]
+        wl = wlmod.make_workload(name, **kw)
+        plan = ep.Plan(wl.W, wl.E, wl.k, wl.H, wl.dtype, wl.sd, wl.M, device=dev)
+        x = torch.from_numpy(wl.x.view(np.int16) if wl.elem_bytes == 2 else wl.x).to(dev)
+        idx = torch.from_numpy(wl.indices).to(dev)
+        w = torch.from_numpy(wl.weights).to(dev)
+        sc = torch.from_numpy(wl.scales).to(dev) if wl.sd else None
+        eo = None
+        if wl.elem_bytes != 2:      # BF16 expert outputs for the FP8 payload's combine
+            eo = torch.zeros((wl.W, wl.W * wl.M, wl.H), dtype=torch.bfloat16, device=dev)
+        d = plan.dispatch(x, w, sc, idx, wl.n_tok)
+        torch.cuda.synchronize()
+        P = int(d.recv_count.sum().item())
+        nb = phase_bytes(wl, P)
+        prot = graph_protocol(plan, wl, dev, x, w, sc, idx, nb, peak, expert_out=eo, rounds=rounds,
+                              samples=samples)
+        entry = {"workload": desc, "tokens": wl.N, "token_dest_pairs": P}
+        for ph in ("dispatch", "combine", "pair"):
+            entry[ph + "_us"] = prot[ph]["p50_us"]
+            entry[ph + "_hot_us"] = prot[ph]["hot_p50_us"]
+            entry[ph + "_gbs"] = prot[ph]["gbs"]
+            entry[ph + "_frac"] = prot[ph]["frac"]
+            entry[ph + "_round_spread"] = prot[ph]["round_spread"]
+        entry["algorithmic_bytes"] = {ph: nb[ph] for ph in ("dispatch", "combine", "pair")}
+        res[key] = entry
+        plan.close()
+        del eo, x, idx, w, sc
+        torch.cuda.empty_cache()
+    res["method"] = (f"graph_protocol: CUDA-graph replay, {rounds} rounds x {samples} samples with "
+                     "a 2x-L2 buffer written before each, p50; GB/s of the minimal bytes")
     return res
 
 
@@ -730,8 +832,8 @@ def run_reference(args):
             "steps": args.steps, "warmup": warm, "ms_per_step": round(ms, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD_DESC, "tokens": sub.N, "token_dest_pairs": P,
-                       "parallelism": "host cores, 1 thread"},
+            "config": run_config(sub, P, 1),
+            "host": "single-threaded C oracle on the host cores",
             "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

@@ -152,7 +152,7 @@ Layout layout_of(int W, int E, int k, int H, int dtype, int sd, int M)
     put(L.recv_count, (size_t)W * 4);
     put(L.expert_map, (size_t)W * rows * k * 4);
     put(L.flags, (size_t)tiles * W * 8);
-    put(L.ticket, 8 + kQueues * 16);   // the route ticket, then the copy kernels' work queues
+    put(L.ticket, kRouteControlWords * 8 + kQueues * 16);   // routing control, then the work queues
     put(L.status, 4);
     L.total = o;
     return L;
@@ -282,7 +282,7 @@ int ep_plan_create(ep_plan** out, int W, int E, int k, int H, int dtype, int sd,
     p->scan_cnt = p->scan_chunks ? (int32_t*)(b + L.scan_cnt) : nullptr;
     p->flags = (unsigned long long*)(b + L.flags);
     p->ticket = (unsigned long long*)(b + L.ticket);
-    p->queues = p->ticket + 1;
+    p->queues = p->ticket + kRouteControlWords;
     p->status = (int*)(b + L.status);
     // the control words start at zero once; scan flags are stamped per call after that
     e = cudaMemset(b + L.recv_count, 0, L.total - L.recv_count);
@@ -350,10 +350,12 @@ int ep_dispatch_route(ep_plan* p, const int32_t* indices, const int32_t* n_tok_h
     a.idx = indices; a.fwd = p->fwd; a.src_pos = p->src_pos; a.recv_count = p->recv_count;
     a.flags = p->flags; a.ticket = p->ticket; a.status = p->status;
     a.rows = p->rows; a.W = p->W; a.E = p->E; a.k = p->k; a.F = p->F; a.M = p->M;
-    a.N = off[p->W]; a.tiles = p->tiles;
+    a.N = off[p->W];
+    // one CTA per 256 tokens of this call (at least one, which writes the counts of an empty
+    // call); the plan's scan words cover the largest call, p->tiles tiles
+    a.tiles = a.N > 0 ? (a.N + kRouteTile - 1) / kRouteTile : 1;
     a.vec16 = (p->k % 4 == 0) && aligned(indices, 16);
     for (int s = 0; s <= p->W; ++s) a.tok_off[s] = off[s];
-    // the routing kernel always runs all `tiles` CTAs: the ticket arithmetic relies on it
     cudaError_t e = launch_route(a, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "ep_dispatch_route: launch");
 
@@ -466,6 +468,19 @@ int ep_combine(ep_plan* p, const void* expert_out, const float* weights, void* o
     cudaError_t e = launch_combine(a, p->dtype == EP_FP16, p->num_sms, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "ep_combine: launch");
     return EP_OK;
+}
+
+// Grouping scan form of the live dispatch.  A rank receives at most one row per routed token,
+// so no rank holds more than N rows: the two-pass scan (per-chunk counts in the plan's scan_cnt)
+// runs only when N spans kScanMinChunks 1024-row chunks, and its chunk stride is the call's,
+// ceil(N / 1024) <= the plan's chunks.  Smaller calls, whatever the plan's capacity, take the
+// one-pass scan, whose chain is then at most two chunks.
+static void set_scan_form(const ep_plan* p, GroupArgs& a)
+{
+    const int64_t chunks = ((int64_t)p->N + kScanChunk - 1) / kScanChunk;
+    const bool two_pass = p->scan_cnt != nullptr && chunks >= kScanMinChunks;
+    a.scan_cnt = two_pass ? p->scan_cnt : nullptr;
+    a.scan_chunks = two_pass ? (int)chunks : 0;
 }
 
 static int check_wire(ep_plan* p, uint64_t epoch, const char* who, int block = 128)
@@ -591,7 +606,7 @@ int ep_group_by_expert(ep_plan* p, void* packed_x, int32_t* packed_count, int32_
     a.map = p->expert_map; a.packed_x = (uint8_t*)packed_x; a.count = packed_count;
     a.src_info = packed_src_info; a.layout_range = (long long*)layout_range;
     a.rows = p->rows; a.row_bytes = p->row_bytes; a.W = p->W; a.E = p->E; a.k = p->k;
-    a.scan_cnt = p->scan_cnt; a.scan_chunks = p->scan_chunks;
+    set_scan_form(p, a);
     cudaError_t e = launch_group(a, p->num_sms, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "ep_group_by_expert: launch");
     p->grouped_epoch = epoch;
@@ -627,7 +642,7 @@ int ep_dispatch_grouped(ep_plan* p, const void* x, const float* weights, const f
     a.recv_idx_out = p->recv_idx; a.recv_w_out = p->recv_w; a.recv_scales_out = p->recv_scales;
     a.rows = p->rows; a.row_bytes = p->row_bytes;
     a.W = p->W; a.E = p->E; a.k = p->k; a.M = p->M; a.F = p->F; a.N = p->N; a.sd = p->sd;
-    a.scan_cnt = p->scan_cnt; a.scan_chunks = p->scan_chunks;
+    set_scan_form(p, a);
     const int ce = pick_chunk_elems(p, p->N);          // rows sliced as the payload scatter's
     a.chunk_bytes = ce * p->elem_bytes;
     a.chunks = (int)((p->H + ce - 1) / ce);

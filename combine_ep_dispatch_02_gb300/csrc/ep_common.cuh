@@ -13,8 +13,9 @@
 //   recv_count   [W]
 //   expert_map   [W][W*M][k]   slot of a received row in its local experts' lists (grouped view)
 //   flags        [tiles][W]    decoupled-lookback scan words of the routing kernel
-//   ticket       u64           monotone tile ticket (never reset; also yields the call stamp),
-//                              followed in its 256-byte block by the work queues, kQueues x 2 u64
+//   ticket       3 x u64       routing: next tile, CTAs finished (both back to zero after every
+//                              launch) and the generation that stamps scan words; followed in
+//                              its 256-byte block by the work queues, kQueues x 2 u64
 //   status       int32         first device-side error
 #pragma once
 
@@ -30,6 +31,12 @@ constexpr int kMaxRanks = 32;       // destination sets are uint32 bit masks
 constexpr int kMaxTopk = 64;        // two 32-slot batches
 constexpr int kRouteTile = 256;     // tokens per routing CTA, one per thread
 constexpr int kRouteThreads = 256;
+constexpr int kRouteControlWords = 3;   // u64: next tile, CTAs done, scan-word generation
+// the routing kernel numbers the grouped view itself for up to this many experts in all (a tile
+// keeps a 256-bit token mask per expert in shared memory) ...
+constexpr int kRouteGroupMaxExperts = 1024;
+// ... when the expert columns' lookback words fit in this
+constexpr long long kRouteGroupMaxFlagBytes = 64ll << 20;
 constexpr int kCopyThreads = 256;   // scatter, wire and grouped-view CTAs: 8 warps, a work unit per warp
 constexpr int kScanChunk = 1024;    // received rows per step of the grouping scan (4 per thread)
 constexpr int kScanMinChunks = 3;   // capacities of this many chunks or more are scanned in two passes
@@ -86,18 +93,32 @@ inline WorkSplit make_work_split(unsigned long long* q, int64_t units, int64_t w
     return s;
 }
 
+// The expert-grouped view numbered by the routing kernel itself (fused dispatch into the grouped
+// view): each tile also scans W*E expert columns, so the lists' slots, counts and layout ranges
+// come out of the same launch as the receive rows.
+struct RouteGroupArgs {
+    unsigned long long* eflags;   // [tiles][W*E] lookback words of the expert columns
+    int32_t* bnd;                 // [W+1][W*E] list prefix at each source's first token (scratch)
+    int32_t* map;                 // [W][W*M][k] slot of a received row in its local experts' lists
+    int32_t* src_info;            // [W*E][W*M] source token index per list slot
+    int32_t* count;               // [W*E] list lengths
+    long long* layout_range;      // [W*E][W] (first slot of source s) << 32 | its slots
+};
+
 struct RouteArgs {
     const int32_t* idx;
     int32_t* fwd;
     int32_t* src_pos;
     int32_t* recv_count;
     unsigned long long* flags;
-    unsigned long long* ticket;
+    unsigned long long* ticket;   // kRouteControlWords: next tile, CTAs done, generation
     int* status;
     int64_t rows;         // W*M
-    int W, E, k, F, M, N, tiles;
+    int W, E, k, F, M, N;
+    int tiles;            // CTAs of this launch: ceil(N / kRouteTile), at least 1
     int vec16;            // index rows may be read as 16-byte vectors (k % 4 == 0, idx 16-B aligned)
     int tok_off[kMaxRanks + 1];   // exclusive prefix of per-rank token counts; tok_off[W] = N
+    RouteGroupArgs grp;   // used by the grouped launch only (launch_route_grouped)
 };
 
 struct ScatterArgs {
@@ -184,6 +205,8 @@ struct GroupArgs {
 
 // Host-side launchers, one per kernel translation unit.
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t stream);
+// routing that also numbers the expert-grouped view (a.grp set; W*E <= kRouteGroupMaxExperts)
+cudaError_t launch_route_grouped(const RouteArgs& a, cudaStream_t stream);
 cudaError_t launch_scatter(const ScatterArgs& a, int num_sms, cudaStream_t stream);
 // BF16 rows in, FP8 e4m3 rows + FP32 scales (one per 128 elements) out.  Here a.row_bytes is
 // the FP8 row (= H), a.chunk_bytes the slice in ELEMENTS (a multiple of 128) and a.sd = H/128.
@@ -271,6 +294,15 @@ __device__ __forceinline__ void st_v4(void* p, const uint4& v)
 {
     asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};"
                  :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
+// 32-byte store (two 16-byte vectors, lo first); p must be 32-byte aligned.  A warp's request
+// then writes whole 32-byte sectors even where lanes are 32 or 64 bytes apart.
+__device__ __forceinline__ void st_v8(void* p, const uint4& lo, const uint4& hi)
+{
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+                 :: "l"(p), "r"(lo.x), "r"(lo.y), "r"(lo.z), "r"(lo.w), "r"(hi.x), "r"(hi.y), "r"(hi.z),
+                    "r"(hi.w) : "memory");
 }
 
 __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p)

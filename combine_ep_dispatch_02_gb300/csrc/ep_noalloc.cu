@@ -29,7 +29,7 @@ int record_error(int code, const char* msg);   // sets the message read by ep_la
 
 namespace {
 
-constexpr int kNoAllocScratchWords = 16384;   // 128 KB: one tile ticket + the scan words
+constexpr int kNoAllocScratchWords = 16384;   // 128 KB: the routing control words + the scan words
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned long long ep_noalloc_scratch[kNoAllocScratchWords];
@@ -107,12 +107,12 @@ extern "C" int ep_route_noalloc(int W, int E, int k, int M, const int32_t* indic
         return ep::record_error(EP_ERR_ARG, "ep_route_noalloc: a pointer is NULL or not 4-byte aligned");
     const int64_t rows = (int64_t)W * M;
     const int tiles = (int)((rows + ep::kRouteTile - 1) / ep::kRouteTile);
-    const int64_t words = 1 + (int64_t)tiles * W;
+    const int64_t words = ep::kRouteControlWords + (int64_t)tiles * W;
     if (words > kNoAllocScratchWords) {
         snprintf(msg, sizeof msg,
                  "ep_route_noalloc: W=%d, max_tok_per_rank=%d needs %lld scan words; the static "
-                 "scratch holds %d (W * ceil(W*M/256) must stay below %d)",
-                 W, M, (long long)words, kNoAllocScratchWords, kNoAllocScratchWords);
+                 "scratch holds %d (W * ceil(W*M/256) must stay within %d)",
+                 W, M, (long long)words, kNoAllocScratchWords, kNoAllocScratchWords - ep::kRouteControlWords);
         return ep::record_error(EP_ERR_ARG, msg);
     }
     ep::RouteArgs a{};
@@ -134,11 +134,16 @@ extern "C" int ep_route_noalloc(int W, int E, int k, int M, const int32_t* indic
     for (int i = 0; i < 5; ++i)
         if ((rc = check_on_device(ptrs[i], names[i], dev)) != EP_OK) return rc;
 
-    // The array keeps the previous call's words: the ticket must restart at 0 and the scan
-    // words must read "not published" for this call's stamp, so both are cleared first.  The
-    // device status is an output and starts clear as well.
+    // One routing CTA per 256 tokens of this call (at least one, which writes the counts of an
+    // empty call).  The array keeps the previous call's words: the control words (ticket,
+    // finished CTAs, generation) must restart at 0 and the scan words this call uses must read
+    // "not published" for its stamp, so they are cleared first.  The device status is an
+    // output and starts clear as well.
+    const int n = a.tok_off[W];
+    const int call_tiles = n > 0 ? (n + ep::kRouteTile - 1) / ep::kRouteTile : 1;
+    const int64_t call_words = ep::kRouteControlWords + (int64_t)call_tiles * W;
     cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t e = cudaMemsetAsync(scratch, 0, (size_t)words * sizeof(unsigned long long), s);
+    cudaError_t e = cudaMemsetAsync(scratch, 0, (size_t)call_words * sizeof(unsigned long long), s);
     if (e == cudaSuccess) e = cudaMemsetAsync(device_status, 0, sizeof(int32_t), s);
     if (e != cudaSuccess) return ep::record_error(EP_ERR_CUDA, cudaGetErrorString(e));
 
@@ -147,12 +152,12 @@ extern "C" int ep_route_noalloc(int W, int E, int k, int M, const int32_t* indic
     a.src_pos = src_token_pos;
     a.recv_count = recv_count;
     a.ticket = scratch;
-    a.flags = scratch + 1;
+    a.flags = scratch + ep::kRouteControlWords;
     a.status = device_status;
     a.rows = rows;
     a.W = W; a.E = E; a.k = k; a.F = W < k ? W : k; a.M = M;
     a.N = a.tok_off[W];
-    a.tiles = tiles;
+    a.tiles = call_tiles;
     a.vec16 = (k % 4 == 0) && ((uintptr_t)indices % 16 == 0);
     e = ep::launch_route(a, s);
     if (e != cudaSuccess) return ep::record_error(EP_ERR_CUDA, cudaGetErrorString(e));

@@ -9,8 +9,9 @@
 // Row numbering.  On every destination rank r, rows go to tokens in flattened (source rank,
 // token) order: slot(s,t,r) = #{earlier tokens that also go to r}.  That is an exclusive
 // prefix sum over tokens of W 0/1 columns, computed here in one pass:
-//   1. one CTA per tile of 256 consecutive tokens takes a tile number from a monotone ticket
-//      (so a CTA only ever waits on tiles whose CTAs are already running);
+//   1. one CTA per tile of 256 consecutive tokens of this call (ceil(N / 256) CTAs, at least
+//      one) takes a tile number from a ticket in launch order (so a CTA only ever waits on
+//      tiles whose CTAs are already running);
 //   2. the destination set of each token is the OR over its k slots of (1 << rank), so a rank
 //      named by several experts counts once; each thread loads its token's whole index row
 //      with 16-byte vectors (top-k 1..64: the pages' run-time routing loops over slot batches,
@@ -21,10 +22,13 @@
 //      over predecessors' words, 256/W' of them per step (W' = W rounded up to a power of 2),
 //      summing until it meets an INCLUSIVE word, and publishes its own INCLUSIVE prefix;
 //   5. each token writes src_pos for each of its rows and its compact forward-map row.
-// Every scan word carries a stamp derived from the ticket (ticket / tiles + 1), so words from
-// the previous call are ignored and no per-call clearing is needed (the pages reuse buffers
-// across calls by means of generation counters).  Waits are bounded: an expired wait
-// records EP_ERR_DEVICE_TIMEOUT and the CTA carries on, so the kernel always terminates.
+// Every scan word carries the call's stamp, a generation count kept on the device, so words
+// from earlier calls are ignored and no per-call clearing is needed (the pages reuse buffers
+// across calls by means of generation counters).  The last CTA to finish returns the ticket to
+// zero and advances the generation, so the next launch on the plan's stream -- eager or a
+// CUDA-graph replay, with any token count -- starts from a clean ticket and a new stamp without
+// a memset.  Waits are bounded: an expired wait records EP_ERR_DEVICE_TIMEOUT and the CTA
+// carries on, so the kernel always terminates.
 #include <climits>
 
 #include "ep_common.cuh"
@@ -90,15 +94,19 @@ __global__ void __launch_bounds__(kRouteThreads) ep_route_kernel(const RouteArgs
     __shared__ int s_excl[kMaxRanks];
     __shared__ int s_incl_at[kMaxRanks];
     __shared__ int s_done[kMaxRanks];
-    __shared__ unsigned long long s_ticket;
+    __shared__ unsigned long long s_ticket, s_gen;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (tid == 0) s_ticket = atomicAdd(a.ticket, 1ull);
+    if (tid == 0) {
+        // ticket[0]: next tile; ticket[1]: CTAs finished; ticket[2]: generation of this launch
+        // (advanced only by the last CTA of the previous launch, which finished before this one)
+        s_ticket = atomicAdd(a.ticket, 1ull);
+        s_gen = ld_relaxed_u64(a.ticket + 2);
+    }
     if (tid <= a.W) s_off[tid] = a.tok_off[tid];
     __syncthreads();
-    const unsigned long long ticket = s_ticket;
-    const int tile = (int)(ticket % (unsigned long long)a.tiles);
-    const uint32_t stamp = (uint32_t)((ticket / (unsigned long long)a.tiles + 1ull) & kStampMask);
+    const int tile = (int)s_ticket;                    // < gridDim.x == a.tiles
+    const uint32_t stamp = (uint32_t)((s_gen + 1ull) & kStampMask);
     const int base = tile * kRouteTile;
 
     const int g = base + tid;
@@ -195,6 +203,18 @@ __global__ void __launch_bounds__(kRouteThreads) ep_route_kernel(const RouteArgs
     }
     if (valid)
         for (; j < a.F; ++j) fwd_row[j] = -1;
+
+    // the last CTA to finish (every CTA has taken its ticket by then) resets the ticket and
+    // advances the generation for the next launch
+    __syncthreads();
+    if (tid == 0) {
+        __threadfence();
+        if (atomicAdd(a.ticket + 1, 1ull) == (unsigned long long)gridDim.x - 1) {
+            atomicExch(a.ticket, 0ull);
+            atomicExch(a.ticket + 1, 0ull);
+            atomicExch(a.ticket + 2, s_gen + 1ull);
+        }
+    }
 }
 
 template <int VEC>

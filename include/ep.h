@@ -305,7 +305,7 @@ int ep_status(ep_plan* p, int* device_status);
  *                  reaches the end of the call                       (output)
  * The kernel's scan words live in one static device array of 16384 64-bit words (128 KB) inside
  * libep.so, held by every GPU that loads the library until the process exits; a shape needs
- * 1 + W * ceil(W*M / 256) words and larger shapes fail with EP_ERR_ARG.  The first call on a
+ * 3 + W * ceil(W*M / 256) words and larger shapes fail with EP_ERR_ARG.  The first call on a
  * device looks up that array's device address (cudaGetSymbolAddress) and should come before any
  * stream capture; the address is kept for the life of the process, so the entry point must not
  * be called on a device after cudaDeviceReset of that device.  The call runs on the current

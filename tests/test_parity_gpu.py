@@ -50,7 +50,8 @@ def test_small_full_scalar_expert(variant):
     _check(wlmod.make_workload("small"), variant)
 
 
-@pytest.mark.parametrize("k", wlmod.TOPK_SWEEP)
+# the workload's sweep, plus 31 and 63: one slot short of a 32-slot batch, in each batch
+@pytest.mark.parametrize("k", sorted(set(wlmod.TOPK_SWEEP) | {31, 63}))
 def test_topk_sweep_fp16(k):
     _check(wlmod.make_workload("topk", k=k))
 
@@ -257,9 +258,72 @@ def test_many_calls_reuse_scan_flags():
     plan.close()
 
 
+def _with_n_tok(wl, n_tok):
+    return wlmod.Workload(**{**wl.__dict__, "n_tok": np.asarray(n_tok, dtype=np.int32)})
+
+
+def test_small_calls_on_a_large_plan():
+    """A plan sized for 2048 tokens per rank (64 routing tiles, 16 grouping chunks per rank)
+    serving calls of 0 to 16384 tokens: the routing grid follows each call (a CTA per 256 of its
+    tokens, at least one), and its ticket and stamp generation reset on the device, so calls of
+    any size interleave on one plan.  Each call is compared with the oracle, and a small call
+    captured in a CUDA graph replays correctly between eager calls of other sizes."""
+    base = wlmod.custom_workload(W=8, E=32, k=8, H=256, M=2048, n_tok=[2048] * 8, seed=31,
+                                 routing="zipf")
+    plan, (x, w, sc, idx) = _setup(base)
+    sizes = [[8] * 8, [0] * 8, [2048] * 8, [1, 0, 0, 0, 0, 0, 0, 2], [300] * 8, [2048] + [0] * 7,
+             [256, 257, 255, 0, 1, 512, 2047, 3], [5] * 8]
+    for n_tok in sizes:
+        wl = _with_n_tok(base, n_tok)
+        disp, _, o_out, o_w = _oracle(wl)
+        gpu_path.compare(wl, gpu_path.run(wl, DEV, plan=plan, do_poison=False), disp, o_out, o_w)
+    # a graph of an 8-token-per-rank dispatch + combine, replayed between eager calls
+    small = _with_n_tok(base, [8] * 8)
+    disp, _, o_out, o_w = _oracle(small)
+    out = torch.zeros((base.W, base.M, base.H), dtype=torch.bfloat16, device=DEV)
+    out_w = torch.zeros((base.W, base.M, base.k), dtype=torch.float32, device=DEV)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        d = plan.dispatch(x, w, sc, idx, small.n_tok, stream=s)
+        plan.combine(d.recv_x, d.recv_w, d.epoch, out=out, out_w=out_w, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        cs = torch.cuda.current_stream()
+        d = plan.dispatch(x, w, sc, idx, small.n_tok, stream=cs)
+        plan.combine(d.recv_x, d.recv_w, d.epoch, out=out, out_w=out_w, stream=cs)
+    for n_tok in ([2048] * 8, [3] * 8, [700] * 8):
+        wl = _with_n_tok(base, n_tok)
+        d_e = plan.dispatch(x, w, sc, idx, wl.n_tok)
+        o = oracle.dispatch(wl.W, wl.E, wl.k, wl.H, wl.elem_bytes, wl.sd, wl.M, wl.x, wl.weights,
+                            wl.scales, wl.indices, wl.n_tok)
+        assert np.array_equal(d_e.recv_count.cpu().numpy(), o["recv_count"])
+        out.zero_()
+        out_w.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(gpu_path.raw(out), o_out)
+        assert np.array_equal(out_w.cpu().numpy().view(np.uint32), o_w.view(np.uint32))
+    assert plan.status() == 0
+    plan.close()
+
+
+def test_grouped_small_call_on_a_two_pass_plan():
+    """Plans whose capacity would take the two-pass grouping scan (16 chunks per rank): a call
+    of 2000 tokens groups with the one-pass scan (no rank can hold more than two chunks of
+    rows), one of 6000 with the two-pass scan at the call's 6-chunk stride."""
+    base = wlmod.custom_workload(W=8, E=4, k=4, H=64, M=2048, n_tok=[2048] * 8, seed=32)
+    for n_tok in ([250] * 8, [750] * 8):
+        wl = _with_n_tok(base, n_tok)
+        _check_grouped(wl)
+        _check_grouped(wl, fused=True)
+
+
 def test_cuda_graph_replay_matches_eager():
     """Dispatch + combine captured once in a CUDA graph and replayed: the per-call stamps live
-    on the device (ticket counter), so replays stay correct and bit-identical to eager calls."""
+    on the device (a generation count), so replays stay correct and bit-identical to eager calls."""
     wl = wlmod.make_workload("small", max_tok=96)
     disp, _, o_out, o_w = _oracle(wl)
     plan, (x, w, sc, idx) = _setup(wl)
@@ -596,6 +660,41 @@ def _check_fp8_wire(wl, variant="auto"):
         assert gpu_path.nan_aware_equal_bf16(out[s, :n], o_out[s, :n]), f"source rank {s}"
         if o_w is not None:
             assert np.array_equal(out_w[s, :n].cpu().numpy().view(np.uint32), o_w[s, :n].view(np.uint32))
+    plan.close()
+
+
+def test_wire_combines_with_16_byte_aligned_out():
+    """The wire combines store an output piece as one 32-byte vector when `out` is 32-byte
+    aligned, and as two 16-byte vectors when it is only 16-byte aligned (the ABI's requirement):
+    both give the oracle's bits."""
+    wl = wlmod.make_workload("dsv3", max_tok=96)
+    disp, _, _, _ = _oracle(wl)
+    plan, (x, w, sc, idx) = _setup(wl)
+    d = plan.dispatch(x, w, sc, idx, wl.n_tok)
+    n_out = wl.W * wl.M * wl.H
+    for fmt in ("fp8", "fp4"):
+        if fmt == "fp8":
+            q, scl = plan.quantize_received(d.recv_x, d.epoch)
+            oq, osc = oracle.quantize_e4m3_blockwise(disp["recv_x"])
+            o_out, _ = oracle.combine_fp8(wl.W, wl.k, wl.H, wl.M, wl.n_tok, disp["slot_of"], oq, osc)
+            comb = plan.combine_fp8
+        else:
+            q, scl = plan.quantize_received_fp4(d.recv_x, d.epoch)
+            oq, osc = oracle.quantize_mxfp4(disp["recv_x"])
+            o_out, _ = oracle.combine_fp4(wl.W, wl.k, wl.H, wl.M, wl.n_tok, disp["slot_of"], oq, osc)
+            comb = plan.combine_fp4
+        buf = torch.zeros(n_out + 16, dtype=torch.bfloat16, device=DEV)
+        for off in (0, 8):                             # 32-byte aligned, then 16 bytes past it
+            out = buf[off:off + n_out].view(wl.W, wl.M, wl.H)
+            assert out.data_ptr() % 32 == (0 if off == 0 else 16)
+            out.zero_()
+            comb(q, scl, None, d.epoch, out=out)
+            torch.cuda.synchronize()
+            got = gpu_path.raw(out)
+            for s_ in range(wl.W):
+                n = int(wl.n_tok[s_])
+                assert gpu_path.nan_aware_equal_bf16(got[s_, :n], o_out[s_, :n]), (fmt, off, s_)
+    assert plan.status() == 0
     plan.close()
 
 
