@@ -94,6 +94,9 @@ __device__ __forceinline__ void add_fp8x16(float (&acc)[16], const uint4& c, flo
     }
 }
 
+// 16 sums as BF16 to dst[0..1]: one 32-byte store when the output is 32-byte aligned (V8), so a
+// warp writes whole sectors although its lanes' pieces are 32 bytes apart; else two 16-byte ones.
+template <bool V8>
 __device__ __forceinline__ void store_bf16x16(uint4* dst, const float (&acc)[16])
 {
     uint32_t w[8];
@@ -102,8 +105,12 @@ __device__ __forceinline__ void store_bf16x16(uint4* dst, const float (&acc)[16]
         const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
         w[i] = *reinterpret_cast<const uint32_t*>(&b);
     }
-    st_v4(dst, make_uint4(w[0], w[1], w[2], w[3]));
-    st_v4(dst + 1, make_uint4(w[4], w[5], w[6], w[7]));
+    if constexpr (V8) {
+        st_v8(dst, make_uint4(w[0], w[1], w[2], w[3]), make_uint4(w[4], w[5], w[6], w[7]));
+    } else {
+        st_v4(dst, make_uint4(w[0], w[1], w[2], w[3]));
+        st_v4(dst + 1, make_uint4(w[4], w[5], w[6], w[7]));
+    }
 }
 
 // Rolling fold of a unit's nd <= 8 rows (lane d of src holds row d): row d's loads of the next
@@ -114,6 +121,7 @@ __device__ __forceinline__ void store_bf16x16(uint4* dst, const float (&acc)[16]
 #endif
 constexpr int kWireDepth = EP_WIRE_DEPTH;
 
+template <bool V8>
 __device__ __forceinline__ void fold_fp8_rows(const WireArgs& a, int src, int nd, int p0, int np,
                                               uint4* dst, int lane)
 {
@@ -155,7 +163,7 @@ __device__ __forceinline__ void fold_fp8_rows(const WireArgs& a, int src, int nd
                     if (pc < np) add_fp8x16(acc, x, xs);
                 }
             }
-            if (pc < np) store_bf16x16(dst + (int64_t)pc * 2, acc);
+            if (pc < np) store_bf16x16<V8>(dst + (int64_t)pc * 2, acc);
         }
     }
 }
@@ -188,13 +196,13 @@ __device__ __forceinline__ void fold_fp8_wide(const WireArgs& a, int src, int nd
             for (int d = 0; d < 8; ++d)
                 if (act && d0 + d < nd) add_fp8x16(acc, b[d], sc[d]);
         }
-        if (act) store_bf16x16(dst + (int64_t)pc * 2, acc);
+        if (act) store_bf16x16<false>(dst + (int64_t)pc * 2, acc);
     }
 }
 
 // A warp owns a (token, slice) unit; lanes own 16-element pieces (16 code bytes, 32 output
 // bytes).  Weight rows are summed as in the 16-bit combine.
-template <bool WIDE>
+template <bool WIDE, bool V8>
 __global__ void __launch_bounds__(kCopyThreads, 2) ep_combine_fp8_kernel(const WireArgs a)
 {
     __shared__ int s_off[kMaxRanks + 1];
@@ -215,7 +223,7 @@ __global__ void __launch_bounds__(kCopyThreads, 2) ep_combine_fp8_kernel(const W
         const int np = (int)min((int64_t)a.chunk_pieces, (a.H >> 4) - p0);
         uint4* dst = reinterpret_cast<uint4*>(a.out + tok * a.H) + (int64_t)p0 * 2;
         if (!WIDE || nd <= 8)
-            fold_fp8_rows(a, src, nd, p0, np, dst, lane);     // nd == 0 stores +0
+            fold_fp8_rows<V8>(a, src, nd, p0, np, dst, lane);     // nd == 0 stores +0
         else
             fold_fp8_wide(a, src, nd, p0, np, dst, lane);
 
@@ -326,6 +334,7 @@ __device__ __forceinline__ void add_fp4x16(float2 (&acc)[8], uint32_t lo, uint32
     }
 }
 
+template <bool V8>
 __device__ __forceinline__ void store_bf16x16(uint4* dst, const float2 (&acc)[8])
 {
     uint32_t w[8];
@@ -334,14 +343,19 @@ __device__ __forceinline__ void store_bf16x16(uint4* dst, const float2 (&acc)[8]
         const __nv_bfloat162 b = __floats2bfloat162_rn(acc[i].x, acc[i].y);
         w[i] = *reinterpret_cast<const uint32_t*>(&b);
     }
-    st_v4(dst, make_uint4(w[0], w[1], w[2], w[3]));
-    st_v4(dst + 1, make_uint4(w[4], w[5], w[6], w[7]));
+    if constexpr (V8) {
+        st_v8(dst, make_uint4(w[0], w[1], w[2], w[3]), make_uint4(w[4], w[5], w[6], w[7]));
+    } else {
+        st_v4(dst, make_uint4(w[0], w[1], w[2], w[3]));
+        st_v4(dst + 1, make_uint4(w[4], w[5], w[6], w[7]));
+    }
 }
 
 // Rolling fold of nd <= 8 rows over the FP4 wire.  A lane owns 32-element blocks (16 code bytes
 // and one scale byte per row); the block's two 16-element halves are summed one after the
 // other, so 16 accumulators are live, and each row's next block is loaded as soon as its
 // upper half has been added.
+template <bool V8>
 __device__ __forceinline__ void fold_fp4_rows(const WireArgs& a, int src, int nd, int b0, int nb,
                                               uint4* dst, int lane)
 {
@@ -367,7 +381,7 @@ __device__ __forceinline__ void fold_fp4_rows(const WireArgs& a, int src, int nd
 #pragma unroll
         for (int d = 0; d < 8; ++d)
             if (d < nd && pc < nb) add_fp4x16(acc, b[d].x, b[d].y, sc[d]);
-        if (pc < nb) store_bf16x16(dst + (int64_t)pc * 4, acc);
+        if (pc < nb) store_bf16x16<V8>(dst + (int64_t)pc * 4, acc);
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = make_float2(0.0f, 0.0f);
 #pragma unroll
@@ -381,7 +395,7 @@ __device__ __forceinline__ void fold_fp4_rows(const WireArgs& a, int src, int nd
                 if (pc < nb) add_fp4x16(acc, z, w, xs);
             }
         }
-        if (pc < nb) store_bf16x16(dst + (int64_t)pc * 4 + 2, acc);
+        if (pc < nb) store_bf16x16<V8>(dst + (int64_t)pc * 4 + 2, acc);
     }
 }
 
@@ -415,14 +429,14 @@ __device__ __forceinline__ void fold_fp4_wide(const WireArgs& a, int src, int nd
                 for (int d = 0; d < 8; ++d)
                     if (act && d0 + d < nd) add_fp4x16(acc, c[d].x, c[d].y, sc[d]);
             }
-            if (act) store_bf16x16(dst + (int64_t)pc * 4 + 2 * half, acc);
+            if (act) store_bf16x16<false>(dst + (int64_t)pc * 4 + 2 * half, acc);
         }
     }
 }
 
 // A warp owns a (token, slice) unit; a.chunk_pieces counts 32-element blocks per slice.
 // Weight rows are summed as in the 16-bit combine.
-template <bool WIDE>
+template <bool WIDE, bool V8>
 __global__ void __launch_bounds__(kCopyThreads, 2) ep_combine_fp4_kernel(const WireArgs a)
 {
     __shared__ int s_off[kMaxRanks + 1];
@@ -442,7 +456,7 @@ __global__ void __launch_bounds__(kCopyThreads, 2) ep_combine_fp4_kernel(const W
         const int nb = (int)min((int64_t)a.chunk_pieces, (a.H >> 5) - b0);
         uint4* dst = reinterpret_cast<uint4*>(a.out + tok * a.H) + (int64_t)b0 * 4;
         if (!WIDE || nd <= 8)
-            fold_fp4_rows(a, src, nd, b0, nb, dst, lane);     // nd == 0 stores +0
+            fold_fp4_rows<V8>(a, src, nd, b0, nb, dst, lane);     // nd == 0 stores +0
         else
             fold_fp4_wide(a, src, nd, b0, nb, dst, lane);
 
@@ -491,16 +505,19 @@ cudaError_t launch_quantise_rows_fp4(const WireArgs& a, int num_sms, cudaStream_
     return cudaGetLastError();
 }
 
+// The output rows take 32-byte stores when `out` is 32-byte aligned (every row offset, tok * 2H,
+// is then too: H is a multiple of 32); a 16-byte aligned `out` takes two 16-byte stores.
+static bool out_32b_aligned(const WireArgs& a) { return ((uintptr_t)a.out & 31u) == 0; }
+
 cudaError_t launch_combine_fp4(const WireArgs& a, int num_sms, cudaStream_t stream)
 {
     const int64_t units = (int64_t)a.N * a.chunks;
     if (units == 0) return cudaSuccess;
-    if (a.F > 8)
-        ep_combine_fp4_kernel<true><<<grid_for((const void*)ep_combine_fp4_kernel<true>, units, num_sms),
-                                      kCopyThreads, 0, stream>>>(a);
-    else
-        ep_combine_fp4_kernel<false><<<grid_for((const void*)ep_combine_fp4_kernel<false>, units, num_sms),
-                                       kCopyThreads, 0, stream>>>(a);
+    const bool v8 = out_32b_aligned(a);
+    // the wide fold (more than 8 rows) stores 16 bytes at a time whatever the alignment
+    void (*k)(WireArgs) = a.F > 8 ? ep_combine_fp4_kernel<true, false>
+                                  : (v8 ? ep_combine_fp4_kernel<false, true> : ep_combine_fp4_kernel<false, false>);
+    k<<<grid_for((const void*)k, units, num_sms), kCopyThreads, 0, stream>>>(a);
     return cudaGetLastError();
 }
 
@@ -508,12 +525,11 @@ cudaError_t launch_combine_fp8(const WireArgs& a, int num_sms, cudaStream_t stre
 {
     const int64_t units = (int64_t)a.N * a.chunks;
     if (units == 0) return cudaSuccess;
-    if (a.F > 8)
-        ep_combine_fp8_kernel<true><<<grid_for((const void*)ep_combine_fp8_kernel<true>, units, num_sms),
-                                      kCopyThreads, 0, stream>>>(a);
-    else
-        ep_combine_fp8_kernel<false><<<grid_for((const void*)ep_combine_fp8_kernel<false>, units, num_sms),
-                                       kCopyThreads, 0, stream>>>(a);
+    const bool v8 = out_32b_aligned(a);
+    // the wide fold (more than 8 rows) stores 16 bytes at a time whatever the alignment
+    void (*k)(WireArgs) = a.F > 8 ? ep_combine_fp8_kernel<true, false>
+                                  : (v8 ? ep_combine_fp8_kernel<false, true> : ep_combine_fp8_kernel<false, false>);
+    k<<<grid_for((const void*)k, units, num_sms), kCopyThreads, 0, stream>>>(a);
     return cudaGetLastError();
 }
 
