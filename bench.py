@@ -271,9 +271,8 @@ def run_ours(args, rank, world, dist):
                                 steps=max(3, min(args.steps, 50)), fmt="fp8")
     wire4 = measure_combine_wire(plan, wl, dev, stream, x, w, idx, P, peak,
                                  steps=max(3, min(args.steps, 50)), fmt="fp4")
-    grouped = measure_grouped(ep, dev, stream, peak, steps=max(3, min(args.steps, 50)))
-    grouped_large = measure_grouped(ep, dev, stream, peak, steps=max(3, min(args.steps, 20)),
-                                    workload="dsv3", max_tok=min(1024, wl.M))
+    grouped = measure_grouped(ep, dev, stream, peak, steps=60)
+    grouped_large = measure_grouped(ep, dev, stream, peak, steps=20, workload="dsv3", max_tok=min(1024, wl.M))
     latency = measure_small_batch_latency(ep, dev, full=(plan, wl, x, w, idx))
     protocol = measure_graph_protocol(plan, wl, dev, x, w, idx, nbytes, peak)
     other = measure_workloads(ep, dev, peak)
@@ -413,61 +412,67 @@ def measure_grouped(ep, dev, stream, peak, steps, workload="small", max_tok=None
     """The expert-grouped (3-D) view and its inverse: by default on the small-batch workload (W=4,
     64 experts per rank, top-8, hidden 7168 BF16, 256 tokens per rank), the regime a grouped GEMM
     consumer runs in; workload="dsv3", max_tok=1024 measures the DeepSeek-V3 shape at 1024
-    tokens per rank, whose grouped view holds 30 GB.  Minimal bytes: grouping reads each
-    received row once and writes one row per (row, local expert) entry; the inverse reads the
-    entries and writes the rows."""
+    tokens per rank, whose grouped view holds 30 GB.  Each call is captured in a CUDA graph and
+    replayed `steps` times (the pages' method): grouping after a dispatch, the inverse, dispatch
+    then grouping, and the fused dispatch into the grouped view; p50 of the replays, back to back
+    (hot) and with a 2x-L2 buffer written before each (l2_flushed, the reported figure).
+    Minimal bytes: grouping reads each received row once and writes one row per (row, local
+    expert) entry; the inverse reads the entries and writes the rows; the fused dispatch reads
+    each source row once and writes the entries and the receive metadata."""
     wl = wlmod.make_workload(workload, max_tok=max_tok)
     plan = ep.Plan(wl.W, wl.E, wl.k, wl.H, "bf16", 0, wl.M, device=dev)
     x = torch.from_numpy(wl.x.view(np.int16)).to(dev)
     idx = torch.from_numpy(wl.indices).to(dev)
     w = torch.from_numpy(wl.weights).to(dev)
-    d = plan.dispatch(x, w, None, idx, wl.n_tok, stream=stream)
-    px, cnt, info, lay = plan.group_by_expert(d.epoch, stream=stream)
-    y = px.view(torch.bfloat16)
-    out = plan.ungroup_by_expert(y, d.epoch, stream=stream)
+    s = torch.cuda.Stream(dev)
+    with torch.cuda.stream(s):
+        d = plan.dispatch(x, w, None, idx, wl.n_tok, stream=s)
+        px, cnt, info, lay = plan.group_by_expert(d.epoch, stream=s)
+        y = px.view(torch.bfloat16)
+        out = plan.ungroup_by_expert(y, d.epoch, stream=s)
+        for _ in range(3):
+            plan.dispatch_grouped(x, w, None, idx, wl.n_tok, packed_x=px, stream=s)
+            d = plan.dispatch(x, w, None, idx, wl.n_tok, stream=s)
+            plan.group_by_expert(d.epoch, packed_x=px, stream=s)
+            plan.ungroup_by_expert(y, d.epoch, out=out, stream=s)
     torch.cuda.synchronize(dev)
     rows = int(d.recv_count.sum())
     entries = int(cnt.sum())
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
-    for e in ev:
-        e[0].record(stream)
-        plan.group_by_expert(d.epoch, packed_x=px, stream=stream)
-        e[1].record(stream)
-        plan.ungroup_by_expert(y, d.epoch, out=out, stream=stream)
-        e[2].record(stream)
-    torch.cuda.synchronize(dev)
-    # unfused (dispatch, then group) against fused (dispatch straight into the grouped view)
-    evf = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
-    for e in evf:
-        e[0].record(stream)
-        d = plan.dispatch(x, w, None, idx, wl.n_tok, stream=stream)
-        plan.group_by_expert(d.epoch, packed_x=px, stream=stream)
-        e[1].record(stream)
-        plan.dispatch_grouped(x, w, None, idx, wl.n_tok, packed_x=px, stream=stream)
-        e[2].record(stream)
-    torch.cuda.synchronize(dev)
+    graphs = {name: torch.cuda.CUDAGraph() for name in ("group", "ungroup", "dispatch_then_group", "fused")}
+    with torch.cuda.graph(graphs["group"], stream=s):
+        plan.group_by_expert(d.epoch, packed_x=px, stream=s)
+    with torch.cuda.graph(graphs["ungroup"], stream=s):
+        plan.ungroup_by_expert(y, d.epoch, out=out, stream=s)
+    with torch.cuda.graph(graphs["dispatch_then_group"], stream=s):
+        d2 = plan.dispatch(x, w, None, idx, wl.n_tok, stream=s)
+        plan.group_by_expert(d2.epoch, packed_x=px, stream=s)
+    with torch.cuda.graph(graphs["fused"], stream=s):
+        plan.dispatch_grouped(x, w, None, idx, wl.n_tok, packed_x=px, stream=s)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    times = _replay_times(graphs, s, flush, steps)
     if plan.status() != 0:
         raise RuntimeError("device status after the grouped layout: %d" % plan.status())
+    p50 = {name: statistics.median(t["l2_flushed"]) for name, t in times.items()}
+    hot = {name: statistics.median(t["hot"]) for name, t in times.items()}
     plan.close()
-    gt = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
-    ut = sum(e[1].elapsed_time(e[2]) for e in ev) / steps
-    unfused = sum(e[0].elapsed_time(e[1]) for e in evf) / steps
-    fused = sum(e[1].elapsed_time(e[2]) for e in evf) / steps
     rb = 2 * wl.H
     gb = rows * (rb + 4 * wl.k) + entries * (rb + 4)
     ub = entries * rb + rows * (rb + 4 * wl.k)
+    fb = wl.N * (rb + 8 * wl.k) + entries * rb + rows * (8 * wl.k + 4)
     desc = ("W=4, 64 experts/rank, top-8, hidden 7168 BF16, 256 tokens/rank" if workload == "small" else
             f"W={wl.W}, {wl.E} experts/rank, top-{wl.k}, hidden {wl.H} BF16, {wl.M} tokens/rank, Zipf(1.2)")
-    del px, y, out
+    del px, y, out, graphs
     torch.cuda.empty_cache()
+    frac = lambda b, us: round(b / (us * 1e-6) / 1e9 / peak, 4)  # noqa: E731
     return {"workload": desc,
             "received_rows": rows, "expert_entries": entries,
-            "group_us": round(gt * 1e3, 2), "group_frac": round(gb / (gt * 1e-3) / 1e9 / peak, 4),
-            "ungroup_us": round(ut * 1e3, 2), "ungroup_frac": round(ub / (ut * 1e-3) / 1e9 / peak, 4),
-            "dispatch_then_group_us": round(unfused * 1e3, 2),
-            "fused_dispatch_grouped_us": round(fused * 1e3, 2),
-            "fused_frac": round((wl.N * (rb + 8 * wl.k) + entries * rb + rows * (8 * wl.k + 4)) /
-                                (fused * 1e-3) / 1e9 / peak, 4)}
+            "group_us": round(p50["group"], 2), "group_frac": frac(gb, p50["group"]),
+            "ungroup_us": round(p50["ungroup"], 2), "ungroup_frac": frac(ub, p50["ungroup"]),
+            "dispatch_then_group_us": round(p50["dispatch_then_group"], 2),
+            "fused_dispatch_grouped_us": round(p50["fused"], 2), "fused_frac": frac(fb, p50["fused"]),
+            "hot_us": {name: round(v, 2) for name, v in hot.items()},
+            "method": f"CUDA-graph replay, p50 of {steps} replays with a 2x-L2 buffer written before each; "
+                      "hot_us: back-to-back replays"}
 
 
 def _replay_times(graphs, s, flush, replays, warm=10):

@@ -31,6 +31,8 @@ struct ep_plan {
     int32_t* expert_map;
     int32_t* scan_cnt;            // two-pass grouping scan counts, or NULL
     int scan_chunks;
+    unsigned long long* eflags;   // grouped routing: expert-column lookback words, or NULL
+    int32_t* bnd;                 // grouped routing: list prefixes at source boundaries
     unsigned long long* flags;
     unsigned long long* ticket;
     unsigned long long* queues;   // kQueues work queues of two words each, after the ticket
@@ -68,8 +70,17 @@ size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 struct Layout {
     size_t recv_x, recv_idx, recv_w, recv_scales, src_pos, fwd, scan_cnt, recv_count, expert_map, flags,
-        ticket, status, total;
+        eflags, bnd, ticket, status, total;
 };
+
+// Whether the routing kernel numbers the grouped view itself (ep_dispatch_grouped in two launches):
+// up to kRouteGroupMaxExperts experts in all, with lookback words [tiles][W*E] within
+// kRouteGroupMaxFlagBytes.  Otherwise the grouped dispatch runs the separate grouping scan.
+bool route_groups(int W, int E, int64_t tiles)
+{
+    const int64_t n_exp = (int64_t)W * E;
+    return n_exp <= kRouteGroupMaxExperts && tiles * n_exp * 8 <= kRouteGroupMaxFlagBytes;
+}
 
 // 1024-row chunks of a rank's receive capacity when the grouping scan runs in two passes (three
 // chunks or more, per-chunk counts within kScanMaxBytes), else 0
@@ -152,6 +163,9 @@ Layout layout_of(int W, int E, int k, int H, int dtype, int sd, int M)
     put(L.recv_count, (size_t)W * 4);
     put(L.expert_map, (size_t)W * rows * k * 4);
     put(L.flags, (size_t)tiles * W * 8);
+    const bool rg = route_groups(W, E, tiles);
+    put(L.eflags, rg ? (size_t)tiles * W * E * 8 : 0);
+    put(L.bnd, rg ? (size_t)(W + 1) * W * E * 4 : 0);
     put(L.ticket, kRouteControlWords * 8 + kQueues * 16);   // routing control, then the work queues
     put(L.status, 4);
     L.total = o;
@@ -281,6 +295,8 @@ int ep_plan_create(ep_plan** out, int W, int E, int k, int H, int dtype, int sd,
     p->scan_chunks = (int)scan_chunks_of(W, E, p->rows);
     p->scan_cnt = p->scan_chunks ? (int32_t*)(b + L.scan_cnt) : nullptr;
     p->flags = (unsigned long long*)(b + L.flags);
+    p->eflags = route_groups(W, E, p->tiles) ? (unsigned long long*)(b + L.eflags) : nullptr;
+    p->bnd = p->eflags ? (int32_t*)(b + L.bnd) : nullptr;
     p->ticket = (unsigned long long*)(b + L.ticket);
     p->queues = p->ticket + kRouteControlWords;
     p->status = (int*)(b + L.status);
@@ -329,8 +345,10 @@ static void fill_out(const ep_plan* p, ep_dispatch_out* out)
     out->epoch = p->epoch;
 }
 
-int ep_dispatch_route(ep_plan* p, const int32_t* indices, const int32_t* n_tok_host, void* stream,
-                      ep_dispatch_out* out)
+// The routing step of every dispatch; with grp set (the grouped dispatch on a plan that has the
+// expert columns' words) the routing kernel also numbers the grouped view.
+static int route_call(ep_plan* p, const int32_t* indices, const int32_t* n_tok_host, void* stream,
+                      ep_dispatch_out* out, const RouteGroupArgs* grp)
 {
     if (!p) return fail(EP_ERR_ARG, "plan is NULL");
     if (!indices || !aligned(indices, 4)) return fail(EP_ERR_ARG, "indices is NULL or not 4-byte aligned");
@@ -356,7 +374,16 @@ int ep_dispatch_route(ep_plan* p, const int32_t* indices, const int32_t* n_tok_h
     a.tiles = a.N > 0 ? (a.N + kRouteTile - 1) / kRouteTile : 1;
     a.vec16 = (p->k % 4 == 0) && aligned(indices, 16);
     for (int s = 0; s <= p->W; ++s) a.tok_off[s] = off[s];
-    cudaError_t e = launch_route(a, (cudaStream_t)stream);
+    cudaError_t e;
+    if (grp) {
+        a.grp = *grp;
+        a.grp.eflags = p->eflags;
+        a.grp.bnd = p->bnd;
+        a.grp.map = p->expert_map;
+        e = launch_route_grouped(a, (cudaStream_t)stream);
+    } else {
+        e = launch_route(a, (cudaStream_t)stream);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "ep_dispatch_route: launch");
 
     p->epoch += 1;
@@ -371,6 +398,12 @@ int ep_dispatch_route(ep_plan* p, const int32_t* indices, const int32_t* n_tok_h
         out->recv_w = p->recv_w;   // filled by the scatter when it is given weights
     }
     return EP_OK;
+}
+
+int ep_dispatch_route(ep_plan* p, const int32_t* indices, const int32_t* n_tok_host, void* stream,
+                      ep_dispatch_out* out)
+{
+    return route_call(p, indices, n_tok_host, stream, out, nullptr);
 }
 
 int ep_dispatch_scatter(ep_plan* p, const void* x, const float* weights, const float* scales,
@@ -629,11 +662,16 @@ int ep_dispatch_grouped(ep_plan* p, const void* x, const float* weights, const f
         !packed_src_info || !aligned(packed_src_info, 4) || !layout_range || !aligned(layout_range, 8))
         return fail(EP_ERR_ARG, "ep_dispatch_grouped: a grouped buffer is NULL or misaligned");
     if (!out) return fail(EP_ERR_ARG, "out is NULL");
-    int rc = ep_dispatch_route(p, indices, n_tok_host, stream, nullptr);
+    // on a plan with the expert columns' words, routing numbers the grouped view as well, and
+    // the copy follows it directly; otherwise the grouping scan runs between them
+    RouteGroupArgs rg{};
+    rg.src_info = packed_src_info; rg.count = packed_count; rg.layout_range = (long long*)layout_range;
+    int rc = route_call(p, indices, n_tok_host, stream, nullptr, p->eflags ? &rg : nullptr);
     if (rc != EP_OK) return rc;
     DeviceGuard g(p->device);
     if (!g.ok) return fail(EP_ERR_CUDA, "cannot select the plan's device %d", p->device);
     GroupArgs a{};
+    a.scan_done = p->eflags != nullptr;
     a.recv_count = p->recv_count; a.src_pos = p->src_pos; a.map = p->expert_map;
     a.packed_x = (uint8_t*)packed_x; a.count = packed_count; a.src_info = packed_src_info;
     a.layout_range = (long long*)layout_range;

@@ -196,6 +196,7 @@ struct GroupArgs {
     int vec16;                   // the index rows grouping reads are 16-byte aligned (k % 4 == 0)
     int32_t* scan_cnt;           // [W*E][scan_chunks][W] plan-owned, or NULL: one-pass scan
     int scan_chunks;             // ceil(W*M / kScanChunk) when scan_cnt is set, else 0
+    int scan_done;               // fused dispatch: routing already numbered the lists (no scan)
     int64_t rows;                // W*M
     int64_t row_bytes;           // payload bytes (grouping) / 16-bit row bytes (inverse)
     int W, E, k, M, F, N, sd;

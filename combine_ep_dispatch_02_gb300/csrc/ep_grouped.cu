@@ -644,7 +644,7 @@ static void launch_group_scan(const GroupArgs& a, int num_sms, cudaStream_t stre
 
 cudaError_t launch_group_from_source(const GroupArgs& a, int num_sms, cudaStream_t stream)
 {
-    launch_group_scan(a, num_sms, stream);
+    if (!a.scan_done) launch_group_scan(a, num_sms, stream);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || a.N == 0) return e;
     const int64_t units = (int64_t)a.N * a.chunks;

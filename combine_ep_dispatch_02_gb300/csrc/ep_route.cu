@@ -85,16 +85,44 @@ __device__ __forceinline__ uint32_t token_mask(const RouteArgs& a, const int32_t
     return m;
 }
 
-template <int VEC>
+// Bounded wait for a predecessor's scan word of this call (stamp); false if it never came.
+__device__ __forceinline__ bool wait_word(const unsigned long long* fp, uint32_t stamp, int* status,
+                                          unsigned long long& f)
+{
+    unsigned ns = 32;
+    for (int it = 0;; ++it) {
+        f = ld_relaxed_u64(fp);
+        if ((uint32_t)(f >> 34) == stamp && ((f >> 32) & 3ull) != 0ull) return true;
+        if (it >= kSpinLimit) {
+            record_status(status, EP_ERR_DEVICE_TIMEOUT);
+            return false;
+        }
+        __nanosleep(ns);
+        if (ns < 256) ns <<= 1;
+    }
+}
+
+// GROUPED: the tile also numbers the expert-grouped view.  Each token marks, for every expert
+// it names (its first top-k slot naming it), its bit in a 256-bit mask of the tile per expert
+// (shared memory, W*E masks); a token's slot in expert e's list is then the tile's exclusive
+// prefix for e, from a decoupled lookback over the W*E expert columns like the one over ranks,
+// plus the marked tokens before it in the tile.  The tile writes the slot into the expert map at
+// the token's receive row on e's rank, the token index into src_info, and, for each source
+// rank whose first token falls in the tile, every list's prefix at that token; the last CTA to
+// finish turns those prefixes into the counts and layout ranges.
+template <int VEC, bool GROUPED>
 __global__ void __launch_bounds__(kRouteThreads) ep_route_kernel(const RouteArgs a)
 {
     __shared__ int s_off[kMaxRanks + 1];
     __shared__ int s_warp[kRouteThreads / 32][kMaxRanks];   // warp totals, then warp prefixes
+    __shared__ unsigned s_rbal[GROUPED ? kRouteThreads / 32 : 1][kMaxRanks];   // ballots per rank
     __shared__ int s_agg[kMaxRanks];
     __shared__ int s_excl[kMaxRanks];
     __shared__ int s_incl_at[kMaxRanks];
     __shared__ int s_done[kMaxRanks];
     __shared__ unsigned long long s_ticket, s_gen;
+    __shared__ int s_last;
+    extern __shared__ uint32_t s_dyn[];   // GROUPED: [W*E][8] token masks, then [W*E] list prefixes
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) {
@@ -116,10 +144,26 @@ __global__ void __launch_bounds__(kRouteThreads) ep_route_kernel(const RouteArgs
         s = rank_of_token(s_off, a.W, g);
         t = g - s_off[s];
     }
-    const uint32_t mask = valid ? token_mask<VEC>(a, a.idx + ((int64_t)s * a.M + t) * a.k) : 0u;
+    const int32_t* ids = a.idx + ((int64_t)s * a.M + t) * a.k;
+    const uint32_t mask = valid ? token_mask<VEC>(a, ids) : 0u;
+    const int n_exp = a.W * a.E;
+    uint64_t firsts = 0;   // GROUPED: top-k slots that are the token's first naming their expert
+    if constexpr (GROUPED) {
+        for (int i = tid; i < n_exp * 8; i += kRouteThreads) s_dyn[i] = 0u;
+        __syncthreads();
+        if (valid)
+            for (int j = 0; j < a.k; ++j) {
+                const int e = __ldg(ids + j);
+                if (e >= 0 && e < n_exp && !(atomicOr(&s_dyn[e * 8 + warp], 1u << lane) & (1u << lane)))
+                    firsts |= 1ull << j;
+            }
+    }
     for (int r = 0; r < a.W; ++r) {
         const unsigned bal = __ballot_sync(0xffffffffu, (mask >> r) & 1u);
-        if (lane == 0) s_warp[warp][r] = __popc(bal);
+        if (lane == 0) {
+            s_warp[warp][r] = __popc(bal);
+            if constexpr (GROUPED) s_rbal[warp][r] = bal;
+        }
     }
     __syncthreads();
 
@@ -142,6 +186,15 @@ __global__ void __launch_bounds__(kRouteThreads) ep_route_kernel(const RouteArgs
         st_relaxed_u64(a.flags + (int64_t)tile * a.W + tid,
                        pack_flag(stamp, tile == 0 ? kFlagInclusive : kFlagAggregate, (uint32_t)run));
     }
+    if constexpr (GROUPED) {   // the tile's total per expert column
+        for (int e = tid; e < n_exp; e += kRouteThreads) {
+            int agg = 0;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) agg += __popc(s_dyn[e * 8 + w]);
+            st_relaxed_u64(a.grp.eflags + (int64_t)tile * n_exp + e,
+                           pack_flag(stamp, tile == 0 ? kFlagInclusive : kFlagAggregate, (uint32_t)agg));
+        }
+    }
     __syncthreads();
 
     if (tile > 0) {
@@ -155,21 +208,7 @@ __global__ void __launch_bounds__(kRouteThreads) ep_route_kernel(const RouteArgs
             unsigned long long f = 0;
             bool have = false;
             if (r < a.W && j >= 0 && !s_done[r]) {
-                const unsigned long long* fp = a.flags + (int64_t)j * a.W + r;
-                unsigned ns = 32;
-                for (int it = 0;; ++it) {
-                    f = ld_relaxed_u64(fp);
-                    if ((uint32_t)(f >> 34) == stamp && ((f >> 32) & 3ull) != 0ull) {
-                        have = true;
-                        break;
-                    }
-                    if (it >= kSpinLimit) {
-                        record_status(a.status, EP_ERR_DEVICE_TIMEOUT);
-                        break;
-                    }
-                    __nanosleep(ns);
-                    if (ns < 256) ns <<= 1;
-                }
+                have = wait_word(a.flags + (int64_t)j * a.W + r, stamp, a.status, f);
                 if (have && ((f >> 32) & 3ull) == kFlagInclusive) atomicMin(&s_incl_at[r], p);
             }
             __syncthreads();
@@ -189,6 +228,60 @@ __global__ void __launch_bounds__(kRouteThreads) ep_route_kernel(const RouteArgs
     if (tile == a.tiles - 1 && tid < a.W) a.recv_count[tid] = s_excl[tid] + s_agg[tid];
     // s_excl / s_warp are final: the loop above ended on a barrier (or tile 0 needs no lookback)
 
+    if constexpr (GROUPED) {
+        // lookback over the expert columns, one thread per column: sum predecessors' words back
+        // to the first INCLUSIVE one (tiles before this one were all issued earlier)
+        int* eex = reinterpret_cast<int*>(s_dyn + n_exp * 8);
+        for (int e = tid; e < n_exp; e += kRouteThreads) {
+            int excl = 0;
+            if (tile > 0) {
+                int agg = 0;
+#pragma unroll
+                for (int w = 0; w < 8; ++w) agg += __popc(s_dyn[e * 8 + w]);
+                for (int j = tile - 1; j >= 0; --j) {
+                    unsigned long long f;
+                    if (!wait_word(a.grp.eflags + (int64_t)j * n_exp + e, stamp, a.status, f)) break;
+                    excl += (int)(uint32_t)f;
+                    if (((f >> 32) & 3ull) == kFlagInclusive) break;
+                }
+                st_relaxed_u64(a.grp.eflags + (int64_t)tile * n_exp + e,
+                               pack_flag(stamp, kFlagInclusive, (uint32_t)(excl + agg)));
+            }
+            eex[e] = excl;
+        }
+        __syncthreads();
+        // each first slot: the list slot, written at the token's receive row on the expert's rank
+        const unsigned lt_ = lanemask_lt();
+        for (uint64_t m = firsts; m; m &= m - 1) {
+            const int j = __ffsll((long long)m) - 1;
+            const int e = __ldg(ids + j);
+            const int r = e / a.E;
+            const uint32_t* bits = s_dyn + e * 8;
+            int slot = eex[e] + __popc(bits[warp] & lt_);
+            for (int w = 0; w < warp; ++w) slot += __popc(bits[w]);
+            const int row = s_excl[r] + s_warp[warp][r] + __popc(s_rbal[warp][r] & lt_);
+            a.grp.map[((int64_t)r * a.rows + row) * a.k + j] = slot;
+            a.grp.src_info[(int64_t)e * a.rows + slot] = t;
+        }
+        // every list's prefix at each source rank's first token that lies in this tile (the end
+        // of the tokens, N, belongs to the last tile)
+        for (int sb = 0; sb <= a.W; ++sb) {
+            const int b = s_off[sb];
+            if (!((b >= base && b < base + kRouteTile) || (b == a.N && tile == a.tiles - 1))) continue;
+            const int pos = b - base;                       // 0..256 tokens of the tile before b
+            for (int e = tid; e < n_exp; e += kRouteThreads) {
+                int pre = eex[e];
+#pragma unroll
+                for (int w = 0; w < 8; ++w) {
+                    const int lo = w * 32;
+                    if (pos >= lo + 32) pre += __popc(s_dyn[e * 8 + w]);
+                    else if (pos > lo) pre += __popc(s_dyn[e * 8 + w] & ((1u << (pos - lo)) - 1u));
+                }
+                a.grp.bnd[(int64_t)sb * n_exp + e] = pre;
+            }
+        }
+    }
+
     int32_t* fwd_row = a.fwd + ((int64_t)s * a.M + t) * a.F;
     const unsigned lt = lanemask_lt();
     int j = 0;
@@ -206,36 +299,65 @@ __global__ void __launch_bounds__(kRouteThreads) ep_route_kernel(const RouteArgs
 
     // the last CTA to finish (every CTA has taken its ticket by then) resets the ticket and
     // advances the generation for the next launch
+    if constexpr (GROUPED) __threadfence();   // this thread's prefixes before the CTA counts itself
     __syncthreads();
     if (tid == 0) {
         __threadfence();
-        if (atomicAdd(a.ticket + 1, 1ull) == (unsigned long long)gridDim.x - 1) {
+        const bool last = atomicAdd(a.ticket + 1, 1ull) == (unsigned long long)gridDim.x - 1;
+        if (last) {
             atomicExch(a.ticket, 0ull);
             atomicExch(a.ticket + 1, 0ull);
             atomicExch(a.ticket + 2, s_gen + 1ull);
+            __threadfence();
+        }
+        s_last = last;
+    }
+    if constexpr (GROUPED) {
+        // the last CTA: list counts and per-source layout ranges from the boundary prefixes,
+        // which every CTA wrote before counting itself finished (L2 reads: other CTAs' stores)
+        __syncthreads();
+        if (s_last) {
+            for (int i = tid; i < n_exp * a.W; i += kRouteThreads) {
+                const int e = i / a.W, sb = i - e * a.W;
+                const int first = __ldcg(a.grp.bnd + (int64_t)sb * n_exp + e);
+                const int next = __ldcg(a.grp.bnd + (int64_t)(sb + 1) * n_exp + e);
+                a.grp.layout_range[i] = ((long long)first << 32) | (long long)(next - first);
+            }
+            for (int e = tid; e < n_exp; e += kRouteThreads)
+                a.grp.count[e] = __ldcg(a.grp.bnd + (int64_t)a.W * n_exp + e);
         }
     }
 }
 
-template <int VEC>
+template <int VEC, bool GROUPED>
 cudaError_t launch_vec(const RouteArgs& a, cudaStream_t stream)
 {
-    ep_route_kernel<VEC><<<a.tiles, kRouteThreads, 0, stream>>>(a);
+    const size_t smem = GROUPED ? (size_t)a.W * a.E * 9 * sizeof(uint32_t) : 0;
+    ep_route_kernel<VEC, GROUPED><<<a.tiles, kRouteThreads, smem, stream>>>(a);
     return cudaGetLastError();
+}
+
+template <bool GROUPED>
+cudaError_t launch_widths(const RouteArgs& a, cudaStream_t stream)
+{
+    // compiled row widths: top-k 4, 8 (the pages' specialised case), 16; others loop at run time
+    if (!a.vec16) return launch_vec<0, GROUPED>(a, stream);
+    switch (a.k) {
+    case 4: return launch_vec<1, GROUPED>(a, stream);
+    case 8: return launch_vec<2, GROUPED>(a, stream);
+    case 16: return launch_vec<4, GROUPED>(a, stream);
+    default: return launch_vec<0, GROUPED>(a, stream);
+    }
 }
 
 }  // namespace
 
-cudaError_t launch_route(const RouteArgs& a, cudaStream_t stream)
+cudaError_t launch_route(const RouteArgs& a, cudaStream_t stream) { return launch_widths<false>(a, stream); }
+
+cudaError_t launch_route_grouped(const RouteArgs& a, cudaStream_t stream)
 {
-    // compiled row widths: top-k 4, 8 (the pages' specialised case), 16; others loop at run time
-    if (!a.vec16) return launch_vec<0>(a, stream);
-    switch (a.k) {
-    case 4: return launch_vec<1>(a, stream);
-    case 8: return launch_vec<2>(a, stream);
-    case 16: return launch_vec<4>(a, stream);
-    default: return launch_vec<0>(a, stream);
-    }
+    if ((int64_t)a.W * a.E > kRouteGroupMaxExperts) return cudaErrorInvalidValue;
+    return launch_widths<true>(a, stream);
 }
 
 }  // namespace ep

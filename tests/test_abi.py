@@ -43,20 +43,31 @@ def _scan_bytes(W, E, M):
     return b if chunks >= 3 and b <= 64 << 20 else 0
 
 
+def _route_group_bytes(W, E, M):
+    # the routing kernel's expert columns (fused grouped dispatch): lookback words [tiles][W*E] u64
+    # and list prefixes [W+1][W*E] int32, for up to 1024 experts and 64 MiB of words
+    tiles = -(-(W * M) // 256)
+    if W * E > 1024 or tiles * W * E * 8 > 64 << 20:
+        return 0, 0
+    return tiles * W * E * 8, (W + 1) * W * E * 4
+
+
 def _layout_bytes(W, E, k, H, eb, sd, M):
     rows = W * M
     F = min(W, k)
     tiles = -(-rows // 256)
     parts = [W * rows * H * eb, W * rows * k * 4, W * rows * k * 4, W * rows * sd * 4, W * rows * 4,
-             rows * F * 4, _scan_bytes(W, E, M), W * 4, W * rows * k * 4, tiles * W * 8, 8, 4]
+             rows * F * 4, _scan_bytes(W, E, M), W * 4, W * rows * k * 4, tiles * W * 8,
+             *_route_group_bytes(W, E, M), 8, 4]
     return sum(_align(p) for p in parts)
 
 
 def test_device_bytes_golden(lib):
     # DeepSeek-V3 shape: recv rows 8 * 32768 * 14336 B, index / weight rows 8 MiB each,
     # src_pos and forward map 1 MiB each, grouping scan counts 256 lists * 32 chunks * 8 sources
-    # * 4 B, the expert-slot map 8 MiB, 128 tiles * 8 scan words, three control words
-    assert lib.ep_plan_device_bytes(8, 32, 8, 7168, ep.EP_BF16, 0, 4096) == 3785630464
+    # * 4 B, the expert-slot map 8 MiB, 128 tiles * 8 scan words, the expert columns' 128 tiles *
+    # 256 words and 9 * 256 list prefixes, the control words
+    assert lib.ep_plan_device_bytes(8, 32, 8, 7168, ep.EP_BF16, 0, 4096) == 3785630464 + 262144 + 9216
     # FP8 with 56 scales per row
     assert lib.ep_plan_device_bytes(8, 96, 6, 7168, ep.EP_FP8_E4M3, 56, 4096) == \
         _layout_bytes(8, 96, 6, 7168, 1, 56, 4096)
@@ -97,6 +108,18 @@ def test_invalid_shapes_rejected_on_host(lib, shape, why):
     assert h.value is None
     assert why in lib.ep_last_error().decode()
     assert lib.ep_plan_device_bytes(*shape) == 0
+
+
+def test_route_group_words_boundary(lib):
+    """The routing kernel's expert columns are allocated for up to 1024 experts in all and 64 MiB
+    of lookback words, else the grouped dispatch keeps the separate grouping scan."""
+    for W, E, M in [(8, 128, 64), (8, 129, 64), (32, 32, 8192), (4, 256, 524288), (4, 256, 524289),
+                    (2, 512, 1 << 20), (2, 512, (1 << 20) + 1)]:
+        assert lib.ep_plan_device_bytes(W, E, 4, 8, ep.EP_BF16, 0, M) == _layout_bytes(W, E, 4, 8, 2, 0, M)
+    assert _route_group_bytes(8, 128, 64)[0] > 0 and _route_group_bytes(8, 129, 64) == (0, 0)
+    # 64 MiB of words exactly (8192 tiles * 1024 experts * 8 B) is kept, one tile more is not
+    assert _route_group_bytes(4, 256, 524288)[0] == 64 << 20
+    assert _route_group_bytes(4, 256, 524289) == (0, 0)
 
 
 def test_combine_offset_limit_boundary(lib):
@@ -153,4 +176,4 @@ def test_mxfp4_dtype_sizes(lib):
     # grouping scan's 256 * 32 * 8 counts
     assert lib.ep_plan_device_bytes(8, 32, 8, 7168, ep.EP_BF16_TO_MXFP4, 0, 4096) == \
         8 * 32768 * 3584 + 3 * (8 << 20) + 8 * 32768 * 224 + 2 * (1 << 20) + 256 * 32 * 8 * 4 + \
-        256 + 8192 + 256 + 256
+        256 + 8192 + 128 * 256 * 8 + 9 * 256 * 4 + 256 + 256

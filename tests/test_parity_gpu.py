@@ -321,6 +321,15 @@ def test_grouped_small_call_on_a_two_pass_plan():
         _check_grouped(wl, fused=True)
 
 
+def test_grouped_fused_routing_tile_boundaries():
+    """The grouped dispatch numbers the lists in its routing kernel: source boundaries on tile
+    edges (256 and 512 tokens, an empty source, the end at exactly three tiles), a single token,
+    and an empty call, each against the oracle, grouped and inverted."""
+    for n_tok in ([256, 256, 0, 256], [0, 0, 1, 0], [0, 0, 0, 0], [255, 1, 257, 0]):
+        wl = wlmod.custom_workload(W=4, E=16, k=5, H=64, M=300, n_tok=n_tok, seed=41)
+        _check_grouped(wl, fused=True, repeats=2)
+
+
 def test_cuda_graph_replay_matches_eager():
     """Dispatch + combine captured once in a CUDA graph and replayed: the per-call stamps live
     on the device (a generation count), so replays stay correct and bit-identical to eager calls."""
