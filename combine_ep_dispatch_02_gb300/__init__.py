@@ -24,7 +24,10 @@ EP_BF16, EP_FP16, EP_FP8_E4M3, EP_BF16_TO_FP8_E4M3, EP_BF16_TO_MXFP4 = 0, 1, 2, 
 DTYPE_CODES = {"bf16": EP_BF16, "fp16": EP_FP16, "fp8": EP_FP8_E4M3, "bf16_fp8": EP_BF16_TO_FP8_E4M3,
                "bf16_mxfp4": EP_BF16_TO_MXFP4}
 EP_OK, EP_ERR_ARG, EP_ERR_ALLOC, EP_ERR_CUDA, EP_ERR_STATE = 0, -1, -2, -3, -4
-EP_ERR_CAPACITY, EP_ERR_INDEX, EP_ERR_DEVICE_TIMEOUT = -5, -6, -7
+EP_ERR_CAPACITY, EP_ERR_INDEX, EP_ERR_DEVICE_TIMEOUT, EP_ERR_DEVICE_BOUNDS = -5, -6, -7, -8
+# phases of ep_probe_read, in the order of its (earliest start, latest end) pairs
+PROBE_PHASES = ("route", "scatter", "combine", "quantise", "wire_combine", "group_scan", "group_copy",
+                "ungroup")
 VARIANTS = {"auto": 0, "whole_row": 1, "tiled_512": 2, "tiled_1024": 3}
 
 # every entry point include/ep.h declares
@@ -32,7 +35,7 @@ EXPORTS = ("ep_plan_create", "ep_plan_destroy", "ep_plan_set_variant", "ep_plan_
            "ep_dispatch", "ep_dispatch_route", "ep_dispatch_scatter", "ep_combine", "ep_reset",
            "ep_status", "ep_strerror", "ep_last_error", "ep_route_noalloc",
            "ep_quantize_received", "ep_combine_fp8", "ep_group_by_expert", "ep_ungroup_by_expert",
-           "ep_dispatch_grouped", "ep_quantize_received_fp4", "ep_combine_fp4")
+           "ep_dispatch_grouped", "ep_quantize_received_fp4", "ep_combine_fp4", "ep_probe_read")
 
 
 class EpError(RuntimeError):
@@ -83,6 +86,7 @@ def load_library(path: Optional[str] = None):
         "ep_dispatch_grouped": (I, [V, V, V, V, V, V, V, V, V, V, V, ctypes.POINTER(DispatchOut)]),
         "ep_quantize_received_fp4": (I, [V, V, V, V, U64, V]),
         "ep_combine_fp4": (I, [V, V, V, V, V, V, U64, V]),
+        "ep_probe_read": (I, [V, ctypes.POINTER(ctypes.c_uint64), I]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -424,6 +428,15 @@ class Plan:
 
     def reset(self, stream=None):
         _check(self._lib.ep_reset(self._h, _stream(stream)))
+
+    def probe(self) -> dict:
+        """``ep_probe_read``: per phase, (earliest start, latest end) in ns of the launches since
+        the last read, or None for a phase that did not run; raises EpError(EP_ERR_STATE) unless
+        the library was built with EP_PROBE."""
+        buf = (ctypes.c_uint64 * (2 * len(PROBE_PHASES)))()
+        _check(self._lib.ep_probe_read(self._h, buf, len(buf)))
+        return {name: (None if buf[2 * i] == 2 ** 64 - 1 else (int(buf[2 * i]), int(buf[2 * i + 1])))
+                for i, name in enumerate(PROBE_PHASES)}
 
     def status(self) -> int:
         v = ctypes.c_int(0)

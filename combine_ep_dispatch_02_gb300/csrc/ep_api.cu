@@ -166,7 +166,10 @@ Layout layout_of(int W, int E, int k, int H, int dtype, int sd, int M)
     const bool rg = route_groups(W, E, tiles);
     put(L.eflags, rg ? (size_t)tiles * W * E * 8 : 0);
     put(L.bnd, rg ? (size_t)(W + 1) * W * E * 4 : 0);
-    put(L.ticket, kRouteControlWords * 8 + kQueues * 16);   // routing control, then the work queues
+    // routing control, the work queues, then the phase probes: one 256-byte block
+    static_assert(kRouteControlWords + 2 * kQueues <= kProbeWordOffset && kProbeWordOffset + 2 * kProbePhases <= 32,
+                  "the control block holds the routing words, the queues and the probes");
+    put(L.ticket, 256);
     put(L.status, 4);
     L.total = o;
     return L;
@@ -186,6 +189,20 @@ struct DeviceGuard {
         if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
     }
 };
+
+// The plan's phase probe words (earliest start, latest end per phase) in its control block.
+unsigned long long* plan_probe(const ep_plan* p) { return p->ticket + kProbeWordOffset; }
+
+// Probe words back to "nothing recorded": earliest start ~0, latest end 0.
+cudaError_t reset_probes(const ep_plan* p)
+{
+    unsigned long long init[2 * kProbePhases];
+    for (int i = 0; i < kProbePhases; ++i) {
+        init[2 * i] = ~0ull;
+        init[2 * i + 1] = 0ull;
+    }
+    return cudaMemcpy(plan_probe(p), init, sizeof init, cudaMemcpyHostToDevice);
+}
 
 int pick_chunk_elems(const ep_plan* p, int N)
 {
@@ -236,6 +253,7 @@ const char* ep_strerror(int code)
     case EP_ERR_CAPACITY: return "token count exceeds max_tok_per_rank";
     case EP_ERR_INDEX: return "expert id out of range (skipped on the device)";
     case EP_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case EP_ERR_DEVICE_BOUNDS: return "device index out of bounds (skipped; EP_CHECKS build)";
     default: return "unknown status";
     }
 }
@@ -302,6 +320,7 @@ int ep_plan_create(ep_plan** out, int W, int E, int k, int H, int dtype, int sd,
     p->status = (int*)(b + L.status);
     // the control words start at zero once; scan flags are stamped per call after that
     e = cudaMemset(b + L.recv_count, 0, L.total - L.recv_count);
+    if (e == cudaSuccess) e = reset_probes(p);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
         cudaFree(p->base);
@@ -365,6 +384,7 @@ static int route_call(ep_plan* p, const int32_t* indices, const int32_t* n_tok_h
     if (!g.ok) return fail(EP_ERR_CUDA, "cannot select the plan's device %d", p->device);
 
     RouteArgs a{};
+    a.probe = plan_probe(p);
     a.idx = indices; a.fwd = p->fwd; a.src_pos = p->src_pos; a.recv_count = p->recv_count;
     a.flags = p->flags; a.ticket = p->ticket; a.status = p->status;
     a.rows = p->rows; a.W = p->W; a.E = p->E; a.k = p->k; a.F = p->F; a.M = p->M;
@@ -425,6 +445,7 @@ int ep_dispatch_scatter(ep_plan* p, const void* x, const float* weights, const f
     if (!g.ok) return fail(EP_ERR_CUDA, "cannot select the plan's device %d", p->device);
 
     ScatterArgs a{};
+    a.status = p->status; a.probe = plan_probe(p);
     a.work.q = p->queues + 2 * kQueueDispatch;
     a.x = (const uint8_t*)x; a.w = weights; a.scales = scales; a.idx = indices; a.fwd = p->fwd;
     a.recv_x = p->recv_x; a.recv_idx = p->recv_idx; a.recv_w = p->recv_w; a.recv_scales = p->recv_scales;
@@ -492,6 +513,7 @@ int ep_combine(ep_plan* p, const void* expert_out, const float* weights, void* o
     if (!g.ok) return fail(EP_ERR_CUDA, "cannot select the plan's device %d", p->device);
 
     CombineArgs a{};
+    a.probe = plan_probe(p);
     a.eo = (const uint16_t*)expert_out; a.w_in = weights; a.fwd = p->fwd;
     a.out = (uint16_t*)out; a.out_w = out_w; a.status = p->status; a.H = p->H;
     a.W = p->W; a.k = p->k; a.F = p->F; a.M = p->M; a.N = p->N;
@@ -538,6 +560,7 @@ int ep_quantize_received(ep_plan* p, const void* expert_out, void* expert_q, flo
     DeviceGuard g(p->device);
     if (!g.ok) return fail(EP_ERR_CUDA, "cannot select the plan's device %d", p->device);
     WireArgs a{};
+    a.status = p->status; a.probe = plan_probe(p);
     a.eo = (const uint16_t*)expert_out; a.q = (uint8_t*)expert_q; a.scales = expert_scales;
     a.recv_count = p->recv_count; a.H = p->H; a.rows = p->rows; a.W = p->W;
     cudaError_t e = launch_quantise_rows(a, p->num_sms, (cudaStream_t)stream);
@@ -562,6 +585,7 @@ int ep_combine_fp8(ep_plan* p, const void* expert_q, const float* expert_scales,
     geo.H = p->H; geo.N = p->N;
     combine_geometry(geo, p->variant, p->num_sms);     // slice size in 8-element vectors
     WireArgs a{};
+    a.status = p->status; a.probe = plan_probe(p);
     a.q = (uint8_t*)expert_q; a.scales = (float*)expert_scales; a.fwd = p->fwd; a.w_in = weights;
     a.out = (uint16_t*)out; a.out_w = out_w; a.H = p->H; a.rows = p->rows;
     a.W = p->W; a.k = p->k; a.F = p->F; a.M = p->M; a.N = p->N;
@@ -584,6 +608,7 @@ int ep_quantize_received_fp4(ep_plan* p, const void* expert_out, void* expert_q,
     DeviceGuard g(p->device);
     if (!g.ok) return fail(EP_ERR_CUDA, "cannot select the plan's device %d", p->device);
     WireArgs a{};
+    a.status = p->status; a.probe = plan_probe(p);
     a.eo = (const uint16_t*)expert_out; a.q = (uint8_t*)expert_q; a.scales = (float*)expert_scales;
     a.recv_count = p->recv_count; a.H = p->H; a.rows = p->rows; a.W = p->W;
     cudaError_t e = launch_quantise_rows_fp4(a, p->num_sms, (cudaStream_t)stream);
@@ -608,6 +633,7 @@ int ep_combine_fp4(ep_plan* p, const void* expert_q, const uint8_t* expert_scale
     geo.H = p->H; geo.N = p->N;
     combine_geometry(geo, p->variant, p->num_sms);     // slice size in 8-element vectors
     WireArgs a{};
+    a.status = p->status; a.probe = plan_probe(p);
     a.q = (uint8_t*)expert_q; a.scales = (float*)expert_scales; a.fwd = p->fwd; a.w_in = weights;
     a.out = (uint16_t*)out; a.out_w = out_w; a.H = p->H; a.rows = p->rows;
     a.W = p->W; a.k = p->k; a.F = p->F; a.M = p->M; a.N = p->N;
@@ -633,6 +659,7 @@ int ep_group_by_expert(ep_plan* p, void* packed_x, int32_t* packed_count, int32_
     DeviceGuard g(p->device);
     if (!g.ok) return fail(EP_ERR_CUDA, "cannot select the plan's device %d", p->device);
     GroupArgs a{};
+    a.status = p->status; a.probe = plan_probe(p);
     a.work.q = p->queues + 2 * kQueueGroup;
     a.vec16 = p->k % 4 == 0;   // receive index rows: 256-byte-aligned buffer, 4k-byte rows
     a.recv_x = p->recv_x; a.recv_idx = p->recv_idx; a.recv_count = p->recv_count; a.src_pos = p->src_pos;
@@ -665,13 +692,15 @@ int ep_dispatch_grouped(ep_plan* p, const void* x, const float* weights, const f
     // on a plan with the expert columns' words, routing numbers the grouped view as well, and
     // the copy follows it directly; otherwise the grouping scan runs between them
     RouteGroupArgs rg{};
-    rg.src_info = packed_src_info; rg.count = packed_count; rg.layout_range = (long long*)layout_range;
+    rg.src_info = packed_src_info;
     int rc = route_call(p, indices, n_tok_host, stream, nullptr, p->eflags ? &rg : nullptr);
     if (rc != EP_OK) return rc;
     DeviceGuard g(p->device);
     if (!g.ok) return fail(EP_ERR_CUDA, "cannot select the plan's device %d", p->device);
     GroupArgs a{};
+    a.status = p->status; a.probe = plan_probe(p);
     a.scan_done = p->eflags != nullptr;
+    a.bnd = p->bnd;
     a.recv_count = p->recv_count; a.src_pos = p->src_pos; a.map = p->expert_map;
     a.packed_x = (uint8_t*)packed_x; a.count = packed_count; a.src_info = packed_src_info;
     a.layout_range = (long long*)layout_range;
@@ -708,6 +737,7 @@ int ep_ungroup_by_expert(ep_plan* p, const void* packed_y, void* out, uint64_t e
     DeviceGuard g(p->device);
     if (!g.ok) return fail(EP_ERR_CUDA, "cannot select the plan's device %d", p->device);
     GroupArgs a{};
+    a.status = p->status; a.probe = plan_probe(p);
     a.recv_idx = p->recv_idx; a.recv_count = p->recv_count; a.map = p->expert_map;
     a.packed_y = (const uint8_t*)packed_y; a.out = (uint8_t*)out;
     a.rows = p->rows; a.row_bytes = (int64_t)p->H * 2; a.W = p->W; a.E = p->E; a.k = p->k;
@@ -724,6 +754,24 @@ int ep_reset(ep_plan* p, void* stream)
     p->routed = false;
     p->live = false;
     return EP_OK;
+}
+
+int ep_probe_read(ep_plan* p, uint64_t* ns_host, int n_words)
+{
+    if (!p || !ns_host || n_words < 0) return fail(EP_ERR_ARG, "ep_probe_read: plan or ns_host is NULL, or n_words < 0");
+#ifndef EP_PROBE
+    return fail(EP_ERR_STATE, "ep_probe_read: this libep.so was built without EP_PROBE");
+#else
+    DeviceGuard g(p->device);
+    if (!g.ok) return fail(EP_ERR_CUDA, "cannot select the plan's device %d", p->device);
+    unsigned long long w[2 * kProbePhases];
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpy(w, plan_probe(p), sizeof w, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = reset_probes(p);
+    if (e != cudaSuccess) return cuda_fail(e, "ep_probe_read");
+    for (int i = 0; i < n_words && i < 2 * kProbePhases; ++i) ns_host[i] = w[i];
+    return EP_OK;
+#endif
 }
 
 int ep_status(ep_plan* p, int* device_status)

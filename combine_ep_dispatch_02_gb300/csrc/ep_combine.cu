@@ -162,6 +162,7 @@ __global__ void __launch_bounds__(kCombThreads, EP_COMBINE_CTAS_PER_SM) ep_combi
 {
     __shared__ int s_off[kMaxRanks + 1];
     if (threadIdx.x <= a.W) s_off[threadIdx.x] = a.tok_off[threadIdx.x];
+    probe_mark(a.probe, kProbeCombine, true);
     __syncthreads();
 
     const int lane = threadIdx.x & 31;
@@ -172,6 +173,7 @@ __global__ void __launch_bounds__(kCombThreads, EP_COMBINE_CTAS_PER_SM) ep_combi
     int src = unit_src(a, s_off, u, lane);
     for (; u < units; u += step) {
         const int src_next = unit_src(a, s_off, u + step, lane);   // lands while this unit folds
+        src = checked_fwd(src, (int64_t)a.W * a.W * a.M, a.status);
         const int nd = __popc(__ballot_sync(0xffffffffu, src >= 0));
         {
             const int g = (int)(u / (uint32_t)a.chunks);
@@ -204,6 +206,7 @@ __global__ void __launch_bounds__(kCombThreads, EP_COMBINE_CTAS_PER_SM) ep_combi
         }
         src = src_next;
     }
+    probe_mark(a.probe, kProbeCombine, false);
 }
 
 template <bool FP16, bool WIDE>

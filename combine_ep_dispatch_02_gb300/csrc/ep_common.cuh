@@ -51,6 +51,15 @@ constexpr uint32_t kStampMask = 0x3FFFFFFFu;
 #endif
 constexpr int kSpinLimit = EP_SPIN_LIMIT;   // polls before a wait gives up with EP_ERR_DEVICE_TIMEOUT
 
+// Phase probes.  Built with -DEP_PROBE, every kernel's warps record, in the plan's control block,
+// the earliest start and the latest end (%globaltimer, ns) of the phase's launches since the
+// last ep_probe_read; other builds record nothing.
+enum ProbePhase {
+    kProbeRoute = 0, kProbeScatter, kProbeCombine, kProbeQuantise, kProbeWireCombine, kProbeGroupScan,
+    kProbeGroupCopy, kProbeUngroup, kProbePhases
+};
+constexpr int kProbeWordOffset = 16;   // u64 words into the 256-byte control block (after the queues)
+
 // Work queues of the persistent copy kernels (see WorkSplit): launches that share a queue must
 // run one after the other, as the calls on one plan do.
 constexpr int kQueueDispatch = 0;   // payload scatters (BF16 / FP8 / MX FP4 rows)
@@ -101,8 +110,6 @@ struct RouteGroupArgs {
     int32_t* bnd;                 // [W+1][W*E] list prefix at each source's first token (scratch)
     int32_t* map;                 // [W][W*M][k] slot of a received row in its local experts' lists
     int32_t* src_info;            // [W*E][W*M] source token index per list slot
-    int32_t* count;               // [W*E] list lengths
-    long long* layout_range;      // [W*E][W] (first slot of source s) << 32 | its slots
 };
 
 struct RouteArgs {
@@ -113,6 +120,7 @@ struct RouteArgs {
     unsigned long long* flags;
     unsigned long long* ticket;   // kRouteControlWords: next tile, CTAs done, generation
     int* status;
+    unsigned long long* probe;    // phase probe words (EP_PROBE builds), or NULL
     int64_t rows;         // W*M
     int W, E, k, F, M, N;
     int tiles;            // CTAs of this launch: ceil(N / kRouteTile), at least 1
@@ -132,6 +140,8 @@ struct ScatterArgs {
     float* recv_w;
     float* recv_scales;
     WorkSplit work;       // q set by the caller, the rest by the launcher
+    int* status;
+    unsigned long long* probe;
     int64_t row_bytes;    // H * element size, a multiple of 16
     int W, k, F, M, sd, N;
     int chunk_bytes;      // bytes of one work unit's slice of a row (multiple of 16)
@@ -146,6 +156,7 @@ struct CombineArgs {
     uint16_t* out;
     float* out_w;
     int* status;
+    unsigned long long* probe;
     int64_t H;
     int W, k, F, M, N;
     int chunk_vecs;       // 16-byte vectors of one work unit's slice of a row
@@ -163,6 +174,8 @@ struct WireArgs {
     const float* w_in;
     uint16_t* out;            // [W][M][H] BF16
     float* out_w;
+    int* status;
+    unsigned long long* probe;
     int64_t H, rows;          // rows = W*M per rank
     int W, k, F, M, N;
     int chunk_pieces;         // 16-element pieces of one combine unit's slice
@@ -193,10 +206,14 @@ struct GroupArgs {
     float* recv_w_out;
     float* recv_scales_out;
     WorkSplit work;              // grouped copy / fused dispatch: q set by the caller
+    int* status;
+    unsigned long long* probe;
     int vec16;                   // the index rows grouping reads are 16-byte aligned (k % 4 == 0)
     int32_t* scan_cnt;           // [W*E][scan_chunks][W] plan-owned, or NULL: one-pass scan
     int scan_chunks;             // ceil(W*M / kScanChunk) when scan_cnt is set, else 0
     int scan_done;               // fused dispatch: routing already numbered the lists (no scan)
+    const int32_t* bnd;          // ... and left every list's prefix at each source's first token,
+                                 // [W+1][W*E], for the copy to write counts and layout ranges
     int64_t rows;                // W*M
     int64_t row_bytes;           // payload bytes (grouping) / 16-bit row bytes (inverse)
     int W, E, k, M, F, N, sd;
@@ -235,6 +252,59 @@ void combine_geometry(CombineArgs& a, int variant, int num_sms);
 __device__ __forceinline__ void record_status(int* status, int code)
 {
     if (*reinterpret_cast<volatile int*>(status) == 0) atomicCAS(status, 0, code);
+}
+
+// EP_CHECKS builds: an index the kernel derived from device data (a forward-map entry, a slot,
+// a receive count) that falls outside its buffer is recorded as EP_ERR_DEVICE_BOUNDS and the
+// access is skipped; other builds compile the check away (the host validated everything else).
+#ifdef EP_CHECKS
+#define EP_IN_BOUNDS(cond, status) ((cond) ? true : (record_status((status), EP_ERR_DEVICE_BOUNDS), false))
+#else
+#define EP_IN_BOUNDS(cond, status) true
+#endif
+
+// A forward-map entry as the copy and combine kernels use it (called by all 32 lanes): in
+// EP_CHECKS builds an entry outside [-1, total rows) makes the whole unit read -1 (skipped), so
+// the unit's valid entries stay packed first.
+__device__ __forceinline__ int checked_fwd(int v, int64_t total_rows, int* status)
+{
+#ifdef EP_CHECKS
+    if (__any_sync(0xffffffffu, v < -1 || (int64_t)v >= total_rows)) {
+        if ((threadIdx.x & 31) == 0) record_status(status, EP_ERR_DEVICE_BOUNDS);
+        return -1;
+    }
+#else
+    (void)total_rows; (void)status;
+#endif
+    return v;
+}
+
+// A rank's receive count as a kernel uses it: in EP_CHECKS builds a count outside [0, rows]
+// reads as 0 (the rank's rows are skipped).
+__device__ __forceinline__ int checked_count(int n, int64_t rows, int* status)
+{
+    return EP_IN_BOUNDS(n >= 0 && (int64_t)n <= rows, status) ? n : 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// EP_PROBE builds: lane 0 of every warp folds its start (begin) or end time into the phase's
+// [earliest start, latest end] pair; `probe` is the plan's probe words (NULL: nothing recorded).
+__device__ __forceinline__ void probe_mark(unsigned long long* probe, int phase, bool begin)
+{
+#ifdef EP_PROBE
+    if (probe != nullptr && (threadIdx.x & 31) == 0) {
+        if (begin) atomicMin(probe + 2 * phase, global_ns());
+        else atomicMax(probe + 2 * phase + 1, global_ns());
+    }
+#else
+    (void)probe; (void)phase; (void)begin;
+#endif
 }
 
 // This warp's first unit, or s.units if it has none.

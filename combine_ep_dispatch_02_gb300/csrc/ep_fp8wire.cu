@@ -23,7 +23,8 @@ constexpr int kQuantUnroll = 4;   // 32-byte pieces per lane in flight
 __global__ void __launch_bounds__(kCopyThreads, 3) ep_quantise_rows_kernel(const WireArgs a)
 {
     __shared__ int s_cnt[kMaxRanks];
-    if (threadIdx.x < a.W) s_cnt[threadIdx.x] = a.recv_count[threadIdx.x];
+    if (threadIdx.x < a.W) s_cnt[threadIdx.x] = checked_count(a.recv_count[threadIdx.x], a.rows, a.status);
+    probe_mark(a.probe, kProbeQuantise, true);
     __syncthreads();
 
     const int lane = threadIdx.x & 31;
@@ -64,6 +65,7 @@ __global__ void __launch_bounds__(kCopyThreads, 3) ep_quantise_rows_kernel(const
             }
         }
     }
+    probe_mark(a.probe, kProbeQuantise, false);
 }
 
 // ---- gather-reduce over the FP8 wire
@@ -207,6 +209,7 @@ __global__ void __launch_bounds__(kCopyThreads, 2) ep_combine_fp8_kernel(const W
 {
     __shared__ int s_off[kMaxRanks + 1];
     if (threadIdx.x <= a.W) s_off[threadIdx.x] = a.tok_off[threadIdx.x];
+    probe_mark(a.probe, kProbeWireCombine, true);
     __syncthreads();
 
     const int lane = threadIdx.x & 31;
@@ -217,7 +220,8 @@ __global__ void __launch_bounds__(kCopyThreads, 2) ep_combine_fp8_kernel(const W
         const int c = (int)(u - (uint32_t)g * (uint32_t)a.chunks);
         const int s = rank_of_token(s_off, a.W, g);
         const int64_t tok = (int64_t)s * a.M + (g - s_off[s]);
-        const int src = lane < a.F ? __ldg(a.fwd + tok * a.F + lane) : -1;
+        const int src = checked_fwd(lane < a.F ? __ldg(a.fwd + tok * a.F + lane) : -1,
+                                    (int64_t)a.W * a.rows, a.status);
         const int nd = __popc(__ballot_sync(0xffffffffu, src >= 0));
         const int p0 = c * a.chunk_pieces;
         const int np = (int)min((int64_t)a.chunk_pieces, (a.H >> 4) - p0);
@@ -239,6 +243,7 @@ __global__ void __launch_bounds__(kCopyThreads, 2) ep_combine_fp8_kernel(const W
             }
         }
     }
+    probe_mark(a.probe, kProbeWireCombine, false);
 }
 
 // ---- the MX FP4 wire (quantiser quantise_mxfp4_32 in ep_common.cuh)
@@ -252,7 +257,8 @@ __device__ __forceinline__ float e8m0_to_float(uint32_t code)
 __global__ void __launch_bounds__(kCopyThreads, 3) ep_quantise_rows_fp4_kernel(const WireArgs a)
 {
     __shared__ int s_cnt[kMaxRanks];
-    if (threadIdx.x < a.W) s_cnt[threadIdx.x] = a.recv_count[threadIdx.x];
+    if (threadIdx.x < a.W) s_cnt[threadIdx.x] = checked_count(a.recv_count[threadIdx.x], a.rows, a.status);
+    probe_mark(a.probe, kProbeQuantise, true);
     __syncthreads();
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = (int64_t)gridDim.x * (kCopyThreads / 32);
@@ -277,6 +283,7 @@ __global__ void __launch_bounds__(kCopyThreads, 3) ep_quantise_rows_fp4_kernel(c
             sc8[u * nblk + b] = (uint8_t)code;
         }
     }
+    probe_mark(a.probe, kProbeQuantise, false);
 }
 
 __device__ __forceinline__ void fma_f32x2(float2& acc, float2 x, unsigned long long ss)
@@ -441,6 +448,7 @@ __global__ void __launch_bounds__(kCopyThreads, 2) ep_combine_fp4_kernel(const W
 {
     __shared__ int s_off[kMaxRanks + 1];
     if (threadIdx.x <= a.W) s_off[threadIdx.x] = a.tok_off[threadIdx.x];
+    probe_mark(a.probe, kProbeWireCombine, true);
     __syncthreads();
     const int lane = threadIdx.x & 31;
     const uint32_t units = (uint32_t)a.N * (uint32_t)a.chunks;
@@ -450,7 +458,8 @@ __global__ void __launch_bounds__(kCopyThreads, 2) ep_combine_fp4_kernel(const W
         const int c = (int)(u - (uint32_t)g * (uint32_t)a.chunks);
         const int s = rank_of_token(s_off, a.W, g);
         const int64_t tok = (int64_t)s * a.M + (g - s_off[s]);
-        const int src = lane < a.F ? __ldg(a.fwd + tok * a.F + lane) : -1;
+        const int src = checked_fwd(lane < a.F ? __ldg(a.fwd + tok * a.F + lane) : -1,
+                                    (int64_t)a.W * a.rows, a.status);
         const int nd = __popc(__ballot_sync(0xffffffffu, src >= 0));
         const int b0 = c * a.chunk_pieces;
         const int nb = (int)min((int64_t)a.chunk_pieces, (a.H >> 5) - b0);
@@ -472,6 +481,7 @@ __global__ void __launch_bounds__(kCopyThreads, 2) ep_combine_fp4_kernel(const W
             }
         }
     }
+    probe_mark(a.probe, kProbeWireCombine, false);
 }
 
 int grid_for(const void* kernel, int64_t warps_needed, int num_sms)

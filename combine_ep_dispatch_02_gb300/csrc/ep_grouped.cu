@@ -138,6 +138,7 @@ __device__ __forceinline__ void assign_chunk(const GroupArgs& a, int r, int64_t 
 template <int VEC>
 __global__ void __launch_bounds__(256) ep_group_kernel(const GroupArgs a)
 {
+    probe_mark(a.probe, kProbeGroupScan, true);
     constexpr int Q = kGroupRowsPerThread;
     __shared__ int s_warp[Q][8];
     __shared__ int s_src[kMaxRanks];
@@ -147,7 +148,7 @@ __global__ void __launch_bounds__(256) ep_group_kernel(const GroupArgs a)
     const int e = blockIdx.x - r * a.E;
     const int32_t ge = r * a.E + e;
     const int64_t list = (int64_t)r * a.E + e;
-    const int n = a.recv_count[r];
+    const int n = checked_count(a.recv_count[r], a.rows, a.status);
     if (tid < kMaxRanks) s_src[tid] = 0;
     if (tid == 0) s_base = 0;
     __syncthreads();
@@ -169,6 +170,7 @@ __global__ void __launch_bounds__(256) ep_group_kernel(const GroupArgs a)
         for (int s = 0; s < tid; ++s) first += s_src[s];
         a.layout_range[list * a.W + tid] = (first << 32) | (long long)s_src[tid];
     }
+    probe_mark(a.probe, kProbeGroupScan, false);
 }
 
 // Two-pass scan, pass 1: grid (W*E lists) x (chunk strides); CTA (list, y) takes chunks y,
@@ -177,6 +179,7 @@ __global__ void __launch_bounds__(256) ep_group_kernel(const GroupArgs a)
 template <int VEC>
 __global__ void __launch_bounds__(256) ep_group_count_kernel(const GroupArgs a)
 {
+    probe_mark(a.probe, kProbeGroupScan, true);
     constexpr int Q = kGroupRowsPerThread;
     __shared__ int s_src[kMaxRanks];
     const int tid = threadIdx.x;
@@ -184,7 +187,7 @@ __global__ void __launch_bounds__(256) ep_group_count_kernel(const GroupArgs a)
     const int e = blockIdx.x - r * a.E;
     const int32_t ge = r * a.E + e;
     const int64_t list = (int64_t)r * a.E + e;
-    const int n = a.recv_count[r];
+    const int n = checked_count(a.recv_count[r], a.rows, a.status);
     for (int c = blockIdx.y; (int64_t)c * kScanChunk < n; c += gridDim.y) {
         if (tid < kMaxRanks) s_src[tid] = 0;
         __syncthreads();
@@ -197,6 +200,7 @@ __global__ void __launch_bounds__(256) ep_group_count_kernel(const GroupArgs a)
         if (tid < a.W) a.scan_cnt[(list * a.scan_chunks + c) * a.W + tid] = s_src[tid];
         __syncthreads();
     }
+    probe_mark(a.probe, kProbeGroupScan, false);
 }
 
 // Pass 2, the same grid: chunk c's base is the sum of scan_cnt over chunks 0..c-1 (all sources),
@@ -206,6 +210,7 @@ __global__ void __launch_bounds__(256) ep_group_count_kernel(const GroupArgs a)
 template <int VEC>
 __global__ void __launch_bounds__(256) ep_group_assign_kernel(const GroupArgs a)
 {
+    probe_mark(a.probe, kProbeGroupScan, true);
     constexpr int Q = kGroupRowsPerThread;
     __shared__ int s_warp[Q][8];
     __shared__ int s_part[8];
@@ -214,7 +219,7 @@ __global__ void __launch_bounds__(256) ep_group_assign_kernel(const GroupArgs a)
     const int e = blockIdx.x - r * a.E;
     const int32_t ge = r * a.E + e;
     const int64_t list = (int64_t)r * a.E + e;
-    const int n = a.recv_count[r];
+    const int n = checked_count(a.recv_count[r], a.rows, a.status);
     const int active = (int)(((int64_t)n + kScanChunk - 1) / kScanChunk);
     const int32_t* cnt = a.scan_cnt + list * a.scan_chunks * a.W;
     if (blockIdx.y == 0 && warp == 0) {       // lane s: source rank s (W <= 32)
@@ -246,6 +251,7 @@ __global__ void __launch_bounds__(256) ep_group_assign_kernel(const GroupArgs a)
         assign_chunk(a, r, list, c * kScanChunk, base, pos, jfirst, s_warp, tid, &total);
         __syncthreads();                      // s_part and s_warp are reused by the next chunk
     }
+    probe_mark(a.probe, kProbeGroupScan, false);
 }
 
 // A received row's top-k entries as the lanes hold them: lane j has entry j and entry j + 32
@@ -283,6 +289,8 @@ __device__ __forceinline__ void resolve_entries(const GroupArgs& a, int r, const
         if (jj < lane && x == e.id0) ok0 = false;
         if (jj < lane + 32 && x == e.id1) ok1 = false;
     }
+    if (ok0) ok0 = EP_IN_BOUNDS(e.slot0 >= 0 && e.slot0 < a.rows, a.status);
+    if (ok1) ok1 = EP_IN_BOUNDS(e.slot1 >= 0 && e.slot1 < a.rows, a.status);
     dest0 = ok0 ? ((int64_t)r * a.E + (e.id0 - lo)) * a.rows + e.slot0 : -1;
     dest1 = ok1 ? ((int64_t)r * a.E + (e.id1 - lo)) * a.rows + e.slot1 : -1;
 }
@@ -299,12 +307,13 @@ __device__ __forceinline__ int64_t received_row(const int* off, int W, int64_t r
 // expert.  The unit count, the rows received by all ranks, is known on the device only.
 __global__ void __launch_bounds__(kCopyThreads) ep_grouped_copy_kernel(const GroupArgs a)
 {
+    probe_mark(a.probe, kProbeGroupCopy, true);
     __shared__ int s_off[kMaxRanks + 1];
     if (threadIdx.x == 0) {
         int run = 0;
         for (int r = 0; r < a.W; ++r) {
             s_off[r] = run;
-            run += a.recv_count[r];
+            run += checked_count(a.recv_count[r], a.rows, a.status);
         }
         s_off[a.W] = run;
     }
@@ -351,6 +360,7 @@ __global__ void __launch_bounds__(kCopyThreads) ep_grouped_copy_kernel(const Gro
         }
     }
     work_retire(ws);
+    probe_mark(a.probe, kProbeGroupCopy, false);
 }
 
 template <bool FP16>
@@ -439,12 +449,13 @@ __device__ __forceinline__ void fold_rd(const uint4* y4, int64_t dest0, int64_t 
 template <bool FP16, bool WIDE>
 __global__ void __launch_bounds__(kCopyThreads, 2) ep_ungroup_kernel(const GroupArgs a)
 {
+    probe_mark(a.probe, kProbeUngroup, true);
     __shared__ int s_off[kMaxRanks + 1];
     if (threadIdx.x == 0) {
         int run = 0;
         for (int r = 0; r < a.W; ++r) {
             s_off[r] = run;
-            run += a.recv_count[r];
+            run += checked_count(a.recv_count[r], a.rows, a.status);
         }
         s_off[a.W] = run;
     }
@@ -519,6 +530,7 @@ __global__ void __launch_bounds__(kCopyThreads, 2) ep_ungroup_kernel(const Group
             }
         }
     }
+    probe_mark(a.probe, kProbeUngroup, false);
 }
 
 // Fused dispatch into the grouped view: warp per source token.  Lane j owns top-k slot j: when
@@ -529,8 +541,21 @@ __global__ void __launch_bounds__(kCopyThreads, 2) ep_ungroup_kernel(const Group
 // rows as in ep_dispatch.  The 2-D payload rows are not written.
 __global__ void __launch_bounds__(kCopyThreads) ep_group_from_source_kernel(const GroupArgs a)
 {
+    probe_mark(a.probe, kProbeGroupCopy, true);
     __shared__ int s_off[kMaxRanks + 1];
     if (threadIdx.x <= a.W) s_off[threadIdx.x] = a.tok_off[threadIdx.x];
+    if (a.scan_done && blockIdx.x == 0) {
+        // routing numbered the lists: the counts and per-source layout ranges follow from each
+        // list's prefix at every source's first token (and at the end of the tokens)
+        const int n_exp = a.W * a.E;
+        for (int i = threadIdx.x; i < n_exp * a.W; i += kCopyThreads) {
+            const int e = i / a.W, sb = i - e * a.W;
+            const int first = a.bnd[(int64_t)sb * n_exp + e];
+            const int next = a.bnd[(int64_t)(sb + 1) * n_exp + e];
+            a.layout_range[i] = ((long long)first << 32) | (long long)(next - first);
+        }
+        for (int e = threadIdx.x; e < n_exp; e += kCopyThreads) a.count[e] = a.bnd[(int64_t)a.W * n_exp + e];
+    }
     __syncthreads();
     const int lane = threadIdx.x & 31;
     const WorkSplit& ws = a.work;
@@ -542,7 +567,8 @@ __global__ void __launch_bounds__(kCopyThreads) ep_group_from_source_kernel(cons
         const int s = rank_of_token(s_off, a.W, g);
         const int64_t tok = (int64_t)s * a.M + (g - s_off[s]);
         const int32_t* ids = a.src_idx + tok * a.k;
-        const int fw = lane < a.F ? __ldg(a.fwd + tok * a.F + lane) : -1;   // receive rows, by rank
+        const int fw = checked_fwd(lane < a.F ? __ldg(a.fwd + tok * a.F + lane) : -1,   // receive rows,
+                                   (int64_t)a.W * a.rows, a.status);                // by rank
         const int nd = __popc(__ballot_sync(0xffffffffu, fw >= 0));
         // metadata rows to the receive rows, as in ep_dispatch (with the first slice)
         for (int d = 0; d < (c == 0 ? nd : 0); ++d) {
@@ -573,7 +599,8 @@ __global__ void __launch_bounds__(kCopyThreads) ep_group_from_source_kernel(cons
             }
             if (rrow >= 0) {
                 const int slot = a.map[rrow * a.k + j];
-                dest = ((int64_t)r * a.E + (e - r * a.E)) * a.rows + slot;
+                if (EP_IN_BOUNDS(slot >= 0 && slot < a.rows, a.status))
+                    dest = ((int64_t)r * a.E + (e - r * a.E)) * a.rows + slot;
             }
             const unsigned has = __ballot_sync(0xffffffffu, dest >= 0);
             if (!has) continue;
@@ -597,6 +624,7 @@ __global__ void __launch_bounds__(kCopyThreads) ep_group_from_source_kernel(cons
         }
     }
     work_retire(ws);
+    probe_mark(a.probe, kProbeGroupCopy, false);
 }
 
 int grid_of(const void* kernel, int64_t warps, int num_sms)
@@ -646,9 +674,10 @@ cudaError_t launch_group_from_source(const GroupArgs& a, int num_sms, cudaStream
 {
     if (!a.scan_done) launch_group_scan(a, num_sms, stream);
     cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess || a.N == 0) return e;
+    if (e != cudaSuccess || (a.N == 0 && !a.scan_done)) return e;   // an empty call still writes the counts
     const int64_t units = (int64_t)a.N * a.chunks;
-    const int grid = grid_of((const void*)ep_group_from_source_kernel, units, num_sms);
+    int grid = grid_of((const void*)ep_group_from_source_kernel, units, num_sms);
+    if (grid < 1) grid = 1;                                // CTA 0 writes the counts of an empty call
     GroupArgs b = a;
     b.work = make_work_split(a.work.q, units, (int64_t)grid * (kCopyThreads / 32));
     ep_group_from_source_kernel<<<grid, kCopyThreads, 0, stream>>>(b);

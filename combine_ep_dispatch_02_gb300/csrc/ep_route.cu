@@ -108,8 +108,8 @@ __device__ __forceinline__ bool wait_word(const unsigned long long* fp, uint32_t
 // prefix for e, from a decoupled lookback over the W*E expert columns like the one over ranks,
 // plus the marked tokens before it in the tile.  The tile writes the slot into the expert map at
 // the token's receive row on e's rank, the token index into src_info, and, for each source
-// rank whose first token falls in the tile, every list's prefix at that token; the last CTA to
-// finish turns those prefixes into the counts and layout ranges.
+// rank whose first token falls in the tile, every list's prefix at that token, from which the
+// copy kernel that follows writes the counts and layout ranges.
 template <int VEC, bool GROUPED>
 __global__ void __launch_bounds__(kRouteThreads) ep_route_kernel(const RouteArgs a)
 {
@@ -121,10 +121,10 @@ __global__ void __launch_bounds__(kRouteThreads) ep_route_kernel(const RouteArgs
     __shared__ int s_incl_at[kMaxRanks];
     __shared__ int s_done[kMaxRanks];
     __shared__ unsigned long long s_ticket, s_gen;
-    __shared__ int s_last;
     extern __shared__ uint32_t s_dyn[];   // GROUPED: [W*E][8] token masks, then [W*E] list prefixes
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    probe_mark(a.probe, kProbeRoute, true);
     if (tid == 0) {
         // ticket[0]: next tile; ticket[1]: CTAs finished; ticket[2]: generation of this launch
         // (advanced only by the last CTA of the previous launch, which finished before this one)
@@ -260,8 +260,10 @@ __global__ void __launch_bounds__(kRouteThreads) ep_route_kernel(const RouteArgs
             int slot = eex[e] + __popc(bits[warp] & lt_);
             for (int w = 0; w < warp; ++w) slot += __popc(bits[w]);
             const int row = s_excl[r] + s_warp[warp][r] + __popc(s_rbal[warp][r] & lt_);
-            a.grp.map[((int64_t)r * a.rows + row) * a.k + j] = slot;
-            a.grp.src_info[(int64_t)e * a.rows + slot] = t;
+            if (EP_IN_BOUNDS(row >= 0 && row < a.rows && slot >= 0 && slot < a.rows, a.status)) {
+                a.grp.map[((int64_t)r * a.rows + row) * a.k + j] = slot;
+                a.grp.src_info[(int64_t)e * a.rows + slot] = t;
+            }
         }
         // every list's prefix at each source rank's first token that lies in this tile (the end
         // of the tokens, N, belongs to the last tile)
@@ -290,8 +292,10 @@ __global__ void __launch_bounds__(kRouteThreads) ep_route_kernel(const RouteArgs
         const unsigned bal = __ballot_sync(0xffffffffu, bit);
         if (bit) {
             const int slot = s_excl[r] + s_warp[warp][r] + __popc(bal & lt);
-            a.src_pos[(int64_t)r * a.rows + slot] = (int32_t)((int64_t)s * a.rows + t);
-            fwd_row[j++] = (int32_t)((int64_t)r * a.rows + slot);
+            if (EP_IN_BOUNDS(slot >= 0 && slot < a.rows, a.status)) {
+                a.src_pos[(int64_t)r * a.rows + slot] = (int32_t)((int64_t)s * a.rows + t);
+                fwd_row[j++] = (int32_t)((int64_t)r * a.rows + slot);
+            }
         }
     }
     if (valid)
@@ -299,32 +303,14 @@ __global__ void __launch_bounds__(kRouteThreads) ep_route_kernel(const RouteArgs
 
     // the last CTA to finish (every CTA has taken its ticket by then) resets the ticket and
     // advances the generation for the next launch
-    if constexpr (GROUPED) __threadfence();   // this thread's prefixes before the CTA counts itself
+    probe_mark(a.probe, kProbeRoute, false);
     __syncthreads();
     if (tid == 0) {
         __threadfence();
-        const bool last = atomicAdd(a.ticket + 1, 1ull) == (unsigned long long)gridDim.x - 1;
-        if (last) {
+        if (atomicAdd(a.ticket + 1, 1ull) == (unsigned long long)gridDim.x - 1) {
             atomicExch(a.ticket, 0ull);
             atomicExch(a.ticket + 1, 0ull);
             atomicExch(a.ticket + 2, s_gen + 1ull);
-            __threadfence();
-        }
-        s_last = last;
-    }
-    if constexpr (GROUPED) {
-        // the last CTA: list counts and per-source layout ranges from the boundary prefixes,
-        // which every CTA wrote before counting itself finished (L2 reads: other CTAs' stores)
-        __syncthreads();
-        if (s_last) {
-            for (int i = tid; i < n_exp * a.W; i += kRouteThreads) {
-                const int e = i / a.W, sb = i - e * a.W;
-                const int first = __ldcg(a.grp.bnd + (int64_t)sb * n_exp + e);
-                const int next = __ldcg(a.grp.bnd + (int64_t)(sb + 1) * n_exp + e);
-                a.grp.layout_range[i] = ((long long)first << 32) | (long long)(next - first);
-            }
-            for (int e = tid; e < n_exp; e += kRouteThreads)
-                a.grp.count[e] = __ldcg(a.grp.bnd + (int64_t)a.W * n_exp + e);
         }
     }
 }

@@ -25,6 +25,7 @@ __global__ void __launch_bounds__(kCopyThreads) ep_scatter_kernel(const ScatterA
 {
     __shared__ int s_off[kMaxRanks + 1];
     if (threadIdx.x <= a.W) s_off[threadIdx.x] = a.tok_off[threadIdx.x];
+    probe_mark(a.probe, kProbeScatter, true);
     __syncthreads();
 
     const int lane = threadIdx.x & 31;
@@ -35,7 +36,7 @@ __global__ void __launch_bounds__(kCopyThreads) ep_scatter_kernel(const ScatterA
         const int gv = (int)(v / a.chunks);
         const int sv = rank_of_token(s_off, a.W, gv);
         const int64_t tv = (int64_t)sv * a.M + (gv - s_off[sv]);
-        return lane < a.F ? __ldg(a.fwd + tv * a.F + lane) : -1;
+        return checked_fwd(lane < a.F ? __ldg(a.fwd + tv * a.F + lane) : -1, (int64_t)a.W * a.W * a.M, a.status);
     };
     const WorkSplit& ws = a.work;
     uint32_t u_next = work_first(ws);
@@ -85,6 +86,7 @@ __global__ void __launch_bounds__(kCopyThreads) ep_scatter_kernel(const ScatterA
             }
         }
     }
+    probe_mark(a.probe, kProbeScatter, false);
     work_retire(ws);
 }
 
@@ -99,6 +101,7 @@ __global__ void __launch_bounds__(kCopyThreads, 3) ep_scatter_quant_kernel(const
 {
     __shared__ int s_off[kMaxRanks + 1];
     if (threadIdx.x <= a.W) s_off[threadIdx.x] = a.tok_off[threadIdx.x];
+    probe_mark(a.probe, kProbeScatter, true);
     __syncthreads();
 
     const int lane = threadIdx.x & 31;
@@ -110,7 +113,8 @@ __global__ void __launch_bounds__(kCopyThreads, 3) ep_scatter_quant_kernel(const
         const int c = (int)(u - (int64_t)g * a.chunks);
         const int s = rank_of_token(s_off, a.W, g);
         const int64_t tok = (int64_t)s * a.M + (g - s_off[s]);
-        const int dest = lane < a.F ? __ldg(a.fwd + tok * a.F + lane) : -1;
+        const int dest = checked_fwd(lane < a.F ? __ldg(a.fwd + tok * a.F + lane) : -1,
+                                     (int64_t)a.W * a.W * a.M, a.status);
         const int nd = __popc(__ballot_sync(0xffffffffu, dest >= 0));
 
         const int64_t h0 = (int64_t)c * a.chunk_bytes;               // elements
@@ -164,6 +168,7 @@ __global__ void __launch_bounds__(kCopyThreads, 3) ep_scatter_quant_kernel(const
             }
         }
     }
+    probe_mark(a.probe, kProbeScatter, false);
     work_retire(ws);
 }
 
@@ -174,6 +179,7 @@ __global__ void __launch_bounds__(kCopyThreads, 3) ep_scatter_quant_fp4_kernel(c
 {
     __shared__ int s_off[kMaxRanks + 1];
     if (threadIdx.x <= a.W) s_off[threadIdx.x] = a.tok_off[threadIdx.x];
+    probe_mark(a.probe, kProbeScatter, true);
     __syncthreads();
 
     const int lane = threadIdx.x & 31;
@@ -187,7 +193,8 @@ __global__ void __launch_bounds__(kCopyThreads, 3) ep_scatter_quant_fp4_kernel(c
         const int c = (int)(u - (int64_t)g * a.chunks);
         const int s = rank_of_token(s_off, a.W, g);
         const int64_t tok = (int64_t)s * a.M + (g - s_off[s]);
-        const int dest = lane < a.F ? __ldg(a.fwd + tok * a.F + lane) : -1;
+        const int dest = checked_fwd(lane < a.F ? __ldg(a.fwd + tok * a.F + lane) : -1,
+                                     (int64_t)a.W * a.W * a.M, a.status);
         const int nd = __popc(__ballot_sync(0xffffffffu, dest >= 0));
 
         const int64_t h0 = (int64_t)c * a.chunk_bytes;                // elements
@@ -223,6 +230,7 @@ __global__ void __launch_bounds__(kCopyThreads, 3) ep_scatter_quant_fp4_kernel(c
             }
         }
     }
+    probe_mark(a.probe, kProbeScatter, false);
     work_retire(ws);
 }
 

@@ -78,7 +78,9 @@ enum ep_status_code {
     EP_ERR_STATE = -4,          /* combine without a live dispatch, or with a stale epoch   */
     EP_ERR_CAPACITY = -5,       /* a rank's token count exceeds max_tok_per_rank            */
     EP_ERR_INDEX = -6,          /* device: an expert id outside [0, W*E) was skipped        */
-    EP_ERR_DEVICE_TIMEOUT = -7  /* device: a bounded wait expired; outputs are not valid    */
+    EP_ERR_DEVICE_TIMEOUT = -7, /* device: a bounded wait expired; outputs are not valid    */
+    EP_ERR_DEVICE_BOUNDS = -8   /* device (EP_CHECKS builds): an index derived on the device
+                                   fell outside its buffer; the access was skipped         */
 };
 
 /* Work split of the payload scatter and of combine (a performance choice; never changes
@@ -317,6 +319,19 @@ int ep_status(ep_plan* p, int* device_status);
 int ep_route_noalloc(int W, int experts_per_rank, int topk, int max_tok_per_rank,
                      const int32_t* indices, const int32_t* n_tok_host, int32_t* src_token_pos,
                      int32_t* recv_count, int32_t* fwd_map, int32_t* device_status, void* stream);
+
+/*
+ * Phase probes (MORI-EP guide, section 11 "Profiling with MORI-VIZ", and the phase probes of the
+ * gfx1250 EPv2 PR's commit log: device timestamps per phase of dispatch and combine).  A
+ * libep.so built with -DEP_PROBE has every kernel's warps record, per phase, the earliest start
+ * and the latest end (%globaltimer, nanoseconds) of the launches on this plan since the last
+ * read.  ep_probe_read waits for the device, copies min(n_words, 16) words into ns_host --
+ * pairs (earliest start, latest end) for the phases route, scatter, combine, quantise (received
+ * rows to a wire), wire combine, grouping scan, grouped copy, ungroup, in that order; a phase
+ * with no launch reads (2^64 - 1, 0) -- and resets them.  A library built without EP_PROBE
+ * records nothing and returns EP_ERR_STATE; EP_ERR_ARG for NULL arguments.
+ */
+int ep_probe_read(ep_plan* p, uint64_t* ns_host, int n_words);
 
 /* Static description of a status code ("unknown status" for any other value); never NULL.
  * With ep_last_error, the host side of the staging PR's caller contract ("refactor(EPv2):

@@ -145,8 +145,10 @@ def test_null_plan_calls_fail_cleanly(lib):
     st = ctypes.c_int(0)
     assert lib.ep_status(None, ctypes.byref(st)) == ep.EP_ERR_ARG
     assert lib.ep_plan_destroy(None) == ep.EP_OK
-    for code in range(-7, 1):
-        assert lib.ep_strerror(code)
+    for code in range(-8, 1):
+        assert lib.ep_strerror(code) and lib.ep_strerror(code) != b"unknown status"
+    buf = (ctypes.c_uint64 * 16)()
+    assert lib.ep_probe_read(None, buf, 16) == ep.EP_ERR_ARG
 
 
 def test_binding_fails_loudly_without_library(tmp_path):
