@@ -364,15 +364,13 @@ static void fill_out(const ep_plan* p, ep_dispatch_out* out)
     out->epoch = p->epoch;
 }
 
-// The routing step of every dispatch; with grp set (the grouped dispatch on a plan that has the
-// expert columns' words) the routing kernel also numbers the grouped view.
-static int route_call(ep_plan* p, const int32_t* indices, const int32_t* n_tok_host, void* stream,
-                      ep_dispatch_out* out, const RouteGroupArgs* grp)
+// Arguments of the routing step of a call, after validating indices and the token counts.
+static int route_prepare(ep_plan* p, const int32_t* indices, const int32_t* n_tok_host, RouteArgs& a,
+                         int (&off)[kMaxRanks + 1])
 {
     if (!p) return fail(EP_ERR_ARG, "plan is NULL");
     if (!indices || !aligned(indices, 4)) return fail(EP_ERR_ARG, "indices is NULL or not 4-byte aligned");
     if (!n_tok_host) return fail(EP_ERR_ARG, "n_tok_host is NULL");
-    int off[kMaxRanks + 1];
     off[0] = 0;
     for (int s = 0; s < p->W; ++s) {
         if (n_tok_host[s] < 0) return fail(EP_ERR_ARG, "n_tok[%d]=%d < 0", s, n_tok_host[s]);
@@ -380,10 +378,7 @@ static int route_call(ep_plan* p, const int32_t* indices, const int32_t* n_tok_h
             return fail(EP_ERR_CAPACITY, "n_tok[%d]=%d exceeds max_tok_per_rank=%d", s, n_tok_host[s], p->M);
         off[s + 1] = off[s] + n_tok_host[s];
     }
-    DeviceGuard g(p->device);
-    if (!g.ok) return fail(EP_ERR_CUDA, "cannot select the plan's device %d", p->device);
-
-    RouteArgs a{};
+    a = RouteArgs{};
     a.probe = plan_probe(p);
     a.idx = indices; a.fwd = p->fwd; a.src_pos = p->src_pos; a.recv_count = p->recv_count;
     a.flags = p->flags; a.ticket = p->ticket; a.status = p->status;
@@ -394,6 +389,32 @@ static int route_call(ep_plan* p, const int32_t* indices, const int32_t* n_tok_h
     a.tiles = a.N > 0 ? (a.N + kRouteTile - 1) / kRouteTile : 1;
     a.vec16 = (p->k % 4 == 0) && aligned(indices, 16);
     for (int s = 0; s <= p->W; ++s) a.tok_off[s] = off[s];
+    return EP_OK;
+}
+
+// Host state of the plan once a routing step is enqueued: a new epoch, routed, not yet live.
+static void route_commit(ep_plan* p, const RouteArgs& a, const int (&off)[kMaxRanks + 1], const int32_t* indices)
+{
+    p->epoch += 1;
+    p->routed = true;
+    p->live = false;
+    p->has_w = false;
+    p->routed_idx = indices;
+    p->N = a.N;
+    memcpy(p->tok_off, off, sizeof off);
+}
+
+// The routing step of every dispatch; with grp set (the grouped dispatch on a plan that has the
+// expert columns' words) the routing kernel also numbers the grouped view.
+static int route_call(ep_plan* p, const int32_t* indices, const int32_t* n_tok_host, void* stream,
+                      ep_dispatch_out* out, const RouteGroupArgs* grp)
+{
+    RouteArgs a;
+    int off[kMaxRanks + 1];
+    int rc = route_prepare(p, indices, n_tok_host, a, off);
+    if (rc != EP_OK) return rc;
+    DeviceGuard g(p->device);
+    if (!g.ok) return fail(EP_ERR_CUDA, "cannot select the plan's device %d", p->device);
     cudaError_t e;
     if (grp) {
         a.grp = *grp;
@@ -405,14 +426,7 @@ static int route_call(ep_plan* p, const int32_t* indices, const int32_t* n_tok_h
         e = launch_route(a, (cudaStream_t)stream);
     }
     if (e != cudaSuccess) return cuda_fail(e, "ep_dispatch_route: launch");
-
-    p->epoch += 1;
-    p->routed = true;
-    p->live = false;
-    p->has_w = false;
-    p->routed_idx = indices;
-    p->N = a.N;
-    memcpy(p->tok_off, off, sizeof off);
+    route_commit(p, a, off, indices);
     if (out) {
         fill_out(p, out);
         out->recv_w = p->recv_w;   // filled by the scatter when it is given weights
@@ -426,8 +440,9 @@ int ep_dispatch_route(ep_plan* p, const int32_t* indices, const int32_t* n_tok_h
     return route_call(p, indices, n_tok_host, stream, out, nullptr);
 }
 
-int ep_dispatch_scatter(ep_plan* p, const void* x, const float* weights, const float* scales,
-                        const int32_t* indices, void* stream)
+// Arguments of the payload scatter of the routed call, after validating the payload arguments.
+static int scatter_prepare(ep_plan* p, const void* x, const float* weights, const float* scales,
+                           const int32_t* indices, ScatterArgs& a)
 {
     if (!p) return fail(EP_ERR_ARG, "plan is NULL");
     if (!p->routed) return fail(EP_ERR_STATE, "ep_dispatch_scatter without a preceding ep_dispatch_route");
@@ -441,10 +456,7 @@ int ep_dispatch_scatter(ep_plan* p, const void* x, const float* weights, const f
         if (p->sd == 0 && scales) return fail(EP_ERR_ARG, "scales given but the plan has scale_dim 0");
     }
     if (indices != p->routed_idx) return fail(EP_ERR_ARG, "indices differ from the routed ones");
-    DeviceGuard g(p->device);
-    if (!g.ok) return fail(EP_ERR_CUDA, "cannot select the plan's device %d", p->device);
-
-    ScatterArgs a{};
+    a = ScatterArgs{};
     a.status = p->status; a.probe = plan_probe(p);
     a.work.q = p->queues + 2 * kQueueDispatch;
     a.x = (const uint8_t*)x; a.w = weights; a.scales = scales; a.idx = indices; a.fwd = p->fwd;
@@ -457,13 +469,29 @@ int ep_dispatch_scatter(ep_plan* p, const void* x, const float* weights, const f
     a.chunks = (int)((p->H + ce - 1) / ce);
     if (int rc = check_units(a.N, a.chunks, "ep_dispatch_scatter")) return rc;
     for (int s = 0; s <= p->W; ++s) a.tok_off[s] = p->tok_off[s];
+    return EP_OK;
+}
+
+static void scatter_commit(ep_plan* p, const float* weights)
+{
+    p->routed = false;
+    p->live = true;
+    p->has_w = weights != nullptr;
+}
+
+int ep_dispatch_scatter(ep_plan* p, const void* x, const float* weights, const float* scales,
+                        const int32_t* indices, void* stream)
+{
+    ScatterArgs a;
+    int rc = scatter_prepare(p, x, weights, scales, indices, a);
+    if (rc != EP_OK) return rc;
+    DeviceGuard g(p->device);
+    if (!g.ok) return fail(EP_ERR_CUDA, "cannot select the plan's device %d", p->device);
     cudaError_t e = p->fp4 ? launch_scatter_quant_fp4(a, p->num_sms, (cudaStream_t)stream)
                     : p->quantise ? launch_scatter_quant(a, p->num_sms, (cudaStream_t)stream)
                                   : launch_scatter(a, p->num_sms, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "ep_dispatch_scatter: launch");
-    p->routed = false;
-    p->live = true;
-    p->has_w = weights != nullptr;
+    scatter_commit(p, weights);
     return EP_OK;
 }
 

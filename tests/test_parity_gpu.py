@@ -321,6 +321,61 @@ def test_grouped_small_call_on_a_two_pass_plan():
         _check_grouped(wl, fused=True)
 
 
+def test_single_tile_calls():
+    """Calls around one routing tile (0, 1, 255, 256 and 257 tokens, and the full 800) through
+    ep_dispatch and through ep_dispatch_route + ep_dispatch_scatter give the oracle's rows; small
+    and large calls, eager and replayed from a CUDA graph, interleave on one plan; an invalid
+    expert id in a small call is skipped and reported."""
+    base = wlmod.custom_workload(W=4, E=8, k=6, H=264, M=200, n_tok=[200] * 4, seed=51, routing="zipf")
+    plan, (x, w, sc, idx) = _setup(base)
+    for n_tok in ([0, 0, 0, 0], [0, 1, 0, 0], [64, 64, 63, 64], [64, 64, 64, 64], [64, 65, 64, 64],
+                  [200, 200, 200, 200], [1, 0, 0, 2]):
+        wl = _with_n_tok(base, n_tok)
+        disp, _, o_out, o_w = _oracle(wl)
+        gpu_path.compare(wl, gpu_path.run(wl, DEV, plan=plan, do_poison=False), disp, o_out, o_w)
+        d = plan.dispatch_route(idx, wl.n_tok)                 # the two phases called apart: same rows
+        plan.dispatch_scatter(x, w, sc, idx)
+        torch.cuda.synchronize()
+        cnt = d.recv_count.cpu().numpy()
+        assert np.array_equal(cnt, disp["recv_count"])
+        for r in range(wl.W):
+            n = int(cnt[r])
+            assert np.array_equal(d.src_token_pos[r, :n].cpu().numpy(), disp["src_pos"][r, :n])
+            assert np.array_equal(gpu_path.raw(d.recv_x)[r, :n], disp["recv_x"][r, :n])
+    # a 40-token call captured in a graph, replayed between multi-tile calls
+    small = _with_n_tok(base, [10, 10, 10, 10])
+    disp, _, o_out, o_w = _oracle(small)
+    out = torch.zeros((base.W, base.M, base.H), dtype=torch.bfloat16, device=DEV)
+    out_w = torch.zeros((base.W, base.M, base.k), dtype=torch.float32, device=DEV)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        d = plan.dispatch(x, w, sc, idx, small.n_tok, stream=s)
+        plan.combine(d.recv_x, d.recv_w, d.epoch, out=out, out_w=out_w, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        cs = torch.cuda.current_stream()
+        d = plan.dispatch(x, w, sc, idx, small.n_tok, stream=cs)
+        plan.combine(d.recv_x, d.recv_w, d.epoch, out=out, out_w=out_w, stream=cs)
+    for n_tok in ([200] * 4, [3, 0, 0, 0], [150] * 4):
+        plan.dispatch(x, w, sc, idx, n_tok)
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(gpu_path.raw(out), o_out)
+        assert np.array_equal(out_w.cpu().numpy().view(np.uint32), o_w.view(np.uint32))
+    assert plan.status() == 0
+    # an invalid id in a small call: skipped on the device and reported
+    bad = wlmod.Workload(**{**small.__dict__, "indices": small.indices.copy()})
+    bad.indices[1, 2, 0] = base.W * base.E + 5
+    ib = torch.from_numpy(bad.indices).to(DEV)
+    plan.dispatch(x, w, sc, ib, bad.n_tok)
+    assert plan.status() == ep.EP_ERR_INDEX
+    plan.close()
+
+
 def test_grouped_fused_routing_tile_boundaries():
     """The grouped dispatch numbers the lists in its routing kernel: source boundaries on tile
     edges (256 and 512 tokens, an empty source, the end at exactly three tiles), a single token,
