@@ -93,9 +93,13 @@ def recorded_traffic(kernel: str, algorithmic_bytes: int):
     if rec.get("code_digest") != cur:
         return None, "kernel changed since the recorded capture"
     ratio = rec["dram_bytes_per_launch"] / rec["algorithmic_bytes_per_launch"]
+    if rec["algorithmic_bytes_per_launch"] == algorithmic_bytes:     # captured at this very size
+        return int(rec["dram_bytes_per_launch"]), (
+            f"ncu dram__bytes_read.sum + dram__bytes_write.sum of {rec['case']} (this launch's size), "
+            f"{ratio:.4f} x algorithmic bytes")
     return int(round(ratio * algorithmic_bytes)), (
         f"ncu dram__bytes_read.sum + dram__bytes_write.sum of {rec['case']}, "
-        f"{ratio:.4f} x algorithmic bytes, scaled to this launch's algorithmic bytes")
+        f"{ratio:.4f} x algorithmic bytes, scaled to this launch's algorithmic bytes (a lower bound)")
 
 
 # ----------------------------------------------------------------------------- clocks
