@@ -611,9 +611,12 @@ def graph_protocol(plan, wl, dev, x, w, sc, idx, nbytes, peak, expert_out=None, 
             per_round = [[sample(True, r * samples + i) for i in range(samples)] for r in range(rounds)]
             hot = [sample(False, i) for i in range(samples)]
             p50_rounds = [statistics.median(v) for v in per_round]
-            p50 = statistics.median([t for v in per_round for t in v])
+            every = sorted(t for v in per_round for t in v)
+            p50 = statistics.median(every)
             gbs = nbytes[name] / (p50 * 1e-6) / 1e9
-            res[name] = {"p50_us": round(p50, 2), "round_p50_us": [round(t, 2) for t in p50_rounds],
+            res[name] = {"p50_us": round(p50, 2), "p10_us": round(every[len(every) // 10], 2),
+                         "p90_us": round(every[(9 * len(every)) // 10], 2),
+                         "round_p50_us": [round(t, 2) for t in p50_rounds],
                          "round_spread": round(max(p50_rounds) / min(p50_rounds), 3),
                          "hot_p50_us": round(statistics.median(hot), 2),
                          "gbs": round(gbs, 1), "frac": round(gbs / peak, 4)}
