@@ -246,8 +246,49 @@ cudaError_t launch_combine_fp4(const WireArgs& a, int num_sms, cudaStream_t stre
 // choose combine's slice of a row per work unit (a.H and a.N set)
 void combine_geometry(CombineArgs& a, int variant, int num_sms);
 
+#ifdef __CUDACC__
+// Launch kernel k as a programmatic dependent of the kernel before it on `stream`: the grid may
+// be scheduled while that kernel still runs (once each of its CTAs has executed
+// allow_dependents() or exited), so its launch and its CTAs' start overlap the predecessor's
+// tail; every thread of k calls wait_for_predecessor() before it reads or writes anything the
+// predecessor wrote or reads, which returns once the predecessor has completed and its memory
+// operations are visible.  Kernels that follow another of this library's kernels within one
+// call (the payload scatter after routing, the grouping passes after routing or after each
+// other) launch this way.
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*k)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                             Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, args...);
+}
+#endif
+
 // ----------------------------------------------------------------------------- device helpers
 #ifdef __CUDACC__
+
+// A dependent kernel's wait for its predecessor (see launch_dependent); returns at once when the
+// kernel was launched in the ordinary way.
+__device__ __forceinline__ void wait_for_predecessor()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Lets the kernel's dependent (launched with launch_dependent) be scheduled before this kernel
+// has finished; the dependent still waits for this kernel's completion before touching its data.
+__device__ __forceinline__ void allow_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 __device__ __forceinline__ void record_status(int* status, int code)
 {
@@ -305,6 +346,17 @@ __device__ __forceinline__ void probe_mark(unsigned long long* probe, int phase,
 #else
     (void)probe; (void)phase; (void)begin;
 #endif
+}
+
+// e / E for 0 <= e < W*E (W <= 32) without an integer division, given inv_e = RN(1/E): the float
+// product lies within 2^-17 of e/E < 32, so it truncates to the exact quotient or one either side
+// of it, and the remainder's sign and size fix that.
+__device__ __forceinline__ int expert_rank(int e, int E, float inv_e)
+{
+    int q = __float2int_rz(__int2float_rn(e) * inv_e);
+    const int rem = e - q * E;
+    q += (rem >= E) - (rem < 0);
+    return q;
 }
 
 // This warp's first unit, or s.units if it has none.

@@ -307,14 +307,27 @@ __device__ __forceinline__ void e2m1x8_to_half2x4(uint32_t w, uint32_t (&h)[4])
         : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3]) : "r"(w));
 }
 
+// acc.x += lo(h) * s and acc.y += hi(h) * s: fused multiply-adds of two f16 operands into FP32
+// (the operands widen exactly; the product and sum round once).
+__device__ __forceinline__ void fma_f16x2_f32(float2& acc, uint32_t h, uint16_t s)
+{
+    asm("{ .reg .b16 l, u;\n\t"
+        "mov.b32 {l, u}, %2;\n\t"
+        "fma.rn.f32.f16 %0, l, %3, %0;\n\t"
+        "fma.rn.f32.f16 %1, u, %3, %1; }"
+        : "+f"(acc.x), "+f"(acc.y) : "r"(h), "h"(s));
+}
+
 // acc[0..7] (element pairs) += the 16 e2m1 codes of (lo, hi) times 2^(code - 127).
 // An e2m1 value has at most two significant bits and the scale is a power of two, so the
 // product is exact in FP32 (down to 2^-128, above FP32's smallest subnormal) unless it
 // overflows; a fused multiply-add therefore rounds exactly as the product followed by an add.
-// Only codes 253 and 254 (an infinite block maximum) can overflow: they take the two-step form.
+// Scales 2^-14 .. 2^15 (codes 113 .. 142, block maxima from 2^-12 to below 2^18) are normal
+// f16 numbers: the f16 code values multiply them in f16-operand FMAs, with no conversion to
+// FP32.  Other codes widen the values first; only codes 253 and 254 (an infinite block maximum)
+// can overflow, and they take the two-step form.
 __device__ __forceinline__ void add_fp4x16(float2 (&acc)[8], uint32_t lo, uint32_t hi, uint32_t code)
 {
-    const float scale = e8m0_to_float(code);
     uint32_t hv[8];
     {
         uint32_t t[4];
@@ -325,6 +338,13 @@ __device__ __forceinline__ void add_fp4x16(float2 (&acc)[8], uint32_t lo, uint32
 #pragma unroll
         for (int i = 0; i < 4; ++i) hv[4 + i] = t[i];
     }
+    if (code - 113u < 30u) {
+        const uint16_t sh = (uint16_t)((code - 112u) << 10);   // f16 bits of 2^(code - 127)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) fma_f16x2_f32(acc[i], hv[i], sh);
+        return;
+    }
+    const float scale = e8m0_to_float(code);
     if (code < 253u) {
         unsigned long long ss;
         asm("mov.b64 %0, {%1, %1};" : "=l"(ss) : "f"(scale));

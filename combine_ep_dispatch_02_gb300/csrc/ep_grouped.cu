@@ -138,6 +138,7 @@ __device__ __forceinline__ void assign_chunk(const GroupArgs& a, int r, int64_t 
 template <int VEC>
 __global__ void __launch_bounds__(256) ep_group_kernel(const GroupArgs a)
 {
+    wait_for_predecessor();   // routing's (or the previous pass's) output
     probe_mark(a.probe, kProbeGroupScan, true);
     constexpr int Q = kGroupRowsPerThread;
     __shared__ int s_warp[Q][8];
@@ -170,6 +171,7 @@ __global__ void __launch_bounds__(256) ep_group_kernel(const GroupArgs a)
         for (int s = 0; s < tid; ++s) first += s_src[s];
         a.layout_range[list * a.W + tid] = (first << 32) | (long long)s_src[tid];
     }
+    allow_dependents();   // the next pass may be scheduled as this one's CTAs finish
     probe_mark(a.probe, kProbeGroupScan, false);
 }
 
@@ -179,6 +181,7 @@ __global__ void __launch_bounds__(256) ep_group_kernel(const GroupArgs a)
 template <int VEC>
 __global__ void __launch_bounds__(256) ep_group_count_kernel(const GroupArgs a)
 {
+    wait_for_predecessor();   // routing's (or the previous pass's) output
     probe_mark(a.probe, kProbeGroupScan, true);
     constexpr int Q = kGroupRowsPerThread;
     __shared__ int s_src[kMaxRanks];
@@ -200,6 +203,7 @@ __global__ void __launch_bounds__(256) ep_group_count_kernel(const GroupArgs a)
         if (tid < a.W) a.scan_cnt[(list * a.scan_chunks + c) * a.W + tid] = s_src[tid];
         __syncthreads();
     }
+    allow_dependents();   // the next pass may be scheduled as this one's CTAs finish
     probe_mark(a.probe, kProbeGroupScan, false);
 }
 
@@ -210,6 +214,7 @@ __global__ void __launch_bounds__(256) ep_group_count_kernel(const GroupArgs a)
 template <int VEC>
 __global__ void __launch_bounds__(256) ep_group_assign_kernel(const GroupArgs a)
 {
+    wait_for_predecessor();   // routing's (or the previous pass's) output
     probe_mark(a.probe, kProbeGroupScan, true);
     constexpr int Q = kGroupRowsPerThread;
     __shared__ int s_warp[Q][8];
@@ -251,6 +256,7 @@ __global__ void __launch_bounds__(256) ep_group_assign_kernel(const GroupArgs a)
         assign_chunk(a, r, list, c * kScanChunk, base, pos, jfirst, s_warp, tid, &total);
         __syncthreads();                      // s_part and s_warp are reused by the next chunk
     }
+    allow_dependents();   // the next pass may be scheduled as this one's CTAs finish
     probe_mark(a.probe, kProbeGroupScan, false);
 }
 
@@ -307,6 +313,7 @@ __device__ __forceinline__ int64_t received_row(const int* off, int W, int64_t r
 // expert.  The unit count, the rows received by all ranks, is known on the device only.
 __global__ void __launch_bounds__(kCopyThreads) ep_grouped_copy_kernel(const GroupArgs a)
 {
+    wait_for_predecessor();   // routing's (or the previous pass's) output
     probe_mark(a.probe, kProbeGroupCopy, true);
     __shared__ int s_off[kMaxRanks + 1];
     if (threadIdx.x == 0) {
@@ -541,6 +548,7 @@ __global__ void __launch_bounds__(kCopyThreads, 2) ep_ungroup_kernel(const Group
 // rows as in ep_dispatch.  The 2-D payload rows are not written.
 __global__ void __launch_bounds__(kCopyThreads) ep_group_from_source_kernel(const GroupArgs a)
 {
+    wait_for_predecessor();   // routing's (or the previous pass's) output
     probe_mark(a.probe, kProbeGroupCopy, true);
     __shared__ int s_off[kMaxRanks + 1];
     if (threadIdx.x <= a.W) s_off[threadIdx.x] = a.tok_off[threadIdx.x];
@@ -558,6 +566,7 @@ __global__ void __launch_bounds__(kCopyThreads) ep_group_from_source_kernel(cons
     }
     __syncthreads();
     const int lane = threadIdx.x & 31;
+    const float inv_e = __frcp_rn((float)a.E);
     const WorkSplit& ws = a.work;
     for (uint32_t u = work_first(ws); u < ws.units; u = work_next(ws, u, lane)) {
         const int g = (int)(u / (uint32_t)a.chunks);
@@ -581,35 +590,47 @@ __global__ void __launch_bounds__(kCopyThreads) ep_group_from_source_kernel(cons
                 a.recv_scales_out[row * a.sd + e] = __ldg(a.scales + tok * a.sd + e);
         }
         const uint8_t* src = a.x + tok * a.row_bytes + off;
+        // the slice's first step of source vectors is read while the destinations are found
+        uint4 buf[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int v = q * 32 + lane;
+            if (v < nvec) buf[q] = ld_stream_v4(src + (int64_t)v * 16);
+        }
         for (int j0 = 0; j0 < a.k; j0 += 32) {
             const int j = j0 + lane;
             int64_t dest = -1;
             int e = -1, r = -1;
-            if (j < a.k) {
-                e = ids[j];
-                bool first = e >= 0 && e < a.W * a.E;
-                for (int jj = 0; jj < j && first; ++jj) first = ids[jj] != e;
-                if (first) r = e / a.E;
+            if (j < a.k) e = __ldg(ids + j);
+            bool first = e >= 0 && e < a.W * a.E;
+            if (j0 == 0) {                                 // slots 0..31: the lanes compare
+                const unsigned same = __match_any_sync(0xffffffffu, e);   // every lane takes part
+                first = first && !(same & lanemask_lt());
+            } else {
+                for (int jj = 0; jj < j && first; ++jj) first = __ldg(ids + jj) != e;
             }
+            if (first) r = expert_rank(e, a.E, inv_e);
             // the token's receive row on rank r: one of the forward-map entries (uniform loop)
             int64_t rrow = -1;
+            const int64_t lo = (int64_t)r * a.rows, hi = lo + a.rows;
             for (int d = 0; d < nd; ++d) {
                 const int64_t row = __shfl_sync(0xffffffffu, fw, d);
-                if (r >= 0 && row / a.rows == r) rrow = row;
+                if (r >= 0 && row >= lo && row < hi) rrow = row;
             }
             if (rrow >= 0) {
                 const int slot = a.map[rrow * a.k + j];
                 if (EP_IN_BOUNDS(slot >= 0 && slot < a.rows, a.status))
-                    dest = ((int64_t)r * a.E + (e - r * a.E)) * a.rows + slot;
+                    dest = (int64_t)e * a.rows + slot;     // list e = r*E + local expert
             }
             const unsigned has = __ballot_sync(0xffffffffu, dest >= 0);
             if (!has) continue;
             for (int v0 = 0; v0 < nvec; v0 += 32 * 4) {
-                uint4 buf[4];
+                if (v0 > 0 || j0 > 0) {                    // (buf holds the first step otherwise)
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int v = v0 + q * 32 + lane;
-                    if (v < nvec) buf[q] = ld_stream_v4(src + (int64_t)v * 16);
+                    for (int q = 0; q < 4; ++q) {
+                        const int v = v0 + q * 32 + lane;
+                        if (v < nvec) buf[q] = ld_stream_v4(src + (int64_t)v * 16);
+                    }
                 }
                 for (unsigned m = has; m; m &= m - 1) {
                     const int64_t prow = __shfl_sync(0xffffffffu, dest, __ffs(m) - 1);
@@ -640,59 +661,54 @@ int grid_of(const void* kernel, int64_t warps, int num_sms)
 
 }  // namespace
 
+// The grouping passes launch as dependents (launch_dependent) of the kernel before each: the
+// scan of the routing kernel or of the dispatch's scatter, the assignment pass of the count
+// pass, the copy of the scan.
 template <int VEC>
-static void launch_group_scan_t(const GroupArgs& a, int num_sms, cudaStream_t stream)
+static cudaError_t launch_group_scan_t(const GroupArgs& a, int num_sms, cudaStream_t stream)
 {
-    if (!a.scan_cnt) {
-        ep_group_kernel<VEC><<<a.W * a.E, 256, 0, stream>>>(a);
-        return;
-    }
+    if (!a.scan_cnt) return launch_dependent(ep_group_kernel<VEC>, dim3(a.W * a.E), dim3(256), 0, stream, a);
     // about 16 CTAs per SM in all; a CTA takes every gridDim.y-th chunk of its list
     const int per = 16 * num_sms / (a.W * a.E);
     int gy = per > 1 ? per : 1;
     if (gy > a.scan_chunks) gy = a.scan_chunks;
     if (gy > 65535) gy = 65535;
     const dim3 grid(a.W * a.E, gy);
-    ep_group_count_kernel<VEC><<<grid, 256, 0, stream>>>(a);
-    ep_group_assign_kernel<VEC><<<grid, 256, 0, stream>>>(a);
+    cudaError_t e = launch_dependent(ep_group_count_kernel<VEC>, grid, dim3(256), 0, stream, a);
+    if (e != cudaSuccess) return e;
+    return launch_dependent(ep_group_assign_kernel<VEC>, grid, dim3(256), 0, stream, a);
 }
 
 // compiled index-row widths: top-k 4, 8 (the pages' specialised case), 16; others loop
-static void launch_group_scan(const GroupArgs& a, int num_sms, cudaStream_t stream)
+static cudaError_t launch_group_scan(const GroupArgs& a, int num_sms, cudaStream_t stream)
 {
-    if (!a.vec16 || (a.k != 4 && a.k != 8 && a.k != 16))
-        launch_group_scan_t<0>(a, num_sms, stream);
-    else if (a.k == 4)
-        launch_group_scan_t<1>(a, num_sms, stream);
-    else if (a.k == 8)
-        launch_group_scan_t<2>(a, num_sms, stream);
-    else
-        launch_group_scan_t<4>(a, num_sms, stream);
+    if (!a.vec16 || (a.k != 4 && a.k != 8 && a.k != 16)) return launch_group_scan_t<0>(a, num_sms, stream);
+    if (a.k == 4) return launch_group_scan_t<1>(a, num_sms, stream);
+    if (a.k == 8) return launch_group_scan_t<2>(a, num_sms, stream);
+    return launch_group_scan_t<4>(a, num_sms, stream);
 }
 
 cudaError_t launch_group_from_source(const GroupArgs& a, int num_sms, cudaStream_t stream)
 {
-    if (!a.scan_done) launch_group_scan(a, num_sms, stream);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess || (a.N == 0 && !a.scan_done)) return e;   // an empty call still writes the counts
+    if (!a.scan_done) {
+        cudaError_t e = launch_group_scan(a, num_sms, stream);
+        if (e != cudaSuccess || a.N == 0) return e;            // an empty call's scan wrote the counts
+    }
     const int64_t units = (int64_t)a.N * a.chunks;
     int grid = grid_of((const void*)ep_group_from_source_kernel, units, num_sms);
     if (grid < 1) grid = 1;                                // CTA 0 writes the counts of an empty call
     GroupArgs b = a;
     b.work = make_work_split(a.work.q, units, (int64_t)grid * (kCopyThreads / 32));
-    ep_group_from_source_kernel<<<grid, kCopyThreads, 0, stream>>>(b);
-    return cudaGetLastError();
+    return launch_dependent(ep_group_from_source_kernel, dim3(grid), dim3(kCopyThreads), 0, stream, b);
 }
 
 cudaError_t launch_group(const GroupArgs& a, int num_sms, cudaStream_t stream)
 {
-    launch_group_scan(a, num_sms, stream);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_group_scan(a, num_sms, stream);
     if (e != cudaSuccess) return e;
     const int64_t units = (int64_t)a.W * a.rows;
-    ep_grouped_copy_kernel<<<grid_of((const void*)ep_grouped_copy_kernel, units, num_sms), kCopyThreads,
-                             0, stream>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(ep_grouped_copy_kernel, dim3(grid_of((const void*)ep_grouped_copy_kernel, units, num_sms)),
+                            dim3(kCopyThreads), 0, stream, a);
 }
 
 template <bool FP16, bool WIDE>

@@ -43,33 +43,25 @@ __device__ __forceinline__ unsigned long long pack_flag(uint32_t stamp, unsigned
 }
 
 // Destination-rank mask of one token: OR over its k top-k slots of (1 << rank), so a rank named
-// by several experts counts once.  The thread loads the whole index row at once (16-byte vectors
-// when every row is 16-byte aligned: k % 4 == 0 and a 16-byte aligned array), so a tile's 256 rows are in flight
-// together rather than one slot batch after another; VEC = k / 4 when known at compile time
-// (the pages' dedicated top-k 8 case is VEC = 2), 0 for the runtime loop.
+// by several experts counts once.  `id` holds the index row, loaded by the caller with 16-byte
+// vectors (VEC = k / 4 known at compile time; the pages' dedicated top-k 8 case is VEC = 2) so a
+// tile's 256 rows are in flight together; VEC = 0 loops over the row at run time.
 template <int VEC>
-__device__ __forceinline__ uint32_t token_mask(const RouteArgs& a, const int32_t* row)
+__device__ __forceinline__ uint32_t token_mask(const RouteArgs& a, const int32_t* row, const int (&id)[VEC > 0 ? 4 * VEC : 1],
+                                               float inv_e)
 {
     const int n_exp = a.W * a.E;
     uint32_t m = 0;
     bool bad = false;
     auto take = [&](int e) {
         if (e >= 0 && e < n_exp)
-            m |= 1u << (e / a.E);
+            m |= 1u << expert_rank(e, a.E, inv_e);
         else
             bad = true;
     };
     if constexpr (VEC > 0) {
-        int4 v[VEC];
 #pragma unroll
-        for (int q = 0; q < VEC; ++q) v[q] = __ldg(reinterpret_cast<const int4*>(row) + q);
-#pragma unroll
-        for (int q = 0; q < VEC; ++q) {
-            take(v[q].x);
-            take(v[q].y);
-            take(v[q].z);
-            take(v[q].w);
-        }
+        for (int j = 0; j < 4 * VEC; ++j) take(id[j]);
     } else if (a.vec16) {
         for (int q = 0; q < (a.k >> 2); ++q) {
             const int4 v = __ldg(reinterpret_cast<const int4*>(row) + q);
@@ -121,9 +113,11 @@ __global__ void __launch_bounds__(kRouteThreads) ep_route_kernel(const RouteArgs
     __shared__ int s_incl_at[kMaxRanks];
     __shared__ int s_done[kMaxRanks];
     __shared__ unsigned long long s_ticket, s_gen;
-    extern __shared__ uint32_t s_dyn[];   // GROUPED: [W*E][8] token masks, then [W*E] list prefixes
+    extern __shared__ uint32_t s_dyn[];   // GROUPED: [W*E][8] token masks, [W*E] list prefixes,
+                                          // [W*E][2] per-warp prefix bytes
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    allow_dependents();   // the copy kernel that follows may be scheduled (it waits for this one)
     probe_mark(a.probe, kProbeRoute, true);
     if (tid == 0) {
         // ticket[0]: next tile; ticket[1]: CTAs finished; ticket[2]: generation of this launch
@@ -145,19 +139,47 @@ __global__ void __launch_bounds__(kRouteThreads) ep_route_kernel(const RouteArgs
         t = g - s_off[s];
     }
     const int32_t* ids = a.idx + ((int64_t)s * a.M + t) * a.k;
-    const uint32_t mask = valid ? token_mask<VEC>(a, ids) : 0u;
+    int id[VEC > 0 ? 4 * VEC : 1];
+    if constexpr (VEC > 0) {
+        if (valid) {
+#pragma unroll
+            for (int q = 0; q < VEC; ++q) {
+                const int4 v = __ldg(reinterpret_cast<const int4*>(ids) + q);
+                id[4 * q] = v.x;
+                id[4 * q + 1] = v.y;
+                id[4 * q + 2] = v.z;
+                id[4 * q + 3] = v.w;
+            }
+        }
+    }
+    const float inv_e = __frcp_rn((float)a.E);
     const int n_exp = a.W * a.E;
     uint64_t firsts = 0;   // GROUPED: top-k slots that are the token's first naming their expert
     if constexpr (GROUPED) {
-        for (int i = tid; i < n_exp * 8; i += kRouteThreads) s_dyn[i] = 0u;
+        for (int i = tid; i < n_exp * 8; i += kRouteThreads) s_dyn[i] = 0u;   // (loads in flight)
         __syncthreads();
-        if (valid)
-            for (int j = 0; j < a.k; ++j) {
-                const int e = __ldg(ids + j);
-                if (e >= 0 && e < n_exp && !(atomicOr(&s_dyn[e * 8 + warp], 1u << lane) & (1u << lane)))
-                    firsts |= 1ull << j;
+        if (valid) {
+            if constexpr (VEC > 0 && VEC <= 2) {         // top-k 4 and 8: compares in registers
+#pragma unroll
+                for (int j = 0; j < 4 * VEC; ++j) {
+                    bool first = id[j] >= 0 && id[j] < n_exp;
+#pragma unroll
+                    for (int jj = 0; jj < j; ++jj) first = first && id[jj] != id[j];
+                    if (first) {
+                        firsts |= 1ull << j;
+                        atomicOr(&s_dyn[id[j] * 8 + warp], 1u << lane);
+                    }
+                }
+            } else {
+                for (int j = 0; j < a.k; ++j) {
+                    const int e = __ldg(ids + j);
+                    if (e >= 0 && e < n_exp && !(atomicOr(&s_dyn[e * 8 + warp], 1u << lane) & (1u << lane)))
+                        firsts |= 1ull << j;
+                }
             }
+        }
     }
+    const uint32_t mask = valid ? token_mask<VEC>(a, ids, id, inv_e) : 0u;
     for (int r = 0; r < a.W; ++r) {
         const unsigned bal = __ballot_sync(0xffffffffu, (mask >> r) & 1u);
         if (lane == 0) {
@@ -186,11 +208,21 @@ __global__ void __launch_bounds__(kRouteThreads) ep_route_kernel(const RouteArgs
         st_relaxed_u64(a.flags + (int64_t)tile * a.W + tid,
                        pack_flag(stamp, tile == 0 ? kFlagInclusive : kFlagAggregate, (uint32_t)run));
     }
-    if constexpr (GROUPED) {   // the tile's total per expert column
+    if constexpr (GROUPED) {   // the tile's total per expert column, and its prefix before each warp
+        int* eex = reinterpret_cast<int*>(s_dyn + n_exp * 8);
+        uint32_t* wpre = s_dyn + n_exp * 9;              // [n_exp][2]: 8 bytes, warp w's prefix in byte w
         for (int e = tid; e < n_exp; e += kRouteThreads) {
             int agg = 0;
+            uint32_t lo = 0, hi = 0;
 #pragma unroll
-            for (int w = 0; w < 8; ++w) agg += __popc(s_dyn[e * 8 + w]);
+            for (int w = 0; w < 8; ++w) {
+                if (w < 4) lo |= (uint32_t)agg << (8 * w);
+                else hi |= (uint32_t)agg << (8 * (w - 4));
+                agg += __popc(s_dyn[e * 8 + w]);         // at most 7 * 32 before warp 7
+            }
+            wpre[2 * e] = lo;
+            wpre[2 * e + 1] = hi;
+            eex[e] = agg;
             st_relaxed_u64(a.grp.eflags + (int64_t)tile * n_exp + e,
                            pack_flag(stamp, tile == 0 ? kFlagInclusive : kFlagAggregate, (uint32_t)agg));
         }
@@ -232,12 +264,11 @@ __global__ void __launch_bounds__(kRouteThreads) ep_route_kernel(const RouteArgs
         // lookback over the expert columns, one thread per column: sum predecessors' words back
         // to the first INCLUSIVE one (tiles before this one were all issued earlier)
         int* eex = reinterpret_cast<int*>(s_dyn + n_exp * 8);
+        const uint32_t* wpre = s_dyn + n_exp * 9;
         for (int e = tid; e < n_exp; e += kRouteThreads) {
             int excl = 0;
             if (tile > 0) {
-                int agg = 0;
-#pragma unroll
-                for (int w = 0; w < 8; ++w) agg += __popc(s_dyn[e * 8 + w]);
+                const int agg = eex[e];
                 for (int j = tile - 1; j >= 0; --j) {
                     unsigned long long f;
                     if (!wait_word(a.grp.eflags + (int64_t)j * n_exp + e, stamp, a.status, f)) break;
@@ -250,19 +281,31 @@ __global__ void __launch_bounds__(kRouteThreads) ep_route_kernel(const RouteArgs
             eex[e] = excl;
         }
         __syncthreads();
+        // list prefix of expert e before position pos (0..255) of the tile
+        auto prefix_at = [&](int e, int pos) {
+            const int w = pos >> 5, b = pos & 31;
+            const int before = (int)((wpre[2 * e + (w >> 2)] >> (8 * (w & 3))) & 0xFFu);
+            return eex[e] + before + __popc(s_dyn[e * 8 + w] & ((1u << b) - 1u));
+        };
         // each first slot: the list slot, written at the token's receive row on the expert's rank
         const unsigned lt_ = lanemask_lt();
-        for (uint64_t m = firsts; m; m &= m - 1) {
-            const int j = __ffsll((long long)m) - 1;
-            const int e = __ldg(ids + j);
-            const int r = e / a.E;
-            const uint32_t* bits = s_dyn + e * 8;
-            int slot = eex[e] + __popc(bits[warp] & lt_);
-            for (int w = 0; w < warp; ++w) slot += __popc(bits[w]);
+        auto place = [&](int j, int e) {
+            const int r = expert_rank(e, a.E, inv_e);
+            const int slot = prefix_at(e, tid);
             const int row = s_excl[r] + s_warp[warp][r] + __popc(s_rbal[warp][r] & lt_);
             if (EP_IN_BOUNDS(row >= 0 && row < a.rows && slot >= 0 && slot < a.rows, a.status)) {
                 a.grp.map[((int64_t)r * a.rows + row) * a.k + j] = slot;
                 a.grp.src_info[(int64_t)e * a.rows + slot] = t;
+            }
+        };
+        if constexpr (VEC > 0 && VEC <= 2) {             // top-k 4 and 8: the row in registers
+#pragma unroll
+            for (int j = 0; j < 4 * VEC; ++j)
+                if ((firsts >> j) & 1ull) place(j, id[j]);
+        } else {
+            for (uint64_t m = firsts; m; m &= m - 1) {
+                const int j = __ffsll((long long)m) - 1;
+                place(j, __ldg(ids + j));
             }
         }
         // every list's prefix at each source rank's first token that lies in this tile (the end
@@ -271,16 +314,10 @@ __global__ void __launch_bounds__(kRouteThreads) ep_route_kernel(const RouteArgs
             const int b = s_off[sb];
             if (!((b >= base && b < base + kRouteTile) || (b == a.N && tile == a.tiles - 1))) continue;
             const int pos = b - base;                       // 0..256 tokens of the tile before b
-            for (int e = tid; e < n_exp; e += kRouteThreads) {
-                int pre = eex[e];
-#pragma unroll
-                for (int w = 0; w < 8; ++w) {
-                    const int lo = w * 32;
-                    if (pos >= lo + 32) pre += __popc(s_dyn[e * 8 + w]);
-                    else if (pos > lo) pre += __popc(s_dyn[e * 8 + w] & ((1u << (pos - lo)) - 1u));
-                }
-                a.grp.bnd[(int64_t)sb * n_exp + e] = pre;
-            }
+            for (int e = tid; e < n_exp; e += kRouteThreads)
+                a.grp.bnd[(int64_t)sb * n_exp + e] =
+                    pos < kRouteTile ? prefix_at(e, pos) : prefix_at(e, kRouteTile - 1) +
+                                                            (int)((s_dyn[e * 8 + 7] >> 31) & 1u);
         }
     }
 
@@ -318,7 +355,7 @@ __global__ void __launch_bounds__(kRouteThreads) ep_route_kernel(const RouteArgs
 template <int VEC, bool GROUPED>
 cudaError_t launch_vec(const RouteArgs& a, cudaStream_t stream)
 {
-    const size_t smem = GROUPED ? (size_t)a.W * a.E * 9 * sizeof(uint32_t) : 0;
+    const size_t smem = GROUPED ? (size_t)a.W * a.E * 11 * sizeof(uint32_t) : 0;
     ep_route_kernel<VEC, GROUPED><<<a.tiles, kRouteThreads, smem, stream>>>(a);
     return cudaGetLastError();
 }

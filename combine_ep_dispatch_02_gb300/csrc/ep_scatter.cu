@@ -25,6 +25,7 @@ __global__ void __launch_bounds__(kCopyThreads) ep_scatter_kernel(const ScatterA
 {
     __shared__ int s_off[kMaxRanks + 1];
     if (threadIdx.x <= a.W) s_off[threadIdx.x] = a.tok_off[threadIdx.x];
+    wait_for_predecessor();   // the routing kernel's forward map
     probe_mark(a.probe, kProbeScatter, true);
     __syncthreads();
 
@@ -101,6 +102,7 @@ __global__ void __launch_bounds__(kCopyThreads, 3) ep_scatter_quant_kernel(const
 {
     __shared__ int s_off[kMaxRanks + 1];
     if (threadIdx.x <= a.W) s_off[threadIdx.x] = a.tok_off[threadIdx.x];
+    wait_for_predecessor();   // the routing kernel's forward map
     probe_mark(a.probe, kProbeScatter, true);
     __syncthreads();
 
@@ -179,6 +181,7 @@ __global__ void __launch_bounds__(kCopyThreads, 3) ep_scatter_quant_fp4_kernel(c
 {
     __shared__ int s_off[kMaxRanks + 1];
     if (threadIdx.x <= a.W) s_off[threadIdx.x] = a.tok_off[threadIdx.x];
+    wait_for_predecessor();   // the routing kernel's forward map
     probe_mark(a.probe, kProbeScatter, true);
     __syncthreads();
 
@@ -234,60 +237,40 @@ __global__ void __launch_bounds__(kCopyThreads, 3) ep_scatter_quant_fp4_kernel(c
     work_retire(ws);
 }
 
+// A persistent grid of the kernel's occupancy times the SM count (at most one warp per unit),
+// launched as a dependent of the routing kernel before it.
+template <typename Kernel>
+cudaError_t launch_copy(Kernel kernel, const ScatterArgs& a, int num_sms, cudaStream_t stream)
+{
+    const int64_t units = (int64_t)a.N * a.chunks;
+    if (units == 0) return cudaSuccess;
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kCopyThreads, 0);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    const int64_t need = (units + kCopyThreads / 32 - 1) / (kCopyThreads / 32);
+    const int64_t cap = (int64_t)per_sm * num_sms;
+    const int grid = (int)(need < cap ? need : cap);
+    ScatterArgs b = a;
+    b.work = make_work_split(a.work.q, units, (int64_t)grid * (kCopyThreads / 32));
+    return launch_dependent(kernel, dim3(grid), dim3(kCopyThreads), 0, stream, b);
+}
+
 }  // namespace
 
 cudaError_t launch_scatter_quant_fp4(const ScatterArgs& a, int num_sms, cudaStream_t stream)
 {
-    const int64_t units = (int64_t)a.N * a.chunks;
-    if (units == 0) return cudaSuccess;
-    int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ep_scatter_quant_fp4_kernel,
-                                                                  kCopyThreads, 0);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1) per_sm = 1;
-    const int64_t need = (units + kCopyThreads / 32 - 1) / (kCopyThreads / 32);
-    const int64_t cap = (int64_t)per_sm * num_sms;
-    const int grid = (int)(need < cap ? need : cap);
-    ScatterArgs b = a;
-    b.work = make_work_split(a.work.q, units, (int64_t)grid * (kCopyThreads / 32));
-    ep_scatter_quant_fp4_kernel<<<grid, kCopyThreads, 0, stream>>>(b);
-    return cudaGetLastError();
+    return launch_copy(ep_scatter_quant_fp4_kernel, a, num_sms, stream);
 }
 
 cudaError_t launch_scatter_quant(const ScatterArgs& a, int num_sms, cudaStream_t stream)
 {
-    const int64_t units = (int64_t)a.N * a.chunks;
-    if (units == 0) return cudaSuccess;
-    int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ep_scatter_quant_kernel,
-                                                                  kCopyThreads, 0);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1) per_sm = 1;
-    const int64_t need = (units + kCopyThreads / 32 - 1) / (kCopyThreads / 32);
-    const int64_t cap = (int64_t)per_sm * num_sms;
-    const int grid = (int)(need < cap ? need : cap);
-    ScatterArgs b = a;
-    b.work = make_work_split(a.work.q, units, (int64_t)grid * (kCopyThreads / 32));
-    ep_scatter_quant_kernel<<<grid, kCopyThreads, 0, stream>>>(b);
-    return cudaGetLastError();
+    return launch_copy(ep_scatter_quant_kernel, a, num_sms, stream);
 }
 
 cudaError_t launch_scatter(const ScatterArgs& a, int num_sms, cudaStream_t stream)
 {
-    const int64_t units = (int64_t)a.N * a.chunks;
-    if (units == 0) return cudaSuccess;
-    int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ep_scatter_kernel,
-                                                                  kCopyThreads, 0);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1) per_sm = 1;
-    const int64_t need = (units + kCopyThreads / 32 - 1) / (kCopyThreads / 32);
-    const int64_t cap = (int64_t)per_sm * num_sms;
-    const int grid = (int)(need < cap ? need : cap);
-    ScatterArgs b = a;
-    b.work = make_work_split(a.work.q, units, (int64_t)grid * (kCopyThreads / 32));
-    ep_scatter_kernel<<<grid, kCopyThreads, 0, stream>>>(b);
-    return cudaGetLastError();
+    return launch_copy(ep_scatter_kernel, a, num_sms, stream);
 }
 
 }  // namespace ep

@@ -886,6 +886,10 @@ def test_fp4_wire_edge_values():
         xf[1, :, 96:128] = np.linspace(-6.5, 6.5, 32, dtype=np.float32) * np.float32(2.0) ** -20
         if H > 160:
             xf[1, :, 128:160] = np.float32(2.0) ** -126 * np.float32(3.0)   # normal/subnormal edge
+        if H >= 128:
+            # rounding ties at the scale codes either side of the f16-scale window (113..142)
+            for i, code in enumerate((112, 113, 142, 143)):
+                xf[2, :, 32 * i:32 * i + 32] = np.tile(np.concatenate([ties, -ties]), 2) * np.float32(2.0) ** (code - 127)
         eo[:] = torch.from_numpy(xf).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
 
     _check_fp4_wire(wl, edit_expert_out=edit)
