@@ -769,6 +769,7 @@ int ep_ungroup_by_expert(ep_plan* p, const void* packed_y, void* out, uint64_t e
     a.recv_idx = p->recv_idx; a.recv_count = p->recv_count; a.map = p->expert_map;
     a.packed_y = (const uint8_t*)packed_y; a.out = (uint8_t*)out;
     a.rows = p->rows; a.row_bytes = (int64_t)p->H * 2; a.W = p->W; a.E = p->E; a.k = p->k;
+    a.N = p->N; a.F = p->F;                               // the dispatch's tokens bound its rows
     cudaError_t e = launch_ungroup(a, p->dtype == EP_FP16, p->num_sms, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "ep_ungroup_by_expert: launch");
     return EP_OK;

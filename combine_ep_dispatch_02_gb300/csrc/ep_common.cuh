@@ -217,7 +217,8 @@ struct GroupArgs {
     int64_t rows;                // W*M
     int64_t row_bytes;           // payload bytes (grouping) / 16-bit row bytes (inverse)
     int W, E, k, M, F, N, sd;
-    int chunk_bytes, chunks;     // fused dispatch: work unit = (token, slice of chunk_bytes)
+    int chunk_bytes, chunks;     // fused dispatch: work unit = (token, slice of chunk_bytes);
+                                 // inverse: (received row, slice of chunk_bytes), chunks per row
     int tok_off[kMaxRanks + 1];
 };
 

@@ -28,6 +28,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <cstdint>
+
 #include "ep_common.cuh"
 
 namespace ep {
@@ -414,9 +416,10 @@ __device__ __forceinline__ uint4 pack8(const float (&acc)[8])
 // about 200 registers; four fit two 8-warp CTAs per SM, which hides more latency.)
 // Entries are found by their rank among the row's valid entries (rank0 / rank1 of lane j belong
 // to top-k entries j and j + 32, whose packed rows are dest0 / dest1).
+// The fold covers vectors [v0, v0 + hv) of rows of stride rs vectors (a slice of each row).
 template <bool FP16, int R, int D>
 __device__ __forceinline__ void fold_rd(const uint4* y4, int64_t dest0, int64_t dest1, int rank0, int rank1,
-                                        int nd, int hv, uint4* dst, int lane)
+                                        int nd, int64_t rs, int v0, int hv, uint4* dst, int lane)
 {
     const uint4* rp[R];
 #pragma unroll
@@ -425,7 +428,7 @@ __device__ __forceinline__ void fold_rd(const uint4* y4, int64_t dest0, int64_t 
         const unsigned m1 = __ballot_sync(0xffffffffu, dest1 >= 0 && rank1 == q);
         const int64_t row = m0 ? __shfl_sync(0xffffffffu, dest0, __ffs(m0) - 1)
                                : __shfl_sync(0xffffffffu, dest1, m1 ? __ffs(m1) - 1 : 0);
-        rp[q] = y4 + row * hv;
+        rp[q] = y4 + row * rs + v0;
     }
     uint4 b[R][D];
 #pragma unroll
@@ -469,19 +472,28 @@ __global__ void __launch_bounds__(kCopyThreads, 2) ep_ungroup_kernel(const Group
     __syncthreads();
     const int lane = threadIdx.x & 31;
     const int nwarps = gridDim.x * (kCopyThreads / 32);
-    const int total = s_off[a.W];
-    const int hv = (int)(a.row_bytes >> 4);       // 16-byte vectors of a 16-bit row
+    // work units: (received row, slice of chunk_bytes), one slice per row for large calls (the
+    // host slices only calls of a few thousand rows, so units stay below 2^31 either way)
+    const int chunks = a.chunks;
+    const int units = s_off[a.W] * chunks;
+    const int rs = (int)(a.row_bytes >> 4);       // 16-byte vectors of a 16-bit row
+    const int cv = a.chunk_bytes >> 4;            // ... of a slice
     const uint4* y4 = reinterpret_cast<const uint4*>(a.packed_y);
+    auto row_of = [&](int unit) { return chunks == 1 ? unit : unit / chunks; };
     int g = blockIdx.x * (kCopyThreads / 32) + (threadIdx.x >> 5);
     RowEntries next{};
-    if (g < total) next = load_entries(a, received_row(s_off, a.W, a.rows, g), lane);
-    for (; g < total; g += nwarps) {
-        const int64_t u = received_row(s_off, a.W, a.rows, g);
+    if (g < units) next = load_entries(a, received_row(s_off, a.W, a.rows, row_of(g)), lane);
+    // (g + nwarps is formed only below units, so it cannot overflow)
+    for (; g < units; g = g < units - nwarps ? g + nwarps : units) {
+        const int gr = row_of(g);
+        const int v0 = (g - gr * chunks) * cv;
+        const int hv = min(cv, rs - v0);
+        const int64_t u = received_row(s_off, a.W, a.rows, gr);
         const int r = (int)(u / a.rows);
         const RowEntries cur = next;
-        if (g + nwarps < total)                            // lands while this row is folded
-            next = load_entries(a, received_row(s_off, a.W, a.rows, g + nwarps), lane);
-        uint4* dst = reinterpret_cast<uint4*>(a.out + u * a.row_bytes);
+        if (g < units - nwarps)                            // lands while this unit is folded
+            next = load_entries(a, received_row(s_off, a.W, a.rows, row_of(g + nwarps)), lane);
+        uint4* dst = reinterpret_cast<uint4*>(a.out + u * a.row_bytes) + v0;
         // the row's local experts in ascending id: lane j holds entry j (and j + 32 for k > 32)
         int64_t dest0, dest1;
         resolve_entries(a, r, cur, lane, dest0, dest1);
@@ -500,13 +512,13 @@ __global__ void __launch_bounds__(kCopyThreads, 2) ep_ungroup_kernel(const Group
             // the rows in ascending expert order, once per received row; then a rolling fold:
             // row d's next columns are requested as soon as its current one is taken
             if (nd <= 1)
-                fold_rd<FP16, 1, 4>(y4, dest0, dest1, rank0, rank1, nd, hv, dst, lane);
+                fold_rd<FP16, 1, 4>(y4, dest0, dest1, rank0, rank1, nd, rs, v0, hv, dst, lane);
             else if (nd == 2)
-                fold_rd<FP16, 2, 2>(y4, dest0, dest1, rank0, rank1, nd, hv, dst, lane);
+                fold_rd<FP16, 2, 2>(y4, dest0, dest1, rank0, rank1, nd, rs, v0, hv, dst, lane);
             else if (nd <= 4)
-                fold_rd<FP16, 4, 1>(y4, dest0, dest1, rank0, rank1, nd, hv, dst, lane);
+                fold_rd<FP16, 4, 1>(y4, dest0, dest1, rank0, rank1, nd, rs, v0, hv, dst, lane);
             else
-                fold_rd<FP16, 8, 1>(y4, dest0, dest1, rank0, rank1, nd, hv, dst, lane);
+                fold_rd<FP16, 8, 1>(y4, dest0, dest1, rank0, rank1, nd, rs, v0, hv, dst, lane);
             continue;
         }
         if constexpr (WIDE) {
@@ -526,7 +538,7 @@ __global__ void __launch_bounds__(kCopyThreads, 2) ep_ungroup_kernel(const Group
                         int64_t row = -1;
                         if (m0) row = __shfl_sync(0xffffffffu, dest0, __ffs(m0) - 1);
                         else if (m1) row = __shfl_sync(0xffffffffu, dest1, __ffs(m1) - 1);
-                        if (row >= 0 && v < hv) b[q] = ld_stream_v4(y4 + row * hv + v);
+                        if (row >= 0 && v < hv) b[q] = ld_stream_v4(y4 + row * rs + v0 + v);
                         if (row < 0) b[q] = make_uint4(0, 0, 0, 0);
                     }
 #pragma unroll
@@ -714,9 +726,24 @@ cudaError_t launch_group(const GroupArgs& a, int num_sms, cudaStream_t stream)
 template <bool FP16, bool WIDE>
 void launch_ungroup_t(const GroupArgs& a, int num_sms, cudaStream_t stream)
 {
-    const int64_t units = (int64_t)a.W * a.rows;
-    ep_ungroup_kernel<FP16, WIDE><<<grid_of((const void*)ep_ungroup_kernel<FP16, WIDE>, units, num_sms),
-                                    kCopyThreads, 0, stream>>>(a);
+    // Rows the call can have received (each token has at most F); calls with fewer than four such
+    // rows per resident warp split rows into 1024-element slices, and into 512-element ones when
+    // that still leaves fewer than two units per warp, as the combine does.
+    const void* kernel = (const void*)ep_ungroup_kernel<FP16, WIDE>;
+    const int64_t rows = min((int64_t)a.W * a.rows, (int64_t)a.N * a.F);
+    const int64_t warps = (int64_t)grid_of(kernel, INT64_MAX / 2, num_sms) * (kCopyThreads / 32);
+    const int rs = (int)(a.row_bytes >> 4);
+    int cv = rs;
+    if (rows < 4 * warps && rs > 128) {
+        cv = 128;
+        if (rows * ((rs + cv - 1) / cv) < 2 * warps) cv = 64;
+    }
+    GroupArgs b = a;
+    b.chunk_bytes = cv * 16;
+    b.chunks = (rs + cv - 1) / cv;
+    int grid = grid_of(kernel, rows * b.chunks, num_sms);
+    if (grid < 1) grid = 1;
+    ep_ungroup_kernel<FP16, WIDE><<<grid, kCopyThreads, 0, stream>>>(b);
 }
 
 cudaError_t launch_ungroup(const GroupArgs& a, bool fp16, int num_sms, cudaStream_t stream)

@@ -102,6 +102,8 @@ __device__ __forceinline__ bool wait_word(const unsigned long long* fp, uint32_t
 // the token's receive row on e's rank, the token index into src_info, and, for each source
 // rank whose first token falls in the tile, every list's prefix at that token, from which the
 // copy kernel that follows writes the counts and layout ranges.
+constexpr int kGroupPrefetch = 4;   // GROUPED: predecessor words of a thread's first column read early
+
 template <int VEC, bool GROUPED>
 __global__ void __launch_bounds__(kRouteThreads) ep_route_kernel(const RouteArgs a)
 {
@@ -155,6 +157,7 @@ __global__ void __launch_bounds__(kRouteThreads) ep_route_kernel(const RouteArgs
     const float inv_e = __frcp_rn((float)a.E);
     const int n_exp = a.W * a.E;
     uint64_t firsts = 0;   // GROUPED: top-k slots that are the token's first naming their expert
+    unsigned long long pre[GROUPED ? kGroupPrefetch : 1];   // GROUPED: prefetched expert-column words
     if constexpr (GROUPED) {
         for (int i = tid; i < n_exp * 8; i += kRouteThreads) s_dyn[i] = 0u;   // (loads in flight)
         __syncthreads();
@@ -226,6 +229,12 @@ __global__ void __launch_bounds__(kRouteThreads) ep_route_kernel(const RouteArgs
             st_relaxed_u64(a.grp.eflags + (int64_t)tile * n_exp + e,
                            pack_flag(stamp, tile == 0 ? kFlagInclusive : kFlagAggregate, (uint32_t)agg));
         }
+        // the first column's nearest predecessor words, read now so that their latency overlaps
+        // the lookback over the rank columns
+#pragma unroll
+        for (int b = 0; b < kGroupPrefetch; ++b)
+            pre[b] = tid < n_exp && tile - 1 - b >= 0
+                         ? ld_relaxed_u64(a.grp.eflags + (int64_t)(tile - 1 - b) * n_exp + tid) : 0ull;
     }
     __syncthreads();
 
@@ -270,8 +279,14 @@ __global__ void __launch_bounds__(kRouteThreads) ep_route_kernel(const RouteArgs
             if (tile > 0) {
                 const int agg = eex[e];
                 for (int j = tile - 1; j >= 0; --j) {
-                    unsigned long long f;
-                    if (!wait_word(a.grp.eflags + (int64_t)j * n_exp + e, stamp, a.status, f)) break;
+                    unsigned long long f = 0;
+                    const int b = tile - 1 - j;
+#pragma unroll
+                    for (int q = 0; q < kGroupPrefetch; ++q)
+                        if (q == b && e == tid) f = pre[q];           // read before the rank lookback
+                    if (!((uint32_t)(f >> 34) == stamp && ((f >> 32) & 3ull) != 0ull) &&
+                        !wait_word(a.grp.eflags + (int64_t)j * n_exp + e, stamp, a.status, f))
+                        break;
                     excl += (int)(uint32_t)f;
                     if (((f >> 32) & 3ull) == kFlagInclusive) break;
                 }
