@@ -25,7 +25,10 @@
  * sd = scale_dim, F = min(W, k).  All arrays are dense and row-major.  Pointers are DEVICE
  * pointers unless marked "host".  A stream argument is a cudaStream_t passed as void*
  * (NULL = the legacy default stream).  Every call on one plan must be ordered on one stream
- * (or otherwise serialised): calls of one plan that overlap on the GPU race.
+ * (or otherwise serialised): calls of one plan that overlap on the GPU race.  Within a call, a
+ * kernel that follows another of the call's kernels is launched as a programmatic dependent of
+ * it (it may be scheduled early, and waits for its predecessor's completion before touching any
+ * data), so results and stream order are those of plain launches.
  *
  * Errors.  Every condition the host can check is reported before any launch, with a negative
  * code and a message readable through ep_last_error().  Problems only the GPU can see (an
