@@ -22,9 +22,13 @@
 //                         hits of earlier chunks;
 //   ep_grouped_copy_kernel warp per received row: the row is read once and written to the slot
 //                         of each of its local experts;
-//   ep_ungroup_kernel     warp per received row: its local experts' output rows, ordered by
-//                         expert id, are loaded together and folded in FP32, with 4 to 8 loads
-//                         per lane in flight however many local experts the row has.
+//   ep_ungroup_kernel     warp per received row (per 512- or 1024-element slice of one, for
+//                         small calls): its local experts' output rows, ordered by expert id,
+//                         are loaded together and folded in FP32, with 4 to 8 loads per lane in
+//                         flight however many local experts the row has;
+//   ep_group_from_source_kernel  the fused dispatch's copy: warp per (source token, slice), the
+//                         row read once and written to each of its experts' lists.
+// Every kernel but the ungroup launches as a programmatic dependent of the kernel before it.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
