@@ -22,6 +22,15 @@ Phases and their kernels:
     quantise_fp4     ep_quantise_rows_fp4_kernel     (expert rows to the MX FP4 wire)
     combine_fp8      ep_combine_fp8_kernel
     combine_fp4      ep_combine_fp4_kernel
+    grouped_route    ep_route_kernel, the form that also numbers the expert-grouped view
+    fused_copy       ep_group_from_source_kernel (the fused dispatch's copy into the grouped view)
+    ungroup          ep_ungroup_kernel (the grouped view's inverse)
+
+The three grouped phases run the small grouped workload instead (W=4, 64 experts per rank,
+top-8, hidden 7168 BF16, uniform routing, --tokens-per-rank 256 by default for them), the regime
+the grouped view's kernels are latency-bound in; its grouped view holds 3.8 GB, and each of
+these kernels moves 0.13-0.17 GB, inside the L2, so their captures are read for issue and
+stall figures rather than DRAM bytes.
 
 Prints one line per run with the phase, the tokens and the algorithmic bytes of one launch of
 the phase's kernel, which a traffic figure is compared with.  `--record RUN_JSON NCU_CSV COMMAND`
@@ -42,11 +51,13 @@ ROOT = os.path.dirname(PKG)
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 
 PHASES = ("route", "scatter", "scatter_fp8", "scatter_fp4", "combine", "quantise_fp8",
-          "quantise_fp4", "combine_fp8", "combine_fp4")
+          "quantise_fp4", "combine_fp8", "combine_fp4", "grouped_route", "fused_copy", "ungroup")
+GROUPED_PHASES = ("grouped_route", "fused_copy", "ungroup")
 # the CUDA source that holds each phase's kernel (its code digest goes beside a recorded figure)
 SOURCES = {"route": "ep_route.cu", "scatter": "ep_scatter.cu", "scatter_fp8": "ep_scatter.cu",
            "scatter_fp4": "ep_scatter.cu", "combine": "ep_combine.cu", "quantise_fp8": "ep_fp8wire.cu",
-           "quantise_fp4": "ep_fp8wire.cu", "combine_fp8": "ep_fp8wire.cu", "combine_fp4": "ep_fp8wire.cu"}
+           "quantise_fp4": "ep_fp8wire.cu", "combine_fp8": "ep_fp8wire.cu", "combine_fp4": "ep_fp8wire.cu",
+           "grouped_route": "ep_route.cu", "fused_copy": "ep_grouped.cu", "ungroup": "ep_grouped.cu"}
 
 
 def code_digest(*files) -> str:
@@ -123,9 +134,10 @@ def record(phase: str, run_line: dict, ncu_csv: str, command: str) -> dict:
     return doc["kernels"][phase]
 
 
-def kernel_bytes(phase: str, N: int, P: int, W: int, H: int, k: int) -> int:
+def kernel_bytes(phase: str, N: int, P: int, W: int, H: int, k: int, entries: int = 0) -> int:
     """Algorithmic bytes of one launch of the phase's kernel (weights given, no caller scales):
-    what the kernel must read and write, each byte once."""
+    what the kernel must read and write, each byte once.  `entries` counts the grouped view's
+    list entries (received rows times their distinct local experts) for the grouped phases."""
     F = min(W, k)
     fp8_row, fp4_row = H + 4 * (H // 128), H // 2 + H // 32
     return {
@@ -138,6 +150,13 @@ def kernel_bytes(phase: str, N: int, P: int, W: int, H: int, k: int) -> int:
         "quantise_fp4": P * (2 * H + fp4_row),
         "combine_fp8": P * (fp8_row + 4 * k) + N * (2 * H + 4 * k) + N * 4 * F,
         "combine_fp4": P * (fp4_row + 4 * k) + N * (2 * H + 4 * k) + N * 4 * F,
+        # routing that also writes each entry's list slot (map) and source token (src_info)
+        "grouped_route": N * 4 * k + P * 4 + entries * 8,
+        # source rows and their index / weight rows read once; a row per entry and the
+        # receive rows' index / weight rows written
+        "fused_copy": N * (2 * H + 8 * k) + entries * 2 * H + P * 8 * k,
+        # the entries' expert outputs read, a row per received row written
+        "ungroup": entries * 2 * H + P * (2 * H + 4 * k),
     }[phase]
 
 
@@ -153,6 +172,8 @@ def run(phase: str, tokens_per_rank: int, launches: int) -> dict:
     build.build()
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
+    if phase in GROUPED_PHASES:
+        return run_grouped(phase, tokens_per_rank, launches)
     wl = workloads.make_workload("dsv3", max_tok=tokens_per_rank)
     plan_dtype = {"scatter_fp8": "bf16_fp8", "scatter_fp4": "bf16_mxfp4"}.get(phase, "bf16")
     plan = ep.Plan(wl.W, wl.E, wl.k, wl.H, plan_dtype, 0, wl.M, device=dev)
@@ -193,10 +214,45 @@ def run(phase: str, tokens_per_rank: int, launches: int) -> dict:
             "launches": launches, "kernel_algorithmic_bytes": kernel_bytes(phase, wl.N, P, wl.W, wl.H, wl.k)}
 
 
+def run_grouped(phase: str, tokens_per_rank: int, launches: int) -> dict:
+    """The grouped phases on the small grouped workload: a fused dispatch into the grouped view
+    sets it up; then `launches` fused dispatches (grouped_route, fused_copy) or inverses (ungroup)."""
+    import numpy as np
+    import torch
+
+    import combine_ep_dispatch_02_gb300 as ep
+    from combine_ep_dispatch_02_gb300 import workloads
+
+    dev = torch.device("cuda", 0)
+    wl = workloads.make_workload("small", max_tok=tokens_per_rank)
+    plan = ep.Plan(wl.W, wl.E, wl.k, wl.H, "bf16", 0, wl.M, device=dev)
+    x = torch.from_numpy(wl.x.view(np.int16)).to(dev)
+    idx = torch.from_numpy(wl.indices).to(dev)
+    w = torch.from_numpy(wl.weights).to(dev)
+    d, px, cnt, _, _ = plan.dispatch_grouped(x, w, None, idx, wl.n_tok)
+    out = None
+    for _ in range(launches):
+        if phase == "ungroup":
+            out = plan.ungroup_by_expert(px.view(torch.bfloat16), d.epoch, out=out)
+        else:
+            d, px, cnt, _, _ = plan.dispatch_grouped(x, w, None, idx, wl.n_tok, packed_x=px)
+    torch.cuda.synchronize()
+    status = plan.status()
+    P = int(d.recv_count.sum().item())
+    entries = int(cnt.sum().item())
+    plan.close()
+    if status != 0:
+        raise RuntimeError(f"device status {status}")
+    return {"phase": phase, "workload": "small", "tokens_per_rank": wl.M, "tokens": wl.N, "token_dest_pairs": P,
+            "expert_entries": entries, "launches": launches,
+            "kernel_algorithmic_bytes": kernel_bytes(phase, wl.N, P, wl.W, wl.H, wl.k, entries)}
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--phase", required=True, choices=PHASES)
-    ap.add_argument("--tokens-per-rank", type=int, default=1024)
+    ap.add_argument("--tokens-per-rank", type=int, default=None,
+                    help="default 1024 (DeepSeek-V3 shape), 256 for the grouped phases")
     ap.add_argument("--launches", type=int, default=4)
     ap.add_argument("--record", nargs=3, metavar=("RUN_JSON", "NCU_CSV", "COMMAND"),
                     help="enter a capture in profiles/dram_traffic.json instead of running: the "
@@ -207,7 +263,8 @@ def main():
             line = json.loads([ln for ln in f if ln.startswith("{")][-1])
         print(json.dumps(record(a.phase, line, a.record[1], a.record[2])), flush=True)
         return
-    print(json.dumps(run(a.phase, a.tokens_per_rank, a.launches)), flush=True)
+    tpr = a.tokens_per_rank or (256 if a.phase in GROUPED_PHASES else 1024)
+    print(json.dumps(run(a.phase, tpr, a.launches)), flush=True)
 
 
 if __name__ == "__main__":
