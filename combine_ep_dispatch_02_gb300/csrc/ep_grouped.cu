@@ -296,10 +296,15 @@ __device__ __forceinline__ void resolve_entries(const GroupArgs& a, int r, const
     const int lo = r * a.E, hi = lo + a.E;
     bool ok0 = lane < a.k && e.id0 >= lo && e.id0 < hi;
     bool ok1 = lane + 32 < a.k && e.id1 >= lo && e.id1 < hi;
-    for (int jj = 0; jj < a.k; ++jj) {                    // warp-uniform loop
-        const int x = __shfl_sync(0xffffffffu, jj < 32 ? e.id0 : e.id1, jj & 31);
-        if (jj < lane && x == e.id0) ok0 = false;
-        if (jj < lane + 32 && x == e.id1) ok1 = false;
+    if (a.k <= 32) {                                       // one warp-wide match (every lane calls it)
+        const unsigned same = __match_any_sync(0xffffffffu, e.id0);
+        ok0 = ok0 && !(same & lanemask_lt());
+    } else {
+        for (int jj = 0; jj < a.k; ++jj) {                 // warp-uniform loop
+            const int x = __shfl_sync(0xffffffffu, jj < 32 ? e.id0 : e.id1, jj & 31);
+            if (jj < lane && x == e.id0) ok0 = false;
+            if (jj < lane + 32 && x == e.id1) ok1 = false;
+        }
     }
     if (ok0) ok0 = EP_IN_BOUNDS(e.slot0 >= 0 && e.slot0 < a.rows, a.status);
     if (ok1) ok1 = EP_IN_BOUNDS(e.slot1 >= 0 && e.slot1 < a.rows, a.status);
@@ -340,8 +345,8 @@ __global__ void __launch_bounds__(kCopyThreads) ep_grouped_copy_kernel(const Gro
     if (g_next < total) next = load_entries(a, received_row(s_off, a.W, a.rows, (int)g_next), lane);
     while (g_next < total) {
         const uint32_t g = g_next;
-        const int64_t u = received_row(s_off, a.W, a.rows, (int)g);
-        const int r = (int)(u / a.rows);
+        const int r = rank_of_token(s_off, a.W, (int)g);
+        const int64_t u = (int64_t)r * a.rows + ((int)g - s_off[r]);
         const RowEntries cur = next;
         g_next = work_next(ws, g, lane);
         if (g_next < total)                                // lands while this row is copied
@@ -492,8 +497,8 @@ __global__ void __launch_bounds__(kCopyThreads, 2) ep_ungroup_kernel(const Group
         const int gr = row_of(g);
         const int v0 = (g - gr * chunks) * cv;
         const int hv = min(cv, rs - v0);
-        const int64_t u = received_row(s_off, a.W, a.rows, gr);
-        const int r = (int)(u / a.rows);
+        const int r = rank_of_token(s_off, a.W, gr);
+        const int64_t u = (int64_t)r * a.rows + (gr - s_off[r]);
         const RowEntries cur = next;
         if (g < units - nwarps)                            // lands while this unit is folded
             next = load_entries(a, received_row(s_off, a.W, a.rows, row_of(g + nwarps)), lane);
@@ -505,12 +510,22 @@ __global__ void __launch_bounds__(kCopyThreads, 2) ep_ungroup_kernel(const Group
         const int e1 = dest1 >= 0 ? cur.id1 : 0x7FFFFFFF;
         const int nd = __popc(__ballot_sync(0xffffffffu, dest0 >= 0)) +
                        __popc(__ballot_sync(0xffffffffu, dest1 >= 0));
-        // rank of each entry among the valid ones (their ids are distinct)
+        // rank of each entry among the valid ones (their ids are distinct): for up to 32 entries
+        // and 64 local experts, a popcount of the row's local-expert mask below the entry's expert
         int rank0 = 0, rank1 = 0;
-        for (int j = 0; j < a.k; ++j) {
-            const int ej = __shfl_sync(0xffffffffu, j < 32 ? e0 : e1, j & 31);
-            rank0 += ej < e0;
-            rank1 += ej < e1;
+        if (a.k <= 32 && a.E <= 64) {
+            const int le = dest0 >= 0 ? e0 - r * a.E : 0;
+            const unsigned long long bit = dest0 >= 0 ? 1ull << le : 0ull;
+            const unsigned long long mask =
+                (unsigned long long)__reduce_or_sync(0xffffffffu, (unsigned)bit) |
+                (unsigned long long)__reduce_or_sync(0xffffffffu, (unsigned)(bit >> 32)) << 32;
+            rank0 = __popcll(mask & (bit - 1ull));
+        } else {
+            for (int j = 0; j < a.k; ++j) {
+                const int ej = __shfl_sync(0xffffffffu, j < 32 ? e0 : e1, j & 31);
+                rank0 += ej < e0;
+                rank1 += ej < e1;
+            }
         }
         if (!WIDE || nd <= 8) {
             // the rows in ascending expert order, once per received row; then a rolling fold:
