@@ -610,6 +610,8 @@ __global__ void __launch_bounds__(kCopyThreads) ep_group_from_source_kernel(cons
         const int fw = checked_fwd(lane < a.F ? __ldg(a.fwd + tok * a.F + lane) : -1,   // receive rows,
                                    (int64_t)a.W * a.rows, a.status);                // by rank
         const int nd = __popc(__ballot_sync(0xffffffffu, fw >= 0));
+        // the token's destination ranks, one bit each (lane d holds the d-th receive row)
+        const unsigned dranks = __reduce_or_sync(0xffffffffu, fw >= 0 ? 1u << (fw / (int)a.rows) : 0u);
         // metadata rows to the receive rows, as in ep_dispatch (with the first slice)
         for (int d = 0; d < (c == 0 ? nd : 0); ++d) {
             const int64_t row = __shfl_sync(0xffffffffu, fw, d);
@@ -641,13 +643,11 @@ __global__ void __launch_bounds__(kCopyThreads) ep_group_from_source_kernel(cons
                 for (int jj = 0; jj < j && first; ++jj) first = __ldg(ids + jj) != e;
             }
             if (first) r = expert_rank(e, a.E, inv_e);
-            // the token's receive row on rank r: one of the forward-map entries (uniform loop)
-            int64_t rrow = -1;
-            const int64_t lo = (int64_t)r * a.rows, hi = lo + a.rows;
-            for (int d = 0; d < nd; ++d) {
-                const int64_t row = __shfl_sync(0xffffffffu, fw, d);
-                if (r >= 0 && row >= lo && row < hi) rrow = row;
-            }
+            // the token's receive row on rank r: the forward map lists the token's destination
+            // ranks in ascending order, so it is entry popc(ranks below r) (every lane shuffles)
+            const int pos = __popc(dranks & ((1u << (r & 31)) - 1u));
+            const int64_t row_r = __shfl_sync(0xffffffffu, fw, pos & 31);
+            const int64_t rrow = r >= 0 && ((dranks >> (r & 31)) & 1u) ? row_r : -1;
             if (rrow >= 0) {
                 const int slot = a.map[rrow * a.k + j];
                 if (EP_IN_BOUNDS(slot >= 0 && slot < a.rows, a.status))
