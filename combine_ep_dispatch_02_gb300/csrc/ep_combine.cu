@@ -113,6 +113,7 @@ __device__ __forceinline__ void fold_rows(const uint4* __restrict__ eo4, int src
                 if (d < nd) {
                     const uint4 x = b[d][t];
                     if (vnext < nv) b[d][t] = ld_stream_v4(eo4 + ro[d] + vnext);
+                    if (vnext + 32 * kDepth < nv) prefetch_l2(eo4 + ro[d] + vnext + 32 * kDepth);
                     if (vcur < nv) add_vec<FP16>(acc, x);
                 }
             }

@@ -360,6 +360,14 @@ __device__ __forceinline__ int expert_rank(int e, int E, float inv_e)
     return q;
 }
 
+// Asks for the 32-byte sector at p to be brought into L2 and returns at once (no register holds
+// the data): a fold that keeps its next column in registers also asks for the column after it,
+// so more bytes are on their way from DRAM than its registers could hold.
+__device__ __forceinline__ void prefetch_l2(const void* p)
+{
+    asm volatile("prefetch.global.L2 [%0];" :: "l"(p));
+}
+
 // This warp's first unit, or s.units if it has none.
 __device__ __forceinline__ uint32_t work_first(const WorkSplit& s)
 {

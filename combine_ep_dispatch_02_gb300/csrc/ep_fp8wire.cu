@@ -162,6 +162,7 @@ __device__ __forceinline__ void fold_fp8_rows(const WireArgs& a, int src, int nd
                         b[d][t] = ld_stream_v4(q4 + ro[d] + pn);
                         sc[d][t] = __ldg(a.scales + ((ro[d] + pn) >> 3));
                     }
+                    if (pn + 32 * kWireDepth < np) prefetch_l2(q4 + ro[d] + pn + 32 * kWireDepth);
                     if (pc < np) add_fp8x16(acc, x, xs);
                 }
             }
@@ -419,6 +420,7 @@ __device__ __forceinline__ void fold_fp4_rows(const WireArgs& a, int src, int nd
                     b[d] = ld_stream_v4(q4 + ro[d] + pn);
                     sc[d] = __ldg(sc8 + ro[d] + pn);
                 }
+                if (pn + 32 < nb) prefetch_l2(q4 + ro[d] + pn + 32);
                 if (pc < nb) add_fp4x16(acc, z, w, xs);
             }
         }

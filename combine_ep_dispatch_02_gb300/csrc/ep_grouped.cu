@@ -457,6 +457,7 @@ __device__ __forceinline__ void fold_rd(const uint4* y4, int64_t dest0, int64_t 
                 if (q < nd) {
                     const uint4 x = b[q][t];
                     if (vn < hv) b[q][t] = ld_stream_v4(rp[q] + vn);
+                    if (vn + 32 * D < hv) prefetch_l2(rp[q] + vn + 32 * D);
                     if (vc < hv) add8<FP16>(acc, x);
                 }
             }
