@@ -114,6 +114,7 @@ __device__ __forceinline__ void fold_rows(const uint4* __restrict__ eo4, int src
                     const uint4 x = b[d][t];
                     if (vnext < nv) b[d][t] = ld_stream_v4(eo4 + ro[d] + vnext);
                     if (vnext + 32 * kDepth < nv) prefetch_l2(eo4 + ro[d] + vnext + 32 * kDepth);
+                    if (vnext + 64 * kDepth < nv) prefetch_l2(eo4 + ro[d] + vnext + 64 * kDepth);
                     if (vcur < nv) add_vec<FP16>(acc, x);
                 }
             }

@@ -49,6 +49,7 @@ __global__ void __launch_bounds__(kCopyThreads, 3) ep_quantise_rows_kernel(const
                     x[t][0] = ld_stream_v4(src + (int64_t)p * 32);
                     x[t][1] = ld_stream_v4(src + (int64_t)p * 32 + 16);
                 }
+                if (p + 32 * kQuantUnroll < npiece) prefetch_l2(src + (int64_t)(p + 32 * kQuantUnroll) * 32);
             }
 #pragma unroll
             for (int t = 0; t < kQuantUnroll; ++t) {
@@ -278,6 +279,10 @@ __global__ void __launch_bounds__(kCopyThreads, 3) ep_quantise_rows_fp4_kernel(c
             uint4 x[4];
 #pragma unroll
             for (int t = 0; t < 4; ++t) x[t] = ld_stream_v4(src + (int64_t)b * 4 + t);
+            if (b + 32 < nblk) {                     // the next step's block: two 32-byte sectors
+                prefetch_l2(src + (int64_t)(b + 32) * 4);
+                prefetch_l2(src + (int64_t)(b + 32) * 4 + 2);
+            }
             uint32_t code;
             const uint4 codes = quantise_mxfp4_32(x, code);
             st_v4(dq + b, codes);
@@ -420,7 +425,11 @@ __device__ __forceinline__ void fold_fp4_rows(const WireArgs& a, int src, int nd
                     b[d] = ld_stream_v4(q4 + ro[d] + pn);
                     sc[d] = __ldg(sc8 + ro[d] + pn);
                 }
-                if (pn + 32 < nb) prefetch_l2(q4 + ro[d] + pn + 32);
+                if (pn + 32 < nb) {
+                    prefetch_l2(q4 + ro[d] + pn + 32);
+                    prefetch_l2(sc8 + ro[d] + pn + 32);
+                }
+                if (pn + 64 < nb) prefetch_l2(q4 + ro[d] + pn + 64);
                 if (pc < nb) add_fp4x16(acc, z, w, xs);
             }
         }
