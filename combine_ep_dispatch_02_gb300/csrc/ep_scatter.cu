@@ -132,6 +132,7 @@ __global__ void __launch_bounds__(kCopyThreads, 3) ep_scatter_quant_kernel(const
                     in[q][0] = ld_stream_v4(src + (int64_t)p * 32);
                     in[q][1] = ld_stream_v4(src + (int64_t)p * 32 + 16);
                 }
+                if (p + 32 * kQUnroll < npiece) prefetch_l2(src + (int64_t)(p + 32 * kQUnroll) * 32);
             }
             uint4 code[kQUnroll];
             float scale[kQUnroll];
@@ -213,6 +214,10 @@ __global__ void __launch_bounds__(kCopyThreads, 3) ep_scatter_quant_fp4_kernel(c
 #pragma unroll
                 for (int t = 0; t < 4; ++t) x[t] = ld_stream_v4(src + (int64_t)b * 4 + t);
                 codes = quantise_mxfp4_32(x, code);
+            }
+            if (b + 32 < nblk) {                       // the next step's block: two 32-byte sectors
+                prefetch_l2(src + (int64_t)(b + 32) * 4);
+                prefetch_l2(src + (int64_t)(b + 32) * 4 + 2);
             }
             for (int d = 0; d < nd; ++d) {
                 const int64_t row = __shfl_sync(0xffffffffu, dest, d);
