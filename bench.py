@@ -412,6 +412,19 @@ def measure_combine_wire(plan, wl, dev, stream, x, w, idx, P, peak, steps, fmt):
             "quantize_frac": round(qbytes / (qt * 1e-3) / 1e9 / peak, 4)}
 
 
+def grouped_bytes(wl, rows, entries):
+    """Minimal bytes of the grouped view's calls for `rows` received rows and `entries` list
+    entries (16-bit rows): grouping reads each received row and its index row once and writes
+    a row (and a source index) per entry; the inverse reads the entries and writes a row per
+    received row (and reads its index row); the fused dispatch reads each source row with its
+    index and weight rows once, writes a row per entry and the receive rows' index, weight and
+    reverse-map entries."""
+    rb = 2 * wl.H
+    return {"group": rows * (rb + 4 * wl.k) + entries * (rb + 4),
+            "ungroup": entries * rb + rows * (rb + 4 * wl.k),
+            "fused": wl.N * (rb + 8 * wl.k) + entries * rb + rows * (8 * wl.k + 4)}
+
+
 def measure_grouped(ep, dev, stream, peak, steps, workload="small", max_tok=None):
     """The expert-grouped (3-D) view and its inverse: by default on the small-batch workload (W=4,
     64 experts per rank, top-8, hidden 7168 BF16, 256 tokens per rank), the regime a grouped GEMM
@@ -459,10 +472,7 @@ def measure_grouped(ep, dev, stream, peak, steps, workload="small", max_tok=None
     p50 = {name: statistics.median(t["l2_flushed"]) for name, t in times.items()}
     hot = {name: statistics.median(t["hot"]) for name, t in times.items()}
     plan.close()
-    rb = 2 * wl.H
-    gb = rows * (rb + 4 * wl.k) + entries * (rb + 4)
-    ub = entries * rb + rows * (rb + 4 * wl.k)
-    fb = wl.N * (rb + 8 * wl.k) + entries * rb + rows * (8 * wl.k + 4)
+    gb, ub, fb = (grouped_bytes(wl, rows, entries)[key] for key in ("group", "ungroup", "fused"))
     desc = ("W=4, 64 experts/rank, top-8, hidden 7168 BF16, 256 tokens/rank" if workload == "small" else
             f"W={wl.W}, {wl.E} experts/rank, top-{wl.k}, hidden {wl.H} BF16, {wl.M} tokens/rank, Zipf(1.2)")
     del px, y, out, graphs

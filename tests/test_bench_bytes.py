@@ -71,6 +71,19 @@ def test_profile_case_kernel_bytes_agree_with_the_bench():
         assert profile_case.kernel_bytes(phase, 32768, 173981, 8, 7168, 8) == got[phase], phase
 
 
+def test_profile_case_grouped_bytes_agree_with_the_bench():
+    """The grouped phases' per-kernel bytes: the inverse's are the bench's ungroup bytes, and
+    the fused copy's are the bench's fused-dispatch bytes less the reverse map's 4 bytes per
+    received row (the fused call's routing writes those)."""
+    from combine_ep_dispatch_02_gb300 import profile_case
+    wl = types.SimpleNamespace(N=1024, H=7168, k=8, W=4)
+    rows, entries = 3689, 8192
+    got = bench.grouped_bytes(wl, rows, entries)
+    assert profile_case.kernel_bytes("ungroup", wl.N, rows, wl.W, wl.H, wl.k, entries) == got["ungroup"]
+    assert profile_case.kernel_bytes("fused_copy", wl.N, rows, wl.W, wl.H, wl.k, entries) == got["fused"] - 4 * rows
+    assert got["ungroup"] == 8192 * 14336 + 3689 * (14336 + 32) == 170444064
+
+
 def test_recorded_traffic_scales_and_expires(tmp_path, monkeypatch):
     """A capture entered by profile_case.record gives bench.recorded_traffic its DRAM bytes per
     algorithmic byte, applied to the full launch; a code digest that no longer matches voids it."""
